@@ -1,0 +1,500 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 sparse MoE feed-forward layer.
+
+`python bench.py --gpus N --steps K --warmup W` times K steps of the layer on synthetic,
+seeded inputs and prints ONE JSON line (rank 0). A step is one full pass of the layer
+(router scores, softmax/top-K/renorm, dispatch, gate_up+SwiGLU, down+scale, fixed-order
+combine) over one batch of tokens, called through the C ABI (`moe_forward`).
+
+Headline workload: decode of one token at the full layer shape (H=2048, 256 experts, top-8,
+inner 512). Steps cycle through 8 distinct seeded layers (12.9 GB of weights), so the ~58 MB
+of weights a step touches were last read 8 steps earlier (>= 460 MB ago) and are not served
+from the 129 MB L2. Weights and inputs are resident in HBM before timing starts.
+
+Extra keys: `roofline` (dominant kernel: algorithmic bytes per launch over its CUDA-event
+duration inside the timed region, against the measured HBM copy bandwidth), `e2e` (the same
+metric with x copied from pinned host memory and the output copied back inside the timed
+region), `cpu_baseline` (the fp64 C oracle on the host cores on a bounded sample of the same
+workload), `clocks` (nvidia-smi samples taken during the timed region), `also` (the decode
+T=64, prefill T=4096 and 40-layer stack workloads, shorter runs of the same measurement).
+
+`--impl reference` times the oracle (the only reference implementation: the pages publish
+no code) on the host cores for the same workload and metric.
+
+With N > 1 (torchrun), every rank runs the same per-GPU workload on its own GPU (tokens are
+independent; no collective on the data path): value = tokens of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from sparse_moe_ffn_router_gb300 import synth  # noqa: E402
+from sparse_moe_ffn_router_gb300.workloads import RMSNORM_EPS, WORKLOADS  # noqa: E402
+
+METRIC = "MoE-layer tokens/s"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "decode_T1"
+ROTATE = 8
+KERNEL_NAMES = ["router_scores", "router_topk", "dispatch_local", "dispatch_scan", "dispatch_scatter", "gate_up",
+                "down", "combine", "rmsnorm"]
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    p.add_argument("--also", default="decode_T64,prefill_T4096_zipf,stack40_decode_T32",
+                   help="comma-separated extra workloads reported under 'also' ('none' to skip)")
+    p.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    a = p.parse_args()
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+# ---------------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU)
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float) -> float:
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+    return v
+
+
+# ---------------------------------------------------------------------------------------
+# peaks, clocks
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of this process's GPU during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            sel = str(device_index)
+        self.sel = sel
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.25)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [c.strip() for c in line.split(",")]
+                if len(f) >= 9 and f[1].replace(".", "").isdigit():
+                    rows.append(f)
+        except OSError:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+# ---------------------------------------------------------------------------------------
+# the workloads on the GPU
+
+
+class LayerSet:
+    """n distinct seeded layers of a workload, resident on the GPU, with their inputs."""
+
+    def __init__(self, wl, n_layers: int, device):
+        import sparse_moe_ffn_router_gb300 as moe
+        self.moe = moe
+        self.wl = wl
+        self.dims = wl.dims
+        self.device = device
+        self.layers = []
+        for l in range(n_layers):
+            w = synth.make_weights(wl.H, wl.E, wl.I, wl.Is, wl.seed, l, wl.zipf_s, device=device)
+            x = synth.make_x(wl.T, wl.H, wl.seed, l, device=device)
+            self.layers.append((moe.Weights.from_dict(w), x))
+        self.ws = moe.new_workspace(self.dims, device)
+        self.out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=device)
+        self._groups = None
+
+    def step(self, i: int):
+        W, x = self.layers[i % len(self.layers)]
+        self.moe.moe_forward(self.dims, x, W, None, self.out, self.ws)
+
+    def routed_groups(self) -> list[list[int]]:
+        """Per layer: rows of each touched expert (for the algorithmic byte count)."""
+        if self._groups is None:
+            T, H, E, K = self.dims[:4]
+            g = []
+            for W, x in self.layers:
+                ids = torch.empty(T, K, dtype=torch.int32, device=self.device)
+                tw = torch.empty(T, K, dtype=torch.float32, device=self.device)
+                counts = torch.empty(E, dtype=torch.int32, device=self.device)
+                offsets = torch.empty(E + 1, dtype=torch.int32, device=self.device)
+                perm = torch.empty(T * K, dtype=torch.int32, device=self.device)
+                self.moe.moe_route(self.dims, x, W, ids, tw, counts, offsets, perm, self.ws)
+                g.append([int(c) for c in counts.cpu().tolist() if c > 0])
+            self._groups = g
+        return self._groups
+
+
+def algorithmic(dims, groups: list[int]) -> dict:
+    """Bytes each kernel must move at least, and the layer's flops, for one call.
+
+    gate_up reads each touched expert's [2I, H] block and the shared [2Is, H] once, the
+    dispatched x rows once and writes h; down reads each touched [H, I] block and the shared
+    [H, Is] once, reads h and writes Y; the layer adds the router [E+1, H], x and out."""
+    T, H, E, K, I, Is = dims
+    P = T * K
+    n = len(groups)
+    gate_up = 2 * (n * 2 * I * H + 2 * Is * H) + 2 * (P + T) * H + 2 * (P * I + T * Is)
+    down = 2 * (n * H * I + H * Is) + 2 * (P * I + T * Is) + 4 * (P + T) * H
+    router = 2 * (E + 1) * H + 2 * T * H
+    layer_bytes = 2 * ((E + 1) * H + n * 3 * I * H + 3 * Is * H) + 2 * 2 * T * H
+    flops = 2 * T * (E + 1) * H + 2 * P * 3 * I * H + 2 * T * 3 * Is * H
+    return dict(gate_up=gate_up, down=down, router_scores=router, layer=layer_bytes, flops=flops)
+
+
+def trace_kernels(moe, names, n):
+    ev = {k: ([torch.cuda.Event(enable_timing=True) for _ in range(n)],
+              [torch.cuda.Event(enable_timing=True) for _ in range(n)]) for k in names}
+    for k, (a, b) in ev.items():
+        moe.moe_set_trace(k, a, b)
+    return ev
+
+
+def clear_traces(moe):
+    for k in KERNEL_NAMES:
+        moe.moe_set_trace(k)
+
+
+def kernel_ms(ev, n) -> dict:
+    return {k: sum(a[i].elapsed_time(b[i]) for i in range(n)) / n for k, (a, b) in ev.items()}
+
+
+def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_index=None):
+    """Warm-up (all kernels traced, to find the dominant one), then the timed region (only
+    the dominant kernel traced). Returns a result dict."""
+    moe = ls.moe
+    ev = trace_kernels(moe, KERNEL_NAMES, warmup)
+    for i in range(warmup):
+        ls.step(i)
+    torch.cuda.synchronize()
+    warm = kernel_ms(ev, warmup)
+    clear_traces(moe)
+    dominant = max(warm, key=warm.get)
+    ev = trace_kernels(moe, [dominant], steps)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(clocks_index) if clocks_index is not None else None
+    if sampler:
+        sampler.__enter__()
+    barrier()
+    torch.cuda.synchronize()
+    n0 = moe.moe_launch_count()
+    start.record()
+    for i in range(steps):
+        ls.step(warmup + i)
+    stop.record()
+    torch.cuda.synchronize()
+    launches = moe.moe_launch_count() - n0
+    barrier()
+    if sampler:
+        sampler.__exit__(None, None, None)
+    ms = max_over_ranks(start.elapsed_time(stop))
+    dom_ms = kernel_ms(ev, steps)[dominant]
+    clear_traces(moe)
+    groups = ls.routed_groups()
+    nl = len(ls.layers)
+    per_step = [algorithmic(ls.dims, groups[(warmup + i) % nl]) for i in range(steps)]
+    alg_bytes = sum(p[dominant] if dominant in p else 0 for p in per_step) / steps
+    layer_bytes = sum(p["layer"] for p in per_step) / steps
+    flops = per_step[0]["flops"]
+    T = ls.dims[0]
+    res = dict(ms_per_step=ms / steps, tokens_per_s=T * steps / (ms / 1e3), launches=launches,
+               dominant=dominant, dominant_ms=dom_ms, warm_kernel_ms=warm,
+               unique_experts=sum(len(groups[(warmup + i) % nl]) for i in range(steps)) / steps,
+               layer_bytes=layer_bytes, layer_flops=flops)
+    if alg_bytes:
+        ach = alg_bytes / (dom_ms * 1e-3) / 1e9
+        res["roofline"] = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1),
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                           "traffic": None, "bytes_per_launch": int(alg_bytes),
+                           "peak_source": peaks["source"]}
+    layer_gbs = layer_bytes / (ms / steps * 1e-3) / 1e9
+    res["layer_hbm_frac"] = round(layer_gbs / peaks["hbm_gbs"], 4)
+    res["layer_tensor_frac"] = round(flops / (ms / steps * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)
+    if sampler:
+        res["clocks"] = sampler.summary()
+    return res
+
+
+def time_e2e(ls: LayerSet, steps: int, warmup: int) -> dict:
+    """Same metric through the public call with host buffers: per step, x is copied from
+    pinned host memory, the layer runs, and the output is copied back to pinned memory."""
+    moe = ls.moe
+    T, H = ls.dims[:2]
+    hx = [x.cpu().pin_memory() for _, x in ls.layers]
+    hout = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty(T, H, dtype=torch.bfloat16, device=ls.device)
+
+    def step(i):
+        W, _ = ls.layers[i % len(ls.layers)]
+        xd.copy_(hx[i % len(hx)], non_blocking=True)
+        moe.moe_forward(ls.dims, xd, W, None, ls.out, ls.ws)
+        hout.copy_(ls.out, non_blocking=True)
+
+    for i in range(warmup):
+        step(i)
+    barrier()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(steps):
+        step(warmup + i)
+    stop.record()
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(start.elapsed_time(stop))
+    return dict(value=T * steps / (ms / 1e3), ms_per_step=ms / steps, h2d=T * H * 2, d2h=T * H * 2)
+
+
+class StackSet:
+    """The 40-layer stack: x_{l+1} = x_l + MoE_l(RMSNorm(x_l)), one distinct layer each."""
+
+    def __init__(self, wl, device):
+        import sparse_moe_ffn_router_gb300 as moe
+        self.moe = moe
+        self.wl = wl
+        self.dims = wl.dims
+        self.layers = [moe.Weights.from_dict(synth.make_weights(wl.H, wl.E, wl.I, wl.Is, wl.seed, l, None,
+                                                                device=device)) for l in range(wl.layers)]
+        self.x0 = synth.make_x(wl.T, wl.H, wl.seed, 0, device=device, tag="x_stack")
+        self.x = torch.empty_like(self.x0)
+        self.xn = torch.empty_like(self.x0)
+        self.ws = moe.new_workspace(self.dims, device)
+
+    def step(self, i: int):
+        self.x.copy_(self.x0)
+        for W in self.layers:
+            self.moe.moe_rmsnorm(self.dims, self.x, None, RMSNORM_EPS, self.xn)
+            self.moe.moe_forward(self.dims, self.xn, W, self.x, self.x, self.ws)
+
+
+def time_stack(ss: StackSet, steps: int, warmup: int) -> dict:
+    for i in range(warmup):
+        ss.step(i)
+    barrier()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(steps):
+        ss.step(i)
+    stop.record()
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(start.elapsed_time(stop))
+    T = ss.dims[0]
+    return dict(ms_per_step=ms / steps, tokens_per_s=T * steps / (ms / 1e3), layers=len(ss.layers))
+
+
+# ---------------------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline and --impl reference)
+
+
+def oracle_steps(wl, steps: int, warmup: int, budget_s=None, device=None) -> dict:
+    """Time the fp64 C oracle on decode-shaped steps of the workload (layer 0 weights)."""
+    import oracle
+    dev = device if device is not None else "cpu"
+    w = synth.make_weights(wl.H, wl.E, wl.I, wl.Is, wl.seed, 0, wl.zipf_s, device=dev)
+    hw = {k: (None if v is None else v.cpu()) for k, v in w.items()}
+    del w
+    x = synth.make_x(wl.T, wl.H, wl.seed, 0)
+    for _ in range(warmup):
+        oracle.forward(wl.dims, x, hw)
+    if budget_s is not None:
+        t0 = time.perf_counter()
+        oracle.forward(wl.dims, x, hw)
+        one = time.perf_counter() - t0
+        steps = max(1, min(steps, int(budget_s / max(one, 1e-6))))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.forward(wl.dims, x, hw)
+    dt = time.perf_counter() - t0
+    cores = min(wl.T, oracle.num_threads())
+    return dict(value=wl.T * steps / dt, steps=steps, seconds=dt, cores=cores)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    r = oracle_steps(wl, args.steps, args.warmup, device=dev)
+    sample = f"{r['steps']} steps of {wl.name} ({wl.T} token(s) each), layer-0 weights, fp64 C oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": round(r["value"], 3), "unit": UNIT, "n_gpus": world,
+            "steps": r["steps"], "warmup": args.warmup, "ms_per_step": round(r["seconds"] / r["steps"] * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded SplitMix64 + Box-Muller, bf16)",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "K": wl.K, "I": wl.I, "Is": wl.Is},
+            "cpu_baseline": {"value": round(r["value"], 3), "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(r["value"], 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the layer has no CPU path)")
+    import sparse_moe_ffn_router_gb300 as moe
+    moe.load_library()
+    device = torch.device("cuda", torch.cuda.current_device())
+    peaks = load_peaks()
+    wl = WORKLOADS[args.workload]
+    if wl.layers > 1:
+        raise SystemExit("use the stack workload under --also")
+    n_rot = ROTATE if wl.T <= 32 else 1
+    ls = LayerSet(wl, n_rot, device)
+    main_res = time_layer_set(ls, args.steps, args.warmup, peaks, clocks_index=torch.cuda.current_device())
+    e2e = time_e2e(ls, args.steps, args.warmup)
+    value = main_res["tokens_per_s"] * world
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(main_res["ms_per_step"], 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64 + Box-Muller, bf16; random-init weights of the full layer shape)",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "K": wl.K, "I": wl.I, "Is": wl.Is,
+                   "layers_rotated": n_rot,
+                   "l2": ("inputs larger than L2: steps cycle through %d distinct layers (%.1f GB)"
+                          % (n_rot, n_rot * wl.weight_bytes_per_layer() / 1e9)) if n_rot > 1 else
+                   "inputs larger than L2 (%.2f GB of weights touched per step)" % (main_res["layer_bytes"] / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": main_res.get("roofline"),
+        "e2e": {"value": round(e2e["value"] * world, 3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["ms_per_step"], 6)},
+        "gpu_launches": main_res["launches"],
+        "clocks": main_res.get("clocks"),
+        "layer": {"unique_experts_per_step": main_res["unique_experts"],
+                  "hbm_frac_of_layer_bytes": main_res["layer_hbm_frac"],
+                  "tensor_frac": main_res["layer_tensor_frac"],
+                  "kernel_ms_warmup": {k: round(v, 5) for k, v in main_res["warm_kernel_ms"].items()}},
+    }
+    del ls
+    torch.cuda.empty_cache()
+    also = {}
+    names = [] if args.also in ("", "none") else [n for n in args.also.split(",") if n]
+    for name in names:
+        w2 = WORKLOADS[name]
+        if w2.layers > 1:
+            ss = StackSet(w2, device)
+            r = time_stack(ss, max(3, min(args.steps, 10)), 3)
+            also[name] = {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 4),
+                          "layers": r["layers"]}
+            del ss
+        else:
+            ls2 = LayerSet(w2, ROTATE if w2.T <= 32 else 1, device)
+            r = time_layer_set(ls2, max(5, min(args.steps, 50)), 3, peaks)
+            also[name] = {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 5),
+                          "roofline": r.get("roofline"), "hbm_frac_of_layer_bytes": r["layer_hbm_frac"],
+                          "tensor_frac": r["layer_tensor_frac"], "unique_experts_per_step": r["unique_experts"],
+                          "kernel_ms_warmup": {k: round(v, 5) for k, v in r["warm_kernel_ms"].items()}}
+            del ls2
+        torch.cuda.empty_cache()
+    line["also"] = also
+    if rank == 0 and world == 1:
+        r = oracle_steps(wl, 10 ** 6, 1, budget_s=args.cpu_budget, device=device)
+        line["cpu_baseline"] = {"value": round(r["value"], 3), "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                                "sample": f"{r['steps']} steps of {wl.name} ({wl.T} token(s) each, layer-0 weights), "
+                                          f"{r['seconds']:.1f} s of fp64 C oracle work"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

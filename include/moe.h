@@ -1,0 +1,152 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) sparse Mixture-of-Experts feed-forward layer.
+ *
+ * The layer (per token t, "Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256 Experts):
+ *   l      = x[t] . Wr^T (+ br)                        router scores, fp32 accumulate
+ *   p      = softmax(l)                                 over the E experts
+ *   ids    = the K experts of highest p, slot 0 first; equal scores go to the lower index
+ *   w_k    = p[ids_k] / sum_j p[ids_j]                  renormalised to sum to 1
+ *   y      = sigmoid(x[t] . ws) * S(x[t]) + sum_k w_k * X_{ids_k}(x[t])
+ *   out[t] = residual[t] + y                            (residual optional)
+ * where every expert is a SwiGLU network X(x) = (SiLU(x . Wg^T) * (x . Wu^T)) . Wd^T
+ * (same page, Experts and Shared Expert; "Qwen3.6 35B-A3B", Blocks: SparseMoe, SwiGlu).
+ *
+ * Data types and layouts (bf16 = IEEE bfloat16 bit patterns; all row-major, [Out, In]
+ * like `Linear` in "Qwen3.6 35B-A3B", Blocks: Linear):
+ *   x, residual, out  [T, H]        bf16
+ *   router_w          [E, H]        bf16       router_b [E] bf16, optional
+ *   gate_up           [E, 2I, H]    bf16       rows [0,I) of each expert = gate, [I,2I) = up
+ *   down              [E, H, I]     bf16
+ *   shared_gate_up    [2Is, H]      bf16       same split as gate_up
+ *   shared_down       [H, Is]       bf16
+ *   shared_gate       [1, H]        bf16       (no bias)
+ *
+ * Ownership and execution. The caller owns every buffer; all pointers are device pointers
+ * (16-byte aligned) unless stated otherwise. The library allocates nothing on the call
+ * path: scratch lives in a caller-provided device workspace of moe_workspace_size() bytes,
+ * zero-filled once before its first use (moe_workspace_init does that); the library leaves
+ * it ready for the next call. Calls are asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream). Argument errors are detected on the host and returned before
+ * anything is launched. A workspace must not be used by two calls that may overlap in time.
+ * Results are deterministic: the same inputs give bit-identical outputs on every call.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Runtime dimensions: T tokens (B*S flattened; "Qwen3.6 35B-A3B", SparseMoe.forward takes
+ * [B, S, H]), H hidden width, E routed experts, K experts per token, I routed inner width,
+ * Is shared inner width. Supported: T >= 0, 128 <= H <= 8192 with H % 128 == 0,
+ * 1 <= K <= 8, K <= E <= 256, 64 <= I, Is <= 2048 with I % 64 == 0 and Is % 64 == 0,
+ * T * (K + 1) < 2^31. T == 0 is a valid no-op. */
+typedef struct {
+    int32_t T, H, E, K, I, Is;
+} moe_dims;
+
+/* Device pointers to one layer's weights; router_b may be NULL. */
+typedef struct {
+    const void* router_w;
+    const void* router_b;
+    const void* gate_up;
+    const void* down;
+    const void* shared_gate_up;
+    const void* shared_down;
+    const void* shared_gate;
+} moe_weights;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,         /* NULL pointer or negative size                       */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,   /* dims outside the supported range above              */
+    MOE_ERR_MISALIGNED = 3,          /* a pointer is not 16-byte aligned                    */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes < moe_workspace_size(d)                    */
+    MOE_ERR_CUDA = 5,                /* a CUDA launch or runtime call failed                */
+    MOE_ERR_TIMEOUT = 6,             /* a bounded device-side wait gave up                  */
+    MOE_ERR_DEVICE = 7               /* a kernel flagged bad data (e.g. a non-finite score) */
+} moe_status;
+
+/* Bytes of device workspace that moe_route / moe_forward need for dims d (0 if d is
+ * unsupported). Host-only; never fails otherwise. */
+size_t moe_workspace_size(const moe_dims* d);
+
+/* Zero-fill a workspace on `stream` (cudaMemsetAsync). Needed once after allocation. */
+moe_status moe_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/* Routing only: router scores, softmax, top-K, renormalisation, and the dispatch of the
+ * (token, slot) pairs to experts ("Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256
+ * Experts, Router; "One Token Through Qwen3.6", The Router).
+ *   x        [T, H] bf16 in
+ *   ids      [T, K] int32 out: expert of each slot, slot 0 = highest score
+ *   topk_w   [T, K] fp32  out: renormalised routing weights (sum to 1 per token)
+ *   counts   [E]    int32 out: pairs routed to each expert
+ *   offsets  [E+1]  int32 out: exclusive prefix sum of counts, offsets[E] = T*K
+ *   perm     [T*K]  int32 out: values t*K+k grouped by expert (ascending), tokens
+ *                              ascending within an expert
+ * Integer outputs are exact and reproducible; topk_w is fp32. */
+moe_status moe_route(const moe_dims* d, const void* x, const moe_weights* w, int32_t* ids, float* topk_w,
+                     int32_t* counts, int32_t* offsets, int32_t* perm, void* workspace, size_t ws_bytes,
+                     void* stream);
+
+/* The whole layer: out = residual + MoE(x), or MoE(x) when residual is NULL. out must not
+ * overlap x; it may be the same buffer as residual. Routed and shared expert outputs are
+ * summed per token in a fixed order (residual, shared, slot 0 .. K-1) in fp32 and rounded
+ * to bf16 once. */
+moe_status moe_forward(const moe_dims* d, const void* x, const moe_weights* w, const void* residual, void* out,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/* RMSNorm of the pre-MoE norm ("RMSNorm -> MoE FFN -> +residual", "Qwen3.6-35B-A3B --
+ * Architecture Overview", Stage 2; "Qwen3.6 35B-A3B", Blocks: RmsNorm):
+ *   xn[t,h] = bf16( x[t,h] / sqrt(mean_h x[t,h]^2 + eps) * gamma[h] )   (fp32 arithmetic)
+ * Uses d->T and d->H only. gamma [H] bf16 may be NULL (all ones). xn must not overlap x. */
+moe_status moe_rmsnorm(const moe_dims* d, const void* x, const void* gamma, float eps, void* xn, void* stream);
+
+/* Synchronise `stream`, then read and clear the device error word kept in `workspace`:
+ * MOE_OK, MOE_ERR_DEVICE (a kernel saw a non-finite router score) or MOE_ERR_TIMEOUT. */
+moe_status moe_last_device_error(void* workspace, void* stream);
+
+/* Where an intermediate lives in the workspace after moe_forward (for inspection):
+ *   tap 0  h      [T*K + T, max(I,Is)] bf16: gated activations, routed rows in perm order
+ *                                             then the T shared-expert rows in token order
+ *   tap 1  Y      [T, K+1, H] fp32: weighted expert outputs per slot, slot K = shared
+ *   tap 2  sgate  [T] fp32: sigmoid(x . ws)
+ *   tap 3  ids    [T, K] int32      tap 4  topk_w [T, K] fp32
+ * Row strides are the widths given. Returns MOE_ERR_INVALID_ARG for an unknown tap. */
+moe_status moe_workspace_tap(const moe_dims* d, int tap, size_t* offset, size_t* bytes);
+
+/* Kernels of the layer, for moe_set_trace. */
+enum {
+    MOE_KERNEL_ROUTER_SCORES = 0,   /* router + shared-gate scores                 */
+    MOE_KERNEL_ROUTER_TOPK = 1,     /* softmax, top-K, renormalisation             */
+    MOE_KERNEL_DISPATCH_LOCAL = 2,  /* per-block expert counts and ranks           */
+    MOE_KERNEL_DISPATCH_SCAN = 3,   /* offsets and block bases                     */
+    MOE_KERNEL_DISPATCH_SCATTER = 4,/* dispatch permutation                        */
+    MOE_KERNEL_GATE_UP = 5,         /* gate/up projections + SwiGLU, all groups    */
+    MOE_KERNEL_DOWN = 6,            /* down projection + routing-weight scale      */
+    MOE_KERNEL_COMBINE = 7,         /* fixed-order sum into the residual           */
+    MOE_KERNEL_RMSNORM = 8,
+    MOE_KERNEL_COUNT = 9
+};
+
+/* Benchmarking aid. While set, every launch of `kernel` made by this library records
+ * start_events[i] on its stream just before the launch and stop_events[i] just after it,
+ * i = 0, 1, ... cycling modulo n_events (cudaEvent_t handles owned by the caller), so the
+ * caller can read that kernel's duration with cudaEventElapsedTime. n_events = 0 clears it.
+ * Process-wide state, not thread-safe; no effect on results. */
+moe_status moe_set_trace(int kernel, void* const* start_events, void* const* stop_events, int n_events);
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t moe_launch_count(void);
+
+/* Human-readable name of a status. Never NULL. */
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,240 @@
+// api.cu -- the C-ABI entry points declared in include/moe.h: host-side validation, the
+// workspace plan, and the stream-ordered launch sequence of the layer.
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <vector>
+
+#include "launch.h"
+
+namespace moe {
+
+static std::atomic<uint64_t> g_launches{0};
+
+struct TraceSlot {
+    int n = 0;
+    int i = 0;
+    std::vector<void*> start, stop;
+};
+static TraceSlot g_trace[MOE_KERNEL_COUNT];
+
+void trace_begin(int kernel, cudaStream_t s) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    TraceSlot& t = g_trace[kernel];
+    if (t.n) cudaEventRecord((cudaEvent_t)t.start[t.i % t.n], s);
+}
+
+void trace_end(int kernel, cudaStream_t s) {
+    TraceSlot& t = g_trace[kernel];
+    if (t.n) {
+        cudaEventRecord((cudaEvent_t)t.stop[t.i % t.n], s);
+        ++t.i;
+    }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + nb && y < x + na;
+}
+
+int sm_count() {
+    static int cache[128];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 148;
+    }
+    return cache[dev];
+}
+
+// Common validation of moe_route / moe_forward. On success fills the plan and the
+// workspace-backed fields of the argument block.
+moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void* ws, size_t ws_bytes, Plan* p,
+                   LayerArgs* a) {
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (!make_plan(*d, p)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (d->T == 0) return MOE_OK;
+    if (!x || !w || !ws || !w->router_w || !w->gate_up || !w->down || !w->shared_gate_up || !w->shared_down ||
+        !w->shared_gate)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(ws) || !aligned16(w->router_w) || !aligned16(w->gate_up) ||
+        !aligned16(w->down) || !aligned16(w->shared_gate_up) || !aligned16(w->shared_down) ||
+        !aligned16(w->shared_gate) || (w->router_b && !aligned16(w->router_b)))
+        return MOE_ERR_MISALIGNED;
+    if (ws_bytes < p->total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    memset(a, 0, sizeof *a);
+    char* base = (char*)ws;
+    a->x = (const bf16*)x;
+    a->router_w = (const bf16*)w->router_w;
+    a->router_b = (const bf16*)w->router_b;
+    a->gate_up = (const bf16*)w->gate_up;
+    a->down = (const bf16*)w->down;
+    a->sgu = (const bf16*)w->shared_gate_up;
+    a->sd = (const bf16*)w->shared_down;
+    a->sg = (const bf16*)w->shared_gate;
+    a->hdr = (WsHeader*)(base + p->o_hdr);
+    a->logits = (float*)(base + p->o_logits);
+    a->ids = (int32_t*)(base + p->o_ids);
+    a->topw = (float*)(base + p->o_topw);
+    a->sgate = (float*)(base + p->o_sgate);
+    a->counts = (int32_t*)(base + p->o_counts);
+    a->offsets = (int32_t*)(base + p->o_offsets);
+    a->perm = (int32_t*)(base + p->o_perm);
+    a->inv = (int32_t*)(base + p->o_inv);
+    a->lr = (int32_t*)(base + p->o_lr);
+    a->cntb = (int32_t*)(base + p->o_cntb);
+    a->base = (int32_t*)(base + p->o_base);
+    a->act = (int32_t*)(base + p->o_act);
+    a->h = (bf16*)(base + p->o_h);
+    a->Y = (float*)(base + p->o_y);
+    a->T = p->T; a->H = p->H; a->E = p->E; a->K = p->K; a->I = p->I; a->Is = p->Is;
+    a->Imax = p->Imax; a->ldl = p->ldl; a->nb = p->nb; a->P = p->P;
+    a->num_sms = sm_count();
+    return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" size_t moe_workspace_size(const moe_dims* d) {
+    Plan p;
+    if (!d || !make_plan(*d, &p)) return 0;
+    return p.total;
+}
+
+extern "C" moe_status moe_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+    if (!workspace) return MOE_ERR_INVALID_ARG;
+    return cuda_status(cudaMemsetAsync(workspace, 0, ws_bytes, (cudaStream_t)stream));
+}
+
+extern "C" moe_status moe_route(const moe_dims* d, const void* x, const moe_weights* w, int32_t* ids,
+                                float* topk_w, int32_t* counts, int32_t* offsets, int32_t* perm, void* workspace,
+                                size_t ws_bytes, void* stream) {
+    Plan p;
+    LayerArgs a;
+    moe_status st = prepare(d, x, w, workspace, ws_bytes, &p, &a);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+    if (d->T == 0) {
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->E, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d->E + 1), s);
+        return cuda_status(e);
+    }
+    if (!ids || !topk_w || !perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ids) || !aligned16(topk_w) || !aligned16(counts) || !aligned16(offsets) || !aligned16(perm))
+        return MOE_ERR_MISALIGNED;
+    a.ids = ids;
+    a.topw = topk_w;
+    a.counts = counts;
+    a.offsets = offsets;
+    a.perm = perm;
+    cudaError_t e = launch_router(a, s);
+    if (e == cudaSuccess) e = launch_dispatch(a, s);
+    return cuda_status(e);
+}
+
+extern "C" moe_status moe_forward(const moe_dims* d, const void* x, const moe_weights* w, const void* residual,
+                                  void* out, void* workspace, size_t ws_bytes, void* stream) {
+    Plan p;
+    LayerArgs a;
+    moe_status st = prepare(d, x, w, workspace, ws_bytes, &p, &a);
+    if (st != MOE_OK || d->T == 0) return st;
+    if (!out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(out) || (residual && !aligned16(residual))) return MOE_ERR_MISALIGNED;
+    const size_t act_bytes = (size_t)d->T * d->H * 2;
+    if (overlap(out, act_bytes, x, act_bytes)) return MOE_ERR_INVALID_ARG;
+    if (residual && residual != out && overlap(out, act_bytes, residual, act_bytes)) return MOE_ERR_INVALID_ARG;
+    a.residual = (const bf16*)residual;
+    a.out = (bf16*)out;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_router(a, s);
+    if (e == cudaSuccess) e = launch_dispatch(a, s);
+    if (e == cudaSuccess) e = launch_experts(a, s);
+    return cuda_status(e);
+}
+
+extern "C" moe_status moe_rmsnorm(const moe_dims* d, const void* x, const void* gamma, float eps, void* xn,
+                                  void* stream) {
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->T < 0 || d->H < 128 || d->H > 8192 || d->H % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (d->T == 0) return MOE_OK;
+    if (!x || !xn || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xn) || (gamma && !aligned16(gamma))) return MOE_ERR_MISALIGNED;
+    const size_t nbytes = (size_t)d->T * d->H * 2;
+    if (overlap(x, nbytes, xn, nbytes)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_rmsnorm((const bf16*)x, (const bf16*)gamma, eps, (bf16*)xn, d->T, d->H,
+                                      (cudaStream_t)stream));
+}
+
+extern "C" moe_status moe_last_device_error(void* workspace, void* stream) {
+    if (!workspace) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t err = 0;
+    WsHeader* hdr = (WsHeader*)workspace;
+    cudaError_t e = cudaMemcpyAsync(&err, &hdr->err, sizeof err, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (err == 0) return MOE_OK;
+    e = cudaMemsetAsync(&hdr->err, 0, sizeof err, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return (err & ERR_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE;
+}
+
+extern "C" moe_status moe_workspace_tap(const moe_dims* d, int tap, size_t* offset, size_t* bytes) {
+    Plan p;
+    if (!d || !offset || !bytes) return MOE_ERR_INVALID_ARG;
+    if (!make_plan(*d, &p)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const size_t T = (size_t)d->T, P = (size_t)p.P;
+    switch (tap) {
+        case 0: *offset = p.o_h; *bytes = (P + T) * p.Imax * 2; return MOE_OK;
+        case 1: *offset = p.o_y; *bytes = T * (d->K + 1) * d->H * 4; return MOE_OK;
+        case 2: *offset = p.o_sgate; *bytes = T * 4; return MOE_OK;
+        case 3: *offset = p.o_ids; *bytes = P * 4; return MOE_OK;
+        case 4: *offset = p.o_topw; *bytes = P * 4; return MOE_OK;
+        default: return MOE_ERR_INVALID_ARG;
+    }
+}
+
+extern "C" moe_status moe_set_trace(int kernel, void* const* start_events, void* const* stop_events, int n_events) {
+    if (kernel < 0 || kernel >= MOE_KERNEL_COUNT || n_events < 0 || n_events > (1 << 20)) return MOE_ERR_INVALID_ARG;
+    if (n_events > 0 && (!start_events || !stop_events)) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < n_events; ++i)
+        if (!start_events[i] || !stop_events[i]) return MOE_ERR_INVALID_ARG;
+    TraceSlot& t = g_trace[kernel];
+    t.n = 0;
+    t.start.assign(start_events, start_events + n_events);
+    t.stop.assign(stop_events, stop_events + n_events);
+    t.n = n_events;
+    t.i = 0;
+    return MOE_OK;
+}
+
+extern "C" uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+extern "C" const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: a required pointer is NULL, buffers overlap, or an argument is out of range";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE: dims outside the supported range";
+        case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL: workspace smaller than moe_workspace_size()";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA launch or runtime call failed";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE: a kernel flagged a non-finite router score";
+        default: return "unknown moe_status";
+    }
+}

@@ -1,0 +1,118 @@
+// common.cuh -- device helpers and the workspace plan shared by the kernels of the MoE layer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+typedef __nv_bfloat16 bf16;
+
+// Bits of the device error word (first word of the workspace header).
+enum : uint32_t { ERR_NONFINITE_SCORE = 1u, ERR_TIMEOUT = 2u, ERR_BAD_ROUTE = 4u };
+
+// Workspace header: a device error word and small counters, zero-filled once by the caller.
+struct WsHeader {
+    uint32_t err;    // OR of ERR_* bits, cleared by moe_last_device_error
+    int32_t n_act;   // experts with at least one routed pair (written by the dispatch scan)
+    uint32_t pad[62];
+};
+
+// Byte offsets of every buffer inside the caller's workspace (256-byte aligned).
+struct Plan {
+    int T, H, E, K, I, Is, Imax;
+    int64_t P;       // T*K routed pairs
+    int ldl;         // row stride of the score matrix (E + 1 scores: E routed + the shared gate)
+    int nb;          // token blocks of the dispatch
+    size_t o_hdr, o_logits, o_ids, o_topw, o_sgate, o_counts, o_offsets, o_perm, o_inv, o_lr, o_cntb, o_base,
+        o_act, o_h, o_y, total;
+};
+
+constexpr int kDispatchTokens = 64;  // tokens per block of the dispatch (counting-sort) kernels
+
+inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Returns false for dims outside the supported range (see moe.h).
+inline bool make_plan(const moe_dims& d, Plan* p) {
+    if (d.T < 0 || d.H < 128 || d.H > 8192 || d.H % 128 || d.K < 1 || d.K > 8 || d.E < d.K || d.E > 256 ||
+        d.I < 64 || d.I > 2048 || d.I % 64 || d.Is < 64 || d.Is > 2048 || d.Is % 64)
+        return false;
+    if ((int64_t)d.T * (d.K + 1) >= (int64_t)1 << 31) return false;
+    p->T = d.T; p->H = d.H; p->E = d.E; p->K = d.K; p->I = d.I; p->Is = d.Is;
+    p->Imax = d.I > d.Is ? d.I : d.Is;
+    p->P = (int64_t)d.T * d.K;
+    p->ldl = (d.E + 1 + 3) & ~3;
+    p->nb = (d.T + kDispatchTokens - 1) / kDispatchTokens;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
+    const size_t T = (size_t)d.T, P = (size_t)p->P;
+    p->o_hdr = take(sizeof(WsHeader));
+    p->o_logits = take(T * p->ldl * 4);
+    p->o_ids = take(P * 4);
+    p->o_topw = take(P * 4);
+    p->o_sgate = take(T * 4);
+    p->o_counts = take((size_t)d.E * 4);
+    p->o_offsets = take((size_t)(d.E + 1) * 4);
+    p->o_perm = take(P * 4);
+    p->o_inv = take(P * 4);
+    p->o_lr = take(P * 4);
+    p->o_cntb = take((size_t)p->nb * d.E * 4);
+    p->o_base = take((size_t)p->nb * d.E * 4);
+    p->o_act = take((size_t)(d.E + 1) * 4);
+    p->o_h = take((P + T) * p->Imax * 2);
+    p->o_y = take(T * (d.K + 1) * d.H * 4);
+    p->total = o;
+    return true;
+}
+
+#ifdef __CUDACC__
+// Streaming 16-byte load for data read once (weights): bypasses L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Ordinary read-only 16-byte load (activations, reused across warps).
+__device__ __forceinline__ uint4 ld_ro(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+// Two bf16 packed in one 32-bit word -> two floats (exact).
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+    f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
+    f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
+}
+
+// acc + sum_i w[i] * x[i], in order i = 0..7 (fixed rounding order).
+__device__ __forceinline__ float dot8(const uint4& w, const float* x, float acc) {
+    acc = fmaf(bf_lo(w.x), x[0], acc); acc = fmaf(bf_hi(w.x), x[1], acc);
+    acc = fmaf(bf_lo(w.y), x[2], acc); acc = fmaf(bf_hi(w.y), x[3], acc);
+    acc = fmaf(bf_lo(w.z), x[4], acc); acc = fmaf(bf_hi(w.z), x[5], acc);
+    acc = fmaf(bf_lo(w.w), x[6], acc); acc = fmaf(bf_hi(w.w), x[7], acc);
+    return acc;
+}
+
+// Butterfly sum over the warp; every lane ends with the same, order-fixed value.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+#endif
+
+}  // namespace moe

@@ -1,0 +1,91 @@
+// dispatch.cu -- exact, reproducible dispatch of (token, slot) pairs to experts.
+//
+// The pages say only that the router "determines which experts should receive this token"
+// ("One Token Through Qwen3.6", The Router). The layout here is a stable counting sort of
+// the pairs p = t*K + k by expert: counts, exclusive offsets, and perm (tokens ascending
+// within an expert), in three integer passes:
+//   1. per block of 64 tokens (one warp): per-expert counts and each pair's rank among the
+//      block's pairs of the same expert, in token order (match_any + popc, no atomics);
+//   2. one CTA: per-expert totals, the exclusive scan, each (block, expert) base, and the
+//      list of experts that received pairs;
+//   3. scatter: perm[base[block, e] + rank] = p, inv[p] = that position.
+#include "launch.h"
+
+namespace moe {
+
+__global__ void __launch_bounds__(32) k_dispatch_local(LayerArgs a) {
+    __shared__ int cnt[256];
+    const int lane = threadIdx.x, b = blockIdx.x;
+    for (int e = lane; e < a.E; e += 32) cnt[e] = 0;
+    __syncwarp();
+    const int64_t p0 = (int64_t)b * kDispatchTokens * a.K;
+    const int64_t p1 = (int64_t)min((b + 1) * kDispatchTokens, a.T) * a.K;
+    for (int64_t base = p0; base < p1; base += 32) {
+        const int64_t i = base + lane;
+        const bool valid = i < p1;
+        const int e = valid ? a.ids[i] : -1;
+        const unsigned m = __match_any_sync(0xffffffffu, e);
+        const int rank_in = __popc(m & ((1u << lane) - 1u));
+        const int c = valid ? cnt[e] : 0;
+        __syncwarp();
+        if (valid) {
+            a.lr[i] = c + rank_in;
+            if (rank_in == 0) cnt[e] = c + __popc(m);
+        }
+        __syncwarp();
+    }
+    for (int e = lane; e < a.E; e += 32) a.cntb[(size_t)b * a.E + e] = cnt[e];
+}
+
+__global__ void __launch_bounds__(256) k_dispatch_scan(LayerArgs a) {
+    __shared__ int tot[256];
+    __shared__ int off[257];
+    const int e = threadIdx.x;
+    if (e < a.E) {
+        int s = 0;
+        for (int b = 0; b < a.nb; ++b) s += a.cntb[(size_t)b * a.E + e];
+        tot[e] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0, na = 0;
+        for (int j = 0; j < a.E; ++j) {
+            off[j] = run;
+            run += tot[j];
+            if (tot[j] > 0) a.act[na++] = j;
+        }
+        off[a.E] = run;
+        a.hdr->n_act = na;
+    }
+    __syncthreads();
+    if (e < a.E) {
+        a.counts[e] = tot[e];
+        a.offsets[e] = off[e];
+        int run = off[e];
+        for (int b = 0; b < a.nb; ++b) {
+            a.base[(size_t)b * a.E + e] = run;
+            run += a.cntb[(size_t)b * a.E + e];
+        }
+    }
+    if (e == 0) a.offsets[a.E] = off[a.E];
+}
+
+__global__ void __launch_bounds__(256) k_dispatch_scatter(LayerArgs a) {
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (i >= a.P) return;
+    const int t = (int)(i / a.K);
+    const int b = t / kDispatchTokens;
+    const int e = a.ids[i];
+    const int j = a.base[(size_t)b * a.E + e] + a.lr[i];
+    a.perm[j] = (int)i;
+    a.inv[i] = j;
+}
+
+cudaError_t launch_dispatch(const LayerArgs& a, cudaStream_t s) {
+    MOE_LAUNCH(MOE_KERNEL_DISPATCH_LOCAL, s, (k_dispatch_local<<<a.nb, 32, 0, s>>>(a)));
+    MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCAN, s, (k_dispatch_scan<<<1, 256, 0, s>>>(a)));
+    MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCATTER, s, (k_dispatch_scatter<<<(unsigned)((a.P + 255) / 256), 256, 0, s>>>(a)));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,175 @@
+// router.cu -- router scores, softmax/top-K/renormalisation, and RMSNorm.
+//
+// Router ("Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256 Experts, Router): a
+// linear map H -> E scores every expert, softmax, the top K are kept and their weights
+// renormalised to sum to 1. The shared-expert gate sigmoid(Linear(x, 1)) (same page, Shared
+// Expert) is one more dot product of the same token, so it is scored here as column E.
+#include <math.h>
+
+#include "launch.h"
+
+namespace moe {
+
+constexpr int kRouterTokens = 8;  // tokens per warp in the score kernel
+
+// logits[t, r] = sum_h x[t,h] * W[r,h] (+ br[r]) for r < E, and x[t] . ws at r = E.
+// One warp per (score row r, block of 8 tokens); fp32 products and sums in a fixed order
+// (16-byte chunks lane-strided, then a butterfly across the warp).
+__global__ void __launch_bounds__(256) k_router_scores(LayerArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + warp;
+    if (r > a.E) return;
+    const bf16* wrow = r < a.E ? a.router_w + (size_t)r * a.H : a.sg;
+    const int t0 = blockIdx.y * kRouterTokens;
+    const int mt = min(kRouterTokens, a.T - t0);
+    float acc[kRouterTokens];
+#pragma unroll
+    for (int i = 0; i < kRouterTokens; ++i) acc[i] = 0.f;
+    for (int c = lane; c < a.H / 8; c += 32) {
+        const uint4 wv = ld_ro(wrow + (size_t)c * 8);
+#pragma unroll
+        for (int tt = 0; tt < kRouterTokens; ++tt) {
+            if (tt < mt) {
+                float xf[8];
+                unpack8(ld_ro(a.x + (size_t)(t0 + tt) * a.H + (size_t)c * 8), xf);
+                acc[tt] = dot8(wv, xf, acc[tt]);
+            }
+        }
+    }
+#pragma unroll
+    for (int tt = 0; tt < kRouterTokens; ++tt) {
+        if (tt < mt) {
+            float s = warp_sum(acc[tt]);
+            if (lane == 0) {
+                if (r < a.E && a.router_b) s += __bfloat162float(a.router_b[r]);
+                a.logits[(size_t)(t0 + tt) * a.ldl + r] = s;
+            }
+        }
+    }
+}
+
+// One warp per token: top-K of the E scores under the total order (score descending, index
+// ascending), renormalised weights, and the shared-expert gate.
+// Softmax is monotone, so selecting on scores selects on probabilities; the renormalised
+// weight p_k / sum_sel p_j equals exp(l_k - l_0) / sum_sel exp(l_j - l_0) (the full
+// softmax denominator cancels), which is what is computed.
+__global__ void __launch_bounds__(256) k_router_topk(LayerArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= a.T) return;
+    const float* l = a.logits + (size_t)t * a.ldl;
+    float v[8];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = -INFINITY;
+        if (e < a.E) {
+            v[j] = l[e];
+            if (!isfinite(v[j])) {
+                bad = true;
+                v[j] = -INFINITY;
+            }
+        }
+    }
+    uint32_t taken = 0;
+    float sel_v[8];
+    int sel_e[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (k < a.K) {
+            float bv = -INFINITY;
+            int be = 0x7fffffff;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = lane + 32 * j;
+                if (e < a.E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
+                    bv = v[j];
+                    be = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (ov > bv || (ov == bv && oe < be)) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+            sel_v[k] = bv;
+            sel_e[k] = be;
+        }
+    }
+    if (lane == 0) {
+        float ex[8], s = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k < a.K) {
+                ex[k] = expf(sel_v[k] - sel_v[0]);
+                s += ex[k];
+            }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k < a.K) {
+                a.ids[(size_t)t * a.K + k] = sel_e[k];
+                a.topw[(size_t)t * a.K + k] = ex[k] / s;
+            }
+        const float z = l[a.E];
+        if (!isfinite(z)) bad = true;
+        a.sgate[t] = 1.0f / (1.0f + expf(-z));
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&a.hdr->err, ERR_NONFINITE_SCORE);
+}
+
+cudaError_t launch_router(const LayerArgs& a, cudaStream_t s) {
+    dim3 g1((a.E + 1 + 7) / 8, (a.T + kRouterTokens - 1) / kRouterTokens);
+    MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (k_router_scores<<<g1, 256, 0, s>>>(a)));
+    MOE_LAUNCH(MOE_KERNEL_ROUTER_TOPK, s, (k_router_topk<<<(a.T + 7) / 8, 256, 0, s>>>(a)));
+    return cudaGetLastError();
+}
+
+// RMSNorm, one CTA per token row: fp32 sum of squares in a fixed order, 1/sqrt, scale, bf16.
+__global__ void __launch_bounds__(256) k_rmsnorm(const bf16* x, const bf16* gamma, float eps, bf16* xn, int H) {
+    __shared__ float wsum[8];
+    const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bf16* xr = x + (size_t)t * H;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < H / 8; c += 256) {
+        float f[8];
+        unpack8(ld_ro(xr + (size_t)c * 8), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) wsum[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += wsum[w];
+    const float r = 1.0f / sqrtf(tot / (float)H + eps);
+    for (int c = threadIdx.x; c < H / 8; c += 256) {
+        float f[8], g[8];
+        unpack8(ld_ro(xr + (size_t)c * 8), f);
+        if (gamma) {
+            unpack8(ld_ro(gamma + (size_t)c * 8), g);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) g[i] = 1.f;
+        }
+        uint4 o;
+        o.x = pack_bf16x2(f[0] * r * g[0], f[1] * r * g[1]);
+        o.y = pack_bf16x2(f[2] * r * g[2], f[3] * r * g[3]);
+        o.z = pack_bf16x2(f[4] * r * g[4], f[5] * r * g[5]);
+        o.w = pack_bf16x2(f[6] * r * g[6], f[7] * r * g[7]);
+        *reinterpret_cast<uint4*>(xn + (size_t)t * H + (size_t)c * 8) = o;
+    }
+}
+
+cudaError_t launch_rmsnorm(const bf16* x, const bf16* gamma, float eps, bf16* xn, int T, int H, cudaStream_t s) {
+    MOE_LAUNCH(MOE_KERNEL_RMSNORM, s, (k_rmsnorm<<<T, 256, 0, s>>>(x, gamma, eps, xn, H)));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

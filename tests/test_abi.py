@@ -1,0 +1,116 @@
+"""Host-only checks of the C ABI: the library loads without a GPU, exports every function
+include/moe.h declares, and rejects bad arguments on the host before any launch.
+
+Every call below fails host validation, so nothing is launched (on a GPU machine too): the
+fake device addresses are never dereferenced."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_moe_ffn_router_gb300 import binding
+from sparse_moe_ffn_router_gb300.binding import CWeights, Dims
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FULL = (64, 2048, 256, 8, 512, 512)
+A = 0x10000000  # a 16-byte aligned fake device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return binding.load_library()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert set(names) == set(binding.EXPORTED), names
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def test_workspace_size_and_taps(lib):
+    n = lib.moe_workspace_size(ctypes.byref(Dims(*FULL)))
+    assert n > 0 and n % 256 == 0
+    # Y [T, K+1, H] fp32 dominates; it must fit
+    assert n >= 64 * 9 * 2048 * 4
+    assert lib.moe_workspace_size(ctypes.byref(Dims(0, 2048, 256, 8, 512, 512))) > 0
+    for bad in [(1, 2000, 256, 8, 512, 512), (1, 2048, 257, 8, 512, 512), (1, 2048, 256, 9, 512, 512),
+                (1, 2048, 4, 8, 512, 512), (1, 2048, 256, 8, 500, 512), (-1, 2048, 256, 8, 512, 512),
+                (1, 2048, 256, 0, 512, 512), (1, 64, 8, 2, 64, 64)]:
+        assert lib.moe_workspace_size(ctypes.byref(Dims(*bad))) == 0, bad
+    off, nb = binding.moe_workspace_tap(FULL, 1)
+    assert off % 256 == 0 and nb == 64 * 9 * 2048 * 4 and off + nb <= n
+    with pytest.raises(binding.MoEError):
+        binding.moe_workspace_tap(FULL, 99)
+
+
+def _weights(**over):
+    w = dict(router_w=A, router_b=None, gate_up=A, down=A, shared_gate_up=A, shared_down=A, shared_gate=A)
+    w.update(over)
+    return CWeights(*[w[f[0]] for f in CWeights._fields_])
+
+
+def _forward(lib, dims=FULL, x=A + 0x100000, w=None, res=None, out=A + 0x200000, ws=A + 0x400000, wsb=None):
+    d = Dims(*dims)
+    if wsb is None:
+        wsb = lib.moe_workspace_size(ctypes.byref(d))
+    w = w or _weights()
+    return lib.moe_forward(ctypes.byref(d), x, ctypes.byref(w), res, out, ws, wsb, None)
+
+
+def test_forward_rejects_bad_arguments(lib):
+    assert lib.moe_forward(None, A, None, None, A, A, 0, None) == 1
+    assert _forward(lib, dims=(1, 2048, 256, 9, 512, 512)) == 2
+    assert _forward(lib, x=None) == 1
+    assert _forward(lib, w=_weights(down=None)) == 1
+    assert _forward(lib, out=None) == 1
+    assert _forward(lib, x=A + 8) == 3
+    assert _forward(lib, w=_weights(gate_up=A + 2)) == 3
+    assert _forward(lib, out=A + 0x200002) == 3
+    assert _forward(lib, ws=A + 0x400004) == 3
+    assert _forward(lib, wsb=1024) == 4
+    # out overlapping x, and out partly overlapping residual
+    assert _forward(lib, out=A + 0x100000 + 64 * 2048) == 1
+    assert _forward(lib, res=A + 0x200000 + 4096) == 1
+
+
+def test_zero_tokens_is_a_noop(lib):
+    assert _forward(lib, dims=(0, 2048, 256, 8, 512, 512), x=None, out=None, ws=None, wsb=0) == 0
+
+
+def test_route_and_rmsnorm_reject_bad_arguments(lib):
+    d = Dims(*FULL)
+    w = _weights()
+    wsb = lib.moe_workspace_size(ctypes.byref(d))
+    assert lib.moe_route(ctypes.byref(d), A, ctypes.byref(w), A, A, None, A, A, A, wsb, None) == 1
+    assert lib.moe_route(ctypes.byref(d), A, ctypes.byref(w), None, A, A, A, A, A, wsb, None) == 1
+    assert lib.moe_route(ctypes.byref(d), A, ctypes.byref(w), A + 4, A, A, A, A, A, wsb, None) == 3
+    assert lib.moe_route(ctypes.byref(d), A, ctypes.byref(w), A, A, A, A, A, A, wsb - 256, None) == 4
+    assert lib.moe_rmsnorm(None, A, None, ctypes.c_float(1e-6), A, None) == 1
+    assert lib.moe_rmsnorm(ctypes.byref(Dims(4, 100, 1, 1, 64, 64)), A, None, ctypes.c_float(1e-6), A, None) == 2
+    assert lib.moe_rmsnorm(ctypes.byref(d), A, None, ctypes.c_float(-1.0), A + 0x100000, None) == 1
+    assert lib.moe_rmsnorm(ctypes.byref(d), A, None, ctypes.c_float(1e-6), A + 8, None) == 3
+    assert lib.moe_rmsnorm(ctypes.byref(d), A, None, ctypes.c_float(1e-6), A + 64, None) == 1  # overlap
+    assert lib.moe_last_device_error(None, None) == 1
+    assert lib.moe_workspace_init(None, 16, None) == 1
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.moe_status_string(s).decode().startswith(binding.MOE_STATUS[s])
+    assert b"unknown" in lib.moe_status_string(42)
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    with pytest.raises(ValueError, match="GPU only"):
+        binding._ptr(torch.zeros(4))
