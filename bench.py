@@ -55,13 +55,16 @@ KERNEL_NAMES = ["router_scores", "router_topk", "dispatch_local", "dispatch_scan
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=0,
+                   help="timed steps (default: enough for about 2 s of timed work, at least 200)")
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     p.add_argument("--also", default="decode_T64,prefill_T4096_zipf,stack40_decode_T32",
                    help="comma-separated extra workloads reported under 'also' ('none' to skip)")
     p.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--rotate", type=int, default=ROTATE,
+                   help="distinct layers cycled through by small-T workloads (keeps weights out of L2)")
     a = p.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -116,7 +119,7 @@ def load_peaks() -> dict:
 class ClockSampler:
     """nvidia-smi samples (every 200 ms) of this process's GPU during a region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -142,6 +145,12 @@ class ClockSampler:
         time.sleep(0.3)
         return self
 
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
     def __exit__(self, *exc):
         time.sleep(0.25)
         if self.proc is not None:
@@ -152,24 +161,33 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self) -> dict:
+        from datetime import datetime
         rows = []
         try:
             for line in open(self.path):
                 f = [c.strip() for c in line.split(",")]
-                if len(f) >= 9 and f[1].replace(".", "").isdigit():
-                    rows.append(f)
+                if len(f) >= 10 and f[2].replace(".", "").isdigit():
+                    try:
+                        ts = datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        ts = None
+                    rows.append((ts, f[1:]))
         except OSError:
             pass
         finally:
             if self.path and os.path.exists(self.path):
                 os.unlink(self.path)
-        if not rows:
+        t0, t1 = getattr(self, "t0", None), getattr(self, "t1", None)
+        inside = [r for ts, r in rows if ts is not None and t0 is not None and t1 is not None and t0 <= ts <= t1]
+        use = inside or [r for _, r in rows]
+        if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
-        sm = [float(r[1]) for r in rows]
+        sm = [float(r[1]) for r in use]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
-                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+        reasons = sorted({n for r in use for n, v in zip(names, r[5:9]) if v.lower().startswith("active")})
+        pw = [float(r[3]) for r in use if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(use[0][2]), "reasons": reasons,
+                "samples": len(use), "samples_in_timed_region": len(inside), "power_w_max": max(pw) if pw else None}
 
 
 # ---------------------------------------------------------------------------------------
@@ -249,7 +267,7 @@ def kernel_ms(ev, n) -> dict:
     return {k: sum(a[i].elapsed_time(b[i]) for i in range(n)) / n for k, (a, b) in ev.items()}
 
 
-def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_index=None):
+def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_index=None, auto=(2.0, 200, 100000)):
     """Warm-up (all kernels traced, to find the dominant one), then the timed region (only
     the dominant kernel traced). Returns a result dict."""
     moe = ls.moe
@@ -260,6 +278,14 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
     warm = kernel_ms(ev, warmup)
     clear_traces(moe)
     dominant = max(warm, key=warm.get)
+    if steps <= 0:  # auto: about 2 s of timed work
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(3):
+            ls.step(i)
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 3
+        steps = int(min(auto[2], max(auto[1], auto[0] / max(per, 1e-6))))
     ev = trace_kernels(moe, [dominant], steps)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(clocks_index) if clocks_index is not None else None
@@ -268,12 +294,16 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
     barrier()
     torch.cuda.synchronize()
     n0 = moe.moe_launch_count()
+    if sampler:
+        sampler.mark(True)
     start.record()
     for i in range(steps):
         ls.step(warmup + i)
     stop.record()
     torch.cuda.synchronize()
     launches = moe.moe_launch_count() - n0
+    if sampler:
+        sampler.mark(False)
     barrier()
     if sampler:
         sampler.__exit__(None, None, None)
@@ -287,7 +317,7 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
     layer_bytes = sum(p["layer"] for p in per_step) / steps
     flops = per_step[0]["flops"]
     T = ls.dims[0]
-    res = dict(ms_per_step=ms / steps, tokens_per_s=T * steps / (ms / 1e3), launches=launches,
+    res = dict(steps=steps, ms_per_step=ms / steps, tokens_per_s=T * steps / (ms / 1e3), launches=launches,
                dominant=dominant, dominant_ms=dom_ms, warm_kernel_ms=warm,
                unique_experts=sum(len(groups[(warmup + i) % nl]) for i in range(steps)) / steps,
                layer_bytes=layer_bytes, layer_flops=flops)
@@ -406,7 +436,7 @@ def run_reference(args, rank, world):
         return
     wl = WORKLOADS[args.workload]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    r = oracle_steps(wl, args.steps, args.warmup, device=dev)
+    r = oracle_steps(wl, args.steps if args.steps > 0 else 100, args.warmup, device=dev)
     sample = f"{r['steps']} steps of {wl.name} ({wl.T} token(s) each), layer-0 weights, fp64 C oracle"
     line = {"impl": "reference", "metric": METRIC, "value": round(r["value"], 3), "unit": UNIT, "n_gpus": world,
             "steps": r["steps"], "warmup": args.warmup, "ms_per_step": round(r["seconds"] / r["steps"] * 1e3, 3),
@@ -437,13 +467,13 @@ def main():
     wl = WORKLOADS[args.workload]
     if wl.layers > 1:
         raise SystemExit("use the stack workload under --also")
-    n_rot = ROTATE if wl.T <= 32 else 1
+    n_rot = max(1, args.rotate) if wl.T <= 32 else 1
     ls = LayerSet(wl, n_rot, device)
     main_res = time_layer_set(ls, args.steps, args.warmup, peaks, clocks_index=torch.cuda.current_device())
-    e2e = time_e2e(ls, args.steps, args.warmup)
+    e2e = time_e2e(ls, main_res["steps"], args.warmup)
     value = main_res["tokens_per_s"] * world
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": main_res["steps"],
         "warmup": args.warmup, "ms_per_step": round(main_res["ms_per_step"], 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded SplitMix64 + Box-Muller, bf16; random-init weights of the full layer shape)",
@@ -471,13 +501,14 @@ def main():
         w2 = WORKLOADS[name]
         if w2.layers > 1:
             ss = StackSet(w2, device)
-            r = time_stack(ss, max(3, min(args.steps, 10)), 3)
+            r = time_stack(ss, 10 if args.steps <= 0 else max(3, min(args.steps, 10)), 3)
             also[name] = {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 4),
                           "layers": r["layers"]}
             del ss
         else:
             ls2 = LayerSet(w2, ROTATE if w2.T <= 32 else 1, device)
-            r = time_layer_set(ls2, max(5, min(args.steps, 50)), 3, peaks)
+            r = time_layer_set(ls2, 0 if args.steps <= 0 else max(5, min(args.steps, 50)), 3, peaks,
+                               auto=(1.0, 5, 500))
             also[name] = {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 5),
                           "roofline": r.get("roofline"), "hbm_frac_of_layer_bytes": r["layer_hbm_frac"],
                           "tensor_frac": r["layer_tensor_frac"], "unique_experts_per_step": r["unique_experts"],
