@@ -49,7 +49,7 @@ UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "decode_T1"
 ROTATE = 8
 KERNEL_NAMES = ["router_scores", "router_topk", "dispatch_local", "dispatch_scan", "dispatch_scatter", "gate_up",
-                "down", "combine", "rmsnorm"]
+                "down", "combine", "rmsnorm", "shared_gate", "gather", "gemm_plan"]
 
 
 def parse_args():

@@ -113,7 +113,9 @@ moe_status moe_last_device_error(void* workspace, void* stream);
 /* Where an intermediate lives in the workspace after moe_forward (for inspection):
  *   tap 0  h      [T*K + T, max(I,Is)] bf16: gated activations, routed rows in perm order
  *                                             then the T shared-expert rows in token order
- *   tap 1  Y      [T, K+1, H] fp32: weighted expert outputs per slot, slot K = shared
+ *   tap 1  Y      [T, K+1, H] weighted expert outputs per slot, slot K = shared; fp32
+ *                 when T < 256 (weight-streaming path), bf16 from T >= 256 (tensor-core
+ *                 path): bytes / (T*(K+1)*H) tells which
  *   tap 2  sgate  [T] fp32: sigmoid(x . ws)
  *   tap 3  ids    [T, K] int32      tap 4  topk_w [T, K] fp32
  * Row strides are the widths given. Returns MOE_ERR_INVALID_ARG for an unknown tap. */
@@ -128,9 +130,13 @@ enum {
     MOE_KERNEL_DISPATCH_SCATTER = 4,/* dispatch permutation                        */
     MOE_KERNEL_GATE_UP = 5,         /* gate/up projections + SwiGLU, all groups    */
     MOE_KERNEL_DOWN = 6,            /* down projection + routing-weight scale      */
+    /* (from T >= 256 the router scores, gate_up and down run as tensor-core GEMMs) */
     MOE_KERNEL_COMBINE = 7,         /* fixed-order sum into the residual           */
     MOE_KERNEL_RMSNORM = 8,
-    MOE_KERNEL_COUNT = 9
+    MOE_KERNEL_SHARED_GATE = 9,     /* shared-expert gate scores (many-token path)  */
+    MOE_KERNEL_GATHER = 10,         /* token rows in dispatch order (many-token path) */
+    MOE_KERNEL_GEMM_PLAN = 11,      /* group/tile tables of the expert GEMMs        */
+    MOE_KERNEL_COUNT = 12
 };
 
 /* Benchmarking aid. While set, every launch of `kernel` made by this library records

@@ -98,6 +98,15 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
     a->act = (int32_t*)(base + p->o_act);
     a->h = (bf16*)(base + p->o_h);
     a->Y = (float*)(base + p->o_y);
+    a->Yb = (bf16*)(base + p->o_y);
+    a->xperm = (bf16*)(base + p->o_xperm);
+    a->up_groups = (GemmGroup*)(base + p->o_upg);
+    a->dn_groups = (GemmGroup*)(base + p->o_dng);
+    a->up_tiles = (int32_t*)(base + p->o_upt);
+    a->dn_tiles = (int32_t*)(base + p->o_dnt);
+    a->n_groups = &a->hdr->n_groups;
+    a->comb_ticket = (uint32_t*)(base + p->o_ctk);
+    a->gemm = p->gemm;
     a->T = p->T; a->H = p->H; a->E = p->E; a->K = p->K; a->I = p->I; a->Is = p->Is;
     a->Imax = p->Imax; a->ldl = p->ldl; a->nb = p->nb; a->P = p->P;
     a->num_sms = sm_count();
@@ -105,6 +114,14 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
 }
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Router scores, top-K and dispatch: one fused launch for few tokens, else separate kernels.
+cudaError_t launch_routing(const LayerArgs& a, cudaStream_t s) {
+    if (a.T <= kFusedRouteTokens) return launch_route_fused(a, s);
+    cudaError_t e = launch_router(a, s);
+    if (e == cudaSuccess) e = launch_dispatch(a, s);
+    return e;
+}
 
 }  // namespace
 
@@ -141,9 +158,7 @@ extern "C" moe_status moe_route(const moe_dims* d, const void* x, const moe_weig
     a.counts = counts;
     a.offsets = offsets;
     a.perm = perm;
-    cudaError_t e = launch_router(a, s);
-    if (e == cudaSuccess) e = launch_dispatch(a, s);
-    return cuda_status(e);
+    return cuda_status(launch_routing(a, s));
 }
 
 extern "C" moe_status moe_forward(const moe_dims* d, const void* x, const moe_weights* w, const void* residual,
@@ -160,9 +175,17 @@ extern "C" moe_status moe_forward(const moe_dims* d, const void* x, const moe_we
     a.residual = (const bf16*)residual;
     a.out = (bf16*)out;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = launch_router(a, s);
-    if (e == cudaSuccess) e = launch_dispatch(a, s);
-    if (e == cudaSuccess) e = launch_experts(a, s);
+    cudaError_t e = launch_routing(a, s);
+    if (a.gemm) {
+        if (e == cudaSuccess) e = launch_gemm_prep(a, s);
+        if (e == cudaSuccess) e = launch_expert_gemms(a, s);
+        if (e == cudaSuccess) e = launch_combine(a, s);
+    } else if (e == cudaSuccess && stream_supported(a)) {
+        e = launch_stream_experts(a, s);  // the combine is fused into its down kernel
+    } else if (e == cudaSuccess) {
+        e = launch_experts(a, s);
+        if (e == cudaSuccess) e = launch_combine(a, s);
+    }
     return cuda_status(e);
 }
 
@@ -201,7 +224,7 @@ extern "C" moe_status moe_workspace_tap(const moe_dims* d, int tap, size_t* offs
     const size_t T = (size_t)d->T, P = (size_t)p.P;
     switch (tap) {
         case 0: *offset = p.o_h; *bytes = (P + T) * p.Imax * 2; return MOE_OK;
-        case 1: *offset = p.o_y; *bytes = T * (d->K + 1) * d->H * 4; return MOE_OK;
+        case 1: *offset = p.o_y; *bytes = T * (d->K + 1) * d->H * (p.gemm ? 2 : 4); return MOE_OK;
         case 2: *offset = p.o_sgate; *bytes = T * 4; return MOE_OK;
         case 3: *offset = p.o_ids; *bytes = P * 4; return MOE_OK;
         case 4: *offset = p.o_topw; *bytes = P * 4; return MOE_OK;

@@ -17,10 +17,24 @@ enum : uint32_t { ERR_NONFINITE_SCORE = 1u, ERR_TIMEOUT = 2u, ERR_BAD_ROUTE = 4u
 
 // Workspace header: a device error word and small counters, zero-filled once by the caller.
 struct WsHeader {
-    uint32_t err;    // OR of ERR_* bits, cleared by moe_last_device_error
-    int32_t n_act;   // experts with at least one routed pair (written by the dispatch scan)
-    uint32_t pad[62];
+    uint32_t err;      // OR of ERR_* bits, cleared by moe_last_device_error
+    int32_t n_act;     // experts with at least one routed pair (written by the dispatch scan)
+    int32_t n_groups;  // GEMM groups: n_act routed experts + the shared expert
+    uint32_t route_ticket;  // CTAs of the fused routing kernel that finished (re-armed to 0)
+    uint32_t pad[60];
 };
+
+// One group of the grouped GEMM: A rows [a_row0, a_row0 + rows) of the activation tensor,
+// B block starting at weight row b_row0, output rows from out_row0; src selects the routed
+// (0) or the shared-expert (1) tensor maps.
+struct GemmGroup {
+    int a_row0, rows, b_row0, out_row0, src;
+};
+
+// Tokens from which the layer runs its GEMMs on the tensor cores (below: weight streaming).
+constexpr int kGemmMinTokens = 256;
+// Tokens up to which routing runs as one fused launch (scores, top-K and dispatch).
+constexpr int kFusedRouteTokens = 64;
 
 // Byte offsets of every buffer inside the caller's workspace (256-byte aligned).
 struct Plan {
@@ -28,8 +42,9 @@ struct Plan {
     int64_t P;       // T*K routed pairs
     int ldl;         // row stride of the score matrix (E + 1 scores: E routed + the shared gate)
     int nb;          // token blocks of the dispatch
+    bool gemm;       // many-token path (tensor-core GEMMs, bf16 Y) instead of weight streaming
     size_t o_hdr, o_logits, o_ids, o_topw, o_sgate, o_counts, o_offsets, o_perm, o_inv, o_lr, o_cntb, o_base,
-        o_act, o_h, o_y, total;
+        o_act, o_h, o_y, o_xperm, o_upg, o_dng, o_upt, o_dnt, o_ctk, total;
 };
 
 constexpr int kDispatchTokens = 64;  // tokens per block of the dispatch (counting-sort) kernels
@@ -64,7 +79,14 @@ inline bool make_plan(const moe_dims& d, Plan* p) {
     p->o_base = take((size_t)p->nb * d.E * 4);
     p->o_act = take((size_t)(d.E + 1) * 4);
     p->o_h = take((P + T) * p->Imax * 2);
-    p->o_y = take(T * (d.K + 1) * d.H * 4);
+    p->gemm = d.T >= kGemmMinTokens;
+    p->o_y = take(T * (d.K + 1) * d.H * (p->gemm ? 2 : 4));
+    p->o_xperm = take(p->gemm ? P * d.H * 2 : 0);
+    p->o_upg = take((size_t)(d.E + 1) * sizeof(GemmGroup));
+    p->o_dng = take((size_t)(d.E + 1) * sizeof(GemmGroup));
+    p->o_upt = take((size_t)(d.E + 2) * 4);
+    p->o_dnt = take((size_t)(d.E + 2) * 4);
+    p->o_ctk = take((size_t)(d.H / 64) * 4);
     p->total = o;
     return true;
 }

@@ -81,6 +81,58 @@ __global__ void __launch_bounds__(256) k_dispatch_scatter(LayerArgs a) {
     a.inv[i] = j;
 }
 
+// Tables of the grouped tensor-core GEMMs: one group per expert that received pairs (in
+// expert order), then the shared expert over all T tokens; each group's first tile.
+__global__ void k_gemm_plan(LayerArgs a, int fh, int bn_dn) {
+    if (threadIdx.x != 0) return;
+    const int n = a.hdr->n_act;
+    int tu = 0, td = 0;
+    for (int g = 0; g <= n; ++g) {
+        GemmGroup up, dn;
+        int rows, nt_up;
+        if (g < n) {
+            const int e = a.act[g];
+            const int r0 = a.offsets[e];
+            rows = a.offsets[e + 1] - r0;
+            up = GemmGroup{r0, rows, e * 2 * a.I, r0, 0};
+            dn = GemmGroup{r0, rows, e * a.H, 0, 0};
+            nt_up = a.I / fh;
+        } else {
+            rows = a.T;
+            up = GemmGroup{0, a.T, 0, (int)a.P, 1};
+            dn = GemmGroup{(int)a.P, a.T, 0, 0, 1};
+            nt_up = a.Is / fh;
+        }
+        const int mt = (rows + 127) / 128;
+        a.up_groups[g] = up;
+        a.up_tiles[g] = tu;
+        tu += mt * nt_up;
+        a.dn_groups[g] = dn;
+        a.dn_tiles[g] = td;
+        td += mt * (a.H / bn_dn);
+    }
+    a.up_tiles[n + 1] = tu;
+    a.dn_tiles[n + 1] = td;
+    *a.n_groups = n + 1;
+}
+
+// xperm[j] = x[perm[j] / K]: the token rows in dispatch order, the A operand of gate_up.
+__global__ void __launch_bounds__(256) k_gather_rows(LayerArgs a) {
+    const int64_t j = blockIdx.x;
+    const int t = a.perm[j] / a.K;
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H);
+    uint4* dst = reinterpret_cast<uint4*>(a.xperm + (size_t)j * a.H);
+    for (int c = threadIdx.x; c < a.H / 8; c += 256) dst[c] = src[c];
+}
+
+cudaError_t launch_gemm_prep(const LayerArgs& a, cudaStream_t s) {
+    const int fh = (a.I % 128 == 0 && a.Is % 128 == 0) ? 128 : 64;
+    const int bn_dn = (a.H % 256 == 0) ? 256 : 128;
+    MOE_LAUNCH(MOE_KERNEL_GEMM_PLAN, s, (k_gemm_plan<<<1, 32, 0, s>>>(a, fh, bn_dn)));
+    MOE_LAUNCH(MOE_KERNEL_GATHER, s, (k_gather_rows<<<(unsigned)a.P, 256, 0, s>>>(a)));
+    return cudaGetLastError();
+}
+
 cudaError_t launch_dispatch(const LayerArgs& a, cudaStream_t s) {
     MOE_LAUNCH(MOE_KERNEL_DISPATCH_LOCAL, s, (k_dispatch_local<<<a.nb, 32, 0, s>>>(a)));
     MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCAN, s, (k_dispatch_scan<<<1, 256, 0, s>>>(a)));

@@ -181,21 +181,25 @@ __global__ void __launch_bounds__(256) k_down(LayerArgs a) {
 // out[t, o] = bf16( residual[t, o] + Y[t, K, o] + Y[t, 0, o] + ... + Y[t, K-1, o] ), summed in
 // fp32 in exactly this order ("RMSNorm -> MoE FFN -> +residual", "Qwen3.6-35B-A3B --
 // Architecture Overview", Stage 2).
-__global__ void __launch_bounds__(256) k_combine(LayerArgs a) {
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const bf16* p) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    return make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
+}
+
+template <typename YT>
+__global__ void __launch_bounds__(256) k_combine(LayerArgs a, const YT* Y) {
     const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
     const int q = a.H / 4;
     if (i >= (int64_t)a.T * q) return;
     const int t = (int)(i / q), o = (int)(i - (int64_t)t * q) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (a.residual) {
-        const uint2 rv = *reinterpret_cast<const uint2*>(a.residual + (size_t)t * a.H + o);
-        acc = make_float4(bf_lo(rv.x), bf_hi(rv.x), bf_lo(rv.y), bf_hi(rv.y));
-    }
-    const float* yt = a.Y + (size_t)t * (a.K + 1) * a.H + o;
-    float4 v = *reinterpret_cast<const float4*>(yt + (size_t)a.K * a.H);
+    if (a.residual) acc = load4(a.residual + (size_t)t * a.H + o);
+    const YT* yt = Y + (size_t)t * (a.K + 1) * a.H + o;
+    float4 v = load4(yt + (size_t)a.K * a.H);
     acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     for (int k = 0; k < a.K; ++k) {
-        v = *reinterpret_cast<const float4*>(yt + (size_t)k * a.H);
+        v = load4(yt + (size_t)k * a.H);
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
     uint2 ov;
@@ -210,8 +214,16 @@ cudaError_t launch_experts(const LayerArgs& a, cudaStream_t s) {
     const int cap = 4 * a.num_sms;
     MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (k_gate_up<<<min(up_items, cap), 256, 0, s>>>(a)));
     MOE_LAUNCH(MOE_KERNEL_DOWN, s, (k_down<<<min(dn_items, cap), 256, 0, s>>>(a)));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const LayerArgs& a, cudaStream_t s) {
     const int64_t nq = (int64_t)a.T * (a.H / 4);
-    MOE_LAUNCH(MOE_KERNEL_COMBINE, s, (k_combine<<<(unsigned)((nq + 255) / 256), 256, 0, s>>>(a)));
+    const unsigned grid = (unsigned)((nq + 255) / 256);
+    if (a.gemm)
+        MOE_LAUNCH(MOE_KERNEL_COMBINE, s, (k_combine<bf16><<<grid, 256, 0, s>>>(a, a.Yb)));
+    else
+        MOE_LAUNCH(MOE_KERNEL_COMBINE, s, (k_combine<float><<<grid, 256, 0, s>>>(a, a.Y)));
     return cudaGetLastError();
 }
 

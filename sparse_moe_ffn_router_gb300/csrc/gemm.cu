@@ -1,0 +1,420 @@
+// gemm.cu -- grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA) for
+// the many-token regime of the MoE layer.
+//
+// D[rows of a group, N tile] = A[rows, K] . B[N tile, K]^T, A = token rows (activations),
+// B = weight rows ([Out, In] storage, "Qwen3.6 35B-A3B", Blocks: Linear), both K-major.
+// Three uses, each with its own epilogue on the fp32 accumulator in TMEM:
+//   kLogits  router scores, x . Wr^T (+ br), stored fp32 ("Qwen3.6-35B-A3B -- Architecture
+//            Overview", MoE FFN: 256 Experts, Router);
+//   kSwiGLU  expert gate/up: the B tile holds FH gate rows then the FH matching up rows of
+//            the merged [2I, H] tensor, so one accumulator row holds g and u of the same
+//            features and h = SiLU(g) * u is formed in registers (same page, Experts);
+//   kScaleY  expert down: y = h . Wd^T scaled by the pair's routing weight (or the shared
+//            expert's sigmoid gate) and written to the pair's slot of Y for the fixed-order
+//            combine.
+//
+// One persistent CTA per SM walks the tile list (group-major, then N tile, then M tile, so
+// the M tiles that share a weight tile run back to back and reuse it from L2). Roles:
+//   warp 0    TMA producer (one lane): A and B tiles into a 4-stage shared-memory ring;
+//   warp 1    TMEM owner and MMA issuer (one lane): 128 x BN x 16 tcgen05.mma steps into one
+//             of two TMEM accumulators, tcgen05.commit frees ring stages / publishes tiles;
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator (warp w reads lanes 32*(w%4)..+31).
+#include "launch.h"
+#include "sm100.cuh"
+
+namespace moe {
+
+constexpr int kBM = 128, kBK = 64, kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kAStage = kBM * kBK * 2;
+
+enum { kLogits = 0, kSwiGLU = 1, kScaleY = 2 };
+
+template <int BN>
+struct GemmSmem {
+    static constexpr uint32_t kBStage = BN * kBK * 2;
+    static constexpr uint32_t kTiles = kStages * (kAStage + kBStage);
+    static constexpr uint32_t kBytes = 1024 + kTiles + 256;  // alignment slack + tiles + barriers
+};
+
+__device__ __forceinline__ void flag_timeout(uint32_t* err, volatile int* abort_flag) {
+    atomicOr(err, ERR_TIMEOUT);
+    *abort_flag = 1;
+}
+
+struct TileInfo {
+    int g, m0, n_idx, rows, a_row, src, kb;
+};
+
+// Locate tile t (tiles are visited in increasing order, so the group cursor only advances).
+__device__ __forceinline__ bool find_tile(const GemmPlan& p, int t, int& g, TileInfo& ti) {
+    const int ng = p.dense_rows > 0 ? 1 : *p.n_groups;
+    if (p.dense_rows > 0) {
+        g = 0;
+    } else {
+        while (g < ng && t >= p.tile_start[g + 1]) ++g;
+        if (g >= ng) return false;
+    }
+    const GemmGroup G = p.dense_rows > 0 ? GemmGroup{0, p.dense_rows, 0, 0, 0} : p.groups[g];
+    const int start = p.dense_rows > 0 ? 0 : p.tile_start[g];
+    const int mt = (G.rows + kBM - 1) / kBM;
+    const int local = t - start;
+    ti.g = g;
+    ti.n_idx = local / mt;
+    ti.m0 = (local - ti.n_idx * mt) * kBM;
+    ti.rows = G.rows;
+    ti.a_row = G.a_row0;
+    ti.src = G.src;
+    ti.kb = (G.src ? p.k_shared : p.k_routed) / kBK;
+    return true;
+}
+
+template <int EPI, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+           const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1, const GemmPlan p,
+           const LayerArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kStages * kAStage;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GemmSmem<BN>::kTiles);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kStages;
+    uint64_t* accf = bars + 2 * kStages;
+    uint64_t* acce = accf + 2;
+    uint64_t* mma_done = acce + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = p.dense_rows > 0 ? p.dense_tiles : p.tile_start[*p.n_groups];
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 4);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA0);
+        tma_prefetch_desc(&tmA1);
+        tma_prefetch_desc(&tmB0);
+        tma_prefetch_desc(&tmB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 2 * BN <= 256 ? 256 : 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        int g = 0, it = 0;
+        uint32_t last_par[kStages];
+        bool issued[kStages];
+        for (int s = 0; s < kStages; ++s) issued[s] = false;
+        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+            TileInfo ti;
+            if (!find_tile(p, t, g, ti)) break;
+            const CUtensorMap* mA = ti.src ? &tmA1 : &tmA0;
+            const CUtensorMap* mB = ti.src ? &tmB1 : &tmB0;
+            const GemmGroup G = p.dense_rows > 0 ? GemmGroup{0, p.dense_rows, 0, 0, 0} : p.groups[ti.g];
+            for (int kb = 0; kb < ti.kb; ++kb, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u)) {
+                    flag_timeout(p.err, abort_flag);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], kAStage + GemmSmem<BN>::kBStage);
+                tma_load_2d(sA + s * kAStage, mA, &full[s], kb * kBK, ti.a_row + ti.m0);
+                if (EPI == kSwiGLU) {
+                    const int fh = BN / 2;
+                    const int half = ti.src ? p.up_off_shared : p.up_off_routed;
+                    tma_load_2d(sB + s * GemmSmem<BN>::kBStage, mB, &full[s], kb * kBK, G.b_row0 + ti.n_idx * fh);
+                    tma_load_2d(sB + s * GemmSmem<BN>::kBStage + fh * kBK * 2, mB, &full[s], kb * kBK,
+                                G.b_row0 + half + ti.n_idx * fh);
+                } else {
+                    tma_load_2d(sB + s * GemmSmem<BN>::kBStage, mB, &full[s], kb * kBK, G.b_row0 + ti.n_idx * BN);
+                }
+                issued[s] = true;
+                last_par[s] = ph;
+            }
+        }
+        // every copy this CTA issued must land before shared memory is released
+        for (int s = 0; s < kStages; ++s)
+            if (issued[s] && !mbar_wait(&full[s], last_par[s])) flag_timeout(p.err, abort_flag);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+        int g = 0, it = 0, local = 0;
+        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++local) {
+            TileInfo ti;
+            if (!find_tile(p, t, g, ti)) break;
+            const int b = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1) & 1u;
+            if (!mbar_wait(&acce[b], use ^ 1u)) {
+                flag_timeout(p.err, abort_flag);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(b * BN);
+            bool ok = true;
+            for (int kb = 0; kb < ti.kb; ++kb, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                if (!mbar_wait(&full[s], ph)) {
+                    flag_timeout(p.err, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sA + s * kAStage);
+                const uint32_t b_addr = smem_u32(sB + s * GemmSmem<BN>::kBStage);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    mma_bf16(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                             (kb | kk) != 0);
+                mma_commit(&empty[s]);
+            }
+            if (!ok) break;
+            mma_commit(&accf[b]);
+        }
+        mma_commit(mma_done);
+        if (!mbar_wait(mma_done, 0)) flag_timeout(p.err, abort_flag);
+    } else if (warp >= 2) {
+        // ---------------- epilogue: TMEM lanes 32*(warp%4) .. +31, one accumulator row each
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        int g = 0, local = 0;
+        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x, ++local) {
+            TileInfo ti;
+            if (!find_tile(p, t, g, ti)) break;
+            const int b = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1) & 1u;
+            // lane 0 waits, the warp follows its verdict (tcgen05.ld needs the whole warp)
+            bool ready = lane == 0 ? mbar_wait(&accf[b], use) : true;
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (!ready) {
+                if (lane == 0) flag_timeout(p.err, abort_flag);
+                break;
+            }
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
+            const int m = ti.m0 + r;  // row inside the group
+            const bool live = m < ti.rows;
+            if (EPI == kLogits) {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    const int col0 = ti.n_idx * BN + c * 32;
+                    if (live) {
+                        float* dst = a.logits + (size_t)(ti.a_row + m) * a.ldl + col0;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = col0 + j;
+                            if (col < a.E) {
+                                float s = __uint_as_float(v[j]);
+                                if (a.router_b) s += __bfloat162float(a.router_b[col]);
+                                dst[j] = s;
+                            }
+                        }
+                    }
+                }
+            } else if (EPI == kSwiGLU) {
+                constexpr int FH = BN / 2;
+                const GemmGroup G = p.groups[ti.g];
+#pragma unroll 1
+                for (int c = 0; c < FH / 32; ++c) {
+                    uint32_t gv[32], uv[32];
+                    tmem_ld32(tbase + c * 32, gv);
+                    tmem_ld32(tbase + FH + c * 32, uv);
+                    tmem_ld_wait();
+                    if (live) {
+                        uint4* dst = reinterpret_cast<uint4*>(a.h + (size_t)(G.out_row0 + m) * a.Imax + ti.n_idx * FH + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 o;
+                            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int k = j * 8 + i * 2;
+                                const float h0 = silu(__uint_as_float(gv[k])) * __uint_as_float(uv[k]);
+                                const float h1 = silu(__uint_as_float(gv[k + 1])) * __uint_as_float(uv[k + 1]);
+                                ow[i] = pack_bf16x2(h0, h1);
+                            }
+                            dst[j] = o;
+                        }
+                    }
+                }
+            } else {  // kScaleY
+                int tok = 0, slot = 0;
+                float sc = 0.f;
+                if (live) {
+                    if (ti.src) {
+                        tok = m;
+                        slot = a.K;
+                        sc = a.sgate[tok];
+                    } else {
+                        const int pv = a.perm[ti.a_row + m];
+                        tok = pv / a.K;
+                        slot = pv - tok * a.K;
+                        sc = a.topw[pv];
+                    }
+                }
+                bf16* yrow = a.Yb + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n_idx * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    if (live) {
+                        uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 o;
+                            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int k = j * 8 + i * 2;
+                                ow[i] = pack_bf16x2(sc * __uint_as_float(v[k]), sc * __uint_as_float(v[k + 1]));
+                            }
+                            dst[j] = o;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 2 * BN <= 256 ? 256 : 512);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// host side: tensor maps and launches
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// 2D K-major bf16 tensor [rows, cols] (row pitch `pitch` elements), box {64, box_rows}, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t pitch, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {pitch * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI, int BN>
+cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, const CUtensorMap& B0, const CUtensorMap& B1,
+                        const GemmPlan& p, const LayerArgs& a, int grid, cudaStream_t s) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)GemmSmem<BN>::kBytes);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    k_gemm<EPI, BN><<<grid, kThreads, GemmSmem<BN>::kBytes, s>>>(A0, A1, B0, B1, p, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Router scores of all T tokens on the tensor cores: logits[:, 0:E] = x . Wr^T (+ br).
+cudaError_t launch_router_gemm(const LayerArgs& a, cudaStream_t s) {
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, a.x, a.T, a.H, a.H, kBM) || !make_map(&mw, a.router_w, a.E, a.H, a.H, 256))
+        return cudaErrorInvalidValue;
+    GemmPlan p{};
+    p.dense_rows = a.T;
+    p.dense_tiles = (a.T + kBM - 1) / kBM;
+    p.k_routed = p.k_shared = a.H;
+    p.err = &a.hdr->err;
+    const int grid = min(p.dense_tiles, a.num_sms);
+    cudaError_t e;
+    MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (e = launch_gemm<kLogits, 256>(mx, mx, mw, mw, p, a, grid, s)));
+    return e;
+}
+
+// Expert GEMMs over the dispatched groups (routed experts + the shared expert).
+cudaError_t launch_expert_gemms(const LayerArgs& a, cudaStream_t s) {
+    const int fh = (a.I % 128 == 0 && a.Is % 128 == 0) ? 128 : 64;
+    CUtensorMap mxp, mx, mgu, msgu, mh, mdn, msd;
+    bool ok = make_map(&mxp, a.xperm, a.P, a.H, a.H, kBM) && make_map(&mx, a.x, a.T, a.H, a.H, kBM) &&
+              make_map(&mgu, a.gate_up, (uint64_t)a.E * 2 * a.I, a.H, a.H, fh) &&
+              make_map(&msgu, a.sgu, (uint64_t)2 * a.Is, a.H, a.H, fh) &&
+              make_map(&mh, a.h, a.P + a.T, a.Imax, a.Imax, kBM);
+    const int bn_dn = (a.H % 256 == 0) ? 256 : 128;
+    ok = ok && make_map(&mdn, a.down, (uint64_t)a.E * a.H, a.I, a.I, bn_dn) &&
+         make_map(&msd, a.sd, a.H, a.Is, a.Is, bn_dn);
+    if (!ok) return cudaErrorInvalidValue;
+    const int grid = a.num_sms;
+    GemmPlan pu{};
+    pu.groups = a.up_groups;
+    pu.tile_start = a.up_tiles;
+    pu.n_groups = a.n_groups;
+    pu.k_routed = pu.k_shared = a.H;
+    pu.up_off_routed = a.I;
+    pu.up_off_shared = a.Is;
+    pu.err = &a.hdr->err;
+    cudaError_t e;
+    if (fh == 128)
+        MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (e = launch_gemm<kSwiGLU, 256>(mxp, mx, mgu, msgu, pu, a, grid, s)));
+    else
+        MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (e = launch_gemm<kSwiGLU, 128>(mxp, mx, mgu, msgu, pu, a, grid, s)));
+    if (e != cudaSuccess) return e;
+    GemmPlan pd{};
+    pd.groups = a.dn_groups;
+    pd.tile_start = a.dn_tiles;
+    pd.n_groups = a.n_groups;
+    pd.k_routed = a.I;
+    pd.k_shared = a.Is;
+    pd.err = &a.hdr->err;
+    if (bn_dn == 256)
+        MOE_LAUNCH(MOE_KERNEL_DOWN, s, (e = launch_gemm<kScaleY, 256>(mh, mh, mdn, msd, pd, a, grid, s)));
+    else
+        MOE_LAUNCH(MOE_KERNEL_DOWN, s, (e = launch_gemm<kScaleY, 128>(mh, mh, mdn, msd, pd, a, grid, s)));
+    return e;
+}
+
+}  // namespace moe

@@ -31,8 +31,17 @@ struct LayerArgs {
     int32_t* base;    // [nb, E] first perm position of each (block, expert)
     int32_t* act;     // experts with pairs, ascending; count in hdr->n_act
     bf16* h;          // [P + T, Imax] gated activations
-    float* Y;         // [T, K+1, H] weighted expert outputs, slot K = shared expert
+    float* Y;         // [T, K+1, H] weighted expert outputs, slot K = shared expert (fp32 path)
+    bf16* Yb;         // the same in bf16 (tensor-core path)
+    bf16* xperm;      // [P, H] x rows in dispatch order (tensor-core path)
+    GemmGroup* up_groups;
+    GemmGroup* dn_groups;
+    int32_t* up_tiles;  // [n_groups + 1] first tile of each gate_up group
+    int32_t* dn_tiles;
+    int32_t* n_groups;
+    uint32_t* comb_ticket;  // [H/64] down items finished per output block (re-armed to 0)
     WsHeader* hdr;
+    bool gemm;
     int T, H, E, K, I, Is, Imax, ldl, nb;
     int64_t P;
     int num_sms;
@@ -50,7 +59,26 @@ void trace_end(int kernel, cudaStream_t s);
         trace_end(kernel_id, stream);              \
     } while (0)
 
+// Grouped-GEMM description consumed by the tensor-core kernel. With dense_rows > 0 there is a
+// single group of dense_rows rows (the router) and the tables are not read.
+struct GemmPlan {
+    const GemmGroup* groups;
+    const int32_t* tile_start;
+    const int32_t* n_groups;
+    int dense_rows, dense_tiles;
+    int k_routed, k_shared;       // reduction length of routed / shared groups
+    int up_off_routed, up_off_shared;  // row offset of the up half in a merged gate_up block
+    uint32_t* err;
+};
+
 cudaError_t launch_router(const LayerArgs& a, cudaStream_t s);
+cudaError_t launch_route_fused(const LayerArgs& a, cudaStream_t s);
+cudaError_t launch_router_gemm(const LayerArgs& a, cudaStream_t s);
+cudaError_t launch_expert_gemms(const LayerArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_prep(const LayerArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const LayerArgs& a, cudaStream_t s);
+bool stream_supported(const LayerArgs& a);
+cudaError_t launch_stream_experts(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_experts(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_rmsnorm(const bf16* x, const bf16* gamma, float eps, bf16* xn, int T, int H, cudaStream_t s);

@@ -123,9 +123,31 @@ __global__ void __launch_bounds__(256) k_router_topk(LayerArgs a) {
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&a.hdr->err, ERR_NONFINITE_SCORE);
 }
 
+// Shared-expert gate score of every token, logits[t, E] = x[t] . ws (one warp per token);
+// the many-token path scores the E router columns on the tensor cores.
+__global__ void __launch_bounds__(256) k_shared_gate_scores(LayerArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= a.T) return;
+    float acc = 0.f;
+    for (int c = lane; c < a.H / 8; c += 32) {
+        float xf[8];
+        unpack8(ld_ro(a.x + (size_t)t * a.H + (size_t)c * 8), xf);
+        acc = dot8(ld_ro(a.sg + (size_t)c * 8), xf, acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) a.logits[(size_t)t * a.ldl + a.E] = acc;
+}
+
 cudaError_t launch_router(const LayerArgs& a, cudaStream_t s) {
-    dim3 g1((a.E + 1 + 7) / 8, (a.T + kRouterTokens - 1) / kRouterTokens);
-    MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (k_router_scores<<<g1, 256, 0, s>>>(a)));
+    if (a.gemm) {
+        cudaError_t e = launch_router_gemm(a, s);
+        if (e != cudaSuccess) return e;
+        MOE_LAUNCH(MOE_KERNEL_SHARED_GATE, s, (k_shared_gate_scores<<<(a.T + 7) / 8, 256, 0, s>>>(a)));
+    } else {
+        dim3 g1((a.E + 1 + 7) / 8, (a.T + kRouterTokens - 1) / kRouterTokens);
+        MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (k_router_scores<<<g1, 256, 0, s>>>(a)));
+    }
     MOE_LAUNCH(MOE_KERNEL_ROUTER_TOPK, s, (k_router_topk<<<(a.T + 7) / 8, 256, 0, s>>>(a)));
     return cudaGetLastError();
 }
@@ -169,6 +191,178 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const bf16* x, const bf16* gamm
 
 cudaError_t launch_rmsnorm(const bf16* x, const bf16* gamma, float eps, bf16* xn, int T, int H, cudaStream_t s) {
     MOE_LAUNCH(MOE_KERNEL_RMSNORM, s, (k_rmsnorm<<<T, 256, 0, s>>>(x, gamma, eps, xn, H)));
+    return cudaGetLastError();
+}
+
+}  // namespace moe
+
+namespace moe {
+
+// ---------------------------------------------------------------------------------------
+// Few-token routing in one launch (T <= kFusedRouteTokens): every CTA scores 8 rows of
+// [Wr; ws] for all tokens; the CTA that finishes last (atomic ticket after a fence, so it sees
+// every score) runs top-K for all tokens and the dispatch of the T*K pairs, then re-arms the
+// ticket. No CTA ever waits on another.
+
+__device__ void topk_one_token(const LayerArgs& a, const float* l, int t, int lane) {
+    float v[8];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = -INFINITY;
+        if (e < a.E) {
+            v[j] = __ldcg(l + e);
+            if (!isfinite(v[j])) {
+                bad = true;
+                v[j] = -INFINITY;
+            }
+        }
+    }
+    uint32_t taken = 0;
+    float sel_v[8];
+    int sel_e[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (k < a.K) {
+            float bv = -INFINITY;
+            int be = 0x7fffffff;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = lane + 32 * j;
+                if (e < a.E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
+                    bv = v[j];
+                    be = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (ov > bv || (ov == bv && oe < be)) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+            sel_v[k] = bv;
+            sel_e[k] = be;
+        }
+    }
+    if (lane == 0) {
+        float ex[8], s = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k < a.K) {
+                ex[k] = expf(sel_v[k] - sel_v[0]);
+                s += ex[k];
+            }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k < a.K) {
+                a.ids[(size_t)t * a.K + k] = sel_e[k];
+                a.topw[(size_t)t * a.K + k] = ex[k] / s;
+            }
+        const float z = __ldcg(l + a.E);
+        if (!isfinite(z)) bad = true;
+        a.sgate[t] = 1.0f / (1.0f + expf(-z));
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&a.hdr->err, ERR_NONFINITE_SCORE);
+}
+
+__global__ void __launch_bounds__(256) k_route_fused(LayerArgs a) {
+    __shared__ int cnt[256];
+    __shared__ int off[257];
+    __shared__ unsigned ticket;
+    // let the expert kernel start its shared-expert work now; its routed work waits for this
+    // grid's completion (griddepcontrol.wait)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // 1. scores of row r for all tokens
+    const int r = blockIdx.x * 8 + warp;
+    if (r <= a.E) {
+        const bf16* wrow = r < a.E ? a.router_w + (size_t)r * a.H : a.sg;
+        const float bias = (r < a.E && a.router_b) ? __bfloat162float(a.router_b[r]) : 0.f;
+        for (int t0 = 0; t0 < a.T; t0 += kRouterTokens) {
+            const int mt = min(kRouterTokens, a.T - t0);
+            float acc[kRouterTokens];
+#pragma unroll
+            for (int i = 0; i < kRouterTokens; ++i) acc[i] = 0.f;
+            for (int c = lane; c < a.H / 8; c += 32) {
+                const uint4 wv = ld_ro(wrow + (size_t)c * 8);
+#pragma unroll
+                for (int tt = 0; tt < kRouterTokens; ++tt) {
+                    if (tt < mt) {
+                        float xf[8];
+                        unpack8(ld_ro(a.x + (size_t)(t0 + tt) * a.H + (size_t)c * 8), xf);
+                        acc[tt] = dot8(wv, xf, acc[tt]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int tt = 0; tt < kRouterTokens; ++tt) {
+                if (tt < mt) {
+                    const float s = warp_sum(acc[tt]);
+                    if (lane == 0) a.logits[(size_t)(t0 + tt) * a.ldl + r] = s + bias;
+                }
+            }
+        }
+    }
+    // 2. the last CTA to finish routes every token
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) ticket = atomicAdd(&a.hdr->route_ticket, 1u);
+    __syncthreads();
+    if (ticket != gridDim.x - 1) return;
+    __threadfence();
+    for (int t = warp; t < a.T; t += 8) topk_one_token(a, a.logits + (size_t)t * a.ldl, t, lane);
+    __syncthreads();
+    // 3. dispatch: counts, offsets, stable permutation (token order within an expert)
+    for (int e = threadIdx.x; e < a.E; e += 256) cnt[e] = 0;
+    __syncthreads();
+    const int P = (int)a.P;
+    if (warp == 0) {
+        for (int base = 0; base < P; base += 32) {
+            const int i = base + lane;
+            const bool valid = i < P;
+            const int e = valid ? a.ids[i] : -1;
+            const unsigned m = __match_any_sync(0xffffffffu, e);
+            const int rank_in = __popc(m & ((1u << lane) - 1u));
+            const int c = valid ? cnt[e] : 0;
+            __syncwarp();
+            if (valid) {
+                a.lr[i] = c + rank_in;
+                if (rank_in == 0) cnt[e] = c + __popc(m);
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0, na = 0;
+        for (int e = 0; e < a.E; ++e) {
+            off[e] = run;
+            run += cnt[e];
+            if (cnt[e] > 0) a.act[na++] = e;
+        }
+        off[a.E] = run;
+        a.hdr->n_act = na;
+        a.hdr->route_ticket = 0;  // re-arm for the next call on this workspace
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e <= a.E; e += 256) {
+        a.offsets[e] = off[e];
+        if (e < a.E) a.counts[e] = cnt[e];
+    }
+    for (int i = threadIdx.x; i < P; i += 256) {
+        const int j = off[a.ids[i]] + a.lr[i];
+        a.perm[j] = i;
+        a.inv[i] = j;
+    }
+}
+
+cudaError_t launch_route_fused(const LayerArgs& a, cudaStream_t s) {
+    MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (k_route_fused<<<(a.E + 1 + 7) / 8, 256, 0, s>>>(a)));
     return cudaGetLastError();
 }
 

@@ -40,7 +40,9 @@ def _check_taps(L: Layer, ws, ref: dict, rows=None):
     Imax = max(I, Is)
     r = oracle.route(L.dims, L.x, L.router_w, L.router_b)
     h = read_tap(ws, L.dims, 0, torch.bfloat16, (T * K + T, Imax)).float().cpu().numpy()
-    Y = read_tap(ws, L.dims, 1, torch.float32, (T, K + 1, H)).cpu().numpy()
+    _, ybytes = moe.moe_workspace_tap(L.dims, 1)
+    ydt = torch.float32 if ybytes == T * (K + 1) * H * 4 else torch.bfloat16
+    Y = read_tap(ws, L.dims, 1, ydt, (T, K + 1, H)).float().cpu().numpy()
     sg = read_tap(ws, L.dims, 2, torch.float32, (T,)).cpu().numpy()
     np.testing.assert_allclose(sg, ref["sg"], rtol=0, atol=2e-6)
     h_pairs = h[r["inv"]][:, :I].reshape(T, K, I)
@@ -87,6 +89,10 @@ EDGE = [
     (129, 384, 40, 3, 192, 64),   # odd E and K, ragged T, I > Is
     (200, 128, 256, 8, 64, 64),   # most experts receive no rows
     (9, 2048, 256, 8, 512, 512),  # full shape, ragged token tile
+    # from T = 256 on, the tensor-core path
+    (256, 256, 16, 4, 64, 128),     # smallest tensor-core case: one 64-feature SwiGLU tile, E < 256
+    (300, 384, 40, 3, 192, 64),     # 128-wide tiles, ragged M tiles, I > Is
+    (1000, 2048, 256, 8, 512, 512), # full shape, many partly filled M tiles
 ]
 
 
