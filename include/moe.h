@@ -149,6 +149,22 @@ moe_status moe_set_trace(int kernel, void* const* start_events, void* const* sto
 /* Number of kernels this library has launched in this process so far. */
 uint64_t moe_launch_count(void);
 
+/* Routing without any device allocation by the caller (the paper has no counterpart: this is
+ * for callers of this library that cannot call cudaMalloc, such as a plugin whose host
+ * framework owns every device allocation, an engine that reserved all of HBM up front, or a
+ * latency-critical path that cannot take an allocation's synchronisation or its failure).
+ * Same inputs, outputs and results as moe_route, but no workspace: its scratch is a fixed
+ * 80 KiB array inside the library, held by every GPU that loads the library until the
+ * process exits. Limits: T <= 64 and the scratch layout must fit (any E <= 256, K <= 8 fit);
+ * larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before anything is launched.
+ * The first call on a device looks up the array's device address on the current device
+ * (cudaGetSymbolAddress); make that first call before any stream capture. Every call shares
+ * the one array: calls that may overlap on the GPU (different streams, or devices sharing it)
+ * race and must be ordered by the caller. Each call clears the part that must start at zero.
+ * A non-finite router score is not reported (there is no workspace error word). */
+moe_status moe_route_noalloc(const moe_dims* d, const void* x, const moe_weights* w, int32_t* ids, float* topk_w,
+                             int32_t* counts, int32_t* offsets, int32_t* perm, void* stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char* moe_status_string(moe_status s);
 

@@ -18,7 +18,7 @@ from . import build as _build
 MOE_STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_MISALIGNED",
               4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE"}
 EXPORTED = ["moe_workspace_size", "moe_workspace_init", "moe_route", "moe_forward", "moe_rmsnorm",
-            "moe_last_device_error", "moe_workspace_tap", "moe_set_trace", "moe_launch_count", "moe_status_string"]
+            "moe_last_device_error", "moe_workspace_tap", "moe_set_trace", "moe_launch_count", "moe_route_noalloc", "moe_status_string"]
 KERNELS = {"router_scores": 0, "router_topk": 1, "dispatch_local": 2, "dispatch_scan": 3, "dispatch_scatter": 4,
            "gate_up": 5, "down": 6, "combine": 7, "rmsnorm": 8, "shared_gate": 9, "gather": 10, "gemm_plan": 11}
 
@@ -97,6 +97,8 @@ def load_library(build_if_missing: bool = True):
             lib.moe_set_trace.argtypes = [ctypes.c_int, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.c_int]
             lib.moe_launch_count.restype = ctypes.c_uint64
             lib.moe_launch_count.argtypes = []
+            lib.moe_route_noalloc.restype = st
+            lib.moe_route_noalloc.argtypes = [D, P, W, P, P, P, P, P, P]
             lib.moe_status_string.restype = ctypes.c_char_p
             lib.moe_status_string.argtypes = [ctypes.c_int]
             _lib = lib
@@ -159,6 +161,14 @@ def moe_route(dims, x, weights: Weights, ids, topk_w, counts, offsets, perm, wor
     _check(load_library().moe_route(ctypes.byref(_dims(dims)), _ptr(x), ctypes.byref(w), _ptr(ids), _ptr(topk_w),
                                     _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)), "moe_route")
+
+
+def moe_route_noalloc(dims, x, weights: Weights, ids, topk_w, counts, offsets, perm, stream=None):
+    """moe_route without a workspace (for callers that cannot allocate device memory)."""
+    w = weights.to_c()
+    _check(load_library().moe_route_noalloc(ctypes.byref(_dims(dims)), _ptr(x), ctypes.byref(w), _ptr(ids),
+                                            _ptr(topk_w), _ptr(counts), _ptr(offsets), _ptr(perm), _stream(stream)),
+           "moe_route_noalloc")
 
 
 def moe_forward(dims, x, weights: Weights, residual, out, workspace, stream=None):
