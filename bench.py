@@ -63,6 +63,7 @@ def parse_args():
     p.add_argument("--also", default="decode_T64,prefill_T4096_zipf,stack40_decode_T32",
                    help="comma-separated extra workloads reported under 'also' ('none' to skip)")
     p.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--no-graph", action="store_true", help="time plain calls instead of CUDA-graph replays")
     p.add_argument("--rotate", type=int, default=ROTATE,
                    help="distinct layers cycled through by small-T workloads (keeps weights out of L2)")
     a = p.parse_args()
@@ -253,6 +254,10 @@ def algorithmic(dims, groups: list[int]) -> dict:
 def trace_kernels(moe, names, n):
     ev = {k: ([torch.cuda.Event(enable_timing=True) for _ in range(n)],
               [torch.cuda.Event(enable_timing=True) for _ in range(n)]) for k in names}
+    for a, b in ev.values():  # torch creates the CUDA event on its first record
+        for e in a + b:
+            e.record()
+    torch.cuda.synchronize()
     for k, (a, b) in ev.items():
         moe.moe_set_trace(k, a, b)
     return ev
@@ -267,9 +272,12 @@ def kernel_ms(ev, n) -> dict:
     return {k: sum(a[i].elapsed_time(b[i]) for i in range(n)) / n for k, (a, b) in ev.items()}
 
 
-def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_index=None, auto=(2.0, 200, 100000)):
+def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_index=None, auto=(2.0, 200, 100000),
+                   graph: bool = False):
     """Warm-up (all kernels traced, to find the dominant one), then the timed region (only
-    the dominant kernel traced). Returns a result dict."""
+    the dominant kernel traced). With graph=True the timed steps are replays of a CUDA graph
+    that holds G steps (and the dominant kernel's trace events); launch overhead on the host
+    is then out of the measurement. Returns a result dict."""
     moe = ls.moe
     ev = trace_kernels(moe, KERNEL_NAMES, warmup)
     for i in range(warmup):
@@ -278,7 +286,7 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
     warm = kernel_ms(ev, warmup)
     clear_traces(moe)
     dominant = max(warm, key=warm.get)
-    if steps <= 0:  # auto: about 2 s of timed work
+    if steps <= 0:  # auto: about `auto[0]` s of timed work
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(3):
@@ -286,7 +294,27 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
         torch.cuda.synchronize()
         per = (time.perf_counter() - t0) / 3
         steps = int(min(auto[2], max(auto[1], auto[0] / max(per, 1e-6))))
-    ev = trace_kernels(moe, [dominant], steps)
+    nl = len(ls.layers)
+    if graph:
+        G = max(nl, min(512, steps) // nl * nl)
+        reps = max(1, -(-steps // G))
+        steps = G * reps
+        ev = trace_kernels(moe, [dominant], G)
+        g = torch.cuda.CUDAGraph()
+        n0 = moe.moe_launch_count()
+        with torch.cuda.graph(g):
+            for i in range(G):
+                ls.step(i)
+        per_graph = moe.moe_launch_count() - n0
+        clear_traces(moe)
+        g.replay()
+        torch.cuda.synchronize()
+        run = lambda: [g.replay() for _ in range(reps)]  # noqa: E731
+        n_ev = G
+    else:
+        ev = trace_kernels(moe, [dominant], steps)
+        run = lambda: [ls.step(warmup + i) for i in range(steps)]  # noqa: E731
+        n_ev = steps
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(clocks_index) if clocks_index is not None else None
     if sampler:
@@ -297,29 +325,28 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
     if sampler:
         sampler.mark(True)
     start.record()
-    for i in range(steps):
-        ls.step(warmup + i)
+    run()
     stop.record()
     torch.cuda.synchronize()
-    launches = moe.moe_launch_count() - n0
+    launches = per_graph * reps if graph else moe.moe_launch_count() - n0
     if sampler:
         sampler.mark(False)
     barrier()
     if sampler:
         sampler.__exit__(None, None, None)
     ms = max_over_ranks(start.elapsed_time(stop))
-    dom_ms = kernel_ms(ev, steps)[dominant]
+    dom_ms = kernel_ms(ev, n_ev)[dominant]
     clear_traces(moe)
     groups = ls.routed_groups()
-    nl = len(ls.layers)
-    per_step = [algorithmic(ls.dims, groups[(warmup + i) % nl]) for i in range(steps)]
-    alg_bytes = sum(p[dominant] if dominant in p else 0 for p in per_step) / steps
-    layer_bytes = sum(p["layer"] for p in per_step) / steps
+    first = 0 if graph else warmup
+    per_step = [algorithmic(ls.dims, groups[(first + i) % nl]) for i in range(n_ev)]
+    alg_bytes = sum(p[dominant] if dominant in p else 0 for p in per_step) / n_ev
+    layer_bytes = sum(p["layer"] for p in per_step) / n_ev
     flops = per_step[0]["flops"]
     T = ls.dims[0]
     res = dict(steps=steps, ms_per_step=ms / steps, tokens_per_s=T * steps / (ms / 1e3), launches=launches,
-               dominant=dominant, dominant_ms=dom_ms, warm_kernel_ms=warm,
-               unique_experts=sum(len(groups[(warmup + i) % nl]) for i in range(steps)) / steps,
+               dominant=dominant, dominant_ms=dom_ms, warm_kernel_ms=warm, graph=graph,
+               unique_experts=sum(len(groups[(first + i) % nl]) for i in range(n_ev)) / n_ev,
                layer_bytes=layer_bytes, layer_flops=flops)
     if alg_bytes:
         ach = alg_bytes / (dom_ms * 1e-3) / 1e9
@@ -469,8 +496,9 @@ def main():
         raise SystemExit("use the stack workload under --also")
     n_rot = max(1, args.rotate) if wl.T <= 32 else 1
     ls = LayerSet(wl, n_rot, device)
-    main_res = time_layer_set(ls, args.steps, args.warmup, peaks, clocks_index=torch.cuda.current_device())
-    e2e = time_e2e(ls, main_res["steps"], args.warmup)
+    main_res = time_layer_set(ls, args.steps, args.warmup, peaks, clocks_index=torch.cuda.current_device(),
+                              graph=not args.no_graph)
+    e2e = time_e2e(ls, min(main_res["steps"], 20000), args.warmup)
     value = main_res["tokens_per_s"] * world
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": main_res["steps"],
@@ -482,7 +510,8 @@ def main():
                    "l2": ("inputs larger than L2: steps cycle through %d distinct layers (%.1f GB)"
                           % (n_rot, n_rot * wl.weight_bytes_per_layer() / 1e9)) if n_rot > 1 else
                    "inputs larger than L2 (%.2f GB of weights touched per step)" % (main_res["layer_bytes"] / 1e9),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "cuda_graph": main_res["graph"]},
         "roofline": main_res.get("roofline"),
         "e2e": {"value": round(e2e["value"] * world, 3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["ms_per_step"], 6)},
@@ -508,7 +537,7 @@ def main():
         else:
             ls2 = LayerSet(w2, ROTATE if w2.T <= 32 else 1, device)
             r = time_layer_set(ls2, 0 if args.steps <= 0 else max(5, min(args.steps, 50)), 3, peaks,
-                               auto=(1.0, 5, 500))
+                               auto=(1.0, 5, 500), graph=not args.no_graph and w2.T <= 64)
             also[name] = {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 5),
                           "roofline": r.get("roofline"), "hbm_frac_of_layer_bytes": r["layer_hbm_frac"],
                           "tensor_frac": r["layer_tensor_frac"], "unique_experts_per_step": r["unique_experts"],

@@ -19,16 +19,27 @@ struct TraceSlot {
 };
 static TraceSlot g_trace[MOE_KERNEL_COUNT];
 
+// Inside a stream capture an event record must be "external" to become an event node of the
+// graph (a plain record only orders the capture); outside a capture only a plain record is valid.
+static void trace_record(void* ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags((cudaEvent_t)ev, s, cudaEventRecordExternal);
+    else
+        cudaEventRecord((cudaEvent_t)ev, s);
+}
+
 void trace_begin(int kernel, cudaStream_t s) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     TraceSlot& t = g_trace[kernel];
-    if (t.n) cudaEventRecord((cudaEvent_t)t.start[t.i % t.n], s);
+    if (t.n) trace_record(t.start[t.i % t.n], s);
 }
 
 void trace_end(int kernel, cudaStream_t s) {
     TraceSlot& t = g_trace[kernel];
     if (t.n) {
-        cudaEventRecord((cudaEvent_t)t.stop[t.i % t.n], s);
+        trace_record(t.stop[t.i % t.n], s);
         ++t.i;
     }
 }

@@ -11,6 +11,13 @@ from sparse_moe_ffn_router_gb300 import synth
 from tests.inputs import gap_controlled_x
 
 TOL_REL, TOL_ABS = 1e-2, 1e-3
+# Renormalised routing weights (fp32 on the GPU, fp64 in the oracle). The GPU scores are fp32
+# sums of H = 2048 bf16 products whose order differs between the CUDA-core and tensor-core
+# paths; with sum|x_h w_h| ~ 26 on these inputs the score error is ~1e-4 (random-walk
+# estimate sqrt(H) * 2^-24 * 26 * a few), and w_k = exp(l_k - l_0) / sum moves by at most
+# about 2 * w_k * max|dl|. 5e-4 covers that and still fails a wrong renormalisation (errors of
+# order 1e-1).
+W_TOL = 5e-4
 
 
 def tolerance(ref: np.ndarray) -> float:
@@ -87,4 +94,4 @@ def check_routing(gpu: dict, ref: dict, what=""):
     assert np.array_equal(gpu["counts"], ref["counts"]), f"{what}: counts differ"
     assert np.array_equal(gpu["offsets"], ref["offsets"]), f"{what}: offsets differ"
     assert np.array_equal(gpu["perm"], ref["perm"]), f"{what}: dispatch permutation differs"
-    np.testing.assert_allclose(gpu["w"], ref["w"], rtol=0, atol=2e-6, err_msg=f"{what}: routing weights")
+    np.testing.assert_allclose(gpu["w"], ref["w"], rtol=0, atol=W_TOL, err_msg=f"{what}: routing weights")
