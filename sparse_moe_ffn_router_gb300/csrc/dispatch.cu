@@ -84,36 +84,55 @@ __global__ void __launch_bounds__(256) k_dispatch_scatter(LayerArgs a) {
 // Tables of the grouped tensor-core GEMMs: one group per expert that received pairs (in
 // expert order), then the shared expert over all T tokens; each group's first tile.
 __global__ void k_gemm_plan(LayerArgs a, int fh, int bn_dn) {
-    if (threadIdx.x != 0) return;
+    // one warp: each group's tile counts, then a warp-wide running prefix over the groups
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x >= 32) return;
     const int n = a.hdr->n_act;
     int tu = 0, td = 0;
-    for (int g = 0; g <= n; ++g) {
-        GemmGroup up, dn;
-        int rows, nt_up;
+    for (int base = 0; base <= n; base += 32) {
+        const int g = base + lane;
+        int cu = 0, cd = 0;
+        GemmGroup up{}, dn{};
         if (g < n) {
             const int e = a.act[g];
             const int r0 = a.offsets[e];
-            rows = a.offsets[e + 1] - r0;
+            const int rows = a.offsets[e + 1] - r0;
             up = GemmGroup{r0, rows, e * 2 * a.I, r0, 0};
             dn = GemmGroup{r0, rows, e * a.H, 0, 0};
-            nt_up = a.I / fh;
-        } else {
-            rows = a.T;
+            const int mt = (rows + 127) / 128;
+            cu = mt * (a.I / fh);
+            cd = mt * (a.H / bn_dn);
+        } else if (g == n) {
             up = GemmGroup{0, a.T, 0, (int)a.P, 1};
             dn = GemmGroup{(int)a.P, a.T, 0, 0, 1};
-            nt_up = a.Is / fh;
+            const int mt = (a.T + 127) / 128;
+            cu = mt * (a.Is / fh);
+            cd = mt * (a.H / bn_dn);
         }
-        const int mt = (rows + 127) / 128;
-        a.up_groups[g] = up;
-        a.up_tiles[g] = tu;
-        tu += mt * nt_up;
-        a.dn_groups[g] = dn;
-        a.dn_tiles[g] = td;
-        td += mt * (a.H / bn_dn);
+        int iu = cu, id = cd;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int yu = __shfl_up_sync(0xffffffffu, iu, o);
+            const int yd = __shfl_up_sync(0xffffffffu, id, o);
+            if (lane >= o) {
+                iu += yu;
+                id += yd;
+            }
+        }
+        if (g <= n) {
+            a.up_groups[g] = up;
+            a.dn_groups[g] = dn;
+            a.up_tiles[g] = tu + iu - cu;
+            a.dn_tiles[g] = td + id - cd;
+        }
+        tu += __shfl_sync(0xffffffffu, iu, 31);
+        td += __shfl_sync(0xffffffffu, id, 31);
     }
-    a.up_tiles[n + 1] = tu;
-    a.dn_tiles[n + 1] = td;
-    *a.n_groups = n + 1;
+    if (lane == 0) {
+        a.up_tiles[n + 1] = tu;
+        a.dn_tiles[n + 1] = td;
+        *a.n_groups = n + 1;
+    }
 }
 
 // xperm[j] = x[perm[j] / K]: the token rows in dispatch order, the A operand of gate_up.

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) k_router_scores(LayerArgs a) {
     float acc[kRouterTokens];
 #pragma unroll
     for (int i = 0; i < kRouterTokens; ++i) acc[i] = 0.f;
+#pragma unroll 8
     for (int c = lane; c < a.H / 8; c += 32) {
         const uint4 wv = ld_ro(wrow + (size_t)c * 8);
 #pragma unroll
@@ -273,6 +274,8 @@ __device__ void topk_one_token(const LayerArgs& a, const float* l, int t, int la
 __global__ void __launch_bounds__(256) k_route_fused(LayerArgs a) {
     __shared__ int cnt[256];
     __shared__ int off[257];
+    __shared__ int sids[kFusedRouteTokens * 8];
+    __shared__ int slr[kFusedRouteTokens * 8];
     __shared__ unsigned ticket;
     // let the expert kernel start its shared-expert work now; its routed work waits for this
     // grid's completion (griddepcontrol.wait)
@@ -288,6 +291,7 @@ __global__ void __launch_bounds__(256) k_route_fused(LayerArgs a) {
             float acc[kRouterTokens];
 #pragma unroll
             for (int i = 0; i < kRouterTokens; ++i) acc[i] = 0.f;
+#pragma unroll 8
             for (int c = lane; c < a.H / 8; c += 32) {
                 const uint4 wv = ld_ro(wrow + (size_t)c * 8);
 #pragma unroll
@@ -316,38 +320,61 @@ __global__ void __launch_bounds__(256) k_route_fused(LayerArgs a) {
     if (ticket != gridDim.x - 1) return;
     __threadfence();
     for (int t = warp; t < a.T; t += 8) topk_one_token(a, a.logits + (size_t)t * a.ldl, t, lane);
-    __syncthreads();
-    // 3. dispatch: counts, offsets, stable permutation (token order within an expert)
     for (int e = threadIdx.x; e < a.E; e += 256) cnt[e] = 0;
     __syncthreads();
     const int P = (int)a.P;
+    for (int i = threadIdx.x; i < P; i += 256) sids[i] = a.ids[i];  // written above by this CTA
+    __syncthreads();
+    // 3. dispatch: per-expert ranks in token order (one warp, no atomics)
     if (warp == 0) {
         for (int base = 0; base < P; base += 32) {
             const int i = base + lane;
             const bool valid = i < P;
-            const int e = valid ? a.ids[i] : -1;
+            const int e = valid ? sids[i] : -1;
             const unsigned m = __match_any_sync(0xffffffffu, e);
             const int rank_in = __popc(m & ((1u << lane) - 1u));
             const int c = valid ? cnt[e] : 0;
             __syncwarp();
             if (valid) {
-                a.lr[i] = c + rank_in;
+                slr[i] = c + rank_in;
                 if (rank_in == 0) cnt[e] = c + __popc(m);
             }
             __syncwarp();
         }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0, na = 0;
-        for (int e = 0; e < a.E; ++e) {
-            off[e] = run;
-            run += cnt[e];
-            if (cnt[e] > 0) a.act[na++] = e;
+        // exclusive scan of the counts and the list of experts with pairs: lane owns 8 experts
+        int loc[8], run = 0, nz = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            loc[j] = e < a.E ? cnt[e] : 0;
+            run += loc[j];
+            nz += loc[j] > 0;
         }
-        off[a.E] = run;
-        a.hdr->n_act = na;
-        a.hdr->route_ticket = 0;  // re-arm for the next call on this workspace
+        int incl = run, inz = nz;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            const int z = __shfl_up_sync(0xffffffffu, inz, o);
+            if (lane >= o) {
+                incl += y;
+                inz += z;
+            }
+        }
+        int pos = incl - run, apos = inz - nz;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            if (e < a.E) {
+                off[e] = pos;
+                if (loc[j] > 0) a.act[apos++] = e;
+            }
+            pos += loc[j];
+        }
+        if (lane == 31) {
+            off[a.E] = incl;
+            a.hdr->n_act = inz;
+            a.hdr->route_ticket = 0;  // re-arm for the next call on this workspace
+        }
     }
     __syncthreads();
     for (int e = threadIdx.x; e <= a.E; e += 256) {
@@ -355,7 +382,7 @@ __global__ void __launch_bounds__(256) k_route_fused(LayerArgs a) {
         if (e < a.E) a.counts[e] = cnt[e];
     }
     for (int i = threadIdx.x; i < P; i += 256) {
-        const int j = off[a.ids[i]] + a.lr[i];
+        const int j = off[sids[i]] + slr[i];
         a.perm[j] = i;
         a.inv[i] = j;
     }

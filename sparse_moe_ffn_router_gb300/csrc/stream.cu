@@ -3,31 +3,89 @@
 // With few tokens every expert the router picked has only a handful of rows, so the layer is
 // bound by reading the touched experts' weights from HBM once (4 MiB gate_up + 2 MiB down per
 // expert at the full shape, "Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256 Experts).
-// Both kernels are persistent (one CTA per SM) and stream weight rows through a 4-stage
-// shared-memory ring filled by 1-D TMA bulk copies (cp.async.bulk) from a dedicated producer
-// warp, with mbarrier full/empty handshakes, so each SM keeps up to 128 KB of loads in flight.
-// Eight consumer warps take dot products of the staged rows with the group's token rows
-// (warp w owns rows w, w+8, ...; lanes split the row into 16-byte chunks; fp32 FMA in a fixed
-// order, then a butterfly sum).
 //
-// k_stream_up:   h = bf16(SiLU(x . Wg^T) * (x . Wu^T)), item = FPI gate rows + the FPI matching
-//                up rows of one group; shared-expert items come first: they do not depend on
+// Both kernels are persistent (one CTA per SM). A producer warp walks the CTA's work items and,
+// for each, fills one stage of a 2-stage shared-memory ring with 1-D TMA bulk copies
+// (cp.async.bulk, one per row so rows land 16 bytes apart modulo 128 and ldmatrix is free of
+// bank conflicts): the item's weight rows plus its activation rows (up to 8 tokens), and writes
+// the item's metadata into the stage before arming its mbarrier. Eight consumer warps multiply
+// the staged rows with warp-level bf16 MMAs (m16n8k16, fp32 accumulate: 16 weight rows by
+// the item's tokens, padded to 8), each warp over a fixed K range, and sum the warps' partial
+// results in a fixed order. A stage is 16 (gate/up) or 64 (down) weight rows, too few rows for
+// the 64/128-row tcgen05 MMA without four times larger stages; the tensor-core work is small
+// either way, the kernels are bound by HBM.
+//
+// k_stream_up:   h = bf16(SiLU(x . Wg^T) * (x . Wu^T)); a stage holds 8 gate rows and the 8
+//                matching up rows of one group, so the 16 x 8 MMA tile gives g and u of the same
+//                features in the same lane. Shared-expert items come first: they need no
 //                routing and run while the routing kernel finishes (programmatic dependent
-//                launch; routed items wait with griddepcontrol.wait).
-// k_stream_down: Y[t, slot] = scale * (h . Wd^T), item = 64 output rows of one group; items are
-//                ordered by output block, and the CTA that completes the last item of a block
-//                (ticket after a fence) sums that block for every token in the fixed order
-//                residual, shared, slot 0..K-1 and writes out (no CTA waits on another).
+//                launch); routed items start after griddepcontrol.wait.
+// k_stream_down: Y[t, slot] = scale * (h . Wd^T); a stage holds 64 output rows of Wd of one
+//                group. Items run output block by output block; the CTA that finishes the last
+//                item of a block (ticket after a fence) sums that block for every token in the
+//                fixed order residual, shared, slot 0..K-1 and writes out. No CTA waits on
+//                another.
 #include "launch.h"
 #include "sm100.cuh"
 
 namespace moe {
 
-constexpr int kStreamStages = 4;
-constexpr int kStageBytes = 32768;
-constexpr int kConsumers = 256;           // 8 consumer warps
+constexpr int kSt = 2;                  // ring stages
+constexpr int kTT = 8;                  // tokens per item (the MMA's N)
+constexpr int kFps = 8;                 // up: features per stage (16 rows: 8 gate + 8 up)
+constexpr int kRows = 64;               // down: output rows per stage (= combine block)
+constexpr int kConsumers = 256;         // 8 consumer warps
+constexpr int kWarps = kConsumers / 32;
 constexpr int kStreamThreads = kConsumers + 32;
-constexpr int kCombineRows = 64;          // output rows per down item / combine block
+constexpr int kPad = 16;                // row padding: rows start 16 B apart modulo 128 B
+constexpr int kMaxH = 2048, kMaxInner = 512;
+constexpr int kPitchH = 2 * kMaxH + kPad, kPitchI = 2 * kMaxInner + kPad;
+constexpr int kStageBytes = 2 * kFps * kPitchH + kTT * kPitchH;  // the larger of the up and down layouts
+static_assert(kRows * kPitchI + kTT * kPitchI <= kStageBytes, "down stage must fit");
+
+struct StageMeta {
+    int mt;          // tokens in this item
+    int row0;        // up: h row of token 0
+    int f0;          // up: first feature / down: first output row
+    int inner;       // down: length of a weight row (I or Is)
+    int block;       // down: output block
+    int expect;      // down: items of that block over all groups
+    int tok[kTT], slot[kTT];
+    float sc[kTT];
+};
+
+struct Ring {
+    uint8_t* st[kSt];
+    StageMeta* meta;
+    float* red;      // [kSt][kWarps][32][4] per-warp partial accumulators
+    uint64_t* full;
+    uint64_t* empty;
+    int* misc;       // [0] abort, [1] combine verdict, [4..] group prefix table (producer)
+};
+
+constexpr int kMiscInts = 4 + 2 * 257;
+constexpr int kRedBytes = kSt * kWarps * 32 * 4 * 4;
+constexpr int kStreamSmemBytes =
+    1024 + kSt * kStageBytes + kRedBytes + kSt * (int)sizeof(StageMeta) + 2 * kSt * 8 + kMiscInts * 4 + 64;
+
+__device__ __forceinline__ Ring carve(uint8_t* raw) {
+    const uint32_t base = smem_u32(raw);
+    uint8_t* p = raw + (((base + 127u) & ~127u) - base);
+    Ring r;
+    for (int s = 0; s < kSt; ++s) {
+        r.st[s] = p;
+        p += kStageBytes;
+    }
+    r.red = reinterpret_cast<float*>(p);
+    p += kRedBytes;
+    r.meta = reinterpret_cast<StageMeta*>(p);
+    p += kSt * sizeof(StageMeta);
+    p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 7) & ~(uintptr_t)7);
+    r.full = reinterpret_cast<uint64_t*>(p);
+    r.empty = r.full + kSt;
+    r.misc = reinterpret_cast<int*>(r.empty + kSt);
+    return r;
+}
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -40,8 +98,8 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
-// Barrier of the consumer warps that also ANDs a predicate over them, so that all consumers
-// take the same branch after a bounded wait (none is left behind in a named barrier).
+// Barrier of the consumer warps that ANDs a predicate over them, so all consumers take the same
+// branch after a bounded wait (none is left behind in a named barrier).
 __device__ __forceinline__ bool consumers_all(bool ok) {
     uint32_t r;
     asm volatile(
@@ -55,350 +113,410 @@ __device__ __forceinline__ bool consumers_all(bool ok) {
     return r != 0;
 }
 
-// Rows of one stage for rows of length L: a power of two <= 64 with rows * L * 2 <= 32 KB.
-__host__ __device__ __forceinline__ int stage_rows(int L) {
-    int r = 64;
-    while (r > 1 && r * L * 2 > kStageBytes) r >>= 1;
-    return r;
+// ---------------------------------------------------------------------------------------
+// Warp-level bf16 MMA (m16n8k16, fp32 accumulate) fed by ldmatrix from padded rows.
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Tokens per shared-memory tile of activations of length L (<= 32 KB).
-__host__ __device__ __forceinline__ int token_tile(int L) {
-    int t = 8;
-    while (t > 1 && t * L * 2 > 32768) t >>= 1;
-    return t;
+// D[16 x 8] += A[16 rows, k0 .. k0+16*ksteps) . B[8 rows, same k]^T, rows `pitch` bytes apart.
+// lane l addresses A row (l % 16) at k + 8*(l / 16) and B row (l % 8) at k + 8*((l / 8) % 2).
+__device__ __forceinline__ void mma_rows(float (&d)[4], uint32_t a_base, uint32_t b_base, int pitch, int k0,
+                                         int ksteps, int lane) {
+    const uint32_t a = a_base + (uint32_t)((lane & 15) * pitch + (k0 + 8 * (lane >> 4)) * 2);
+    const uint32_t b = b_base + (uint32_t)((lane & 7) * pitch + (k0 + 8 * ((lane >> 3) & 1)) * 2);
+#pragma unroll 4
+    for (int k = 0; k < ksteps; ++k) {
+        uint32_t a0, a1, a2, a3, b0, b1;
+        ldsm_x4(a + k * 32, a0, a1, a2, a3);
+        ldsm_x2(b + k * 32, b0, b1);
+        mma16816(d, a0, a1, a2, a3, b0, b1);
+    }
 }
 
-struct StreamSmem {
-    uint8_t* ring;
-    bf16* xs;        // [tile tokens, L] activations of the current token tile
-    uint64_t* full;
-    uint64_t* empty;
-    int* flag;       // [0] = abort, [1] = combine ticket
-};
+// ---------------------------------------------------------------------------------------
 
-__device__ __forceinline__ StreamSmem carve(uint8_t* raw, int T) {
-    const uint32_t base = smem_u32(raw);
-    uint8_t* p = raw + (((base + 127u) & ~127u) - base);
-    StreamSmem s;
-    s.ring = p;
-    p += kStreamStages * kStageBytes;
-    s.xs = reinterpret_cast<bf16*>(p);
-    p += 32768;
-    s.full = reinterpret_cast<uint64_t*>(p);
-    s.empty = s.full + kStreamStages;
-    s.flag = reinterpret_cast<int*>(s.empty + kStreamStages);
-    return s;
-}
-
-constexpr int kStreamSmemBytes = 128 + kStreamStages * kStageBytes + 32768 + 2 * kStreamStages * 8 + 16;
-
-__device__ __forceinline__ void stream_init(StreamSmem& s) {
+__device__ __forceinline__ void ring_init(Ring& r) {
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStreamStages; ++i) {
-            mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], kConsumers / 32);
+        for (int s = 0; s < kSt; ++s) {
+            mbar_init(&r.full[s], 1);
+            mbar_init(&r.empty[s], kWarps);
         }
-        s.flag[0] = 0;
+        r.misc[0] = 0;
         fence_mbar_init();
     }
     __syncthreads();
 }
 
-// Producer side of one stage: wait until consumers freed it, then start the copy.
-__device__ __forceinline__ bool produce(StreamSmem& s, int& it, const void* src, uint32_t bytes, uint32_t* err) {
-    const int st = it % kStreamStages;
-    const uint32_t ph = (uint32_t)(it / kStreamStages) & 1u;
-    if (!mbar_wait(&s.empty[st], ph ^ 1u)) {
+// Producer warp: wait for stage `it` to be free; lane 0 polls, the warp follows its verdict.
+__device__ __forceinline__ bool acquire_stage(Ring& r, int it, uint32_t* err) {
+    const int lane = threadIdx.x & 31;
+    bool ok = lane == 0 ? mbar_wait(&r.empty[it % kSt], (((uint32_t)(it / kSt)) & 1u) ^ 1u) : true;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok && lane == 0) {
         atomicOr(err, ERR_TIMEOUT);
-        *(volatile int*)&s.flag[0] = 1;
-        return false;
+        *(volatile int*)&r.misc[0] = 1;
     }
-    mbar_arrive_expect_tx(&s.full[st], bytes);
-    bulk_load(s.ring + (size_t)st * kStageBytes, src, bytes, &s.full[st]);
-    ++it;
-    return true;
-}
-
-// Consumer side: wait for stage `it`; returns its buffer or nullptr on timeout.
-__device__ __forceinline__ const bf16* consume(StreamSmem& s, int it, uint32_t* err) {
-    const int st = it % kStreamStages;
-    const uint32_t ph = (uint32_t)(it / kStreamStages) & 1u;
-    if (!mbar_wait(&s.full[st], ph)) {
-        atomicOr(err, ERR_TIMEOUT);
-        *(volatile int*)&s.flag[0] = 1;
-        return nullptr;
-    }
-    return reinterpret_cast<const bf16*>(s.ring + (size_t)st * kStageBytes);
-}
-
-__device__ __forceinline__ void release(StreamSmem& s, int it) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[it % kStreamStages]);
+    return ok;
 }
 
-// Copy `mt` activation rows of length L into xs (row tt from src_row(tt)).
-template <typename RowFn>
-__device__ __forceinline__ void stage_rows_to_smem(bf16* xs, int L, int mt, RowFn src_row) {
-    const int chunks = L / 8;
-    for (int i = threadIdx.x; i < mt * chunks; i += kConsumers) {
-        const int tt = i / chunks, c = i - tt * chunks;
-        reinterpret_cast<uint4*>(xs + (size_t)tt * L)[c] = ld_ro(src_row(tt) + (size_t)c * 8);
+// Consumer warp: wait for stage `it`; lane 0 polls, the warp follows its verdict.
+__device__ __forceinline__ bool wait_stage(Ring& r, int it, uint32_t* err) {
+    const int lane = threadIdx.x & 31;
+    bool ok = lane == 0 ? mbar_wait(&r.full[it % kSt], ((uint32_t)(it / kSt)) & 1u) : true;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok && lane == 0) {
+        atomicOr(err, ERR_TIMEOUT);
+        *(volatile int*)&r.misc[0] = 1;
+    }
+    __syncwarp();
+    return ok;
+}
+
+__device__ __forceinline__ void release_stage(Ring& r, int it) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[it % kSt]);
+}
+
+// Producer drain: every copy issued must land before the CTA releases its shared memory.
+__device__ __forceinline__ void drain(Ring& r, int issued, uint32_t* err) {
+    for (int k = 0; k < kSt && issued - 1 - k >= 0; ++k) {
+        const int j = issued - 1 - k;
+        if (!mbar_wait(&r.full[j % kSt], ((uint32_t)(j / kSt)) & 1u)) atomicOr(err, ERR_TIMEOUT);
     }
 }
 
-// Dot products of one staged row (length L) with mt staged activation rows; every lane gets
-// the sums. Chunk order per lane and the butterfly are fixed, so results are reproducible.
-template <int TT>
-__device__ __forceinline__ void row_dots(const bf16* wrow, const bf16* xs, int L, int mt, int lane, float* out) {
-    float acc[TT];
-#pragma unroll
-    for (int tt = 0; tt < TT; ++tt) acc[tt] = 0.f;
-    for (int c = lane; c < L / 8; c += 32) {
-        const uint4 w = *reinterpret_cast<const uint4*>(wrow + (size_t)c * 8);
-#pragma unroll
-        for (int tt = 0; tt < TT; ++tt) {
-            if (tt < mt) {
-                float xf[8];
-                unpack8(*reinterpret_cast<const uint4*>(xs + (size_t)tt * L + (size_t)c * 8), xf);
-                acc[tt] = dot8(w, xf, acc[tt]);
-            }
+// Group prefix table built by the producer warp: tiles[g] = first item of routed group g
+// (in items of `per_tile` per token tile), n_act + 1 entries.
+__device__ void build_tiles(const LayerArgs& a, int* tiles, int per_tile) {
+    const int lane = threadIdx.x & 31;
+    const int n = a.hdr->n_act;
+    int run = 0;
+    for (int base = 0; base < n; base += 32) {
+        const int g = base + lane;
+        int v = 0;
+        if (g < n) {
+            const int e = a.act[g];
+            v = ((a.offsets[e + 1] - a.offsets[e] + kTT - 1) / kTT) * per_tile;
         }
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (g < n) tiles[g] = run + incl - v;
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tiles[n] = run;
+    __syncwarp();
+}
+
+// Routed token tiles over all groups (computed by each consumer warp).
+__device__ __forceinline__ int routed_tiles(const LayerArgs& a, int lane) {
+    int tot = 0;
+    const int n = a.hdr->n_act;
+    for (int g = lane; g < n; g += 32) {
+        const int e = a.act[g];
+        tot += (a.offsets[e + 1] - a.offsets[e] + kTT - 1) / kTT;
     }
 #pragma unroll
-    for (int tt = 0; tt < TT; ++tt) out[tt] = tt < mt ? warp_sum(acc[tt]) : 0.f;
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    return tot;
+}
+
+// Largest g with tiles[g] <= i (tiles ascending, tiles[0] = 0).
+__device__ __forceinline__ int find_group(const int* tiles, int n, int i) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tiles[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Producer warp: copy `nrows` rows of `rowbytes` from src (rows `src_pitch` elements apart) to
+// dst rows kPad-padded, lanes in parallel.
+__device__ __forceinline__ void copy_rows(uint8_t* dst, int dst_pitch, const bf16* src, size_t src_pitch, int nrows,
+                                          uint32_t rowbytes, uint64_t* bar, int lane) {
+    for (int i = lane; i < nrows; i += 32) bulk_load(dst + (size_t)i * dst_pitch, src + (size_t)i * src_pitch, rowbytes, bar);
 }
 
 // ---------------------------------------------------------------------------------------
-
-struct UpItem {
-    const bf16* W;
-    int inner, row0, rows, f0;
-    bool shared;
-};
-
-__device__ __forceinline__ UpItem up_item(const LayerArgs& a, int it, int n_shared_items, int fpi) {
-    UpItem u;
-    if (it < n_shared_items) {
-        u = UpItem{a.sgu, a.Is, (int)a.P, a.T, it * fpi, true};
-    } else {
-        const int ipr = a.I / fpi;
-        const int k = it - n_shared_items;
-        const int g = k / ipr;
-        const int e = a.act[g];
-        u.W = a.gate_up + (size_t)e * 2 * a.I * a.H;
-        u.inner = a.I;
-        u.row0 = a.offsets[e];
-        u.rows = a.offsets[e + 1] - u.row0;
-        u.f0 = (k - g * ipr) * fpi;
-        u.shared = false;
-    }
-    return u;
-}
+// Stage layout, up:   rows 0..7 gate features f0..f0+7, rows 8..15 the matching up rows
+//                     (pitch 2H + 16), then kTT activation rows (same pitch).
+//           down:     kRows rows of Wd (pitch 2*inner + 16), then kTT h rows (same pitch).
 
 __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up(LayerArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    StreamSmem s = carve(smem_raw, a.T);
-    stream_init(s);
+    Ring r = carve(smem_raw);
+    ring_init(r);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int fpi = stage_rows(a.H);
-    const int n_shared = a.Is / fpi;
     uint32_t* err = &a.hdr->err;
-    // routed items need the routing: everything below `n_shared` can start at once
-    int n_items = -1;
+    const int fb_s = a.Is / kFps, fb_r = a.I / kFps;          // feature blocks per group
+    const int n_shared = fb_s * ((a.T + kTT - 1) / kTT);       // shared items first
+    const int pitch = 2 * a.H + kPad;
 
-    if (warp == kConsumers / 32) {
-        if (lane == 0) {
-            int it = 0;
-            bool waited = false;
-            for (int i = blockIdx.x;; i += gridDim.x) {
-                if (i >= n_shared && !waited) {
-                    grid_dep_wait();
-                    waited = true;
-                    n_items = n_shared + a.hdr->n_act * (a.I / fpi);
-                }
-                if (n_items >= 0 && i >= n_items) break;
-                if (*(volatile int*)&s.flag[0]) break;
-                const UpItem u = up_item(a, i, n_shared, fpi);
-                const uint32_t bytes = (uint32_t)(fpi * a.H * 2);
-                if (!produce(s, it, u.W + (size_t)u.f0 * a.H, bytes, err)) break;
-                if (!produce(s, it, u.W + (size_t)(u.inner + u.f0) * a.H, bytes, err)) break;
+    if (warp == kWarps) {
+        // ---------------- producer
+        int* tiles = r.misc + 4;
+        int it = 0, n_items = -1, n_act = 0;
+        for (int i = blockIdx.x;; i += gridDim.x) {
+            if (i >= n_shared && n_items < 0) {
+                grid_dep_wait();
+                n_act = a.hdr->n_act;
+                build_tiles(a, tiles, fb_r);
+                n_items = n_shared + tiles[n_act];
             }
-            // every copy issued must land before the CTA's shared memory is released
-            for (int k = 0; k < kStreamStages && it - 1 - k >= 0; ++k) {
-                const int j = it - 1 - k;
-                if (!mbar_wait(&s.full[j % kStreamStages], (uint32_t)(j / kStreamStages) & 1u)) atomicOr(err, ERR_TIMEOUT);
+            if (n_items >= 0 && i >= n_items) break;
+            if (__shfl_sync(0xffffffffu, *(volatile int*)&r.misc[0], 0)) break;
+            const bf16* W;
+            int inner, row0, f0, mt, t0;
+            bool shared;
+            if (i < n_shared) {
+                const int tile = i / fb_s, fb = i - tile * fb_s;
+                W = a.sgu;
+                inner = a.Is;
+                t0 = tile * kTT;
+                mt = min(kTT, a.T - t0);
+                row0 = (int)a.P;
+                f0 = fb * kFps;
+                shared = true;
+            } else {
+                const int k = i - n_shared;
+                const int g = find_group(tiles, n_act, k);
+                const int local = k - tiles[g];
+                const int tile = local / fb_r, fb = local - tile * fb_r;
+                const int e = a.act[g];
+                W = a.gate_up + (size_t)e * 2 * a.I * a.H;
+                inner = a.I;
+                row0 = a.offsets[e];
+                t0 = tile * kTT;
+                mt = min(kTT, a.offsets[e + 1] - row0 - t0);
+                f0 = fb * kFps;
+                shared = false;
             }
+            const int s = it % kSt;
+            if (!acquire_stage(r, it, err)) break;
+            if (lane == 0) {
+                StageMeta& m = r.meta[s];
+                m.mt = mt;
+                m.row0 = row0 + t0;
+                m.f0 = f0;
+                mbar_arrive_expect_tx(&r.full[s], (uint32_t)((2 * kFps + mt) * a.H * 2));
+            }
+            __syncwarp();
+            uint8_t* st = r.st[s];
+            copy_rows(st, pitch, W + (size_t)f0 * a.H, a.H, kFps, a.H * 2, &r.full[s], lane);
+            copy_rows(st + kFps * pitch, pitch, W + (size_t)(inner + f0) * a.H, a.H, kFps, a.H * 2, &r.full[s], lane);
+            if (lane < mt) {
+                const int j = row0 + t0 + lane;
+                const int t = shared ? j - (int)a.P : a.perm[j] / a.K;
+                bulk_load(st + (size_t)(2 * kFps + lane) * pitch, a.x + (size_t)t * a.H, a.H * 2, &r.full[s]);
+            }
+            ++it;
         }
+        if (lane == 0) drain(r, it, err);
         return;
     }
 
-    // consumers
-    const int TT = token_tile(a.H);
-    int it = 0;
-    bool waited = false;
-    for (int i = blockIdx.x;; i += gridDim.x) {
-        if (i >= n_shared && !waited) {
+    // ---------------- consumers: warp w takes K range [w*H/8, (w+1)*H/8) of all 16 rows
+    const int kw = a.H / kWarps;
+    int it = 0, n_items = -1;
+    for (int i = blockIdx.x;; i += gridDim.x, ++it) {
+        if (i >= n_shared && n_items < 0) {
             grid_dep_wait();
-            waited = true;
-            n_items = n_shared + a.hdr->n_act * (a.I / fpi);
+            n_items = n_shared + routed_tiles(a, lane) * fb_r;
         }
         if (n_items >= 0 && i >= n_items) break;
-        const UpItem u = up_item(a, i, n_shared, fpi);
-        const bf16* wgs = consume(s, it, err);
-        const bf16* wus = wgs ? consume(s, it + 1, err) : nullptr;
-        if (!consumers_all(wus != nullptr)) break;
-        for (int r0 = 0; r0 < u.rows; r0 += TT) {
-            const int mt = min(TT, u.rows - r0);
-            stage_rows_to_smem(s.xs, a.H, mt, [&](int tt) {
-                const int j = u.row0 + r0 + tt;
-                const int t = u.shared ? j - (int)a.P : a.perm[j] / a.K;
-                return a.x + (size_t)t * a.H;
-            });
-            consumers_sync();
-            for (int f = warp; f < fpi; f += kConsumers / 32) {
-                float g[8], uu[8];
-                row_dots<8>(wgs + (size_t)f * a.H, s.xs, a.H, mt, lane, g);
-                row_dots<8>(wus + (size_t)f * a.H, s.xs, a.H, mt, lane, uu);
+        const bool ok = wait_stage(r, it, err);
+        if (!consumers_all(ok)) break;
+        const int s = it % kSt;
+        const StageMeta& m = r.meta[s];  // read in place: rewritten only after the stage is released
+        const int mt = m.mt, row0 = m.row0, f0 = m.f0;
+        const uint32_t sa = smem_u32(r.st[s]);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_rows(d, sa, sa + 2 * kFps * pitch, pitch, warp * kw, kw / 16, lane);
+        release_stage(r, it);
+        // fixed-order sum of the 8 warps' K ranges: lane l holds gate (d0, d1) and up (d2, d3)
+        // of feature l/4 for tokens 2*(l%4) and 2*(l%4)+1
+        float* red = r.red + (size_t)s * kWarps * 128;
+        *reinterpret_cast<float4*>(red + (warp * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
+        consumers_sync();
+        if (warp == 0) {
+            float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
 #pragma unroll
-                for (int tt = 0; tt < 8; ++tt)
-                    if (lane == tt && tt < mt)
-                        a.h[(size_t)(u.row0 + r0 + tt) * a.Imax + u.f0 + f] = __float2bfloat16_rn(silu(g[tt]) * uu[tt]);
+            for (int w = 0; w < kWarps; ++w) {
+                const float4 v = *reinterpret_cast<const float4*>(red + (w * 32 + lane) * 4);
+                g0 += v.x; g1 += v.y; u0 += v.z; u1 += v.w;
             }
-            consumers_sync();
+            const int f = lane >> 2, t = 2 * (lane & 3);
+            if (t < mt) a.h[(size_t)(row0 + t) * a.Imax + f0 + f] = __float2bfloat16_rn(silu(g0) * u0);
+            if (t + 1 < mt) a.h[(size_t)(row0 + t + 1) * a.Imax + f0 + f] = __float2bfloat16_rn(silu(g1) * u1);
         }
-        release(s, it);
-        release(s, it + 1);
-        it += 2;
     }
     grid_dep_launch();
 }
 
 // ---------------------------------------------------------------------------------------
 
-struct DownItem {
-    const bf16* W;
-    int inner, row0, rows, o0;
-    bool shared;
-};
-
-__device__ __forceinline__ DownItem down_item(const LayerArgs& a, int it, int n_groups) {
-    const int ob = it / n_groups, g = it - ob * n_groups;
-    DownItem d;
-    d.o0 = ob * kCombineRows;
-    if (g == n_groups - 1) {
-        d.W = a.sd;
-        d.inner = a.Is;
-        d.row0 = (int)a.P;
-        d.rows = a.T;
-        d.shared = true;
-    } else {
-        const int e = a.act[g];
-        d.W = a.down + (size_t)e * a.H * a.I;
-        d.inner = a.I;
-        d.row0 = a.offsets[e];
-        d.rows = a.offsets[e + 1] - d.row0;
-        d.shared = false;
-    }
-    return d;
-}
-
 __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    StreamSmem s = carve(smem_raw, a.T);
-    stream_init(s);
+    Ring r = carve(smem_raw);
+    ring_init(r);
     grid_dep_wait();  // h comes from k_stream_up; the routing from before it
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_groups = a.hdr->n_act + 1;
-    const int n_items = n_groups * (a.H / kCombineRows);
     uint32_t* err = &a.hdr->err;
+    const int n_act = a.hdr->n_act;
+    const int tiles_s = (a.T + kTT - 1) / kTT;
+    const int n_blocks = a.H / kRows;
 
-    if (warp == kConsumers / 32) {
-        if (lane == 0) {
-            int it = 0;
-            for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
-                if (*(volatile int*)&s.flag[0]) break;
-                const DownItem d = down_item(a, i, n_groups);
-                const int rps = stage_rows(d.inner);
-                bool ok = true;
-                for (int r = 0; r < kCombineRows && ok; r += rps)
-                    ok = produce(s, it, d.W + (size_t)(d.o0 + r) * d.inner, (uint32_t)(rps * d.inner * 2), err);
-                if (!ok) break;
+    if (warp == kWarps) {
+        // ---------------- producer: items ordered block-major: (block, group, token tile)
+        int* tiles = r.misc + 4;
+        build_tiles(a, tiles, 1);
+        const int per_block = tiles[n_act] + tiles_s;
+        const int n_items = per_block * n_blocks;
+        int it = 0;
+        for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+            if (__shfl_sync(0xffffffffu, *(volatile int*)&r.misc[0], 0)) break;
+            const int blk = i / per_block, k = i - blk * per_block;
+            const bf16* W;
+            int inner, hrow0, mt;
+            bool shared;
+            if (k >= tiles[n_act]) {
+                const int t0 = (k - tiles[n_act]) * kTT;
+                W = a.sd;
+                inner = a.Is;
+                hrow0 = (int)a.P + t0;
+                mt = min(kTT, a.T - t0);
+                shared = true;
+            } else {
+                const int g = find_group(tiles, n_act, k);
+                const int t0 = (k - tiles[g]) * kTT;
+                const int e = a.act[g];
+                W = a.down + (size_t)e * a.H * a.I;
+                inner = a.I;
+                hrow0 = a.offsets[e] + t0;
+                mt = min(kTT, a.offsets[e + 1] - a.offsets[e] - t0);
+                shared = false;
             }
-            for (int k = 0; k < kStreamStages && it - 1 - k >= 0; ++k) {
-                const int j = it - 1 - k;
-                if (!mbar_wait(&s.full[j % kStreamStages], (uint32_t)(j / kStreamStages) & 1u)) atomicOr(err, ERR_TIMEOUT);
+            const int s = it % kSt;
+            if (!acquire_stage(r, it, err)) break;
+            StageMeta& m = r.meta[s];
+            if (lane < mt) {
+                const int j = hrow0 + lane;
+                if (shared) {
+                    m.tok[lane] = j - (int)a.P;
+                    m.slot[lane] = a.K;
+                    m.sc[lane] = a.sgate[j - (int)a.P];
+                } else {
+                    const int pv = a.perm[j];
+                    m.tok[lane] = pv / a.K;
+                    m.slot[lane] = pv - (pv / a.K) * a.K;
+                    m.sc[lane] = a.topw[pv];
+                }
             }
+            const int pitch = 2 * inner + kPad;
+            if (lane == 0) {
+                m.mt = mt;
+                m.f0 = blk * kRows;
+                m.inner = inner;
+                m.block = blk;
+                m.expect = per_block;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&r.full[s], (uint32_t)((kRows + mt) * inner * 2));
+            __syncwarp();
+            uint8_t* st = r.st[s];
+            copy_rows(st, pitch, W + (size_t)blk * kRows * inner, inner, kRows, inner * 2, &r.full[s], lane);
+            if (lane < mt)
+                bulk_load(st + (size_t)(kRows + lane) * pitch, a.h + (size_t)(hrow0 + lane) * a.Imax, inner * 2,
+                          &r.full[s]);
+            ++it;
         }
+        if (lane == 0) drain(r, it, err);
         return;
     }
 
+    // ---------------- consumers: warp w takes M tile (w % 4) and K half (w / 4)
+    const int per_block = routed_tiles(a, lane) + tiles_s;
+    const int n_items = per_block * n_blocks;
     int it = 0;
-    for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
-        const DownItem d = down_item(a, i, n_groups);
-        const int rps = stage_rows(d.inner);
-        const int TT = token_tile(d.inner);
-        bool ok = true;
-        for (int r = 0; r < kCombineRows && ok; r += rps, ++it) {
-            const bf16* ws = consume(s, it, err);
-            if (!consumers_all(ws != nullptr)) {
-                ok = false;
-                break;
-            }
-            for (int r0 = 0; r0 < d.rows; r0 += TT) {
-                const int mt = min(TT, d.rows - r0);
-                stage_rows_to_smem(s.xs, d.inner, mt, [&](int tt) { return a.h + (size_t)(d.row0 + r0 + tt) * a.Imax; });
-                consumers_sync();
-                int tok[8], slot[8];
-                float sc[8];
-#pragma unroll
-                for (int tt = 0; tt < 8; ++tt) {
-                    tok[tt] = 0;
-                    slot[tt] = 0;
-                    sc[tt] = 0.f;
-                    if (tt < mt) {
-                        const int j = d.row0 + r0 + tt;
-                        if (d.shared) {
-                            tok[tt] = j - (int)a.P;
-                            slot[tt] = a.K;
-                            sc[tt] = a.sgate[tok[tt]];
-                        } else {
-                            const int pv = a.perm[j];
-                            tok[tt] = pv / a.K;
-                            slot[tt] = pv - tok[tt] * a.K;
-                            sc[tt] = a.topw[pv];
-                        }
-                    }
-                }
-                for (int rr = warp; rr < rps; rr += kConsumers / 32) {
-                    float y[8];
-                    row_dots<8>(ws + (size_t)rr * d.inner, s.xs, d.inner, mt, lane, y);
-                    const int o = d.o0 + r + rr;
-#pragma unroll
-                    for (int tt = 0; tt < 8; ++tt)
-                        if (lane == tt && tt < mt) a.Y[((size_t)tok[tt] * (a.K + 1) + slot[tt]) * a.H + o] = sc[tt] * y[tt];
-                }
-                consumers_sync();
-            }
-            release(s, it);
+    for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++it) {
+        const bool ok = wait_stage(r, it, err);
+        if (!consumers_all(ok)) break;
+        const int s = it % kSt;
+        const StageMeta& m = r.meta[s];  // read in place: rewritten only after the stage is released
+        const int mt = m.mt, inner = m.inner, f0 = m.f0, blk = m.block, expect = m.expect;
+        const int pitch = 2 * inner + kPad;
+        const int mtile = warp & 3, khalf = warp >> 2;
+        const int kh = inner / 2;
+        const uint32_t sa = smem_u32(r.st[s]);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_rows(d, sa + (uint32_t)(mtile * 16 * pitch), sa + (uint32_t)(kRows * pitch), pitch, khalf * kh, kh / 16,
+                 lane);
+        // tokens of this lane's accumulator columns
+        const int t0 = 2 * (lane & 3);
+        size_t y0 = 0, y1 = 0;
+        float s0 = 0.f, s1 = 0.f;
+        if (t0 < mt) {
+            y0 = ((size_t)m.tok[t0] * (a.K + 1) + m.slot[t0]) * a.H + f0;
+            s0 = m.sc[t0];
         }
-        if (!ok) break;
-        // fixed-order combine of this output block once every group has written it
+        if (t0 + 1 < mt) {
+            y1 = ((size_t)m.tok[t0 + 1] * (a.K + 1) + m.slot[t0 + 1]) * a.H + f0;
+            s1 = m.sc[t0 + 1];
+        }
+        release_stage(r, it);
+        // fixed-order sum of the two K halves, then scale and store: lane l holds rows l/4 and
+        // l/4 + 8 of the M tile for tokens t0, t0 + 1
+        float* red = r.red + (size_t)s * kWarps * 128;
+        if (khalf == 1) *reinterpret_cast<float4*>(red + (mtile * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
+        consumers_sync();
+        if (khalf == 0) {
+            const float4 v = *reinterpret_cast<const float4*>(red + (mtile * 32 + lane) * 4);
+            const int row = mtile * 16 + (lane >> 2);
+            if (t0 < mt) {
+                a.Y[y0 + row] = s0 * (d[0] + v.x);
+                a.Y[y0 + row + 8] = s0 * (d[2] + v.z);
+            }
+            if (t0 + 1 < mt) {
+                a.Y[y1 + row] = s1 * (d[1] + v.y);
+                a.Y[y1 + row + 8] = s1 * (d[3] + v.w);
+            }
+        }
+        // fixed-order combine of the block once every item of it is written
         __threadfence();
         consumers_sync();
-        if (threadIdx.x == 0) s.flag[1] = (int)atomicAdd(&a.comb_ticket[d.o0 / kCombineRows], 1u);
+        if (threadIdx.x == 0) r.misc[1] = (int)atomicAdd(&a.comb_ticket[blk], 1u);
         consumers_sync();
-        if (s.flag[1] == n_groups - 1) {
+        if (r.misc[1] == expect - 1) {
             __threadfence();
-            for (int idx = threadIdx.x; idx < a.T * kCombineRows; idx += kConsumers) {
-                const int t = idx / kCombineRows, o = d.o0 + (idx - t * kCombineRows);
+            for (int idx = threadIdx.x; idx < a.T * kRows; idx += kConsumers) {
+                const int t = idx / kRows, o = f0 + (idx - t * kRows);
                 const float* yt = a.Y + (size_t)t * (a.K + 1) * a.H + o;
                 float acc = a.residual ? __bfloat162float(a.residual[(size_t)t * a.H + o]) : 0.f;
                 acc += __ldcg(yt + (size_t)a.K * a.H);
                 for (int k = 0; k < a.K; ++k) acc += __ldcg(yt + (size_t)k * a.H);
                 a.out[(size_t)t * a.H + o] = __float2bfloat16_rn(acc);
             }
-            if (threadIdx.x == 0) a.comb_ticket[d.o0 / kCombineRows] = 0;  // re-arm
+            if (threadIdx.x == 0) a.comb_ticket[blk] = 0;  // re-arm
         }
     }
 }
@@ -425,9 +543,10 @@ cudaError_t launch_pdl(K kernel, int grid, int smem, cudaStream_t s, const Layer
 }  // namespace
 
 bool stream_supported(const LayerArgs& a) {
-    // the shared-memory ring holds at least one row, the activation tile at least one token,
-    // and the gate results of an up item fit the [64, 256] buffer
-    return a.H * 2 <= kStageBytes && a.Imax * 2 <= kStageBytes && a.T <= 256 && stage_rows(a.H) <= 64;
+    // stages are laid out for rows of at most 2048 (gate/up) and 512 (down) elements; the K
+    // range of each consumer warp must be a whole number of 16-element MMA steps
+    return a.T >= 1 && a.T < kGemmMinTokens && a.H <= kMaxH && a.Imax <= kMaxInner && a.H % (kWarps * 16) == 0 &&
+           a.I % 32 == 0 && a.Is % 32 == 0;
 }
 
 cudaError_t launch_stream_experts(const LayerArgs& a, cudaStream_t s) {
