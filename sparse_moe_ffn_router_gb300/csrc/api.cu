@@ -128,6 +128,7 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 
 // Router scores, top-K and dispatch: one fused launch for few tokens, else separate kernels.
 cudaError_t launch_routing(const LayerArgs& a, cudaStream_t s) {
+    if (route_cluster_supported(a)) return launch_route_cluster(a, s);
     if (a.T <= kFusedRouteTokens) return launch_route_fused(a, s);
     cudaError_t e = launch_router(a, s);
     if (e == cudaSuccess) e = launch_dispatch(a, s);

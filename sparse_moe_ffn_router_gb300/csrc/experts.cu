@@ -189,6 +189,8 @@ __device__ __forceinline__ float4 load4(const bf16* p) {
 
 template <typename YT>
 __global__ void __launch_bounds__(256) k_combine(LayerArgs a, const YT* Y) {
+    // no-op unless launched as a programmatic dependent: then wait for the producer of Y
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
     const int q = a.H / 4;
     if (i >= (int64_t)a.T * q) return;
@@ -215,6 +217,24 @@ cudaError_t launch_experts(const LayerArgs& a, cudaStream_t s) {
     MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (k_gate_up<<<min(up_items, cap), 256, 0, s>>>(a)));
     MOE_LAUNCH(MOE_KERNEL_DOWN, s, (k_down<<<min(dn_items, cap), 256, 0, s>>>(a)));
     return cudaGetLastError();
+}
+
+// The combine as a programmatic dependent launch of the preceding kernel (fp32 Y).
+cudaError_t launch_combine_pdl(const LayerArgs& a, cudaStream_t s) {
+    const int64_t nq = (int64_t)a.T * (a.H / 4);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((nq + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    const float* Y = a.Y;
+    MOE_LAUNCH(MOE_KERNEL_COMBINE, s, (e = cudaLaunchKernelEx(&cfg, k_combine<float>, a, Y)));
+    return e;
 }
 
 cudaError_t launch_combine(const LayerArgs& a, cudaStream_t s) {

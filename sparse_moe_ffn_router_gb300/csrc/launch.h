@@ -73,10 +73,13 @@ struct GemmPlan {
 
 cudaError_t launch_router(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_route_fused(const LayerArgs& a, cudaStream_t s);
+bool route_cluster_supported(const LayerArgs& a);
+cudaError_t launch_route_cluster(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_router_gemm(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_expert_gemms(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_prep(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const LayerArgs& a, cudaStream_t s);
+cudaError_t launch_combine_pdl(const LayerArgs& a, cudaStream_t s);
 bool stream_supported(const LayerArgs& a);
 cudaError_t launch_stream_experts(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch(const LayerArgs& a, cudaStream_t s);

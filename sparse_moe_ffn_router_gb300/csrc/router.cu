@@ -7,6 +7,7 @@
 #include <math.h>
 
 #include "launch.h"
+#include "sm100.cuh"
 
 namespace moe {
 
@@ -391,6 +392,283 @@ __global__ void __launch_bounds__(256) k_route_fused(LayerArgs a) {
 cudaError_t launch_route_fused(const LayerArgs& a, cudaStream_t s) {
     MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (k_route_fused<<<(a.E + 1 + 7) / 8, 256, 0, s>>>(a)));
     return cudaGetLastError();
+}
+
+}  // namespace moe
+
+namespace moe {
+
+// ---------------------------------------------------------------------------------------
+// Few-token routing on one thread-block cluster of 8 CTAs (T <= 64, H <= 2048, E <= 256).
+// CTA c bulk-copies its ~(E+1)/8 rows of [Wr; ws] into shared memory (one TMA bulk copy),
+// scores them for every token, and stores the scores straight into CTA 0's shared memory
+// (distributed shared memory). After one cluster barrier CTA 0 runs top-K for all tokens and
+// the dispatch from its own shared memory and writes the routing to global memory.
+
+constexpr int kRouteCluster = 8;
+constexpr int kRouteStageX = 8;  // tokens whose rows are staged in shared memory
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t local_addr, int rank, float v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(bytes), "r"((uint32_t)__cvta_generic_to_shared(bar))
+                 : "memory");
+}
+
+struct RouteSmem {
+    __host__ __device__ static size_t rows(int E) { return (size_t)(E + 1 + kRouteCluster - 1) / kRouteCluster; }
+    static size_t bytes(int T, int H, int E, int ldl) {
+        return 128 + rows(E) * H * 2 + (T <= kRouteStageX ? (size_t)T * H * 2 : 0) + (size_t)T * ldl * 4 + 64;
+    }
+};
+
+__global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int cnt[256];
+    __shared__ int off[257];
+    __shared__ int sids[kFusedRouteTokens * 8];
+    __shared__ int slr[kFusedRouteTokens * 8];
+    __shared__ uint64_t bar;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;  // == rank in the (single) cluster
+    const int R = (int)RouteSmem::rows(a.E);
+    const int r0 = c * R, r1 = min(a.E + 1, r0 + R);
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    uint8_t* p = smem_raw + (((base + 127u) & ~127u) - base);
+    bf16* wsm = reinterpret_cast<bf16*>(p);
+    p += (size_t)R * a.H * 2;
+    bf16* xsm = reinterpret_cast<bf16*>(p);
+    const bool stage_x = a.T <= kRouteStageX;
+    if (stage_x) p += (size_t)a.T * a.H * 2;
+    float* lg = reinterpret_cast<float*>(p);  // [T, ldl] scores, used in CTA 0
+
+    // 1. bulk-copy this CTA's rows (routed rows are contiguous; row E is the shared gate)
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        const int rr1 = min(r1, a.E);
+        const uint32_t bytes = (uint32_t)((max(rr1 - r0, 0) + (r1 > a.E ? 1 : 0)) * a.H * 2 +
+                                          (stage_x ? a.T * a.H * 2 : 0));
+        mbar_arrive_expect_tx(&bar, bytes);
+        if (rr1 > r0) bulk_g2s(wsm, a.router_w + (size_t)r0 * a.H, (uint32_t)((rr1 - r0) * a.H * 2), &bar);
+        if (r1 > a.E) bulk_g2s(wsm + (size_t)(a.E - r0) * a.H, a.sg, (uint32_t)(a.H * 2), &bar);
+        if (stage_x) bulk_g2s(xsm, a.x, (uint32_t)(a.T * a.H * 2), &bar);
+    }
+    __syncthreads();
+    bool ok = mbar_wait(&bar, 0);
+    if (!ok) atomicOr(&a.hdr->err, ERR_TIMEOUT);
+    const bf16* xs = stage_x ? xsm : a.x;
+    // 2. scores of this CTA's rows, stored into CTA 0's shared memory
+    for (int r = r0 + warp; r < r1 && ok; r += 8) {
+        const bf16* wrow = wsm + (size_t)(r - r0) * a.H;
+        const float bias = (r < a.E && a.router_b) ? __bfloat162float(a.router_b[r]) : 0.f;
+        for (int t0 = 0; t0 < a.T; t0 += kRouterTokens) {
+            const int mt = min(kRouterTokens, a.T - t0);
+            float acc[kRouterTokens];
+#pragma unroll
+            for (int i = 0; i < kRouterTokens; ++i) acc[i] = 0.f;
+#pragma unroll 4
+            for (int ch = lane; ch < a.H / 8; ch += 32) {
+                float wf[8];
+                unpack8(*reinterpret_cast<const uint4*>(wrow + (size_t)ch * 8), wf);
+#pragma unroll
+                for (int tt = 0; tt < kRouterTokens; ++tt) {
+                    if (tt < mt) {
+                        const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)(t0 + tt) * a.H + (size_t)ch * 8);
+                        float s = acc[tt];
+                        s = fmaf(wf[0], bf_lo(xv.x), s); s = fmaf(wf[1], bf_hi(xv.x), s);
+                        s = fmaf(wf[2], bf_lo(xv.y), s); s = fmaf(wf[3], bf_hi(xv.y), s);
+                        s = fmaf(wf[4], bf_lo(xv.z), s); s = fmaf(wf[5], bf_hi(xv.z), s);
+                        s = fmaf(wf[6], bf_lo(xv.w), s); s = fmaf(wf[7], bf_hi(xv.w), s);
+                        acc[tt] = s;
+                    }
+                }
+            }
+#pragma unroll
+            for (int tt = 0; tt < kRouterTokens; ++tt) {
+                if (tt < mt) {
+                    const float s = warp_sum(acc[tt]) + bias;
+                    if (lane == 0)
+                        st_cluster_f32((uint32_t)__cvta_generic_to_shared(lg + (size_t)(t0 + tt) * a.ldl + r), 0, s);
+                }
+            }
+        }
+    }
+    cluster_sync_all();
+    if (c != 0) return;
+
+    // 3. CTA 0: top-K of every token from shared memory, then the dispatch
+    for (int t = warp; t < a.T; t += 8) {
+        const float* l = lg + (size_t)t * a.ldl;
+        float v[8];
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane + 32 * j;
+            v[j] = -INFINITY;
+            if (e < a.E) {
+                v[j] = l[e];
+                if (!isfinite(v[j])) {
+                    bad = true;
+                    v[j] = -INFINITY;
+                }
+            }
+        }
+        uint32_t taken = 0;
+        float sel_v[8];
+        int sel_e[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (k < a.K) {
+                float bv = -INFINITY;
+                int be = 0x7fffffff;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int e = lane + 32 * j;
+                    if (e < a.E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
+                        bv = v[j];
+                        be = e;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                    if (ov > bv || (ov == bv && oe < be)) {
+                        bv = ov;
+                        be = oe;
+                    }
+                }
+                if ((be & 31) == lane) taken |= 1u << (be >> 5);
+                sel_v[k] = bv;
+                sel_e[k] = be;
+            }
+        }
+        if (lane == 0) {
+            float ex[8], s = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k < a.K) {
+                    ex[k] = expf(sel_v[k] - sel_v[0]);
+                    s += ex[k];
+                }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k < a.K) {
+                    sids[t * a.K + k] = sel_e[k];
+                    a.ids[(size_t)t * a.K + k] = sel_e[k];
+                    a.topw[(size_t)t * a.K + k] = ex[k] / s;
+                }
+            const float z = l[a.E];
+            if (!isfinite(z)) bad = true;
+            a.sgate[t] = 1.0f / (1.0f + expf(-z));
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&a.hdr->err, ERR_NONFINITE_SCORE);
+    }
+    for (int e = threadIdx.x; e < a.E; e += 256) cnt[e] = 0;
+    __syncthreads();
+    const int P = (int)a.P;
+    if (warp == 0) {
+        for (int b0 = 0; b0 < P; b0 += 32) {
+            const int i = b0 + lane;
+            const bool valid = i < P;
+            const int e = valid ? sids[i] : -1;
+            const unsigned m = __match_any_sync(0xffffffffu, e);
+            const int rank_in = __popc(m & ((1u << lane) - 1u));
+            const int cc = valid ? cnt[e] : 0;
+            __syncwarp();
+            if (valid) {
+                slr[i] = cc + rank_in;
+                if (rank_in == 0) cnt[e] = cc + __popc(m);
+            }
+            __syncwarp();
+        }
+        int loc[8], run = 0, nz = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            loc[j] = e < a.E ? cnt[e] : 0;
+            run += loc[j];
+            nz += loc[j] > 0;
+        }
+        int incl = run, inz = nz;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            const int z = __shfl_up_sync(0xffffffffu, inz, o);
+            if (lane >= o) {
+                incl += y;
+                inz += z;
+            }
+        }
+        int pos = incl - run, apos = inz - nz;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane * 8 + j;
+            if (e < a.E) {
+                off[e] = pos;
+                if (loc[j] > 0) a.act[apos++] = e;
+            }
+            pos += loc[j];
+        }
+        if (lane == 31) {
+            off[a.E] = incl;
+            a.hdr->n_act = inz;
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e <= a.E; e += 256) {
+        a.offsets[e] = off[e];
+        if (e < a.E) a.counts[e] = cnt[e];
+    }
+    for (int i = threadIdx.x; i < P; i += 256) {
+        const int j = off[sids[i]] + slr[i];
+        a.perm[j] = i;
+        a.inv[i] = j;
+    }
+}
+
+bool route_cluster_supported(const LayerArgs& a) {
+    return a.T >= 1 && a.T <= kFusedRouteTokens && a.E <= 256 &&
+           RouteSmem::bytes(a.T, a.H, a.E, a.ldl) <= 200 * 1024;
+}
+
+cudaError_t launch_route_cluster(const LayerArgs& a, cudaStream_t s) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(k_route_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kRouteCluster);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = RouteSmem::bytes(a.T, a.H, a.E, a.ldl);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kRouteCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (e = cudaLaunchKernelEx(&cfg, k_route_cluster, a)));
+    return e;
 }
 
 }  // namespace moe

@@ -21,10 +21,8 @@
 //                routing and run while the routing kernel finishes (programmatic dependent
 //                launch); routed items start after griddepcontrol.wait.
 // k_stream_down: Y[t, slot] = scale * (h . Wd^T); a stage holds 64 output rows of Wd of one
-//                group. Items run output block by output block; the CTA that finishes the last
-//                item of a block (ticket after a fence) sums that block for every token in the
-//                fixed order residual, shared, slot 0..K-1 and writes out. No CTA waits on
-//                another.
+//                group. The fixed-order combine runs next as its own kernel (launched as a
+//                programmatic dependent, so its launch overlaps this kernel's tail).
 #include "launch.h"
 #include "sm100.cuh"
 
@@ -501,24 +499,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
                 a.Y[y1 + row + 8] = s1 * (d[3] + v.w);
             }
         }
-        // fixed-order combine of the block once every item of it is written
-        __threadfence();
-        consumers_sync();
-        if (threadIdx.x == 0) r.misc[1] = (int)atomicAdd(&a.comb_ticket[blk], 1u);
-        consumers_sync();
-        if (r.misc[1] == expect - 1) {
-            __threadfence();
-            for (int idx = threadIdx.x; idx < a.T * kRows; idx += kConsumers) {
-                const int t = idx / kRows, o = f0 + (idx - t * kRows);
-                const float* yt = a.Y + (size_t)t * (a.K + 1) * a.H + o;
-                float acc = a.residual ? __bfloat162float(a.residual[(size_t)t * a.H + o]) : 0.f;
-                acc += __ldcg(yt + (size_t)a.K * a.H);
-                for (int k = 0; k < a.K; ++k) acc += __ldcg(yt + (size_t)k * a.H);
-                a.out[(size_t)t * a.H + o] = __float2bfloat16_rn(acc);
-            }
-            if (threadIdx.x == 0) a.comb_ticket[blk] = 0;  // re-arm
-        }
     }
+    grid_dep_launch();
 }
 
 // ---------------------------------------------------------------------------------------
@@ -565,7 +547,8 @@ cudaError_t launch_stream_experts(const LayerArgs& a, cudaStream_t s) {
     MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (e = launch_pdl(k_stream_up, a.num_sms, kStreamSmemBytes, s, a)));
     if (e != cudaSuccess) return e;
     MOE_LAUNCH(MOE_KERNEL_DOWN, s, (e = launch_pdl(k_stream_down, a.num_sms, kStreamSmemBytes, s, a)));
-    return e;
+    if (e != cudaSuccess) return e;
+    return launch_combine_pdl(a, s);
 }
 
 }  // namespace moe
