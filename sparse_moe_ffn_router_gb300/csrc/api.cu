@@ -116,7 +116,7 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
     a->up_tiles = (int32_t*)(base + p->o_upt);
     a->dn_tiles = (int32_t*)(base + p->o_dnt);
     a->n_groups = &a->hdr->n_groups;
-    a->comb_ticket = (uint32_t*)(base + p->o_ctk);
+    a->uprec = p->T <= kRecTokens ? (UpRec*)(base + p->o_uprec) : nullptr;
     a->gemm = p->gemm;
     a->T = p->T; a->H = p->H; a->E = p->E; a->K = p->K; a->I = p->I; a->Is = p->Is;
     a->Imax = p->Imax; a->ldl = p->ldl; a->nb = p->nb; a->P = p->P;

@@ -21,8 +21,23 @@ struct WsHeader {
     int32_t n_act;     // experts with at least one routed pair (written by the dispatch scan)
     int32_t n_groups;  // GEMM groups: n_act routed experts + the shared expert
     uint32_t route_ticket;  // CTAs of the fused routing kernel that finished (re-armed to 0)
-    uint32_t pad[60];
+    int32_t n_uprec;        // routed gate_up work records written by the few-token router
+    uint32_t pad[59];
 };
+
+// One routed gate_up work item of the few-token path (T <= 8), written by the router: expert,
+// first h row of its tokens, first of its 8 features, token count, and the tokens themselves
+// (4 bits each, in h-row order).
+struct UpRec {
+    int32_t e;
+    int32_t row0;
+    int16_t f0;
+    int16_t mt;
+    uint32_t toks;
+};
+
+// Tokens up to which the router writes UpRec records (and x rows are staged once per CTA).
+constexpr int kRecTokens = 8;
 
 // One group of the grouped GEMM: A rows [a_row0, a_row0 + rows) of the activation tensor,
 // B block starting at weight row b_row0, output rows from out_row0; src selects the routed
@@ -44,7 +59,7 @@ struct Plan {
     int nb;          // token blocks of the dispatch
     bool gemm;       // many-token path (tensor-core GEMMs, bf16 Y) instead of weight streaming
     size_t o_hdr, o_logits, o_ids, o_topw, o_sgate, o_counts, o_offsets, o_perm, o_inv, o_lr, o_cntb, o_base,
-        o_act, o_h, o_y, o_xperm, o_upg, o_dng, o_upt, o_dnt, o_ctk, total;
+        o_act, o_h, o_y, o_xperm, o_upg, o_dng, o_upt, o_dnt, o_uprec, total;
 };
 
 constexpr int kDispatchTokens = 64;  // tokens per block of the dispatch (counting-sort) kernels
@@ -86,7 +101,7 @@ inline bool make_plan(const moe_dims& d, Plan* p) {
     p->o_dng = take((size_t)(d.E + 1) * sizeof(GemmGroup));
     p->o_upt = take((size_t)(d.E + 2) * 4);
     p->o_dnt = take((size_t)(d.E + 2) * 4);
-    p->o_ctk = take((size_t)(d.H / 64) * 4);
+    p->o_uprec = take(d.T <= kRecTokens ? P * (size_t)(d.I / 8) * sizeof(UpRec) : 0);
     p->total = o;
     return true;
 }

@@ -39,7 +39,7 @@ struct LayerArgs {
     int32_t* up_tiles;  // [n_groups + 1] first tile of each gate_up group
     int32_t* dn_tiles;
     int32_t* n_groups;
-    uint32_t* comb_ticket;  // [H/64] down items finished per output block (re-armed to 0)
+    UpRec* uprec;     // routed gate_up records (few-token path), nullptr when not produced
     WsHeader* hdr;
     bool gemm;
     int T, H, E, K, I, Is, Imax, ldl, nb;

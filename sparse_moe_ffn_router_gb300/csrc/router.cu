@@ -399,14 +399,17 @@ cudaError_t launch_route_fused(const LayerArgs& a, cudaStream_t s) {
 namespace moe {
 
 // ---------------------------------------------------------------------------------------
-// Few-token routing on one thread-block cluster of 8 CTAs (T <= 64, H <= 2048, E <= 256).
-// CTA c bulk-copies its ~(E+1)/8 rows of [Wr; ws] into shared memory (one TMA bulk copy),
-// scores them for every token, and stores the scores straight into CTA 0's shared memory
+// Few-token routing on one thread-block cluster of 8 CTAs (T <= 8, H <= 2048, E <= 256).
+// CTA c bulk-copies its ~(E+1)/8 rows of [Wr; ws] and the token rows into shared memory (one
+// copy per row, rows 16 bytes apart modulo 128 so ldmatrix is conflict-free), scores them with
+// warp-level bf16 MMAs (m16n8k16, fp32 accumulate; 16 rows by the tokens, K split over the 8
+// warps and summed in a fixed order), and stores the scores straight into CTA 0's shared memory
 // (distributed shared memory). After one cluster barrier CTA 0 runs top-K for all tokens and
 // the dispatch from its own shared memory and writes the routing to global memory.
 
 constexpr int kRouteCluster = 8;
-constexpr int kRouteStageX = 8;  // tokens whose rows are staged in shared memory
+constexpr int kRouteMaxT = 8;
+constexpr int kRoutePad = 16;
 
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -425,10 +428,30 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                  : "memory");
 }
 
+__device__ __forceinline__ void ldsm_x4_r(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_r(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void mma16816_r(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 struct RouteSmem {
-    __host__ __device__ static size_t rows(int E) { return (size_t)(E + 1 + kRouteCluster - 1) / kRouteCluster; }
+    __host__ __device__ static int rows(int E) { return (E + 1 + kRouteCluster - 1) / kRouteCluster; }
+    __host__ __device__ static int mtiles(int E) { return (rows(E) + 15) / 16; }
     static size_t bytes(int T, int H, int E, int ldl) {
-        return 128 + rows(E) * H * 2 + (T <= kRouteStageX ? (size_t)T * H * 2 : 0) + (size_t)T * ldl * 4 + 64;
+        const size_t pitch = (size_t)H * 2 + kRoutePad;
+        return 128 + (size_t)(rows(E) + kRouteMaxT) * pitch + (size_t)T * ldl * 4 +
+               (size_t)8 * mtiles(E) * 128 * 4 + 64;
     }
 };
 
@@ -436,71 +459,91 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int cnt[256];
     __shared__ int off[257];
-    __shared__ int sids[kFusedRouteTokens * 8];
-    __shared__ int slr[kFusedRouteTokens * 8];
+    __shared__ int sids[kRouteMaxT * 8];
+    __shared__ int slr[kRouteMaxT * 8];
+    __shared__ int sperm[kRouteMaxT * 8];
+    __shared__ int sact[256];
+    __shared__ int s_nact;
     __shared__ uint64_t bar;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;  // == rank in the (single) cluster
-    const int R = (int)RouteSmem::rows(a.E);
-    const int r0 = c * R, r1 = min(a.E + 1, r0 + R);
+    const int R = RouteSmem::rows(a.E), MT = RouteSmem::mtiles(a.E);
+    const int r0 = c * R, r1 = min(a.E + 1, r0 + R), nr = max(r1 - r0, 0);
+    const int pitch = a.H * 2 + kRoutePad;
     const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem_raw);
     uint8_t* p = smem_raw + (((base + 127u) & ~127u) - base);
-    bf16* wsm = reinterpret_cast<bf16*>(p);
-    p += (size_t)R * a.H * 2;
-    bf16* xsm = reinterpret_cast<bf16*>(p);
-    const bool stage_x = a.T <= kRouteStageX;
-    if (stage_x) p += (size_t)a.T * a.H * 2;
-    float* lg = reinterpret_cast<float*>(p);  // [T, ldl] scores, used in CTA 0
+    uint8_t* wsm = p;                                   // [R rows][pitch]
+    uint8_t* xsm = p + (size_t)R * pitch;               // [kRouteMaxT rows][pitch]
+    float* lg = reinterpret_cast<float*>(xsm + (size_t)kRouteMaxT * pitch);  // [T, ldl] (CTA 0)
+    float* red = lg + (size_t)a.T * a.ldl;              // [8 warps][MT][32 lanes][4]
 
-    // 1. bulk-copy this CTA's rows (routed rows are contiguous; row E is the shared gate)
+    // 1. one bulk copy per row: this CTA's rows of [Wr; ws] (row E is the shared gate), tokens
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
         fence_mbar_init();
-        const int rr1 = min(r1, a.E);
-        const uint32_t bytes = (uint32_t)((max(rr1 - r0, 0) + (r1 > a.E ? 1 : 0)) * a.H * 2 +
-                                          (stage_x ? a.T * a.H * 2 : 0));
-        mbar_arrive_expect_tx(&bar, bytes);
-        if (rr1 > r0) bulk_g2s(wsm, a.router_w + (size_t)r0 * a.H, (uint32_t)((rr1 - r0) * a.H * 2), &bar);
-        if (r1 > a.E) bulk_g2s(wsm + (size_t)(a.E - r0) * a.H, a.sg, (uint32_t)(a.H * 2), &bar);
-        if (stage_x) bulk_g2s(xsm, a.x, (uint32_t)(a.T * a.H * 2), &bar);
+        mbar_arrive_expect_tx(&bar, (uint32_t)((nr + a.T) * a.H * 2));
     }
     __syncthreads();
+    if (warp == 0) {
+        for (int i = lane; i < nr + a.T; i += 32) {
+            const bf16* src;
+            uint8_t* dst;
+            if (i < nr) {
+                const int r = r0 + i;
+                src = r < a.E ? a.router_w + (size_t)r * a.H : a.sg;
+                dst = wsm + (size_t)i * pitch;
+            } else {
+                src = a.x + (size_t)(i - nr) * a.H;
+                dst = xsm + (size_t)(i - nr) * pitch;
+            }
+            bulk_g2s(dst, src, (uint32_t)(a.H * 2), &bar);
+        }
+    }
     bool ok = mbar_wait(&bar, 0);
     if (!ok) atomicOr(&a.hdr->err, ERR_TIMEOUT);
-    const bf16* xs = stage_x ? xsm : a.x;
-    // 2. scores of this CTA's rows, stored into CTA 0's shared memory
-    for (int r = r0 + warp; r < r1 && ok; r += 8) {
-        const bf16* wrow = wsm + (size_t)(r - r0) * a.H;
-        const float bias = (r < a.E && a.router_b) ? __bfloat162float(a.router_b[r]) : 0.f;
-        for (int t0 = 0; t0 < a.T; t0 += kRouterTokens) {
-            const int mt = min(kRouterTokens, a.T - t0);
-            float acc[kRouterTokens];
-#pragma unroll
-            for (int i = 0; i < kRouterTokens; ++i) acc[i] = 0.f;
+
+    // 2. scores: warp w sums K range [w*H/8, (w+1)*H/8) for every 16-row tile and the tokens
+    if (ok) {
+        const int kw = a.H / 8, k0 = warp * kw;
+        const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(wsm);
+        const uint32_t xbase = (uint32_t)__cvta_generic_to_shared(xsm);
+        const uint32_t b_lane = xbase + (uint32_t)((lane & 7) * pitch + (k0 + 8 * ((lane >> 3) & 1)) * 2);
+        for (int mt = 0; mt < MT; ++mt) {
+            int row = mt * 16 + (lane & 15);
+            row = row < nr ? row : 0;  // rows past this CTA's share read row 0; their results are dropped
+            const uint32_t a_lane = wbase + (uint32_t)(row * pitch + (k0 + 8 * (lane >> 4)) * 2);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-            for (int ch = lane; ch < a.H / 8; ch += 32) {
-                float wf[8];
-                unpack8(*reinterpret_cast<const uint4*>(wrow + (size_t)ch * 8), wf);
-#pragma unroll
-                for (int tt = 0; tt < kRouterTokens; ++tt) {
-                    if (tt < mt) {
-                        const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)(t0 + tt) * a.H + (size_t)ch * 8);
-                        float s = acc[tt];
-                        s = fmaf(wf[0], bf_lo(xv.x), s); s = fmaf(wf[1], bf_hi(xv.x), s);
-                        s = fmaf(wf[2], bf_lo(xv.y), s); s = fmaf(wf[3], bf_hi(xv.y), s);
-                        s = fmaf(wf[4], bf_lo(xv.z), s); s = fmaf(wf[5], bf_hi(xv.z), s);
-                        s = fmaf(wf[6], bf_lo(xv.w), s); s = fmaf(wf[7], bf_hi(xv.w), s);
-                        acc[tt] = s;
-                    }
-                }
+            for (int k = 0; k < kw / 16; ++k) {
+                uint32_t a0, a1, a2, a3, b0, b1;
+                ldsm_x4_r(a_lane + k * 32, a0, a1, a2, a3);
+                ldsm_x2_r(b_lane + k * 32, b0, b1);
+                mma16816_r(d, a0, a1, a2, a3, b0, b1);
             }
+            *reinterpret_cast<float4*>(red + ((size_t)(warp * MT + mt) * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
+        }
+    }
+    __syncthreads();
+    // fixed-order sum over the 8 warps; lane l of tile mt holds rows mt*16 + l/4 (+8), tokens
+    // 2*(l%4) (+1); the score goes to CTA 0's shared memory
+    if (ok) {
+        for (int idx = threadIdx.x; idx < MT * 32; idx += 256) {
+            const int mt = idx >> 5, l = idx & 31;
+            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int w = 0; w < 8; ++w) {
+                const float4 v = *reinterpret_cast<const float4*>(red + ((size_t)(w * MT + mt) * 32 + l) * 4);
+                s4.x += v.x; s4.y += v.y; s4.z += v.z; s4.w += v.w;
+            }
+            const float vals[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-            for (int tt = 0; tt < kRouterTokens; ++tt) {
-                if (tt < mt) {
-                    const float s = warp_sum(acc[tt]) + bias;
-                    if (lane == 0)
-                        st_cluster_f32((uint32_t)__cvta_generic_to_shared(lg + (size_t)(t0 + tt) * a.ldl + r), 0, s);
+            for (int q = 0; q < 4; ++q) {
+                const int rl = mt * 16 + (l >> 2) + (q >= 2 ? 8 : 0);
+                const int t = 2 * (l & 3) + (q & 1);
+                if (rl < nr && t < a.T) {
+                    const int r = r0 + rl;
+                    const float bias = (r < a.E && a.router_b) ? __bfloat162float(a.router_b[r]) : 0.f;
+                    st_cluster_f32((uint32_t)__cvta_generic_to_shared(lg + (size_t)t * a.ldl + r), 0, vals[q] + bias);
                 }
             }
         }
@@ -618,13 +661,17 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
             const int e = lane * 8 + j;
             if (e < a.E) {
                 off[e] = pos;
-                if (loc[j] > 0) a.act[apos++] = e;
+                if (loc[j] > 0) {
+                    sact[apos] = e;
+                    a.act[apos++] = e;
+                }
             }
             pos += loc[j];
         }
         if (lane == 31) {
             off[a.E] = incl;
             a.hdr->n_act = inz;
+            s_nact = inz;
         }
     }
     __syncthreads();
@@ -636,11 +683,30 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
         const int j = off[sids[i]] + slr[i];
         a.perm[j] = i;
         a.inv[i] = j;
+        sperm[j] = i;
     }
+    if (!a.uprec) return;
+    __syncthreads();
+    // gate_up work records of the routed experts: expert, first h row, 8 features, tokens
+    const int fbs = a.I / 8, n = s_nact;
+    for (int idx = threadIdx.x; idx < n * fbs; idx += 256) {
+        const int g = idx / fbs, fb = idx - g * fbs;
+        const int e = sact[g];
+        uint32_t toks = 0;
+        for (int j = 0; j < cnt[e]; ++j) toks |= (uint32_t)(sperm[off[e] + j] / a.K) << (4 * j);
+        UpRec rec;
+        rec.e = e;
+        rec.row0 = off[e];
+        rec.f0 = (int16_t)(fb * 8);
+        rec.mt = (int16_t)cnt[e];
+        rec.toks = toks;
+        a.uprec[idx] = rec;
+    }
+    if (threadIdx.x == 0) a.hdr->n_uprec = n * fbs;
 }
 
 bool route_cluster_supported(const LayerArgs& a) {
-    return a.T >= 1 && a.T <= kFusedRouteTokens && a.E <= 256 &&
+    return a.T >= 1 && a.T <= kRouteMaxT && a.E <= 256 && a.H % 128 == 0 &&
            RouteSmem::bytes(a.T, a.H, a.E, a.ldl) <= 200 * 1024;
 }
 

@@ -373,11 +373,206 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up(LayerArgs a) {
 
 // ---------------------------------------------------------------------------------------
 
+// Few tokens (T <= 8, routing from the cluster router): the token rows are staged once per
+// CTA, a stage holds only the 16 weight rows, and up to 3 stages are in flight. Routed items
+// come from the router's work records (one 16-byte load each).
+constexpr int kMaxSt = 3;
+constexpr int kUpStage = 2 * kFps * kPitchH;
+
+struct RingSmall {
+    uint8_t* xs;
+    uint8_t* st[kMaxSt];
+    float* red;
+    StageMeta* meta;
+    uint32_t* toks;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* xbar;
+};
+
+constexpr int kSmallSmemCap = 220 * 1024;
+
+__host__ __device__ inline size_t small_smem_bytes(int T, int nst) {
+    return 1024 + (size_t)T * kPitchH + (size_t)nst * kUpStage + (size_t)nst * kWarps * 128 * 4 +
+           (size_t)nst * (sizeof(StageMeta) + 4) + (2 * nst + 1) * 8 + 64;
+}
+
+__device__ __forceinline__ RingSmall carve_small(uint8_t* raw, int T, int nst) {
+    const uint32_t base = smem_u32(raw);
+    uint8_t* p = raw + (((base + 127u) & ~127u) - base);
+    RingSmall r;
+    r.xs = p;
+    p += (size_t)((T * kPitchH + 127) & ~127);
+    for (int s = 0; s < kMaxSt; ++s) {
+        r.st[s] = p;
+        if (s < nst) p += kUpStage;
+    }
+    r.red = reinterpret_cast<float*>(p);
+    p += (size_t)nst * kWarps * 128 * 4;
+    r.meta = reinterpret_cast<StageMeta*>(p);
+    p += (size_t)nst * sizeof(StageMeta);
+    r.toks = reinterpret_cast<uint32_t*>(p);
+    p += (size_t)nst * 4;
+    p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 7) & ~(uintptr_t)7);
+    r.full = reinterpret_cast<uint64_t*>(p);
+    r.empty = r.full + nst;
+    r.xbar = r.empty + nst;
+    return r;
+}
+
+__global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up_small(LayerArgs a, int nst) {
+    extern __shared__ uint8_t smem_raw[];
+    RingSmall r = carve_small(smem_raw, a.T, nst);
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t* err = &a.hdr->err;
+    const int pitch = 2 * a.H + kPad;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(&r.full[s], 1);
+            mbar_init(&r.empty[s], kWarps);
+        }
+        mbar_init(r.xbar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int n_shared = a.Is / kFps;  // one token tile: all T tokens
+
+    if (warp == kWarps) {
+        // ---------------- producer: the token rows once, then 16 weight rows per item
+        if (lane == 0) mbar_arrive_expect_tx(r.xbar, (uint32_t)(a.T * a.H * 2));
+        __syncwarp();
+        if (lane < a.T) bulk_load(r.xs + (size_t)lane * pitch, a.x + (size_t)lane * a.H, a.H * 2, r.xbar);
+        int it = 0, n_items = -1;
+        for (int i = blockIdx.x;; i += gridDim.x) {
+            if (i >= n_shared && n_items < 0) {
+                grid_dep_wait();
+                n_items = n_shared + *(volatile int*)&a.hdr->n_uprec;
+            }
+            if (n_items >= 0 && i >= n_items) break;
+            if (__shfl_sync(0xffffffffu, *(volatile int*)&abort_flag, 0)) break;
+            const bf16* W;
+            int inner, row0, f0, mt;
+            uint32_t toks;
+            if (i < n_shared) {
+                W = a.sgu;
+                inner = a.Is;
+                row0 = (int)a.P;
+                f0 = i * kFps;
+                mt = a.T;
+                toks = 0x76543210u;
+            } else {
+                const UpRec rec = a.uprec[i - n_shared];
+                W = a.gate_up + (size_t)rec.e * 2 * a.I * a.H;
+                inner = a.I;
+                row0 = rec.row0;
+                f0 = rec.f0;
+                mt = rec.mt;
+                toks = rec.toks;
+            }
+            const int s = it % nst;
+            bool ok = lane == 0 ? mbar_wait(&r.empty[s], (((uint32_t)(it / nst)) & 1u) ^ 1u) : true;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    atomicOr(err, ERR_TIMEOUT);
+                    abort_flag = 1;
+                }
+                break;
+            }
+            if (lane == 0) {
+                StageMeta& m = r.meta[s];
+                m.mt = mt;
+                m.row0 = row0;
+                m.f0 = f0;
+                r.toks[s] = toks;
+                mbar_arrive_expect_tx(&r.full[s], (uint32_t)(2 * kFps * a.H * 2));
+            }
+            __syncwarp();
+            copy_rows(r.st[s], pitch, W + (size_t)f0 * a.H, a.H, kFps, a.H * 2, &r.full[s], lane);
+            copy_rows(r.st[s] + kFps * pitch, pitch, W + (size_t)(inner + f0) * a.H, a.H, kFps, a.H * 2, &r.full[s],
+                      lane);
+            ++it;
+        }
+        if (lane == 0) {
+            for (int k = 0; k < nst && it - 1 - k >= 0; ++k) {
+                const int j = it - 1 - k;
+                if (!mbar_wait(&r.full[j % nst], ((uint32_t)(j / nst)) & 1u)) atomicOr(err, ERR_TIMEOUT);
+            }
+            if (!mbar_wait(r.xbar, 0)) atomicOr(err, ERR_TIMEOUT);
+        }
+        return;
+    }
+
+    // ---------------- consumers: warp w takes K range [w*H/8, (w+1)*H/8) of all 16 rows
+    bool xok = lane == 0 ? mbar_wait(r.xbar, 0) : true;
+    xok = __shfl_sync(0xffffffffu, xok, 0);
+    if (!consumers_all(xok)) {
+        if (threadIdx.x == 0) atomicOr(err, ERR_TIMEOUT);
+        grid_dep_launch();
+        return;
+    }
+    const int kw = a.H / kWarps;
+    int it = 0, n_items = -1;
+    for (int i = blockIdx.x;; i += gridDim.x, ++it) {
+        if (i >= n_shared && n_items < 0) {
+            grid_dep_wait();
+            n_items = n_shared + *(volatile int*)&a.hdr->n_uprec;
+        }
+        if (n_items >= 0 && i >= n_items) break;
+        const int s = it % nst;
+        bool ok = lane == 0 ? mbar_wait(&r.full[s], ((uint32_t)(it / nst)) & 1u) : true;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!consumers_all(ok)) {
+            if (threadIdx.x == 0) atomicOr(err, ERR_TIMEOUT);
+            break;
+        }
+        const int mt = r.meta[s].mt, row0 = r.meta[s].row0, f0 = r.meta[s].f0;
+        const uint32_t toks = r.toks[s];
+        // B operand: lane l addresses token row (l % 8) of this item (rows past mt read row 0)
+        const int tt = lane & 7;
+        const int tok = tt < mt ? (int)((toks >> (4 * tt)) & 15u) : 0;
+        const uint32_t sa = smem_u32(r.st[s]);
+        const uint32_t b_lane = smem_u32(r.xs) + (uint32_t)(tok * pitch + (warp * kw + 8 * ((lane >> 3) & 1)) * 2);
+        const uint32_t a_lane = sa + (uint32_t)((lane & 15) * pitch + (warp * kw + 8 * (lane >> 4)) * 2);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int k = 0; k < kw / 16; ++k) {
+            uint32_t a0, a1, a2, a3, b0, b1;
+            ldsm_x4(a_lane + k * 32, a0, a1, a2, a3);
+            ldsm_x2(b_lane + k * 32, b0, b1);
+            mma16816(d, a0, a1, a2, a3, b0, b1);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&r.empty[s]);
+        float* red = r.red + (size_t)s * kWarps * 128;
+        *reinterpret_cast<float4*>(red + (warp * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
+        consumers_sync();
+        if (warp == 0) {
+            float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float4 v = *reinterpret_cast<const float4*>(red + (w * 32 + lane) * 4);
+                g0 += v.x; g1 += v.y; u0 += v.z; u1 += v.w;
+            }
+            const int f = lane >> 2, t = 2 * (lane & 3);
+            if (t < mt) a.h[(size_t)(row0 + t) * a.Imax + f0 + f] = __float2bfloat16_rn(silu(g0) * u0);
+            if (t + 1 < mt) a.h[(size_t)(row0 + t + 1) * a.Imax + f0 + f] = __float2bfloat16_rn(silu(g1) * u1);
+        }
+    }
+    grid_dep_launch();
+}
+
+// ---------------------------------------------------------------------------------------
+
 __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) {
     extern __shared__ uint8_t smem_raw[];
     Ring r = carve(smem_raw);
     ring_init(r);
-    grid_dep_wait();  // h comes from k_stream_up; the routing from before it
+    // The routing is complete (the gate_up kernel waited for it before it let this kernel
+    // launch); only the h rows come from the gate_up kernel: the producer streams the weights
+    // of its first stages, then waits for that kernel before copying any h row.
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint32_t* err = &a.hdr->err;
     const int n_act = a.hdr->n_act;
@@ -391,7 +586,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
         const int per_block = tiles[n_act] + tiles_s;
         const int n_items = per_block * n_blocks;
         int it = 0;
-        for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+        bool waited = false;
+        int pend_row[kSt], pend_mt[kSt], pend_inner[kSt];
+        for (int i = blockIdx.x;; i += gridDim.x) {
+            // after the first kSt stages (or at the end), wait for h and copy the pending rows
+            if (!waited && (it == kSt || i >= n_items)) {
+                grid_dep_wait();
+                waited = true;
+                for (int q = 0; q < it; ++q)
+                    if (lane < pend_mt[q])
+                        bulk_load(r.st[q] + (size_t)(kRows + lane) * (2 * pend_inner[q] + kPad),
+                                  a.h + (size_t)(pend_row[q] + lane) * a.Imax, pend_inner[q] * 2, &r.full[q]);
+            }
+            if (i >= n_items) break;
             if (__shfl_sync(0xffffffffu, *(volatile int*)&r.misc[0], 0)) break;
             const int blk = i / per_block, k = i - blk * per_block;
             const bf16* W;
@@ -443,9 +650,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
             __syncwarp();
             uint8_t* st = r.st[s];
             copy_rows(st, pitch, W + (size_t)blk * kRows * inner, inner, kRows, inner * 2, &r.full[s], lane);
-            if (lane < mt)
-                bulk_load(st + (size_t)(kRows + lane) * pitch, a.h + (size_t)(hrow0 + lane) * a.Imax, inner * 2,
-                          &r.full[s]);
+            if (waited) {
+                if (lane < mt)
+                    bulk_load(st + (size_t)(kRows + lane) * pitch, a.h + (size_t)(hrow0 + lane) * a.Imax, inner * 2,
+                              &r.full[s]);
+            } else {
+                pend_row[it] = hrow0;
+                pend_mt[it] = mt;
+                pend_inner[it] = inner;
+            }
             ++it;
         }
         if (lane == 0) drain(r, it, err);
@@ -544,7 +757,30 @@ cudaError_t launch_stream_experts(const LayerArgs& a, cudaStream_t s) {
         configured[dev] = true;
     }
     cudaError_t e;
-    MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (e = launch_pdl(k_stream_up, a.num_sms, kStreamSmemBytes, s, a)));
+    if (a.uprec && a.T <= kRecTokens && route_cluster_supported(a)) {
+        // 3 stages in flight while they fit next to the token rows (T <= 2), else 2
+        const int nst = small_smem_bytes(a.T, 3) <= kSmallSmemCap ? 3 : 2;
+        const int bytes = (int)small_smem_bytes(a.T, nst);
+        static bool conf_small[64] = {};
+        if (!conf_small[dev]) {
+            e = cudaFuncSetAttribute(k_stream_up_small, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallSmemCap);
+            if (e != cudaSuccess) return e;
+            conf_small[dev] = true;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(a.num_sms);
+        cfg.blockDim = dim3(kStreamThreads);
+        cfg.dynamicSmemBytes = bytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (e = cudaLaunchKernelEx(&cfg, k_stream_up_small, a, nst)));
+    } else {
+        MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (e = launch_pdl(k_stream_up, a.num_sms, kStreamSmemBytes, s, a)));
+    }
     if (e != cudaSuccess) return e;
     MOE_LAUNCH(MOE_KERNEL_DOWN, s, (e = launch_pdl(k_stream_down, a.num_sms, kStreamSmemBytes, s, a)));
     if (e != cudaSuccess) return e;
