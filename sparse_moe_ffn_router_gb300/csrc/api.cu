@@ -117,6 +117,7 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
     a->dn_tiles = (int32_t*)(base + p->o_dnt);
     a->n_groups = &a->hdr->n_groups;
     a->uprec = p->T <= kRecTokens ? (UpRec*)(base + p->o_uprec) : nullptr;
+    a->dflags = (uint32_t*)(base + p->o_dflags);
     a->gemm = p->gemm;
     a->T = p->T; a->H = p->H; a->E = p->E; a->K = p->K; a->I = p->I; a->Is = p->Is;
     a->Imax = p->Imax; a->ldl = p->ldl; a->nb = p->nb; a->P = p->P;
@@ -187,6 +188,7 @@ extern "C" moe_status moe_forward(const moe_dims* d, const void* x, const moe_we
     a.residual = (const bf16*)residual;
     a.out = (bf16*)out;
     cudaStream_t s = (cudaStream_t)stream;
+    if (decode_fused_supported(a)) return cuda_status(launch_decode_fused(a, s));  // whole layer, one launch
     cudaError_t e = launch_routing(a, s);
     if (a.gemm) {
         if (e == cudaSuccess) e = launch_gemm_prep(a, s);

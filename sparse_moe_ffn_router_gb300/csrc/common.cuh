@@ -22,7 +22,10 @@ struct WsHeader {
     int32_t n_groups;  // GEMM groups: n_act routed experts + the shared expert
     uint32_t route_ticket;  // CTAs of the fused routing kernel that finished (re-armed to 0)
     int32_t n_uprec;        // routed gate_up work records written by the few-token router
-    uint32_t pad[59];
+    uint32_t dec_flag;      // fused decode kernel: routing published for call number dec_epoch + 1
+    uint32_t dec_epoch;     // fused decode kernel: calls completed on this workspace
+    uint32_t dec_final;     // fused decode kernel: CTAs finished (re-armed to 0)
+    uint32_t pad[56];
 };
 
 // One routed gate_up work item of the few-token path (T <= 8), written by the router: expert,
@@ -59,7 +62,7 @@ struct Plan {
     int nb;          // token blocks of the dispatch
     bool gemm;       // many-token path (tensor-core GEMMs, bf16 Y) instead of weight streaming
     size_t o_hdr, o_logits, o_ids, o_topw, o_sgate, o_counts, o_offsets, o_perm, o_inv, o_lr, o_cntb, o_base,
-        o_act, o_h, o_y, o_xperm, o_upg, o_dng, o_upt, o_dnt, o_uprec, total;
+        o_act, o_h, o_y, o_xperm, o_upg, o_dng, o_upt, o_dnt, o_uprec, o_dflags, total;
 };
 
 constexpr int kDispatchTokens = 64;  // tokens per block of the dispatch (counting-sort) kernels
@@ -102,6 +105,7 @@ inline bool make_plan(const moe_dims& d, Plan* p) {
     p->o_upt = take((size_t)(d.E + 2) * 4);
     p->o_dnt = take((size_t)(d.E + 2) * 4);
     p->o_uprec = take(d.T <= kRecTokens ? P * (size_t)(d.I / 8) * sizeof(UpRec) : 0);
+    p->o_dflags = take((size_t)(d.E + 1 + d.H / 32) * 4);
     p->total = o;
     return true;
 }

@@ -40,6 +40,7 @@ struct LayerArgs {
     int32_t* dn_tiles;
     int32_t* n_groups;
     UpRec* uprec;     // routed gate_up records (few-token path), nullptr when not produced
+    uint32_t* dflags; // fused decode counters: [E+1] gate_up completions, [H/32] combine tickets
     WsHeader* hdr;
     bool gemm;
     int T, H, E, K, I, Is, Imax, ldl, nb;
@@ -81,6 +82,8 @@ cudaError_t launch_gemm_prep(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_combine_pdl(const LayerArgs& a, cudaStream_t s);
 bool stream_supported(const LayerArgs& a);
+bool decode_fused_supported(const LayerArgs& a);
+cudaError_t launch_decode_fused(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_stream_experts(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_experts(const LayerArgs& a, cudaStream_t s);

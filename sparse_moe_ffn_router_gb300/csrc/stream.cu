@@ -24,6 +24,7 @@
 //                group. The fixed-order combine runs next as its own kernel (launched as a
 //                programmatic dependent, so its launch overlaps this kernel's tail).
 #include "launch.h"
+#include "ring.cuh"
 #include "sm100.cuh"
 
 namespace moe {
@@ -32,9 +33,9 @@ constexpr int kSt = 2;                  // ring stages
 constexpr int kTT = 8;                  // tokens per item (the MMA's N)
 constexpr int kFps = 8;                 // up: features per stage (16 rows: 8 gate + 8 up)
 constexpr int kRows = 64;               // down: output rows per stage (= combine block)
-constexpr int kConsumers = 256;         // 8 consumer warps
-constexpr int kWarps = kConsumers / 32;
-constexpr int kStreamThreads = kConsumers + 32;
+
+
+
 constexpr int kPad = 16;                // row padding: rows start 16 B apart modulo 128 B
 constexpr int kMaxH = 2048, kMaxInner = 512;
 constexpr int kPitchH = 2 * kMaxH + kPad, kPitchI = 2 * kMaxInner + kPad;
@@ -83,52 +84,6 @@ __device__ __forceinline__ Ring carve(uint8_t* raw) {
     r.empty = r.full + kSt;
     r.misc = reinterpret_cast<int*>(r.empty + kSt);
     return r;
-}
-
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
-
-// Barrier of the consumer warps that ANDs a predicate over them, so all consumers take the same
-// branch after a bounded wait (none is left behind in a named barrier).
-__device__ __forceinline__ bool consumers_all(bool ok) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)ok), "n"(kConsumers)
-        : "memory");
-    return r != 0;
-}
-
-// ---------------------------------------------------------------------------------------
-// Warp-level bf16 MMA (m16n8k16, fp32 accumulate) fed by ldmatrix from padded rows.
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // D[16 x 8] += A[16 rows, k0 .. k0+16*ksteps) . B[8 rows, same k]^T, rows `pitch` bytes apart.
