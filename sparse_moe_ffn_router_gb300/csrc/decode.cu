@@ -23,9 +23,11 @@
 //  * a down item (32 output rows of one expert) streams its weights as soon as the routing is
 //    known, and copies its h rows only once the expert's counter is complete (acquire, then an
 //    async-proxy fence). It writes Y[t, slot] = scale * (h . Wd^T).
-//  * the CTA whose down item completes an output block (acq_rel ticket, checked one item later
-//    so nobody waits on the atomic) sums that block in the fixed order residual, shared,
-//    slot 0..K-1 and writes out.
+//  * the CTA whose down item completes an output block (release ticket, its value checked one
+//    item later so nobody waits on the atomic; the last one fences before reading) sums that
+//    block in the fixed order residual, shared, slot 0..K-1 and writes out.
+// Only the producer warp polls flags (with backoff); the consumer warps learn everything,
+// including the end of the work, from the stage metadata behind the stage barrier.
 // The launch is cooperative, so all CTAs are resident and the ordering argument holds. The last
 // CTA to finish re-arms every counter for the next call on the same workspace.
 #include "launch.h"
@@ -42,7 +44,7 @@ constexpr int kDnRows = 32;                     // down rows per item = combine 
 constexpr int kDMaxSt = 3;
 static_assert(kDnRows * (2 * kDMaxI + 16) + kDTT * (2 * kDMaxI + 16) <= kDStage, "down stage must fit");
 
-enum { kItemRoute = 0, kItemUp = 1, kItemDown = 2 };
+enum { kItemRoute = 0, kItemUp = 1, kItemDown = 2, kItemEnd = 3 };
 
 struct DMeta {
     int type;
@@ -52,6 +54,7 @@ struct DMeta {
     int inner;     // down: row length of Wd (I or Is)
     int grp;       // up: counter slot (expert id, E = shared)
     int block;     // down: output block
+    int nact;      // down: experts with rows (a block is complete after nact + 1 items)
     uint32_t toks; // up: token of each of its mt rows, 4 bits each
     int tok[kDTT], slot[kDTT];
     float sc[kDTT];
@@ -447,6 +450,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
                     m.f0 = blk * kDnRows;
                     m.inner = inner;
                     m.block = blk;
+                    m.nact = n_act;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive_expect_tx(&r.full[s], (uint32_t)((kDnRows + mt) * inner * 2));
@@ -472,6 +476,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
             atomicOr(err, ERR_TIMEOUT);
             s_flag[0] = 1;
         }
+        // end marker: one more stage whose metadata says there is no more work
+        if (lane == 0) {
+            const int s = it % nst;
+            if (mbar_wait(&r.empty[s], (((uint32_t)(it / nst)) & 1u) ^ 1u)) {
+                r.meta[s].type = kItemEnd;
+                mbar_arrive(&r.full[s]);
+            } else {
+                atomicOr(err, ERR_TIMEOUT);
+            }
+        }
         // every copy issued must land before the CTA releases its shared memory
         if (lane == 0) {
             for (int k = 0; k < nst && it - 1 - k >= 0; ++k) {
@@ -487,22 +501,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
     bool xok = lane == 0 ? mbar_wait(r.xbar, 0) : true;
     xok = __shfl_sync(0xffffffffu, xok, 0);
     xok = consumers_all(xok);
-    int it = 0, n_items = -1, n_u = 0, n_act = 0;
     int pend_blk = -1;          // down item whose combine ticket is still in flight
     uint32_t pend_old = 0;      // (thread 0) the ticket's previous value
-    for (int i = blockIdx.x; xok; i += gridDim.x, ++it) {
-        if (i >= kRouteItems + n_s && n_items < 0) {
-            bool ok = lane == 0 ? wait_at_least(fl.route_flag, epoch + 1) : true;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!consumers_all(ok)) {
-                if (threadIdx.x == 0) atomicOr(err, ERR_TIMEOUT);
-                break;
-            }
-            n_u = *(volatile int*)&a.hdr->n_uprec;
-            n_act = *(volatile int*)&a.hdr->n_act;
-            n_items = kRouteItems + n_s + n_u + (n_act + 1) * n_blocks;
-        }
-        if (n_items >= 0 && i >= n_items) break;
+    int pend_need = 0;          // tickets that complete that block
+    for (int it = 0; xok; ++it) {
         const int s = it % nst;
         bool ok = lane == 0 ? mbar_wait(&r.full[s], ((uint32_t)(it / nst)) & 1u) : true;
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -512,9 +514,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
         }
         const DMeta& m = r.meta[s];
         const int type = m.type, mt = m.mt;
+        if (type == kItemEnd) break;
         const uint32_t sa = smem_u32(r.st[s]);
         float* red = r.red + (size_t)s * kWarps * 128;
-        int combine_now = -1;
+        int combine_now = -1, pend_need_next = 0;
         if (type == kItemRoute) {
             const int row0 = m.row0;
             const int tt = lane & 7;
@@ -578,6 +581,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
             }
         } else {
             const int inner = m.inner, f0 = m.f0, blk = m.block;
+            pend_need_next = m.nact;
             const int dp = 2 * inner + 16;
             const int mtile = warp & 1, kq = warp >> 1;  // 2 row tiles x 4 K quarters
             const int kqlen = inner / 4;
@@ -624,10 +628,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
         if (pend_blk >= 0) {
             if (threadIdx.x == 0) {
                 s_flag[1] = (int)pend_old;
-                if ((int)pend_old == n_act) __threadfence();  // acquire the other CTAs' Y rows
+                if ((int)pend_old == pend_need) __threadfence();  // acquire the other CTAs' Y rows
             }
             consumers_sync();
-            if (s_flag[1] == n_act) decode_combine_block(a, pend_blk);
+            if (s_flag[1] == pend_need) decode_combine_block(a, pend_blk);
             consumers_sync();
             pend_blk = -1;
         }
@@ -635,15 +639,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
             // release-only ticket: its value is read one item later, when it has long returned
             if (threadIdx.x == 0) pend_old = atom_release_add(&fl.comb[combine_now], 1u);
             pend_blk = combine_now;
+            pend_need = pend_need_next;
         }
     }
     if (pend_blk >= 0) {
         if (threadIdx.x == 0) {
             s_flag[1] = (int)pend_old;
-            if ((int)pend_old == n_act) __threadfence();
+            if ((int)pend_old == pend_need) __threadfence();
         }
         consumers_sync();
-        if (s_flag[1] == n_act) decode_combine_block(a, pend_blk);
+        if (s_flag[1] == pend_need) decode_combine_block(a, pend_blk);
     }
     // the last CTA to finish re-arms the counters for the next call on this workspace
     consumers_sync();

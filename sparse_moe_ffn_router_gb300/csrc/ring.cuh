@@ -89,13 +89,16 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Poll until *p >= target (acquire); false after ~1 s.
+// Poll until *p >= target (acquire), backing off from 32 ns to 1 us between polls so that
+// many waiters do not hammer one L2 line; false after ~1 s.
 __device__ __forceinline__ bool wait_at_least(const uint32_t* p, uint32_t target) {
     if (ld_acquire(p) >= target) return true;
     const uint64_t t0 = global_ns();
+    uint32_t ns = 32;
     for (;;) {
-        __nanosleep(128);
+        __nanosleep(ns);
         if (ld_acquire(p) >= target) return true;
+        if (ns < 1024) ns <<= 1;
         if (global_ns() - t0 > 1000000000ull) return false;
     }
 }
