@@ -476,8 +476,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
             atomicOr(err, ERR_TIMEOUT);
             s_flag[0] = 1;
         }
-        // end marker: one more stage whose metadata says there is no more work
         if (lane == 0) {
+            // every copy issued must land before the CTA releases its shared memory (checked
+            // before the end marker below reuses a stage slot)
+            for (int k = 0; k < nst && it - 1 - k >= 0; ++k) {
+                const int j = it - 1 - k;
+                if (!mbar_wait(&r.full[j % nst], ((uint32_t)(j / nst)) & 1u)) atomicOr(err, ERR_TIMEOUT);
+            }
+            if (!mbar_wait(r.xbar, 0)) atomicOr(err, ERR_TIMEOUT);
+            // end marker: one more stage whose metadata says there is no more work
             const int s = it % nst;
             if (mbar_wait(&r.empty[s], (((uint32_t)(it / nst)) & 1u) ^ 1u)) {
                 r.meta[s].type = kItemEnd;
@@ -485,14 +492,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
             } else {
                 atomicOr(err, ERR_TIMEOUT);
             }
-        }
-        // every copy issued must land before the CTA releases its shared memory
-        if (lane == 0) {
-            for (int k = 0; k < nst && it - 1 - k >= 0; ++k) {
-                const int j = it - 1 - k;
-                if (!mbar_wait(&r.full[j % nst], ((uint32_t)(j / nst)) & 1u)) atomicOr(err, ERR_TIMEOUT);
-            }
-            if (!mbar_wait(r.xbar, 0)) atomicOr(err, ERR_TIMEOUT);
         }
         return;
     }
