@@ -6,30 +6,25 @@
 // -> sum. Separate kernels would drain and refill the GPU at every step. Here one CTA per SM
 // walks one global, ordered list of work items:
 //
-//   [24 router items] [shared-expert gate_up items] [routed gate_up items] [down items]
+//   [24 router items] [shared gate_up] [shared down] [routed gate_up] [routed down]
 //
-// (item i belongs to CTA i mod gridDim). A producer warp streams each item's weight rows into a
-// ring of shared-memory stages with 1-D TMA bulk copies (one per row, 16 bytes apart modulo 128
-// so ldmatrix is conflict-free) while 8 consumer warps multiply the previous stage with
-// warp-level bf16 MMAs (m16n8k16, fp32 accumulate; weight rows x up to 8 tokens, K split over
-// the warps and summed in a fixed order). The token rows are staged once per CTA.
-//
-// Dependencies, all on lower-numbered items, all waits bounded (~1 s, then MOE_ERR_TIMEOUT):
-//  * router items score 11 rows of [Wr; ws] each; the CTA that finishes the last one (an
-//    acq_rel ticket, nobody waits) runs top-K, the dispatch and the gate_up work records, then
-//    publishes a routing flag (release). Shared-expert items need nothing and run meanwhile.
-//  * routed gate_up items wait for the routing flag; each finished item adds 1 (release) to its
-//    expert's counter.
-//  * a down item (32 output rows of one expert) streams its weights as soon as the routing is
-//    known, and copies its h rows only once the expert's counter is complete (acquire, then an
-//    async-proxy fence). It writes Y[t, slot] = scale * (h . Wd^T).
-//  * the CTA whose down item completes an output block (release ticket, its value checked one
-//    item later so nobody waits on the atomic; the last one fences before reading) sums that
-//    block in the fixed order residual, shared, slot 0..K-1 and writes out.
-// Only the producer warp polls flags (with backoff); the consumer warps learn everything,
-// including the end of the work, from the stage metadata behind the stage barrier.
-// The launch is cooperative, so all CTAs are resident and the ordering argument holds. The last
-// CTA to finish re-arms every counter for the next call on the same workspace.
+// (item i belongs to CTA i mod gridDim), so the whole shared expert streams while the router
+// runs. Each CTA has three roles:
+//  * a producer warp streams each item's weight rows into a ring of shared-memory stages with
+//    1-D TMA bulk copies (one per row, 16 bytes apart modulo 128 so ldmatrix is conflict-free),
+//    and the item's activation rows when they are ready;
+//  * 8 consumer warps multiply a stage with warp-level bf16 MMAs (m16n8k16, fp32 accumulate;
+//    weight rows x up to 8 tokens, K split over the warps and summed in a fixed order), write the
+//    results, and hand the finished item to the signaller through a shared-memory queue;
+//  * a signaller warp does every cross-CTA step off the compute path: gpu-scope release counts,
+//    tickets, the routing (top-K, dispatch, work records, then a release flag) when it holds the
+//    last router ticket, and the fixed-order combine of an output block (residual, shared,
+//    slot 0..K-1) when it holds that block's last ticket.
+// Dependencies point only to lower-numbered items, every wait is bounded (~1 s, then
+// MOE_ERR_TIMEOUT), and the launch is cooperative (all CTAs resident). Routed gate_up items wait
+// for the routing flag; a down item streams its weights at once and copies its h rows only when
+// its expert's gate_up count is complete (acquire, then an async-proxy fence). The last CTA to
+// finish re-arms the counters for the next call on the same workspace.
 #include "launch.h"
 #include "ring.cuh"
 
@@ -45,6 +40,13 @@ constexpr int kDMaxSt = 3;
 static_assert(kDnRows * (2 * kDMaxI + 16) + kDTT * (2 * kDMaxI + 16) <= kDStage, "down stage must fit");
 
 enum { kItemRoute = 0, kItemUp = 1, kItemDown = 2, kItemEnd = 3 };
+constexpr int kDThreads = kConsumers + 64;  // 8 consumer warps, the producer, the signaller
+constexpr int kProducerWarp = kWarps, kSignalWarp = kWarps + 1;
+constexpr int kQ = 4;                       // signaller queue entries
+
+struct Event {
+    int type, grp, blk, need;
+};
 
 struct DMeta {
     int type;
@@ -65,14 +67,17 @@ struct DSmem {
     uint8_t* st[kDMaxSt];
     float* red;
     DMeta* meta;
+    Event* ev;
     uint64_t* full;
     uint64_t* empty;
     uint64_t* xbar;
+    uint64_t* evfull;
+    uint64_t* evempty;
 };
 
 __host__ __device__ inline size_t decode_smem_bytes(int T, int nst) {
     return 1024 + (size_t)((T * kDPitchH + 127) & ~127) + (size_t)nst * kDStage + (size_t)nst * kWarps * 128 * 4 +
-           (size_t)nst * sizeof(DMeta) + (2 * nst + 1) * 8 + 64;
+           (size_t)nst * sizeof(DMeta) + kQ * sizeof(Event) + (2 * nst + 1 + 2 * kQ) * 8 + 64;
 }
 
 __device__ __forceinline__ DSmem decode_carve(uint8_t* raw, int T, int nst) {
@@ -89,10 +94,14 @@ __device__ __forceinline__ DSmem decode_carve(uint8_t* raw, int T, int nst) {
     p += (size_t)nst * kWarps * 128 * 4;
     r.meta = reinterpret_cast<DMeta*>(p);
     p += (size_t)nst * sizeof(DMeta);
+    r.ev = reinterpret_cast<Event*>(p);
+    p += kQ * sizeof(Event);
     p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 7) & ~(uintptr_t)7);
     r.full = reinterpret_cast<uint64_t*>(p);
     r.empty = r.full + nst;
     r.xbar = r.empty + nst;
+    r.evfull = r.xbar + 1;
+    r.evempty = r.evfull + kQ;
     return r;
 }
 
@@ -136,8 +145,8 @@ __device__ __forceinline__ void stage_mma(float (&d)[4], uint32_t a_rows, int nr
 }
 
 // ---------------------------------------------------------------------------------------
-// Top-K of every token and the dispatch, run by the consumer warps of the CTA that finished
-// the last router item (scores read back from L2).
+// Routing in one warp (the signaller of the CTA that finished the last router item): top-K of
+// every token from the scores in L2, renormalised weights, shared gate, dispatch, work records.
 
 struct RouteScratch {
     int cnt[256];
@@ -146,12 +155,10 @@ struct RouteScratch {
     int slr[kDTT * 8];
     int sperm[kDTT * 8];
     int sact[256];
-    int nact;
 };
 
-__device__ void decode_route(const LayerArgs& a, RouteScratch& rs) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int t = warp; t < a.T; t += kWarps) {
+__device__ void signal_route(const LayerArgs& a, RouteScratch& rs, int lane) {
+    for (int t = 0; t < a.T; ++t) {
         const float* l = a.logits + (size_t)t * a.ldl;
         float v[8];
         bool bad = false;
@@ -218,75 +225,70 @@ __device__ void decode_route(const LayerArgs& a, RouteScratch& rs) {
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&a.hdr->err, ERR_NONFINITE_SCORE);
     }
-    for (int e = threadIdx.x; e < a.E; e += kConsumers) rs.cnt[e] = 0;
-    consumers_sync();
+    for (int e = lane; e < a.E; e += 32) rs.cnt[e] = 0;
+    __syncwarp();
     const int P = (int)a.P;
-    if (warp == 0) {
-        for (int b0 = 0; b0 < P; b0 += 32) {
-            const int i = b0 + lane;
-            const bool valid = i < P;
-            const int e = valid ? rs.sids[i] : -1;
-            const unsigned m = __match_any_sync(0xffffffffu, e);
-            const int rank_in = __popc(m & ((1u << lane) - 1u));
-            const int cc = valid ? rs.cnt[e] : 0;
-            __syncwarp();
-            if (valid) {
-                rs.slr[i] = cc + rank_in;
-                if (rank_in == 0) rs.cnt[e] = cc + __popc(m);
-            }
-            __syncwarp();
+    for (int b0 = 0; b0 < P; b0 += 32) {
+        const int i = b0 + lane;
+        const bool valid = i < P;
+        const int e = valid ? rs.sids[i] : -1;
+        const unsigned m = __match_any_sync(0xffffffffu, e);
+        const int rank_in = __popc(m & ((1u << lane) - 1u));
+        const int cc = valid ? rs.cnt[e] : 0;
+        __syncwarp();
+        if (valid) {
+            rs.slr[i] = cc + rank_in;
+            if (rank_in == 0) rs.cnt[e] = cc + __popc(m);
         }
-        int loc[8], run = 0, nz = 0;
+        __syncwarp();
+    }
+    int loc[8], run = 0, nz = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = lane * 8 + j;
-            loc[j] = e < a.E ? rs.cnt[e] : 0;
-            run += loc[j];
-            nz += loc[j] > 0;
-        }
-        int incl = run, inz = nz;
+    for (int j = 0; j < 8; ++j) {
+        const int e = lane * 8 + j;
+        loc[j] = e < a.E ? rs.cnt[e] : 0;
+        run += loc[j];
+        nz += loc[j] > 0;
+    }
+    int incl = run, inz = nz;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            const int z = __shfl_up_sync(0xffffffffu, inz, o);
-            if (lane >= o) {
-                incl += y;
-                inz += z;
-            }
-        }
-        int pos = incl - run, apos = inz - nz;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = lane * 8 + j;
-            if (e < a.E) {
-                rs.off[e] = pos;
-                if (loc[j] > 0) {
-                    rs.sact[apos] = e;
-                    a.act[apos++] = e;
-                }
-            }
-            pos += loc[j];
-        }
-        if (lane == 31) {
-            rs.off[a.E] = incl;
-            rs.nact = inz;
-            a.hdr->n_act = inz;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        const int z = __shfl_up_sync(0xffffffffu, inz, o);
+        if (lane >= o) {
+            incl += y;
+            inz += z;
         }
     }
-    consumers_sync();
-    for (int e = threadIdx.x; e <= a.E; e += kConsumers) {
+    int pos = incl - run, apos = inz - nz;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int e = lane * 8 + j;
+        if (e < a.E) {
+            rs.off[e] = pos;
+            if (loc[j] > 0) {
+                rs.sact[apos] = e;
+                a.act[apos++] = e;
+            }
+        }
+        pos += loc[j];
+    }
+    const int n_act = __shfl_sync(0xffffffffu, inz, 31);
+    if (lane == 31) rs.off[a.E] = incl;
+    __syncwarp();
+    for (int e = lane; e <= a.E; e += 32) {
         a.offsets[e] = rs.off[e];
         if (e < a.E) a.counts[e] = rs.cnt[e];
     }
-    for (int i = threadIdx.x; i < P; i += kConsumers) {
+    for (int i = lane; i < P; i += 32) {
         const int j = rs.off[rs.sids[i]] + rs.slr[i];
         a.perm[j] = i;
         a.inv[i] = j;
         rs.sperm[j] = i;
     }
-    consumers_sync();
-    const int fbs = a.I / 8, n = rs.nact;
-    for (int idx = threadIdx.x; idx < n * fbs; idx += kConsumers) {
+    __syncwarp();
+    const int fbs = a.I / 8;
+    for (int idx = lane; idx < n_act * fbs; idx += 32) {
         const int g = idx / fbs, fb = idx - g * fbs;
         const int e = rs.sact[g];
         uint32_t toks = 0;
@@ -299,16 +301,23 @@ __device__ void decode_route(const LayerArgs& a, RouteScratch& rs) {
         rec.toks = toks;
         a.uprec[idx] = rec;
     }
-    if (threadIdx.x == 0) a.hdr->n_uprec = n * fbs;
+    if (lane == 0) {
+        a.hdr->n_act = n_act;
+        a.hdr->n_uprec = n_act * fbs;
+    }
+    __syncwarp();
 }
 
-// Fixed-order sum of one output block of 32 rows for every token.
-__device__ __forceinline__ void decode_combine_block(const LayerArgs& a, int blk) {
-    for (int idx = threadIdx.x; idx < a.T * kDnRows; idx += kConsumers) {
+// Fixed-order sum of one output block of 32 rows for every token, by one warp. The shared
+// expert's slot holds its unscaled output; its gate is applied (and stored back) here.
+__device__ void signal_combine_block(const LayerArgs& a, int blk, int lane) {
+    for (int idx = lane; idx < a.T * kDnRows; idx += 32) {
         const int t = idx / kDnRows, o = blk * kDnRows + (idx - t * kDnRows);
-        const float* yt = a.Y + (size_t)t * (a.K + 1) * a.H + o;
+        float* yt = a.Y + (size_t)t * (a.K + 1) * a.H + o;
         float acc = a.residual ? __bfloat162float(a.residual[(size_t)t * a.H + o]) : 0.f;
-        acc += __ldcg(yt + (size_t)a.K * a.H);
+        const float shared = a.sgate[t] * __ldcg(yt + (size_t)a.K * a.H);
+        yt[(size_t)a.K * a.H] = shared;
+        acc += shared;
         for (int k = 0; k < a.K; ++k) acc += __ldcg(yt + (size_t)k * a.H);
         a.out[(size_t)t * a.H + o] = __float2bfloat16_rn(acc);
     }
@@ -316,10 +325,9 @@ __device__ __forceinline__ void decode_combine_block(const LayerArgs& a, int blk
 
 // ---------------------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a, int nst) {
+__global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, int nst) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ RouteScratch rs;
-    __shared__ int s_flag[4];  // [0] abort, [1] verdict broadcast
     DSmem r = decode_carve(smem_raw, a.T, nst);
     const DFlags fl = decode_flags(a);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -327,20 +335,24 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
     const int pitch = 2 * a.H + 16;
     const uint32_t epoch = *(volatile uint32_t*)fl.epoch;
     const int R = (a.E + 1 + kRouteItems - 1) / kRouteItems;  // router rows per item
-    const int n_s = a.Is / 8;
-    const int n_blocks = a.H / kDnRows;
+    const int n_sup = a.Is / 8;          // shared gate_up items (8 features each)
+    const int n_blocks = a.H / kDnRows;  // shared down items (one per output block)
+    const int base_u = kRouteItems + n_sup + n_blocks;
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(&r.full[s], 1);
             mbar_init(&r.empty[s], kWarps);
         }
         mbar_init(r.xbar, 1);
-        s_flag[0] = 0;
+        for (int q = 0; q < kQ; ++q) {
+            mbar_init(&r.evfull[q], 1);
+            mbar_init(&r.evempty[q], 1);
+        }
         fence_mbar_init();
     }
     __syncthreads();
 
-    if (warp == kWarps) {
+    if (warp == kProducerWarp) {
         // ================= producer
         if (lane == 0) mbar_arrive_expect_tx(r.xbar, (uint32_t)(a.T * a.H * 2));
         __syncwarp();
@@ -348,8 +360,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
         int it = 0, n_items = -1, n_u = 0, n_act = 0;
         bool fail = false;
         for (int i = blockIdx.x;; i += gridDim.x) {
-            if (__shfl_sync(0xffffffffu, *(volatile int*)&s_flag[0], 0)) break;
-            if (i >= kRouteItems + n_s && n_items < 0) {
+            if (i >= base_u && n_items < 0) {
                 bool ok = lane == 0 ? wait_at_least(fl.route_flag, epoch + 1) : true;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 __syncwarp();  // orders the other lanes' reads after lane 0's acquire
@@ -359,7 +370,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
                 }
                 n_u = *(volatile int*)&a.hdr->n_uprec;
                 n_act = *(volatile int*)&a.hdr->n_act;
-                n_items = kRouteItems + n_s + n_u + (n_act + 1) * n_blocks;
+                n_items = base_u + n_u + n_act * n_blocks;
             }
             if (n_items >= 0 && i >= n_items) break;
             const int s = it % nst;
@@ -371,6 +382,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
             }
             DMeta& m = r.meta[s];
             uint8_t* st = r.st[s];
+            const bool up = (i >= kRouteItems && i < kRouteItems + n_sup) || (i >= base_u && i < base_u + n_u);
             if (i < kRouteItems) {
                 const int r0 = i * R, nr = max(0, min(a.E + 1, r0 + R) - r0);
                 if (lane == 0) {
@@ -385,11 +397,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
                     bulk_load(st + (size_t)lane * pitch, row < a.E ? a.router_w + (size_t)row * a.H : a.sg, a.H * 2,
                               &r.full[s]);
                 }
-            } else if (i < kRouteItems + n_s + n_u) {
+            } else if (up) {
                 const bf16* W;
                 int inner, row0, f0, mt, grp;
                 uint32_t toks;
-                if (i < kRouteItems + n_s) {
+                if (i < kRouteItems + n_sup) {
                     W = a.sgu;
                     inner = a.Is;
                     row0 = (int)a.P;
@@ -398,7 +410,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
                     toks = 0x76543210u;
                     grp = a.E;
                 } else {
-                    const UpRec rec = a.uprec[i - kRouteItems - n_s];
+                    const UpRec rec = a.uprec[i - base_u];
                     W = a.gate_up + (size_t)rec.e * 2 * a.I * a.H;
                     inner = a.I;
                     row0 = rec.row0;
@@ -422,23 +434,29 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
                 else if (lane < 16)
                     bulk_load(st + (size_t)lane * pitch, W + (size_t)(inner + f0 + lane - 8) * a.H, a.H * 2, &r.full[s]);
             } else {
-                const int d = i - kRouteItems - n_s - n_u;
-                const int blk = d / (n_act + 1), g = d - blk * (n_act + 1);
-                const bool shared = g == n_act;
-                const int e = shared ? a.E : a.act[g];
+                // down item: the shared expert's blocks first (no routing needed), then routed
+                const bool shared = i < base_u;
+                int blk, e;
+                if (shared) {
+                    blk = i - kRouteItems - n_sup;
+                    e = a.E;
+                } else {
+                    const int d = i - base_u - n_u;
+                    blk = d / n_act;
+                    e = a.act[d - blk * n_act];
+                }
                 const int inner = shared ? a.Is : a.I;
                 const bf16* W = shared ? a.sd : a.down + (size_t)e * a.H * a.I;
                 const int hrow0 = shared ? (int)a.P : a.offsets[e];
                 const int mt = shared ? a.T : a.offsets[e + 1] - hrow0;
                 const int dp = 2 * inner + 16;
                 if (lane < mt) {
-                    const int j = hrow0 + lane;
                     if (shared) {
                         m.tok[lane] = lane;
                         m.slot[lane] = a.K;
-                        m.sc[lane] = a.sgate[lane];
+                        m.sc[lane] = 1.f;  // the gate is applied in the combine
                     } else {
-                        const int pv = a.perm[j];
+                        const int pv = a.perm[hrow0 + lane];
                         m.tok[lane] = pv / a.K;
                         m.slot[lane] = pv - (pv / a.K) * a.K;
                         m.sc[lane] = a.topw[pv];
@@ -450,15 +468,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
                     m.f0 = blk * kDnRows;
                     m.inner = inner;
                     m.block = blk;
-                    m.nact = n_act;
+                    m.nact = -1;  // filled by the signaller from the routing
+                    mbar_arrive_expect_tx(&r.full[s], (uint32_t)((kDnRows + mt) * inner * 2));
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_expect_tx(&r.full[s], (uint32_t)((kDnRows + mt) * inner * 2));
                 __syncwarp();
                 bulk_load(st + (size_t)lane * dp, W + (size_t)(blk * kDnRows + lane) * inner, inner * 2, &r.full[s]);
                 // h rows only once this expert's gate_up items are all done
-                const uint32_t target = (uint32_t)(inner / 8);
-                bool hok = lane == 0 ? wait_at_least(&fl.up_done[e], target) : true;
+                bool hok = lane == 0 ? wait_at_least(&fl.up_done[e], (uint32_t)(inner / 8)) : true;
                 hok = __shfl_sync(0xffffffffu, hok, 0);
                 __syncwarp();
                 if (!hok) {
@@ -472,10 +488,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
             }
             ++it;
         }
-        if (fail && lane == 0) {
-            atomicOr(err, ERR_TIMEOUT);
-            s_flag[0] = 1;
-        }
+        if (fail && lane == 0) atomicOr(err, ERR_TIMEOUT);
         if (lane == 0) {
             // every copy issued must land before the CTA releases its shared memory (checked
             // before the end marker below reuses a stage slot)
@@ -484,7 +497,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
                 if (!mbar_wait(&r.full[j % nst], ((uint32_t)(j / nst)) & 1u)) atomicOr(err, ERR_TIMEOUT);
             }
             if (!mbar_wait(r.xbar, 0)) atomicOr(err, ERR_TIMEOUT);
-            // end marker: one more stage whose metadata says there is no more work
             const int s = it % nst;
             if (mbar_wait(&r.empty[s], (((uint32_t)(it / nst)) & 1u) ^ 1u)) {
                 r.meta[s].type = kItemEnd;
@@ -496,27 +508,108 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
         return;
     }
 
+    if (warp == kSignalWarp) {
+        // ================= signaller: cross-CTA counts, tickets, routing and combines
+        bool live = true, routed = false;
+        int n_act_sig = 0;
+        for (int q_it = 0; live; ++q_it) {
+            const int q = q_it % kQ;
+            bool ok = lane == 0 ? mbar_wait(&r.evfull[q], ((uint32_t)(q_it / kQ)) & 1u) : true;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();
+            if (!ok) {
+                if (lane == 0) atomicOr(err, ERR_TIMEOUT);
+                break;
+            }
+            const Event ev = r.ev[q];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&r.evempty[q]);
+            if (ev.type == kItemRoute) {
+                uint32_t old = 0;
+                if (lane == 0) old = atom_acq_rel_add(fl.route_ticket, 1u);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                __syncwarp();
+                if (old == kRouteItems - 1) {
+                    signal_route(a, rs, lane);
+                    if (lane == 0) st_release(fl.route_flag, epoch + 1);
+                }
+            } else if (ev.type == kItemUp) {
+                if (lane == 0) red_release_add(&fl.up_done[ev.grp], 1u);
+            } else if (ev.type == kItemDown) {
+                // a block is complete after the shared item and one item per routed expert; the
+                // expert count comes from the routing (a shared item can finish before it)
+                if (!routed) {
+                    bool ok2 = lane == 0 ? wait_at_least(fl.route_flag, epoch + 1) : true;
+                    ok2 = __shfl_sync(0xffffffffu, ok2, 0);
+                    __syncwarp();
+                    if (!ok2) {
+                        if (lane == 0) atomicOr(err, ERR_TIMEOUT);
+                        break;
+                    }
+                    n_act_sig = *(volatile int*)&a.hdr->n_act;
+                    routed = true;
+                }
+                uint32_t old = 0;
+                if (lane == 0) {
+                    old = atom_release_add(&fl.comb[ev.blk], 1u);
+                    if (old == (uint32_t)n_act_sig) __threadfence();
+                }
+                old = __shfl_sync(0xffffffffu, old, 0);
+                __syncwarp();
+                if (old == (uint32_t)n_act_sig) signal_combine_block(a, ev.blk, lane);
+            } else {
+                live = false;
+            }
+        }
+        // the last CTA to finish re-arms the counters for the next call on this workspace
+        uint32_t fin = 0;
+        if (lane == 0) fin = atom_acq_rel_add(fl.final_ticket, 1u);
+        fin = __shfl_sync(0xffffffffu, fin, 0);
+        if (fin == gridDim.x - 1) {
+            for (int e = lane; e <= a.E; e += 32) fl.up_done[e] = 0;
+            for (int b = lane; b < n_blocks; b += 32) fl.comb[b] = 0;
+            __syncwarp();
+            if (lane == 0) {
+                *fl.route_ticket = 0;
+                *fl.final_ticket = 0;
+                *fl.epoch = epoch + 1;
+            }
+        }
+        return;
+    }
+
     // ================= consumers
     bool xok = lane == 0 ? mbar_wait(r.xbar, 0) : true;
     xok = __shfl_sync(0xffffffffu, xok, 0);
     xok = consumers_all(xok);
-    int pend_blk = -1;          // down item whose combine ticket is still in flight
-    uint32_t pend_old = 0;      // (thread 0) the ticket's previous value
-    int pend_need = 0;          // tickets that complete that block
-    for (int it = 0; xok; ++it) {
+    int q_it = 0;
+    // hand a finished item to the signaller (warp 0, lane 0; after the item's writes)
+    auto push = [&](int type, int grp, int blk) {
+        if (threadIdx.x == 0) {
+            const int q = q_it % kQ;
+            if (!mbar_wait(&r.evempty[q], (((uint32_t)(q_it / kQ)) & 1u) ^ 1u)) atomicOr(err, ERR_TIMEOUT);
+            r.ev[q] = Event{type, grp, blk, 0};
+            mbar_arrive(&r.evfull[q]);
+        }
+        ++q_it;
+    };
+    for (int it = 0;; ++it) {
         const int s = it % nst;
-        bool ok = lane == 0 ? mbar_wait(&r.full[s], ((uint32_t)(it / nst)) & 1u) : true;
+        bool ok = xok && (lane == 0 ? mbar_wait(&r.full[s], ((uint32_t)(it / nst)) & 1u) : true);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!consumers_all(ok)) {
             if (threadIdx.x == 0) atomicOr(err, ERR_TIMEOUT);
+            push(kItemEnd, 0, 0);
             break;
         }
         const DMeta& m = r.meta[s];
         const int type = m.type, mt = m.mt;
-        if (type == kItemEnd) break;
+        if (type == kItemEnd) {
+            push(kItemEnd, 0, 0);
+            break;
+        }
         const uint32_t sa = smem_u32(r.st[s]);
         float* red = r.red + (size_t)s * kWarps * 128;
-        int combine_now = -1, pend_need_next = 0;
         if (type == kItemRoute) {
             const int row0 = m.row0;
             const int tt = lane & 7;
@@ -531,8 +624,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
                 float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) {
-                    const float4 q = *reinterpret_cast<const float4*>(red + (w * 32 + lane) * 4);
-                    v[0] += q.x; v[1] += q.y; v[2] += q.z; v[3] += q.w;
+                    const float4 q4 = *reinterpret_cast<const float4*>(red + (w * 32 + lane) * 4);
+                    v[0] += q4.x; v[1] += q4.y; v[2] += q4.z; v[3] += q4.w;
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -544,15 +637,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
                     }
                 }
                 __syncwarp();
-                if (lane == 0) s_flag[1] = (int)atom_acq_rel_add(fl.route_ticket, 1u);
             }
-            consumers_sync();
-            if (s_flag[1] == kRouteItems - 1) {
-                // last router item: every score is in L2; route all tokens, then publish
-                decode_route(a, rs);
-                consumers_sync();
-                if (threadIdx.x == 0) st_release(fl.route_flag, epoch + 1);
-            }
+            push(kItemRoute, 0, 0);
         } else if (type == kItemUp) {
             const int row0 = m.row0, f0 = m.f0, grp = m.grp;
             const uint32_t toks = m.toks;
@@ -569,18 +655,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
                 float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) {
-                    const float4 q = *reinterpret_cast<const float4*>(red + (w * 32 + lane) * 4);
-                    g0 += q.x; g1 += q.y; u0 += q.z; u1 += q.w;
+                    const float4 q4 = *reinterpret_cast<const float4*>(red + (w * 32 + lane) * 4);
+                    g0 += q4.x; g1 += q4.y; u0 += q4.z; u1 += q4.w;
                 }
                 const int f = lane >> 2, t = 2 * (lane & 3);
                 if (t < mt) a.h[(size_t)(row0 + t) * a.Imax + f0 + f] = __float2bfloat16_rn(silu(g0) * u0);
                 if (t + 1 < mt) a.h[(size_t)(row0 + t + 1) * a.Imax + f0 + f] = __float2bfloat16_rn(silu(g1) * u1);
                 __syncwarp();
-                if (lane == 0) red_release_add(&fl.up_done[grp], 1u);
             }
+            push(kItemUp, grp, 0);
         } else {
             const int inner = m.inner, f0 = m.f0, blk = m.block;
-            pend_need_next = m.nact;
             const int dp = 2 * inner + 16;
             const int mtile = warp & 1, kq = warp >> 1;  // 2 row tiles x 4 K quarters
             const int kqlen = inner / 4;
@@ -620,47 +705,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_decode_fused(LayerArgs a,
                     a.Y[y1 + row + 8] = s1 * v[3];
                 }
             }
-            consumers_sync();
-            combine_now = blk;
-        }
-        // the previous down item's combine verdict (its ticket has long returned)
-        if (pend_blk >= 0) {
-            if (threadIdx.x == 0) {
-                s_flag[1] = (int)pend_old;
-                if ((int)pend_old == pend_need) __threadfence();  // acquire the other CTAs' Y rows
-            }
-            consumers_sync();
-            if (s_flag[1] == pend_need) decode_combine_block(a, pend_blk);
-            consumers_sync();
-            pend_blk = -1;
-        }
-        if (combine_now >= 0) {
-            // release-only ticket: its value is read one item later, when it has long returned
-            if (threadIdx.x == 0) pend_old = atom_release_add(&fl.comb[combine_now], 1u);
-            pend_blk = combine_now;
-            pend_need = pend_need_next;
-        }
-    }
-    if (pend_blk >= 0) {
-        if (threadIdx.x == 0) {
-            s_flag[1] = (int)pend_old;
-            if ((int)pend_old == pend_need) __threadfence();
-        }
-        consumers_sync();
-        if (s_flag[1] == pend_need) decode_combine_block(a, pend_blk);
-    }
-    // the last CTA to finish re-arms the counters for the next call on this workspace
-    consumers_sync();
-    if (threadIdx.x == 0) s_flag[2] = (int)atom_acq_rel_add(fl.final_ticket, 1u);
-    consumers_sync();
-    if (s_flag[2] == (int)gridDim.x - 1) {
-        for (int e = threadIdx.x; e <= a.E; e += kConsumers) fl.up_done[e] = 0;
-        for (int b = threadIdx.x; b < n_blocks; b += kConsumers) fl.comb[b] = 0;
-        consumers_sync();
-        if (threadIdx.x == 0) {
-            *fl.route_ticket = 0;
-            *fl.final_ticket = 0;
-            *fl.epoch = epoch + 1;
+            consumers_sync();  // warp 1's rows are written before warp 0 hands the item over
+            push(kItemDown, 0, blk);
         }
     }
 }
@@ -685,7 +731,7 @@ cudaError_t launch_decode_fused(const LayerArgs& a, cudaStream_t s) {
     const int nst = decode_smem_bytes(a.T, 3) <= (size_t)cap ? 3 : 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.num_sms);
-    cfg.blockDim = dim3(kStreamThreads);
+    cfg.blockDim = dim3(kDThreads);
     cfg.dynamicSmemBytes = decode_smem_bytes(a.T, nst);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
