@@ -49,7 +49,7 @@ UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "decode_T1"
 ROTATE = 8
 KERNEL_NAMES = ["router_scores", "router_topk", "dispatch_local", "dispatch_scan", "dispatch_scatter", "gate_up",
-                "down", "combine", "rmsnorm", "shared_gate", "gather", "gemm_plan"]
+                "down", "combine", "rmsnorm", "shared_gate", "gather", "gemm_plan", "decode_fused"]
 
 
 def parse_args():
@@ -254,9 +254,12 @@ def algorithmic(dims, groups: list[int]) -> dict:
 def trace_kernels(moe, names, n):
     ev = {k: ([torch.cuda.Event(enable_timing=True) for _ in range(n)],
               [torch.cuda.Event(enable_timing=True) for _ in range(n)]) for k in names}
-    for a, b in ev.values():  # torch creates the CUDA event on its first record
-        for e in a + b:
-            e.record()
+    # torch creates the CUDA event on its first record; each start/stop pair is recorded back
+    # to back, so a kernel that never launches reads ~0 ms
+    for a, b in ev.values():
+        for x, y in zip(a, b):
+            x.record()
+            y.record()
     torch.cuda.synchronize()
     for k, (a, b) in ev.items():
         moe.moe_set_trace(k, a, b)

@@ -136,7 +136,8 @@ enum {
     MOE_KERNEL_SHARED_GATE = 9,     /* shared-expert gate scores (many-token path)  */
     MOE_KERNEL_GATHER = 10,         /* token rows in dispatch order (many-token path) */
     MOE_KERNEL_GEMM_PLAN = 11,      /* group/tile tables of the expert GEMMs        */
-    MOE_KERNEL_COUNT = 12
+    MOE_KERNEL_DECODE_FUSED = 12,   /* whole layer in one persistent kernel (T <= 8) */
+    MOE_KERNEL_COUNT = 13
 };
 
 /* Benchmarking aid. While set, every launch of `kernel` made by this library records

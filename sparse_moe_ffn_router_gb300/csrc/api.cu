@@ -117,7 +117,7 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
     a->dn_tiles = (int32_t*)(base + p->o_dnt);
     a->n_groups = &a->hdr->n_groups;
     a->uprec = p->T <= kRecTokens ? (UpRec*)(base + p->o_uprec) : nullptr;
-    a->dflags = (uint32_t*)(base + p->o_dflags);
+    a->dlog = p->T <= kRecTokens ? (uint64_t*)(base + p->o_dlog) : nullptr;
     a->gemm = p->gemm;
     a->T = p->T; a->H = p->H; a->E = p->E; a->K = p->K; a->I = p->I; a->Is = p->Is;
     a->Imax = p->Imax; a->ldl = p->ldl; a->nb = p->nb; a->P = p->P;

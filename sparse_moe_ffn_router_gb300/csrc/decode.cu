@@ -1,738 +1,751 @@
 // decode.cu -- the whole MoE layer for a few tokens (T <= 8) in one persistent kernel.
 //
-// At decode the layer reads ~58 MB of weights per token ("Qwen3.6-35B-A3B -- Architecture
-// Overview", MoE FFN: 256 Experts: router 2048 -> 256, 8 SwiGLU experts of 3 x 512 x 2048, the
-// shared expert), and every step depends on the one before: scores -> top-K -> gate_up -> down
-// -> sum. Separate kernels would drain and refill the GPU at every step. Here one CTA per SM
-// walks one global, ordered list of work items:
+// At decode the layer streams ~55 MB of weights per token ("Qwen3.6-35B-A3B -- Architecture
+// Overview", MoE FFN: router 2048 -> 256 plus the shared-expert gate, 8 routed SwiGLU experts
+// with merged gate_up [1024 x 2048] and down [2048 x 512], one always-on shared expert of the
+// same shape), and every step depends on the one before. One CTA per SM runs the whole layer
+// with two grid-wide exchanges:
 //
-//   [24 router items] [shared gate_up] [shared down] [routed gate_up] [routed down]
+//   1. router rows: CTA c scores its ceil((E+1)/G) rows of the router (the shared-gate row is
+//      row E) for every token and stores each score as one 64-bit word together with the tag
+//      of this call, so a reader recognises fresh scores by their tag (no flag, no fence);
+//   2. shared gate_up: CTA c's even share of the shared expert's features (no routing needed),
+//      computed while the other CTAs' scores arrive;
+//   3. routing: EVERY CTA reads the T x (E+1) tagged scores and computes top-K, the
+//      renormalised weights, the shared gate and the dispatch (counts, offsets, permutation)
+//      itself. All CTAs derive the same tables, so no second exchange is needed for them;
+//   4. routed gate_up: CTA c's even share of the n_act x I (expert, feature) pairs; it writes its
+//      h values and counts itself in on a gpu-scope counter (release);
+//   5. down + combine: CTA c owns output rows [c*H/G, (c+1)*H/G) of every expert, shared and
+//      routed. Their weight rows stream through the ring behind step 4; when every CTA's h rows
+//      are written, one warp copies all h rows into shared memory, the CTA multiplies, and it
+//      sums residual + gated shared output + weighted slots 0..K-1 of its rows in that fixed
+//      order.
 //
-// (item i belongs to CTA i mod gridDim), so the whole shared expert streams while the router
-// runs. Each CTA has three roles:
-//  * a producer warp streams each item's weight rows into a ring of shared-memory stages with
-//    1-D TMA bulk copies (one per row, 16 bytes apart modulo 128 so ldmatrix is conflict-free),
-//    and the item's activation rows when they are ready;
-//  * 8 consumer warps multiply a stage with warp-level bf16 MMAs (m16n8k16, fp32 accumulate;
-//    weight rows x up to 8 tokens, K split over the warps and summed in a fixed order), write the
-//    results, and hand the finished item to the signaller through a shared-memory queue;
-//  * a signaller warp does every cross-CTA step off the compute path: gpu-scope release counts,
-//    tickets, the routing (top-K, dispatch, work records, then a release flag) when it holds the
-//    last router ticket, and the fixed-order combine of an output block (residual, shared,
-//    slot 0..K-1) when it holds that block's last ticket.
-// Dependencies point only to lower-numbered items, every wait is bounded (~1 s, then
-// MOE_ERR_TIMEOUT), and the launch is cooperative (all CTAs resident). Routed gate_up items wait
-// for the routing flag; a down item streams its weights at once and copies its h rows only when
-// its expert's gate_up count is complete (acquire, then an async-proxy fence). The last CTA to
-// finish re-arms the counters for the next call on the same workspace.
+// Roles: a producer warp streams each stage's rows into a ring of shared-memory stages with 1-D
+// TMA bulk copies (one per row; rows 16 bytes apart modulo 128 so ldmatrix is conflict-free);
+// 8 consumer warps compute (router rows as warp dot products; gate_up and down with warp-level
+// bf16 MMAs, m16n8k16, fp32 accumulate, partial sums added in a fixed order) and the routing; a
+// tenth warp waits for the grid's h rows and copies them in. Every wait is bounded (~1 s): a
+// timeout sets MOE_ERR_TIMEOUT and the kernel still runs to its end with in-range indices.
+// The call tag and the gate_up counter's base advance once every CTA is past both exchanges,
+// so nothing has to be re-armed between calls.
 #include "launch.h"
 #include "ring.cuh"
 
 namespace moe {
 
-constexpr int kDTT = 8;                         // max tokens
-constexpr int kDMaxH = 2048, kDMaxI = 512;
-constexpr int kDPitchH = 2 * kDMaxH + 16;
-constexpr int kDStage = 16 * kDPitchH;          // largest stage: 16 rows of H
-constexpr int kRouteItems = 24;
-constexpr int kDnRows = 32;                     // down rows per item = combine block
-constexpr int kDMaxSt = 3;
-static_assert(kDnRows * (2 * kDMaxI + 16) + kDTT * (2 * kDMaxI + 16) <= kDStage, "down stage must fit");
+constexpr int kDTT = 8;                     // max tokens
+constexpr int kDMaxH = 2048, kDMaxI = 512;  // largest hidden size / expert width
+constexpr int kDMaxP = kDTT * 8;            // max (token, slot) pairs
+constexpr int kDBlk = 4;                    // max down blocks per ring stage
+constexpr int kDThreads = kConsumers + 64;  // 8 consumer warps, the producer, the h loader
+constexpr int kProducerWarp = kWarps, kHWarp = kWarps + 1;
+constexpr uint32_t kPollNs = 128;           // longest sleep between two polls
 
-enum { kItemRoute = 0, kItemUp = 1, kItemDown = 2, kItemEnd = 3 };
-constexpr int kDThreads = kConsumers + 64;  // 8 consumer warps, the producer, the signaller
-constexpr int kProducerWarp = kWarps, kSignalWarp = kWarps + 1;
-constexpr int kQ = 4;                       // signaller queue entries
+enum { kStRoute = 0, kStUp = 1, kStTopK = 2, kStUpDone = 3, kStDown = 4, kStEnd = 5 };
 
-struct Event {
-    int type, grp, blk, need;
-};
-
+// What one ring stage holds (written by the producer before the stage's barrier completes).
 struct DMeta {
     int type;
-    int mt;        // tokens (up, down); rows (route)
-    int row0;      // up: first h row; route: first router row
-    int f0;        // up: first feature; down: first output row
-    int inner;     // down: row length of Wd (I or Is)
-    int grp;       // up: counter slot (expert id, E = shared)
-    int block;     // down: output block
-    int nact;      // down: experts with rows (a block is complete after nact + 1 items)
-    uint32_t toks; // up: token of each of its mt rows, 4 bits each
-    int tok[kDTT], slot[kDTT];
-    float sc[kDTT];
+    int n;           // route: rows; up: features; down: blocks
+    int row0;        // route: first router row; up: first h row
+    int f0;          // up: first feature
+    int mt;          // up: tokens
+    uint32_t toks;   // up: token of each of its mt h rows, 4 bits each
+    int blk[kDBlk];  // down: expert slot of each block (0: shared expert, j >= 1: act[j - 1])
 };
 
-struct DSmem {
-    uint8_t* xs;
-    uint8_t* st[kDMaxSt];
-    float* red;
-    DMeta* meta;
-    Event* ev;
-    uint64_t* full;
-    uint64_t* empty;
-    uint64_t* xbar;
-    uint64_t* evfull;
-    uint64_t* evempty;
+// Shared-memory geometry of one launch, fixed on the host.
+struct DGeom {
+    int sf;     // features per gate_up stage (8 or 4); a stage holds 2 * sf rows of H
+    int nst;    // ring stages
+    int xp;     // pitch of x rows and H-long weight rows (2H + 16 bytes)
+    int dp;     // pitch of h rows and down rows (2 Imax + 16 bytes)
+    int rr;     // router rows per CTA
+    int ro;     // output rows per CTA (at most)
+    int nbs;    // down blocks per ring stage (1, 2 or 4); a block holds ro rows
+    int stage;  // stage bytes
+    int o_xs, o_hs, o_ys, o_red, o_st, o_meta, o_bar, smem;
 };
 
-__host__ __device__ inline size_t decode_smem_bytes(int T, int nst) {
-    return 1024 + (size_t)((T * kDPitchH + 127) & ~127) + (size_t)nst * kDStage + (size_t)nst * kWarps * 128 * 4 +
-           (size_t)nst * sizeof(DMeta) + kQ * sizeof(Event) + (2 * nst + 1 + 2 * kQ) * 8 + 64;
+// Routing tables, identical in every CTA.
+struct DRoute {
+    int sid[kDMaxP];    // expert of pair p = t*K + k
+    float sw[kDMaxP];   // renormalised weight of pair p
+    int less[kDMaxP];   // pairs whose expert is lower than pair p's
+    int rank[kDMaxP];   // earlier pairs with pair p's expert
+    int pcnt[kDMaxP];   // pairs with pair p's expert
+    int perm[kDMaxP];   // pair at each dispatch position
+    int inv[kDMaxP];    // dispatch position of each pair
+    int act[kDMaxP];    // used experts, ascending
+    int aoff[kDMaxP];   // first dispatch position of act[j]
+    int acnt[kDMaxP];   // pairs of act[j]
+    float sgate[kDTT];
+    int n_act;
+};
+
+inline int round_up128(int b) { return (b + 127) & ~127; }
+
+// Geometry for sf features per stage and nst stages; false if the layer does not fit it.
+inline bool decode_geom(const LayerArgs& a, int G, int sf, int nst, DGeom* g) {
+    g->sf = sf;
+    g->nst = nst;
+    g->xp = 2 * a.H + 16;
+    g->dp = 2 * a.Imax + 16;
+    g->rr = (a.E + 1 + G - 1) / G;
+    g->ro = (a.H + G - 1) / G;
+    g->stage = 2 * sf * g->xp;
+    const int nb = g->stage / (g->ro * g->dp);
+    g->nbs = nb >= 4 ? 4 : nb >= 2 ? 2 : nb;
+    if (g->rr > 2 * sf || g->ro > 16 || g->nbs < 1) return false;
+    const int P = a.T * a.K;
+    int o = 0;
+    g->o_xs = o; o += round_up128(a.T * g->xp);
+    g->o_hs = o; o += round_up128((P + a.T) * g->dp);
+    g->o_ys = o; o += round_up128((P + a.T) * 16 * 4);
+    g->o_red = o; o += 2 * kWarps * 32 * 16;
+    g->o_st = o; o += nst * g->stage;
+    g->o_meta = o; o += round_up128(nst * (int)sizeof(DMeta));
+    g->o_bar = o; o += round_up128((2 * nst + 3) * 8);
+    g->smem = o + 128;  // room to align the dynamic base to 128 bytes
+    return true;
 }
 
-__device__ __forceinline__ DSmem decode_carve(uint8_t* raw, int T, int nst) {
-    const uint32_t base = smem_u32(raw);
-    uint8_t* p = raw + (((base + 127u) & ~127u) - base);
-    DSmem r;
-    r.xs = p;
-    p += (size_t)((T * kDPitchH + 127) & ~127);
-    for (int s = 0; s < kDMaxSt; ++s) {
-        r.st[s] = p;
-        if (s < nst) p += kDStage;
+// Order-preserving unsigned key of a score: larger score, larger key; -0 is taken as +0.
+__device__ __forceinline__ uint32_t score_key(float v) {
+    if (v == 0.f) v = 0.f;
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Poll until *p - base >= n (unsigned, acquire), sleeping up to kPollNs between polls; false
+// after ~1 s.
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t base, uint32_t n) {
+    if (ld_acquire(p) - base >= n) return true;
+    const uint64_t t0 = global_ns();
+    uint32_t ns = 32;
+    for (;;) {
+        __nanosleep(ns);
+        if (ld_acquire(p) - base >= n) return true;
+        if (ns < kPollNs) ns <<= 1;
+        if (global_ns() - t0 > 1000000000ull) return false;
     }
-    r.red = reinterpret_cast<float*>(p);
-    p += (size_t)nst * kWarps * 128 * 4;
-    r.meta = reinterpret_cast<DMeta*>(p);
-    p += (size_t)nst * sizeof(DMeta);
-    r.ev = reinterpret_cast<Event*>(p);
-    p += kQ * sizeof(Event);
-    p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 7) & ~(uintptr_t)7);
-    r.full = reinterpret_cast<uint64_t*>(p);
-    r.empty = r.full + nst;
-    r.xbar = r.empty + nst;
-    r.evfull = r.xbar + 1;
-    r.evempty = r.evfull + kQ;
-    return r;
 }
 
-// Counters of the fused kernel (in the workspace): routing flag and ticket in the header,
-// per-expert gate_up completion [E+1], per-block combine tickets [H/kDnRows], final ticket.
-struct DFlags {
-    uint32_t* route_flag;
-    uint32_t* route_ticket;
-    uint32_t* epoch;
-    uint32_t* final_ticket;
-    uint32_t* up_done;
-    uint32_t* comb;
-};
-
-__device__ __forceinline__ DFlags decode_flags(const LayerArgs& a) {
-    DFlags f;
-    f.route_flag = &a.hdr->dec_flag;
-    f.route_ticket = &a.hdr->route_ticket;
-    f.epoch = &a.hdr->dec_epoch;
-    f.final_ticket = &a.hdr->dec_final;
-    f.up_done = a.dflags;
-    f.comb = a.dflags + (a.E + 1);
-    return f;
+// Lane 0 waits for a barrier phase (bounded); the warp shares the outcome and, through the
+// warp barrier, the visibility of what completed the phase.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane) {
+    bool ok = lane == 0 ? mbar_wait(bar, parity) : true;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok;
 }
 
-// MMA of one stage: D[16 x 8] for 16 A rows at `a_rows` (rows past `nrows` read row 0) and the
-// B rows given per lane (token row of lane % 8), K range [k0, k0 + 16 * ksteps).
-__device__ __forceinline__ void stage_mma(float (&d)[4], uint32_t a_rows, int nrows, uint32_t b_row, int pitch, int k0,
-                                          int ksteps, int lane) {
-    int ra = lane & 15;
-    ra = ra < nrows ? ra : 0;
-    const uint32_t a = a_rows + (uint32_t)(ra * pitch + (k0 + 8 * (lane >> 4)) * 2);
+// Barrier of the consumer warps that also counts the threads whose predicate is true.
+__device__ __forceinline__ int consumers_count(bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.popc.u32 %0, 1, %2, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)p), "n"(kConsumers)
+        : "memory");
+    return (int)r;
+}
+
+// D[16 x 8] += A[16 x 16 ksteps] B for this lane's A row (a_row: byte address of the row the
+// lane feeds to ldmatrix, i.e. tile row lane % 16) and B row (token row of lane % 8), K range
+// starting at element k0. Even and odd K steps go to two accumulators (two short dependency
+// chains), added at the end.
+__device__ __forceinline__ void mma_rows(float (&d)[4], uint32_t a_row, uint32_t b_row, int k0, int ksteps, int lane) {
+    const uint32_t a = a_row + (uint32_t)((k0 + 8 * (lane >> 4)) * 2);
     const uint32_t b = b_row + (uint32_t)((k0 + 8 * ((lane >> 3) & 1)) * 2);
-#pragma unroll 4
-    for (int k = 0; k < ksteps; ++k) {
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
+    int k = 0;
+#pragma unroll 2
+    for (; k + 1 < ksteps; k += 2) {
+        uint32_t a0, a1, a2, a3, b0, b1, c0, c1, c2, c3, f0, f1;
+        ldsm_x4(a + k * 32, a0, a1, a2, a3);
+        ldsm_x2(b + k * 32, b0, b1);
+        ldsm_x4(a + k * 32 + 32, c0, c1, c2, c3);
+        ldsm_x2(b + k * 32 + 32, f0, f1);
+        mma16816(d, a0, a1, a2, a3, b0, b1);
+        mma16816(e, c0, c1, c2, c3, f0, f1);
+    }
+    if (k < ksteps) {
         uint32_t a0, a1, a2, a3, b0, b1;
         ldsm_x4(a + k * 32, a0, a1, a2, a3);
         ldsm_x2(b + k * 32, b0, b1);
         mma16816(d, a0, a1, a2, a3, b0, b1);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] += e[i];
 }
 
 // ---------------------------------------------------------------------------------------
-// Routing in one warp (the signaller of the CTA that finished the last router item): top-K of
-// every token from the scores in L2, renormalised weights, shared gate, dispatch, work records.
+// Routing ("Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: softmax over the 256 router
+// scores, the 8 highest kept and renormalised; ties go to the lower expert index).
 
-struct RouteScratch {
-    int cnt[256];
-    int off[257];
-    int sids[kDTT * 8];
-    int slr[kDTT * 8];
-    int sperm[kDTT * 8];
-    int sact[256];
-};
-
-__device__ void signal_route(const LayerArgs& a, RouteScratch& rs, int lane) {
-    for (int t = 0; t < a.T; ++t) {
-        const float* l = a.logits + (size_t)t * a.ldl;
-        float v[8];
-        bool bad = false;
+// Top-K of token t by one warp. Lane l polls the tagged scores of experts l, l+32, ... (lane 0
+// also the shared-gate score) until all carry this call's tag; each of K rounds then takes the
+// largest remaining key (warp max) and, among equal keys, the lowest expert index (warp min).
+// The weights are the softmax over the kept scores, which equals the full softmax renormalised
+// over them; lane k holds slot k.
+__device__ void route_token(const LayerArgs& a, DRoute& rt, int t, int lane, uint32_t tag) {
+    const uint64_t* l = a.dlog + (size_t)t * (a.E + 1);
+    uint32_t val[9];
+    uint32_t need = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = lane + 32 * j;
-            v[j] = -INFINITY;
-            if (e < a.E) {
-                v[j] = __ldcg(l + e);
-                if (!isfinite(v[j])) {
-                    bad = true;
-                    v[j] = -INFINITY;
-                }
-            }
-        }
-        uint32_t taken = 0;
-        float sel_v[8];
-        int sel_e[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            if (k < a.K) {
-                float bv = -INFINITY;
-                int be = 0x7fffffff;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int e = lane + 32 * j;
-                    if (e < a.E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
-                        bv = v[j];
-                        be = e;
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                    if (ov > bv || (ov == bv && oe < be)) {
-                        bv = ov;
-                        be = oe;
-                    }
-                }
-                if ((be & 31) == lane) taken |= 1u << (be >> 5);
-                sel_v[k] = bv;
-                sel_e[k] = be;
-            }
-        }
-        if (lane == 0) {
-            float ex[8], s = 0.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k < a.K) {
-                    ex[k] = expf(sel_v[k] - sel_v[0]);
-                    s += ex[k];
-                }
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k < a.K) {
-                    rs.sids[t * a.K + k] = sel_e[k];
-                    a.ids[(size_t)t * a.K + k] = sel_e[k];
-                    a.topw[(size_t)t * a.K + k] = ex[k] / s;
-                }
-            const float z = __ldcg(l + a.E);
-            if (!isfinite(z)) bad = true;
-            a.sgate[t] = 1.0f / (1.0f + expf(-z));
-        }
-        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&a.hdr->err, ERR_NONFINITE_SCORE);
+    for (int j = 0; j < 9; ++j) {
+        val[j] = 0u;  // a score of 0 if the wait times out
+        const int e = j < 8 ? lane + 32 * j : a.E;
+        if ((j < 8 && e < a.E) || (j == 8 && lane == 0)) need |= 1u << j;
     }
-    for (int e = lane; e < a.E; e += 32) rs.cnt[e] = 0;
-    __syncwarp();
-    const int P = (int)a.P;
-    for (int b0 = 0; b0 < P; b0 += 32) {
-        const int i = b0 + lane;
-        const bool valid = i < P;
-        const int e = valid ? rs.sids[i] : -1;
-        const unsigned m = __match_any_sync(0xffffffffu, e);
-        const int rank_in = __popc(m & ((1u << lane) - 1u));
-        const int cc = valid ? rs.cnt[e] : 0;
-        __syncwarp();
-        if (valid) {
-            rs.slr[i] = cc + rank_in;
-            if (rank_in == 0) rs.cnt[e] = cc + __popc(m);
+    const uint64_t t0 = global_ns();
+    bool timed_out = false;
+    for (;;) {
+        // all pending words are requested before any is examined (one round trip per poll)
+        uint64_t w[9];
+#pragma unroll
+        for (int j = 0; j < 9; ++j) w[j] = ((need >> j) & 1u) ? ld_relaxed_u64(l + (j < 8 ? lane + 32 * j : a.E)) : 0ull;
+        uint32_t still = need;
+#pragma unroll
+        for (int j = 0; j < 9; ++j)
+            if (((need >> j) & 1u) && (uint32_t)(w[j] >> 32) == tag) {
+                val[j] = (uint32_t)w[j];
+                still &= ~(1u << j);
+            }
+        need = still;
+        if (!__any_sync(0xffffffffu, need != 0)) break;
+        if (global_ns() - t0 > 1000000000ull) {
+            timed_out = true;
+            break;
         }
-        __syncwarp();
+        __nanosleep(64);
     }
-    int loc[8], run = 0, nz = 0;
+    bool bad = false;
+    uint32_t key[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const int e = lane * 8 + j;
-        loc[j] = e < a.E ? rs.cnt[e] : 0;
-        run += loc[j];
-        nz += loc[j] > 0;
-    }
-    int incl = run, inz = nz;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        const int z = __shfl_up_sync(0xffffffffu, inz, o);
-        if (lane >= o) {
-            incl += y;
-            inz += z;
+        key[j] = 0u;  // below every score: never taken while a real expert remains
+        if (lane + 32 * j < a.E) {
+            float v = __uint_as_float(val[j]);
+            if (!isfinite(v)) {
+                bad = true;
+                v = -INFINITY;
+            }
+            key[j] = score_key(v);
         }
     }
-    int pos = incl - run, apos = inz - nz;
+    uint32_t taken = 0;
+    float v0 = 0.f, myv = 0.f;
+    int mye = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int e = lane * 8 + j;
-        if (e < a.E) {
-            rs.off[e] = pos;
-            if (loc[j] > 0) {
-                rs.sact[apos] = e;
-                a.act[apos++] = e;
+    for (int k = 0; k < 8; ++k) {
+        if (k < a.K) {
+            uint32_t bk = 0;
+            int bj = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (!((taken >> j) & 1u) && key[j] > bk) {
+                    bk = key[j];
+                    bj = j;
+                }
+            const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t win = __reduce_min_sync(0xffffffffu, bk == m ? (uint32_t)(lane + 32 * bj) : 0xffffffffu);
+            if ((int)(win & 31u) == lane) taken |= 1u << (win >> 5);
+            if (k == 0) v0 = key_score(m);
+            if (k == lane) {
+                myv = key_score(m);
+                mye = (int)win;
             }
         }
-        pos += loc[j];
     }
-    const int n_act = __shfl_sync(0xffffffffu, inz, 31);
-    if (lane == 31) rs.off[a.E] = incl;
-    __syncwarp();
-    for (int e = lane; e <= a.E; e += 32) {
-        a.offsets[e] = rs.off[e];
-        if (e < a.E) a.counts[e] = rs.cnt[e];
-    }
-    for (int i = lane; i < P; i += 32) {
-        const int j = rs.off[rs.sids[i]] + rs.slr[i];
-        a.perm[j] = i;
-        a.inv[i] = j;
-        rs.sperm[j] = i;
-    }
-    __syncwarp();
-    const int fbs = a.I / 8;
-    for (int idx = lane; idx < n_act * fbs; idx += 32) {
-        const int g = idx / fbs, fb = idx - g * fbs;
-        const int e = rs.sact[g];
-        uint32_t toks = 0;
-        for (int j = 0; j < rs.cnt[e]; ++j) toks |= (uint32_t)(rs.sperm[rs.off[e] + j] / a.K) << (4 * j);
-        UpRec rec;
-        rec.e = e;
-        rec.row0 = rs.off[e];
-        rec.f0 = (int16_t)(fb * 8);
-        rec.mt = (int16_t)rs.cnt[e];
-        rec.toks = toks;
-        a.uprec[idx] = rec;
+    const float ex = lane < a.K ? expf(myv - v0) : 0.f;
+    const float s = warp_sum(ex);
+    if (lane < a.K) {
+        rt.sid[t * a.K + lane] = mye;
+        rt.sw[t * a.K + lane] = ex / s;
     }
     if (lane == 0) {
-        a.hdr->n_act = n_act;
-        a.hdr->n_uprec = n_act * fbs;
+        const float z = __uint_as_float(val[8]);
+        if (!isfinite(z)) bad = true;
+        rt.sgate[t] = 1.0f / (1.0f + expf(-z));
+        if (timed_out) atomicOr(&a.hdr->err, ERR_TIMEOUT);
     }
-    __syncwarp();
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&a.hdr->err, ERR_NONFINITE_SCORE);
 }
 
-// Fixed-order sum of one output block of 32 rows for every token, by one warp. The shared
-// expert's slot holds its unscaled output; its gate is applied (and stored back) here.
-__device__ void signal_combine_block(const LayerArgs& a, int blk, int lane) {
-    for (int idx = lane; idx < a.T * kDnRows; idx += 32) {
-        const int t = idx / kDnRows, o = blk * kDnRows + (idx - t * kDnRows);
-        float* yt = a.Y + (size_t)t * (a.K + 1) * a.H + o;
-        float acc = a.residual ? __bfloat162float(a.residual[(size_t)t * a.H + o]) : 0.f;
-        const float shared = a.sgate[t] * __ldcg(yt + (size_t)a.K * a.H);
-        yt[(size_t)a.K * a.H] = shared;
-        acc += shared;
-        for (int k = 0; k < a.K; ++k) acc += __ldcg(yt + (size_t)k * a.H);
-        a.out[(size_t)t * a.H + o] = __float2bfloat16_rn(acc);
+// Dispatch of the P pairs by the consumer threads (thread p takes pair p): a stable counting
+// sort by expert -- pair p goes to position #{pairs with a lower expert} + #{earlier pairs with
+// its expert} -- and the ascending list of used experts with their first position and count.
+// Starts and ends with a barrier of the consumers.
+__device__ void route_dispatch(DRoute& rt, int P, int tid) {
+    if (tid < P) {
+        const int e = rt.sid[tid];
+        int less = 0, cnt = 0, rank = 0;
+        for (int q = 0; q < P; ++q) {
+            const int eq = rt.sid[q];
+            less += eq < e;
+            cnt += eq == e;
+            rank += (eq == e) & (q < tid);
+        }
+        rt.less[tid] = less;
+        rt.rank[tid] = rank;
+        rt.pcnt[tid] = cnt;
     }
+    consumers_count(false);  // barrier: pass 1 complete
+    int first = 0;
+    if (tid < P) {
+        const int e = rt.sid[tid], pos = rt.less[tid] + rt.rank[tid];
+        rt.perm[pos] = tid;
+        rt.inv[tid] = pos;
+        if (rt.rank[tid] == 0) {
+            first = 1;
+            int j = 0;
+            for (int q = 0; q < P; ++q) j += (rt.rank[q] == 0) & (rt.sid[q] < e);
+            rt.act[j] = e;
+            rt.aoff[j] = rt.less[tid];
+            rt.acnt[j] = rt.pcnt[tid];
+        }
+    }
+    const int na = consumers_count(first != 0);  // barrier: tables complete
+    if (tid == 0) rt.n_act = na;
+    consumers_sync();
 }
 
 // ---------------------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, int nst) {
+__global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeom g) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ RouteScratch rs;
-    DSmem r = decode_carve(smem_raw, a.T, nst);
-    const DFlags fl = decode_flags(a);
+    __shared__ DRoute rt;
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* base = smem_raw + (((raw + 127u) & ~127u) - raw);
+    uint8_t* xs = base + g.o_xs;
+    uint8_t* hs = base + g.o_hs;
+    float* Ys = reinterpret_cast<float*>(base + g.o_ys);  // [P + T][16] unscaled down outputs
+    float* red = reinterpret_cast<float*>(base + g.o_red);
+    uint8_t* stg = base + g.o_st;
+    DMeta* meta = reinterpret_cast<DMeta*>(base + g.o_meta);
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + g.o_bar);
+    uint64_t* empty = full + g.nst;
+    uint64_t* xbar = empty + g.nst;
+    uint64_t* hbar = xbar + 1;
+    uint64_t* routed = hbar + 1;
+
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, c = blockIdx.x;
+    const int T = a.T, H = a.H, E = a.E, K = a.K, P = T * K;
     uint32_t* err = &a.hdr->err;
-    const int pitch = 2 * a.H + 16;
-    const uint32_t epoch = *(volatile uint32_t*)fl.epoch;
-    const int R = (a.E + 1 + kRouteItems - 1) / kRouteItems;  // router rows per item
-    const int n_sup = a.Is / 8;          // shared gate_up items (8 features each)
-    const int n_blocks = a.H / kDnRows;  // shared down items (one per output block)
-    const int base_u = kRouteItems + n_sup + n_blocks;
+    // this call's score tag and the gate_up arrivals of earlier calls (both advanced by CTA 0
+    // of the previous call)
+    const uint32_t epoch = *(volatile uint32_t*)&a.hdr->dec_epoch;
+    const uint32_t tag = epoch + 1u;
+    const uint32_t ubase = *(volatile uint32_t*)&a.hdr->dec_u_base;
+    const int o0 = c * H / G, ro = (c + 1) * H / G - o0;  // this CTA's output rows
+
     if (threadIdx.x == 0) {
-        for (int s = 0; s < nst; ++s) {
-            mbar_init(&r.full[s], 1);
-            mbar_init(&r.empty[s], kWarps);
+        for (int s = 0; s < g.nst; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
         }
-        mbar_init(r.xbar, 1);
-        for (int q = 0; q < kQ; ++q) {
-            mbar_init(&r.evfull[q], 1);
-            mbar_init(&r.evempty[q], 1);
-        }
+        mbar_init(xbar, 1);
+        mbar_init(hbar, 1);
+        mbar_init(routed, 1);
         fence_mbar_init();
     }
     __syncthreads();
 
     if (warp == kProducerWarp) {
-        // ================= producer
-        if (lane == 0) mbar_arrive_expect_tx(r.xbar, (uint32_t)(a.T * a.H * 2));
+        // ================= producer: fills the stages in the order the consumers take them
+        if (lane == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(T * H * 2));
         __syncwarp();
-        if (lane < a.T) bulk_load(r.xs + (size_t)lane * pitch, a.x + (size_t)lane * a.H, a.H * 2, r.xbar);
-        int it = 0, n_items = -1, n_u = 0, n_act = 0;
-        bool fail = false;
-        for (int i = blockIdx.x;; i += gridDim.x) {
-            if (i >= base_u && n_items < 0) {
-                bool ok = lane == 0 ? wait_at_least(fl.route_flag, epoch + 1) : true;
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                __syncwarp();  // orders the other lanes' reads after lane 0's acquire
-                if (!ok) {
-                    fail = true;
-                    break;
-                }
-                n_u = *(volatile int*)&a.hdr->n_uprec;
-                n_act = *(volatile int*)&a.hdr->n_act;
-                n_items = base_u + n_u + n_act * n_blocks;
+        if (lane < T) bulk_load(xs + (size_t)lane * g.xp, a.x + (size_t)lane * H, H * 2, xbar);
+        int it = 0;
+        bool ok = true;
+        auto claim = [&]() -> int {  // next stage, once the consumers have released it
+            const int s = it % g.nst;
+            if (!warp_wait(&empty[s], (((uint32_t)(it / g.nst)) & 1u) ^ 1u, lane)) ok = false;
+            return s;
+        };
+        auto post = [&](int type) {  // a stage without copies
+            const int s = claim();
+            if (!ok) return;
+            if (lane == 0) {
+                meta[s].type = type;
+                mbar_arrive(&full[s]);
             }
-            if (n_items >= 0 && i >= n_items) break;
-            const int s = it % nst;
-            bool ok = lane == 0 ? mbar_wait(&r.empty[s], (((uint32_t)(it / nst)) & 1u) ^ 1u) : true;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) {
-                fail = true;
-                break;
+            __syncwarp();
+            ++it;
+        };
+        // gate rows f0.. to stage rows 0.., up rows (inner + f0).. to stage rows sf..
+        auto issue_up = [&](const bf16* W, int inner, int f0, int n, int row0, int mt, uint32_t toks) {
+            const int s = claim();
+            if (!ok) return;
+            uint8_t* st = stg + (size_t)s * g.stage;
+            if (lane == 0) {
+                DMeta& m = meta[s];
+                m.type = kStUp;
+                m.n = n;
+                m.row0 = row0;
+                m.f0 = f0;
+                m.mt = mt;
+                m.toks = toks;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * n * H * 2));
             }
-            DMeta& m = r.meta[s];
-            uint8_t* st = r.st[s];
-            const bool up = (i >= kRouteItems && i < kRouteItems + n_sup) || (i >= base_u && i < base_u + n_u);
-            if (i < kRouteItems) {
-                const int r0 = i * R, nr = max(0, min(a.E + 1, r0 + R) - r0);
+            __syncwarp();
+            if (lane < n)
+                bulk_load(st + (size_t)lane * g.xp, W + (size_t)(f0 + lane) * H, H * 2, &full[s]);
+            else if (lane >= 16 && lane < 16 + n)
+                bulk_load(st + (size_t)(g.sf + lane - 16) * g.xp, W + (size_t)(inner + f0 + lane - 16) * H, H * 2,
+                          &full[s]);
+            ++it;
+        };
+
+        // 1. router rows (row E is the shared-expert gate)
+        const int r0 = c * g.rr, nrr = max(0, min(E + 1, r0 + g.rr) - r0);
+        if (nrr > 0) {
+            const int s = claim();
+            if (ok) {
+                uint8_t* st = stg + (size_t)s * g.stage;
                 if (lane == 0) {
-                    m.type = kItemRoute;
-                    m.mt = nr;
-                    m.row0 = r0;
-                    mbar_arrive_expect_tx(&r.full[s], (uint32_t)(nr * a.H * 2));
+                    meta[s].type = kStRoute;
+                    meta[s].n = nrr;
+                    meta[s].row0 = r0;
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nrr * H * 2));
                 }
                 __syncwarp();
-                if (lane < nr) {
+                if (lane < nrr) {
                     const int row = r0 + lane;
-                    bulk_load(st + (size_t)lane * pitch, row < a.E ? a.router_w + (size_t)row * a.H : a.sg, a.H * 2,
-                              &r.full[s]);
+                    bulk_load(st + (size_t)lane * g.xp, row < E ? a.router_w + (size_t)row * H : a.sg, H * 2,
+                              &full[s]);
                 }
-            } else if (up) {
-                const bf16* W;
-                int inner, row0, f0, mt, grp;
-                uint32_t toks;
-                if (i < kRouteItems + n_sup) {
-                    W = a.sgu;
-                    inner = a.Is;
-                    row0 = (int)a.P;
-                    f0 = (i - kRouteItems) * 8;
-                    mt = a.T;
-                    toks = 0x76543210u;
-                    grp = a.E;
-                } else {
-                    const UpRec rec = a.uprec[i - base_u];
-                    W = a.gate_up + (size_t)rec.e * 2 * a.I * a.H;
-                    inner = a.I;
-                    row0 = rec.row0;
-                    f0 = rec.f0;
-                    mt = rec.mt;
-                    toks = rec.toks;
-                    grp = rec.e;
+                ++it;
+            }
+        }
+        // 2. shared gate_up: features [c*Is/G, (c+1)*Is/G), all tokens, h rows P..P+T-1
+        const int fs0 = c * a.Is / G, fs1 = (c + 1) * a.Is / G;
+        for (int f = fs0; f < fs1 && ok; f += g.sf)
+            issue_up(a.sgu, a.Is, f, min(g.sf, fs1 - f), P, T, 0x76543210u);
+        // 3. the consumers compute the routing and hand the tables over through `routed`
+        if (ok) post(kStTopK);
+        if (ok && !warp_wait(routed, 0, lane)) ok = false;
+        // 4. routed gate_up: (expert, feature) pairs [c*F/G, (c+1)*F/G) of the F = n_act * I
+        const int n_act = ok ? rt.n_act : 0;
+        const int F = n_act * a.I;
+        const int g1 = (int)((long long)(c + 1) * F / G);
+        for (int gi = (int)((long long)c * F / G); gi < g1 && ok;) {
+            const int j = gi / a.I, f = gi - j * a.I;
+            const int n = min(g.sf, min(g1 - gi, a.I - f));
+            const int e = rt.act[j];
+            const int row0 = rt.aoff[j], mt = rt.acnt[j];
+            uint32_t toks = 0;
+            for (int q = 0; q < mt; ++q) toks |= (uint32_t)(rt.perm[row0 + q] / K) << (4 * q);
+            issue_up(a.gate_up + (size_t)e * 2 * a.I * H, a.I, f, n, row0, mt, toks);
+            gi += n;
+        }
+        if (ok) post(kStUpDone);
+        // 5. down rows o0..o0+ro-1 of the shared expert (slot 0) and of each used expert
+        for (int j0 = 0; ro > 0 && j0 <= n_act && ok; j0 += g.nbs) {
+            const int nb = min(g.nbs, n_act + 1 - j0);
+            const int s = claim();
+            if (!ok) break;
+            uint8_t* st = stg + (size_t)s * g.stage;
+            if (lane == 0) {
+                uint32_t bytes = 0;
+                DMeta& m = meta[s];
+                m.type = kStDown;
+                m.n = nb;
+                for (int b = 0; b < nb; ++b) {
+                    m.blk[b] = j0 + b;
+                    bytes += (uint32_t)(ro * (j0 + b == 0 ? a.Is : a.I) * 2);
                 }
-                if (lane == 0) {
-                    m.type = kItemUp;
-                    m.mt = mt;
-                    m.row0 = row0;
-                    m.f0 = f0;
-                    m.grp = grp;
-                    m.toks = toks;
-                    mbar_arrive_expect_tx(&r.full[s], (uint32_t)(16 * a.H * 2));
-                }
-                __syncwarp();
-                if (lane < 8)
-                    bulk_load(st + (size_t)lane * pitch, W + (size_t)(f0 + lane) * a.H, a.H * 2, &r.full[s]);
-                else if (lane < 16)
-                    bulk_load(st + (size_t)lane * pitch, W + (size_t)(inner + f0 + lane - 8) * a.H, a.H * 2, &r.full[s]);
-            } else {
-                // down item: the shared expert's blocks first (no routing needed), then routed
-                const bool shared = i < base_u;
-                int blk, e;
-                if (shared) {
-                    blk = i - kRouteItems - n_sup;
-                    e = a.E;
-                } else {
-                    const int d = i - base_u - n_u;
-                    blk = d / n_act;
-                    e = a.act[d - blk * n_act];
-                }
-                const int inner = shared ? a.Is : a.I;
-                const bf16* W = shared ? a.sd : a.down + (size_t)e * a.H * a.I;
-                const int hrow0 = shared ? (int)a.P : a.offsets[e];
-                const int mt = shared ? a.T : a.offsets[e + 1] - hrow0;
-                const int dp = 2 * inner + 16;
-                if (lane < mt) {
-                    if (shared) {
-                        m.tok[lane] = lane;
-                        m.slot[lane] = a.K;
-                        m.sc[lane] = 1.f;  // the gate is applied in the combine
-                    } else {
-                        const int pv = a.perm[hrow0 + lane];
-                        m.tok[lane] = pv / a.K;
-                        m.slot[lane] = pv - (pv / a.K) * a.K;
-                        m.sc[lane] = a.topw[pv];
-                    }
-                }
-                if (lane == 0) {
-                    m.type = kItemDown;
-                    m.mt = mt;
-                    m.f0 = blk * kDnRows;
-                    m.inner = inner;
-                    m.block = blk;
-                    m.nact = -1;  // filled by the signaller from the routing
-                    mbar_arrive_expect_tx(&r.full[s], (uint32_t)((kDnRows + mt) * inner * 2));
-                }
-                __syncwarp();
-                bulk_load(st + (size_t)lane * dp, W + (size_t)(blk * kDnRows + lane) * inner, inner * 2, &r.full[s]);
-                // h rows only once this expert's gate_up items are all done
-                bool hok = lane == 0 ? wait_at_least(&fl.up_done[e], (uint32_t)(inner / 8)) : true;
-                hok = __shfl_sync(0xffffffffu, hok, 0);
-                __syncwarp();
-                if (!hok) {
-                    fail = true;
-                    break;
-                }
-                fence_proxy_async_global();
-                if (lane < mt)
-                    bulk_load(st + (size_t)(kDnRows + lane) * dp, a.h + (size_t)(hrow0 + lane) * a.Imax, inner * 2,
-                              &r.full[s]);
+                mbar_arrive_expect_tx(&full[s], bytes);
+            }
+            __syncwarp();
+            for (int idx = lane; idx < nb * ro; idx += 32) {
+                const int b = idx / ro, r = idx - b * ro, j = j0 + b;
+                const int inner = j == 0 ? a.Is : a.I;
+                const bf16* W = j == 0 ? a.sd : a.down + (size_t)rt.act[j - 1] * H * a.I;
+                bulk_load(st + (size_t)(b * g.ro + r) * g.dp, W + (size_t)(o0 + r) * inner, inner * 2, &full[s]);
             }
             ++it;
         }
-        if (fail && lane == 0) atomicOr(err, ERR_TIMEOUT);
+        if (!ok && lane == 0) atomicOr(err, ERR_TIMEOUT);
+        // every copy issued must land before the CTA can exit
         if (lane == 0) {
-            // every copy issued must land before the CTA releases its shared memory (checked
-            // before the end marker below reuses a stage slot)
-            for (int k = 0; k < nst && it - 1 - k >= 0; ++k) {
+            for (int k = 0; k < g.nst && it - 1 - k >= 0; ++k) {
                 const int j = it - 1 - k;
-                if (!mbar_wait(&r.full[j % nst], ((uint32_t)(j / nst)) & 1u)) atomicOr(err, ERR_TIMEOUT);
+                if (!mbar_wait(&full[j % g.nst], ((uint32_t)(j / g.nst)) & 1u)) atomicOr(err, ERR_TIMEOUT);
             }
-            if (!mbar_wait(r.xbar, 0)) atomicOr(err, ERR_TIMEOUT);
-            const int s = it % nst;
-            if (mbar_wait(&r.empty[s], (((uint32_t)(it / nst)) & 1u) ^ 1u)) {
-                r.meta[s].type = kItemEnd;
-                mbar_arrive(&r.full[s]);
-            } else {
-                atomicOr(err, ERR_TIMEOUT);
-            }
+            if (!mbar_wait(xbar, 0)) atomicOr(err, ERR_TIMEOUT);
         }
+        __syncwarp();
+        if (ok) post(kStEnd);
         return;
     }
 
-    if (warp == kSignalWarp) {
-        // ================= signaller: cross-CTA counts, tickets, routing and combines
-        bool live = true, routed = false;
-        int n_act_sig = 0;
-        for (int q_it = 0; live; ++q_it) {
-            const int q = q_it % kQ;
-            bool ok = lane == 0 ? mbar_wait(&r.evfull[q], ((uint32_t)(q_it / kQ)) & 1u) : true;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            __syncwarp();
-            if (!ok) {
-                if (lane == 0) atomicOr(err, ERR_TIMEOUT);
-                break;
+    if (warp == kHWarp) {
+        // ================= h loader: all h rows of this call, once every CTA has written its own
+        if (lane == 0) {
+            if (!wait_count(&a.hdr->dec_u_cnt, ubase, (uint32_t)G)) atomicOr(err, ERR_TIMEOUT);
+            if (c == 0) {
+                // every CTA has passed both exchanges of this call: advance the tag and the base
+                a.hdr->dec_epoch = tag == 0xffffffffu ? 0u : tag;
+                a.hdr->dec_u_base = ubase + (uint32_t)G;
             }
-            const Event ev = r.ev[q];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&r.evempty[q]);
-            if (ev.type == kItemRoute) {
-                uint32_t old = 0;
-                if (lane == 0) old = atom_acq_rel_add(fl.route_ticket, 1u);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                __syncwarp();
-                if (old == kRouteItems - 1) {
-                    signal_route(a, rs, lane);
-                    if (lane == 0) st_release(fl.route_flag, epoch + 1);
-                }
-            } else if (ev.type == kItemUp) {
-                if (lane == 0) red_release_add(&fl.up_done[ev.grp], 1u);
-            } else if (ev.type == kItemDown) {
-                // a block is complete after the shared item and one item per routed expert; the
-                // expert count comes from the routing (a shared item can finish before it)
-                if (!routed) {
-                    bool ok2 = lane == 0 ? wait_at_least(fl.route_flag, epoch + 1) : true;
-                    ok2 = __shfl_sync(0xffffffffu, ok2, 0);
-                    __syncwarp();
-                    if (!ok2) {
-                        if (lane == 0) atomicOr(err, ERR_TIMEOUT);
-                        break;
-                    }
-                    n_act_sig = *(volatile int*)&a.hdr->n_act;
-                    routed = true;
-                }
-                uint32_t old = 0;
-                if (lane == 0) {
-                    old = atom_release_add(&fl.comb[ev.blk], 1u);
-                    if (old == (uint32_t)n_act_sig) __threadfence();
-                }
-                old = __shfl_sync(0xffffffffu, old, 0);
-                __syncwarp();
-                if (old == (uint32_t)n_act_sig) signal_combine_block(a, ev.blk, lane);
-            } else {
-                live = false;
-            }
+            mbar_arrive_expect_tx(hbar, (uint32_t)(P * a.I * 2 + T * a.Is * 2));
         }
-        // the last CTA to finish re-arms the counters for the next call on this workspace
-        uint32_t fin = 0;
-        if (lane == 0) fin = atom_acq_rel_add(fl.final_ticket, 1u);
-        fin = __shfl_sync(0xffffffffu, fin, 0);
-        if (fin == gridDim.x - 1) {
-            for (int e = lane; e <= a.E; e += 32) fl.up_done[e] = 0;
-            for (int b = lane; b < n_blocks; b += 32) fl.comb[b] = 0;
-            __syncwarp();
-            if (lane == 0) {
-                *fl.route_ticket = 0;
-                *fl.final_ticket = 0;
-                *fl.epoch = epoch + 1;
-            }
-        }
+        __syncwarp();  // orders the lanes' copies after lane 0's acquire
+        fence_proxy_async_global();
+        for (int i = lane; i < P + T; i += 32)
+            bulk_load(hs + (size_t)i * g.dp, a.h + (size_t)i * a.Imax, (i < P ? a.I : a.Is) * 2, hbar);
+        if (lane == 0 && !mbar_wait(hbar, 0)) atomicOr(err, ERR_TIMEOUT);
         return;
     }
 
     // ================= consumers
-    bool xok = lane == 0 ? mbar_wait(r.xbar, 0) : true;
-    xok = __shfl_sync(0xffffffffu, xok, 0);
-    xok = consumers_all(xok);
-    int q_it = 0;
-    // hand a finished item to the signaller (warp 0, lane 0; after the item's writes)
-    auto push = [&](int type, int grp, int blk) {
-        if (threadIdx.x == 0) {
-            const int q = q_it % kQ;
-            if (!mbar_wait(&r.evempty[q], (((uint32_t)(q_it / kQ)) & 1u) ^ 1u)) atomicOr(err, ERR_TIMEOUT);
-            r.ev[q] = Event{type, grp, blk, 0};
-            mbar_arrive(&r.evfull[q]);
-        }
-        ++q_it;
-    };
+    const int tid = threadIdx.x;
+    if (!consumers_all(warp_wait(xbar, 0, lane)) && tid == 0) atomicOr(err, ERR_TIMEOUT);
+    int rb = 0;  // reduction buffer in use (alternates between the stages that reduce)
+    bool hready = false;
+    const uint32_t xs_a = smem_u32(xs), hs_a = smem_u32(hs);
     for (int it = 0;; ++it) {
-        const int s = it % nst;
-        bool ok = xok && (lane == 0 ? mbar_wait(&r.full[s], ((uint32_t)(it / nst)) & 1u) : true);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!consumers_all(ok)) {
-            if (threadIdx.x == 0) atomicOr(err, ERR_TIMEOUT);
-            push(kItemEnd, 0, 0);
+        const int s = it % g.nst;
+        if (!consumers_all(warp_wait(&full[s], ((uint32_t)(it / g.nst)) & 1u, lane))) {
+            if (tid == 0) atomicOr(err, ERR_TIMEOUT);
             break;
         }
-        const DMeta& m = r.meta[s];
-        const int type = m.type, mt = m.mt;
-        if (type == kItemEnd) {
-            push(kItemEnd, 0, 0);
-            break;
-        }
-        const uint32_t sa = smem_u32(r.st[s]);
-        float* red = r.red + (size_t)s * kWarps * 128;
-        if (type == kItemRoute) {
-            const int row0 = m.row0;
-            const int tt = lane & 7;
-            const uint32_t b_row = smem_u32(r.xs) + (uint32_t)((tt < a.T ? tt : 0) * pitch);
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            stage_mma(d, sa, mt, b_row, pitch, warp * (a.H / kWarps), a.H / kWarps / 16, lane);
+        const DMeta m = meta[s];
+        const uint8_t* stp = stg + (size_t)s * g.stage;
+        const uint32_t sa = smem_u32(stp);
+        float* rbuf = red + rb * kWarps * 32 * 4;
+        auto release = [&]() {
             __syncwarp();
-            if (lane == 0) mbar_arrive(&r.empty[s]);
-            *reinterpret_cast<float4*>(red + (warp * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
+            if (lane == 0) mbar_arrive(&empty[s]);
+        };
+
+        if (m.type == kStEnd) {
+            consumers_sync();  // every block's Ys rows are written
+            // residual + gated shared output + weighted slots 0..K-1, in that order
+            for (int idx = tid; idx < T * ro; idx += kConsumers) {
+                const int t = idx / ro, r = idx - t * ro, o = o0 + r;
+                float acc = a.residual ? __bfloat162float(a.residual[(size_t)t * H + o]) : 0.f;
+                float* yt = a.Y + (size_t)t * (K + 1) * H + o;
+                const float sh = rt.sgate[t] * Ys[(P + t) * 16 + r];
+                yt[(size_t)K * H] = sh;
+                acc += sh;
+                for (int k = 0; k < K; ++k) {
+                    const int p = t * K + k;
+                    const float v = rt.sw[p] * Ys[p * 16 + r];
+                    yt[(size_t)k * H] = v;
+                    acc += v;
+                }
+                a.out[(size_t)t * H + o] = __float2bfloat16_rn(acc);
+            }
+            break;
+        }
+
+        if (m.type == kStTopK) {
+            release();
+            if (warp < T) route_token(a, rt, warp, lane, tag);
             consumers_sync();
+            route_dispatch(rt, P, tid);
+            if (tid == 0) mbar_arrive(routed);
+            if (c == 0) {
+                // the routing results of this call, for the caller and the workspace taps
+                for (int p = tid; p < P; p += kConsumers) {
+                    a.ids[p] = rt.sid[p];
+                    a.topw[p] = rt.sw[p];
+                    a.perm[p] = rt.perm[p];
+                    a.inv[p] = rt.inv[p];
+                }
+                for (int e = tid; e <= E; e += kConsumers) {
+                    int less = 0, cnt = 0;
+                    for (int q = 0; q < P; ++q) {
+                        less += rt.sid[q] < e;
+                        cnt += rt.sid[q] == e;
+                    }
+                    a.offsets[e] = less;
+                    if (e < E) a.counts[e] = cnt;
+                }
+                for (int j = tid; j < rt.n_act; j += kConsumers) a.act[j] = rt.act[j];
+                if (tid < T) a.sgate[tid] = rt.sgate[tid];
+                if (tid == 0) a.hdr->n_act = rt.n_act;
+            }
+            continue;
+        }
+
+        if (m.type == kStUpDone) {
+            release();
+            // every h value of this CTA was written by warp 0
+            if (warp == 0) {
+                __syncwarp();
+                if (lane == 0) red_release_add(&a.hdr->dec_u_cnt, 1u);
+            }
+            continue;
+        }
+
+        if (m.type == kStRoute) {
+            // warp w < n: router row row0 + w for every token; lane l takes elements 8l + 256i
+            if (warp < m.n) {
+                const int row = m.row0 + warp;
+                const float bias = (row < E && a.router_b) ? __bfloat162float(a.router_b[row]) : 0.f;
+                const uint8_t* wr = stp + (size_t)warp * g.xp;
+                float acc[kDTT];
+#pragma unroll
+                for (int t = 0; t < kDTT; ++t) acc[t] = 0.f;
+                for (int k = lane * 8; k < H; k += 256) {
+                    const uint4 wv = *reinterpret_cast<const uint4*>(wr + k * 2);
+#pragma unroll
+                    for (int t = 0; t < kDTT; ++t)
+                        if (t < T) {
+                            float xf[8];
+                            unpack8(*reinterpret_cast<const uint4*>(xs + (size_t)t * g.xp + k * 2), xf);
+                            acc[t] = dot8(wv, xf, acc[t]);
+                        }
+                }
+                float mine = 0.f;
+#pragma unroll
+                for (int t = 0; t < kDTT; ++t)
+                    if (t < T) {
+                        const float v = warp_sum(acc[t]);
+                        if (lane == t) mine = v + bias;
+                    }
+                if (lane < T)
+                    st_relaxed_u64(a.dlog + (size_t)lane * (E + 1) + row,
+                                   ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(mine));
+            }
+            release();
+            continue;
+        }
+
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        if (m.type == kStUp) {
+            const int r = lane & 15, gi = r & 7;  // tile rows 0-7: gate of feature f0+gi, 8-15: its up row
+            const int srow = gi < m.n ? (r >> 3) * g.sf + gi : 0;
+            const int tt = lane & 7;
+            const int tok = tt < m.mt ? (int)((m.toks >> (4 * tt)) & 15u) : 0;
+            mma_rows(d, sa + (uint32_t)(srow * g.xp), xs_a + (uint32_t)(tok * g.xp), warp * (H / kWarps),
+                     H / kWarps / 16, lane);
+            release();
+            *reinterpret_cast<float4*>(rbuf + (warp * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
+            consumers_sync();
+            rb ^= 1;
             if (warp == 0) {
                 float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) {
-                    const float4 q4 = *reinterpret_cast<const float4*>(red + (w * 32 + lane) * 4);
+                    const float4 q4 = *reinterpret_cast<const float4*>(rbuf + (w * 32 + lane) * 4);
                     v[0] += q4.x; v[1] += q4.y; v[2] += q4.z; v[3] += q4.w;
                 }
+                const int rl = lane >> 2, t = 2 * (lane & 3);
+                if (rl < m.n) {
+                    bf16* hrow = a.h + (size_t)(m.row0 + t) * a.Imax + m.f0 + rl;
+                    if (t < m.mt) hrow[0] = __float2bfloat16_rn(silu(v[0]) * v[2]);
+                    if (t + 1 < m.mt) hrow[a.Imax] = __float2bfloat16_rn(silu(v[1]) * v[3]);
+                }
+            }
+            continue;
+        }
+
+        // kStDown: block b of this stage by warps b*wpb .. b*wpb+wpb-1, each one K slice
+        if (!hready) {
+            if (!warp_wait(hbar, 0, lane) && lane == 0) atomicOr(err, ERR_TIMEOUT);
+            hready = true;
+        }
+        const int wpb = min(4, kWarps / g.nbs);
+        const int b = warp / wpb, kq = warp - b * wpb;
+        int j = 0, mt = 0, hrow0 = 0;
+        if (b < m.n) {
+            j = meta[s].blk[b];
+            const int inner = j == 0 ? a.Is : a.I;
+            hrow0 = j == 0 ? P : rt.aoff[j - 1];
+            mt = j == 0 ? T : rt.acnt[j - 1];
+            const int r = lane & 15, tt = lane & 7;
+            const uint32_t a_row = sa + (uint32_t)((b * g.ro + (r < ro ? r : 0)) * g.dp);
+            const uint32_t b_row = hs_a + (uint32_t)((hrow0 + (tt < mt ? tt : 0)) * g.dp);
+            const int kl = inner / wpb;
+            mma_rows(d, a_row, b_row, kq * kl, kl / 16, lane);
+        }
+        release();
+        *reinterpret_cast<float4*>(rbuf + (warp * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
+        consumers_sync();
+        rb ^= 1;
+        if (b < m.n && kq == 0) {
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int q = 0; q < wpb; ++q) {
+                const float4 q4 = *reinterpret_cast<const float4*>(rbuf + ((b * wpb + q) * 32 + lane) * 4);
+                v[0] += q4.x; v[1] += q4.y; v[2] += q4.z; v[3] += q4.w;
+            }
+            const int rl = lane >> 2, i0 = 2 * (lane & 3);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int rl = (lane >> 2) + (q >= 2 ? 8 : 0), t = 2 * (lane & 3) + (q & 1);
-                    if (rl < mt && t < a.T) {
-                        const int row = row0 + rl;
-                        const float bias = (row < a.E && a.router_b) ? __bfloat162float(a.router_b[row]) : 0.f;
-                        a.logits[(size_t)t * a.ldl + row] = v[q] + bias;
-                    }
-                }
-                __syncwarp();
+            for (int q = 0; q < 4; ++q) {
+                const int r = rl + (q >= 2 ? 8 : 0), i = i0 + (q & 1);
+                if (r < ro && i < mt) Ys[(j == 0 ? P + i : rt.perm[hrow0 + i]) * 16 + r] = v[q];
             }
-            push(kItemRoute, 0, 0);
-        } else if (type == kItemUp) {
-            const int row0 = m.row0, f0 = m.f0, grp = m.grp;
-            const uint32_t toks = m.toks;
-            const int tt = lane & 7;
-            const int tok = tt < mt ? (int)((toks >> (4 * tt)) & 15u) : 0;
-            const uint32_t b_row = smem_u32(r.xs) + (uint32_t)(tok * pitch);
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            stage_mma(d, sa, 16, b_row, pitch, warp * (a.H / kWarps), a.H / kWarps / 16, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&r.empty[s]);
-            *reinterpret_cast<float4*>(red + (warp * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
-            consumers_sync();
-            if (warp == 0) {
-                float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float4 q4 = *reinterpret_cast<const float4*>(red + (w * 32 + lane) * 4);
-                    g0 += q4.x; g1 += q4.y; u0 += q4.z; u1 += q4.w;
-                }
-                const int f = lane >> 2, t = 2 * (lane & 3);
-                if (t < mt) a.h[(size_t)(row0 + t) * a.Imax + f0 + f] = __float2bfloat16_rn(silu(g0) * u0);
-                if (t + 1 < mt) a.h[(size_t)(row0 + t + 1) * a.Imax + f0 + f] = __float2bfloat16_rn(silu(g1) * u1);
-                __syncwarp();
-            }
-            push(kItemUp, grp, 0);
-        } else {
-            const int inner = m.inner, f0 = m.f0, blk = m.block;
-            const int dp = 2 * inner + 16;
-            const int mtile = warp & 1, kq = warp >> 1;  // 2 row tiles x 4 K quarters
-            const int kqlen = inner / 4;
-            const int tt = lane & 7;
-            const uint32_t b_row = sa + (uint32_t)((kDnRows + (tt < mt ? tt : 0)) * dp);
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            stage_mma(d, sa + (uint32_t)(mtile * 16 * dp), 16, b_row, dp, kq * kqlen, kqlen / 16, lane);
-            const int t0 = 2 * (lane & 3);
-            size_t y0 = 0, y1 = 0;
-            float s0 = 0.f, s1 = 0.f;
-            if (t0 < mt) {
-                y0 = ((size_t)m.tok[t0] * (a.K + 1) + m.slot[t0]) * a.H + f0;
-                s0 = m.sc[t0];
-            }
-            if (t0 + 1 < mt) {
-                y1 = ((size_t)m.tok[t0 + 1] * (a.K + 1) + m.slot[t0 + 1]) * a.H + f0;
-                s1 = m.sc[t0 + 1];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&r.empty[s]);
-            *reinterpret_cast<float4*>(red + (warp * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
-            consumers_sync();
-            if (kq == 0) {
-                float v[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 w4 = *reinterpret_cast<const float4*>(red + ((q * 2 + mtile) * 32 + lane) * 4);
-                    v[0] += w4.x; v[1] += w4.y; v[2] += w4.z; v[3] += w4.w;
-                }
-                const int row = mtile * 16 + (lane >> 2);
-                if (t0 < mt) {
-                    a.Y[y0 + row] = s0 * v[0];
-                    a.Y[y0 + row + 8] = s0 * v[2];
-                }
-                if (t0 + 1 < mt) {
-                    a.Y[y1 + row] = s1 * v[1];
-                    a.Y[y1 + row + 8] = s1 * v[3];
-                }
-            }
-            consumers_sync();  // warp 1's rows are written before warp 0 hands the item over
-            push(kItemDown, 0, blk);
         }
     }
 }
 
-bool decode_fused_supported(const LayerArgs& a) {
-    return a.T >= 1 && a.T <= kDTT && a.uprec && a.dflags && a.H <= kDMaxH && a.H % 128 == 0 &&
-           a.Imax <= kDMaxI && a.I % 32 == 0 && a.Is % 32 == 0 && a.E <= 256 &&
-           (a.E + 1 + kRouteItems - 1) / kRouteItems <= 16;
+// Geometry for this layer: the most bytes in flight that fit the shared memory of one CTA.
+static bool pick_geom(const LayerArgs& a, int cap, DGeom* g) {
+    static const int cfg[][2] = {{8, 3}, {4, 6}, {4, 5}, {4, 4}, {4, 3}, {8, 2}, {4, 2}};
+    for (const auto& c : cfg)
+        if (decode_geom(a, a.num_sms, c[0], c[1], g) && g->smem <= cap) return true;
+    return false;
 }
 
-cudaError_t launch_decode_fused(const LayerArgs& a, cudaStream_t s) {
-    static bool configured[64] = {};
+// Dynamic shared memory one CTA of the kernel may use on the current device (0 on failure).
+static int dynamic_smem_cap() {
+    static int cap[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    const int cap = 220 * 1024;
-    if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(k_decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, cap);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
+    if (!cap[dev]) {
+        int optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa, k_decode_fused) != cudaSuccess)
+            return 0;
+        const int c = optin - (int)fa.sharedSizeBytes - 1024;
+        if (c <= 0 ||
+            cudaFuncSetAttribute(k_decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, c) != cudaSuccess)
+            return 0;
+        cap[dev] = c;
     }
-    const int nst = decode_smem_bytes(a.T, 3) <= (size_t)cap ? 3 : 2;
+    return cap[dev];
+}
+
+bool decode_fused_supported(const LayerArgs& a) {
+    if (!(a.T >= 1 && a.T <= kDTT && a.K <= 8 && a.H <= kDMaxH && a.H % 128 == 0 && a.Imax <= kDMaxI &&
+          a.I % 64 == 0 && a.Is % 64 == 0 && a.E <= 256 && a.num_sms >= 1 && a.dlog))
+        return false;
+    DGeom g;
+    return pick_geom(a, dynamic_smem_cap(), &g);
+}
+
+cudaError_t launch_decode_fused(const LayerArgs& a, cudaStream_t s) {
+    DGeom g;
+    if (!pick_geom(a, dynamic_smem_cap(), &g)) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.num_sms);
     cfg.blockDim = dim3(kDThreads);
-    cfg.dynamicSmemBytes = decode_smem_bytes(a.T, nst);
+    cfg.dynamicSmemBytes = (size_t)g.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -740,7 +753,7 @@ cudaError_t launch_decode_fused(const LayerArgs& a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e;
-    MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (e = cudaLaunchKernelEx(&cfg, k_decode_fused, a, nst)));
+    MOE_LAUNCH(MOE_KERNEL_DECODE_FUSED, s, (e = cudaLaunchKernelEx(&cfg, k_decode_fused, a, g)));
     return e;
 }
 

@@ -40,7 +40,7 @@ struct LayerArgs {
     int32_t* dn_tiles;
     int32_t* n_groups;
     UpRec* uprec;     // routed gate_up records (few-token path), nullptr when not produced
-    uint32_t* dflags; // fused decode counters: [E+1] gate_up completions, [H/32] combine tickets
+    uint64_t* dlog;   // [T, E+1] router scores tagged with their call (fused few-token kernel)
     WsHeader* hdr;
     bool gemm;
     int T, H, E, K, I, Is, Imax, ldl, nb;

@@ -12,6 +12,7 @@ import oracle
 import sparse_moe_ffn_router_gb300 as moe
 from sparse_moe_ffn_router_gb300 import synth
 from sparse_moe_ffn_router_gb300.workloads import WORKLOADS
+from tests.inputs import gap_controlled_x
 from tests.gpu_helpers import Layer, assert_close, check_routing, read_tap, run_forward, run_route
 
 pytestmark = pytest.mark.gpu
@@ -88,6 +89,8 @@ EDGE = [
     (67, 256, 8, 8, 64, 128),     # K = E (dense mixture), ragged T, Is > I
     (129, 384, 40, 3, 192, 64),   # odd E and K, ragged T, I > Is
     (200, 128, 256, 8, 64, 64),   # most experts receive no rows
+    (5, 1024, 64, 6, 256, 128),   # one persistent kernel: odd T, I > Is
+    (8, 2048, 256, 8, 512, 512),  # one persistent kernel: full shape, 64 (token, slot) pairs
     (9, 2048, 256, 8, 512, 512),  # full shape, ragged token tile
     # from T = 256 on, the tensor-core path
     (256, 256, 16, 4, 64, 128),     # smallest tensor-core case: one 64-feature SwiGLU tile, E < 256
@@ -135,7 +138,33 @@ def test_residual_and_in_place_output():
     assert torch.equal(inplace, out)
 
 
-@pytest.mark.parametrize("name", ["decode_T64", "prefill_T4096_zipf"])
+def test_few_token_calls_in_a_row_share_one_workspace():
+    """Up to 8 tokens the layer runs as one persistent kernel whose grid-wide exchange state
+    (score tag, gate_up counter) carries over from call to call on a workspace. Three calls in
+    a row on one workspace, each with another x (so other experts), the last with a residual
+    and its output written over the residual; outputs and the routing left in the workspace
+    are checked against the oracle."""
+    L = layer("decode_T1")
+    T, K = L.T, L.K
+    ws = moe.new_workspace(L.dims)
+    for seed in (11, 12):
+        x, _ = gap_controlled_x(L.dims, L.router_w, L.router_b, seed)
+        ref = oracle.forward(L.dims, x, L.host_weights())
+        out, _ = run_forward(L.dims, x.cuda(), L.W, ws=ws)
+        assert moe.moe_last_device_error(ws) == 0
+        assert_close(out.float().cpu().numpy(), ref["out"], f"x seed {seed}")
+        r = oracle.route(L.dims, x, L.router_w, L.router_b)
+        ids = read_tap(ws, L.dims, 3, torch.int32, (T, K)).cpu().numpy()
+        assert np.array_equal(ids, r["ids"]), f"x seed {seed}: expert ids"
+    res = synth.make_x(T, L.H, 13)
+    ref = oracle.forward(L.dims, L.x, L.host_weights(), residual=res)
+    inplace = res.cuda()
+    run_forward(L.dims, L.xd, L.W, residual=inplace, out=inplace, ws=ws)
+    assert moe.moe_last_device_error(ws) == 0
+    assert_close(inplace.float().cpu().numpy(), ref["out"], "residual, output in place")
+
+
+@pytest.mark.parametrize("name", ["tiny_T8", "decode_T1", "decode_T64", "prefill_T4096_zipf"])
 def test_bitwise_deterministic(name):
     L = layer(name)
     o1, ws = run_forward(L.dims, L.xd, L.W)
