@@ -118,6 +118,7 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
     a->n_groups = &a->hdr->n_groups;
     a->uprec = p->T <= kRecTokens ? (UpRec*)(base + p->o_uprec) : nullptr;
     a->dlog = p->T <= kRecTokens ? (uint64_t*)(base + p->o_dlog) : nullptr;
+    a->dh = p->T <= kRecTokens ? (uint64_t*)(base + p->o_dh) : nullptr;
     a->gemm = p->gemm;
     a->T = p->T; a->H = p->H; a->E = p->E; a->K = p->K; a->I = p->I; a->Is = p->Is;
     a->Imax = p->Imax; a->ldl = p->ldl; a->nb = p->nb; a->P = p->P;

@@ -22,13 +22,13 @@ struct WsHeader {
     int32_t n_groups;  // GEMM groups: n_act routed experts + the shared expert
     uint32_t route_ticket;  // CTAs of the fused routing kernel that finished (re-armed to 0)
     int32_t n_uprec;        // routed gate_up work records written by the few-token router
-    // Fused few-token kernel. Its router scores carry the tag epoch + 1 of the call that wrote
-    // them; its gate_up counter only grows: a call waits for its own arrivals above the base.
-    // Both advance once every CTA of a call is past both exchanges.
+    // Fused few-token kernel. Its router scores and gate_up outputs carry the tag epoch + 1 of
+    // the call that wrote them. Every CTA of a call counts itself in on dec_start (which only
+    // grows); CTA 0 advances the epoch and the base once all of them are in.
     uint32_t dec_epoch;       // calls completed on this workspace
-    uint32_t dec_u_base;      // gate_up arrivals of all earlier calls
+    uint32_t dec_start_base;  // CTA starts of all earlier calls
     uint32_t pad0[25];
-    uint32_t dec_u_cnt;       // CTAs whose gate_up rows are written (own 128-byte line)
+    uint32_t dec_start;       // CTAs started (own 128-byte line)
     uint32_t pad1[63];
 };
 static_assert(sizeof(WsHeader) == 384, "header layout");
@@ -67,7 +67,7 @@ struct Plan {
     int nb;          // token blocks of the dispatch
     bool gemm;       // many-token path (tensor-core GEMMs, bf16 Y) instead of weight streaming
     size_t o_hdr, o_logits, o_ids, o_topw, o_sgate, o_counts, o_offsets, o_perm, o_inv, o_lr, o_cntb, o_base,
-        o_act, o_h, o_y, o_xperm, o_upg, o_dng, o_upt, o_dnt, o_uprec, o_dlog, total;
+        o_act, o_h, o_y, o_xperm, o_upg, o_dng, o_upt, o_dnt, o_uprec, o_dlog, o_dh, total;
 };
 
 constexpr int kDispatchTokens = 64;  // tokens per block of the dispatch (counting-sort) kernels
@@ -111,6 +111,7 @@ inline bool make_plan(const moe_dims& d, Plan* p) {
     p->o_dnt = take((size_t)(d.E + 2) * 4);
     p->o_uprec = take(d.T <= kRecTokens ? P * (size_t)(d.I / 8) * sizeof(UpRec) : 0);
     p->o_dlog = take(d.T <= kRecTokens ? T * (size_t)(d.E + 1) * 8 : 0);
+    p->o_dh = take(d.T <= kRecTokens ? (P + T) * (size_t)(p->Imax / 2) * 8 : 0);
     p->total = o;
     return true;
 }

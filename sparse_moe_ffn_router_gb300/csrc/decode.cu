@@ -14,22 +14,23 @@
 //   3. routing: EVERY CTA reads the T x (E+1) tagged scores and computes top-K, the
 //      renormalised weights, the shared gate and the dispatch (counts, offsets, permutation)
 //      itself. All CTAs derive the same tables, so no second exchange is needed for them;
-//   4. routed gate_up: CTA c's even share of the n_act x I (expert, feature) pairs; it writes its
-//      h values and counts itself in on a gpu-scope counter (release);
+//   4. routed gate_up: CTA c's even share of the n_act x I (expert, feature) pairs. Like the
+//      scores, its h values are stored as tagged 64-bit words (two bf16 values and the tag);
 //   5. down + combine: CTA c owns output rows [c*H/G, (c+1)*H/G) of every expert, shared and
-//      routed. Their weight rows stream through the ring behind step 4; when every CTA's h rows
-//      are written, one warp copies all h rows into shared memory, the CTA multiplies, and it
+//      routed. The shared expert's block comes right after the routing (its h values were
+//      written in step 2), the routed blocks stream in behind step 4; the CTA gathers the
+//      tagged h rows into shared memory as soon as they carry this call's tag, multiplies, and
 //      sums residual + gated shared output + weighted slots 0..K-1 of its rows in that fixed
 //      order.
 //
 // Roles: a producer warp streams each stage's rows into a ring of shared-memory stages with 1-D
 // TMA bulk copies (one per row; rows 16 bytes apart modulo 128 so ldmatrix is conflict-free);
 // 8 consumer warps compute (router rows as warp dot products; gate_up and down with warp-level
-// bf16 MMAs, m16n8k16, fp32 accumulate, partial sums added in a fixed order) and the routing; a
-// tenth warp waits for the grid's h rows and copies them in. Every wait is bounded (~1 s): a
-// timeout sets MOE_ERR_TIMEOUT and the kernel still runs to its end with in-range indices.
-// The call tag and the gate_up counter's base advance once every CTA is past both exchanges,
-// so nothing has to be re-armed between calls.
+// bf16 MMAs, m16n8k16, fp32 accumulate, partial sums added in a fixed order), the routing and
+// the gathers. No exchange needs a flag or a fence: a word is fresh when it carries this
+// call's tag. Every wait is bounded (~1 s): a timeout sets MOE_ERR_TIMEOUT and the kernel still
+// runs to its end with in-range indices. Each CTA counts itself in when it starts; CTA 0 moves
+// the tag on at its end once all are in, so nothing has to be re-armed between calls.
 #include "launch.h"
 #include "ring.cuh"
 
@@ -39,11 +40,11 @@ constexpr int kDTT = 8;                     // max tokens
 constexpr int kDMaxH = 2048, kDMaxI = 512;  // largest hidden size / expert width
 constexpr int kDMaxP = kDTT * 8;            // max (token, slot) pairs
 constexpr int kDBlk = 4;                    // max down blocks per ring stage
-constexpr int kDThreads = kConsumers + 64;  // 8 consumer warps, the producer, the h loader
-constexpr int kProducerWarp = kWarps, kHWarp = kWarps + 1;
+constexpr int kDThreads = kConsumers + 32;  // 8 consumer warps and the producer
+constexpr int kProducerWarp = kWarps;
 constexpr uint32_t kPollNs = 128;           // longest sleep between two polls
 
-enum { kStRoute = 0, kStUp = 1, kStTopK = 2, kStUpDone = 3, kStDown = 4, kStEnd = 5 };
+enum { kStRoute = 0, kStUp = 1, kStTopK = 2, kStDown = 3, kStEnd = 4 };
 
 // What one ring stage holds (written by the producer before the stage's barrier completes).
 struct DMeta {
@@ -53,7 +54,8 @@ struct DMeta {
     int f0;          // up: first feature
     int mt;          // up: tokens
     uint32_t toks;   // up: token of each of its mt h rows, 4 bits each
-    int blk[kDBlk];  // down: expert slot of each block (0: shared expert, j >= 1: act[j - 1])
+    int blk[kDBlk];  // down: expert slot of each block (0: shared expert, j >= 1: act[j - 1]);
+                     // a stage holds the shared block alone or routed blocks only
 };
 
 // Shared-memory geometry of one launch, fixed on the host.
@@ -98,7 +100,7 @@ inline bool decode_geom(const LayerArgs& a, int G, int sf, int nst, DGeom* g) {
     g->stage = 2 * sf * g->xp;
     const int nb = g->stage / (g->ro * g->dp);
     g->nbs = nb >= 4 ? 4 : nb >= 2 ? 2 : nb;
-    if (g->rr > 2 * sf || g->ro > 16 || g->nbs < 1) return false;
+    if (g->rr > 2 * sf || g->ro > 16 || g->nbs < 1 || (a.I | a.Is) & 1) return false;
     const int P = a.T * a.K;
     int o = 0;
     g->o_xs = o; o += round_up128(a.T * g->xp);
@@ -107,7 +109,7 @@ inline bool decode_geom(const LayerArgs& a, int G, int sf, int nst, DGeom* g) {
     g->o_red = o; o += 2 * kWarps * 32 * 16;
     g->o_st = o; o += nst * g->stage;
     g->o_meta = o; o += round_up128(nst * (int)sizeof(DMeta));
-    g->o_bar = o; o += round_up128((2 * nst + 3) * 8);
+    g->o_bar = o; o += round_up128((2 * nst + 2) * 8);
     g->smem = o + 128;  // room to align the dynamic base to 128 bytes
     return true;
 }
@@ -328,6 +330,46 @@ __device__ void route_dispatch(DRoute& rt, int P, int tid) {
     consumers_sync();
 }
 
+// Even split of n items over G CTAs, boundaries rounded down to even (h values travel in pairs).
+__device__ __forceinline__ int even_split(int n, int c, int G) { return (int)((long long)c * n / G) & ~1; }
+
+// Copies h rows r0 .. r0+nr-1 (features 0 .. inner-1) of this call from their tagged words into
+// shared memory (pitch dp), each consumer thread polling its words until they carry `tag`.
+// False after ~1 s; the words not yet fresh are then copied as they are.
+__device__ bool gather_h(const LayerArgs& a, uint8_t* hs, int dp, int r0, int nr, int inner, uint32_t tag, int tid) {
+    constexpr int kB = 16;  // words in flight per thread
+    const int wpr = inner / 2, ldw = a.Imax / 2, n = nr * wpr;
+    const uint64_t t0 = global_ns();
+    bool ok = true;
+    for (int base = 0; base < n; base += kConsumers * kB) {
+        uint32_t need = 0;
+#pragma unroll
+        for (int q = 0; q < kB; ++q)
+            if (base + q * kConsumers + tid < n) need |= 1u << q;
+        while (need) {
+            uint64_t w[kB];
+#pragma unroll
+            for (int q = 0; q < kB; ++q) {
+                const int idx = base + q * kConsumers + tid, r = idx / wpr;
+                w[q] = ((need >> q) & 1u) ? ld_relaxed_u64(a.dh + (size_t)(r0 + r) * ldw + (idx - r * wpr)) : 0ull;
+            }
+            const bool give_up = !ok || global_ns() - t0 > 1000000000ull;
+            uint32_t still = need;
+#pragma unroll
+            for (int q = 0; q < kB; ++q)
+                if (((need >> q) & 1u) && ((uint32_t)(w[q] >> 32) == tag || give_up)) {
+                    const int idx = base + q * kConsumers + tid, r = idx / wpr;
+                    *reinterpret_cast<uint32_t*>(hs + (size_t)(r0 + r) * dp + (idx - r * wpr) * 4) = (uint32_t)w[q];
+                    still &= ~(1u << q);
+                }
+            if (give_up) ok = false;
+            need = still;
+            if (need) __nanosleep(64);
+        }
+    }
+    return ok;
+}
+
 // ---------------------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeom g) {
@@ -344,18 +386,17 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
     uint64_t* full = reinterpret_cast<uint64_t*>(base + g.o_bar);
     uint64_t* empty = full + g.nst;
     uint64_t* xbar = empty + g.nst;
-    uint64_t* hbar = xbar + 1;
-    uint64_t* routed = hbar + 1;
+    uint64_t* routed = xbar + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
     const int T = a.T, H = a.H, E = a.E, K = a.K, P = T * K;
     uint32_t* err = &a.hdr->err;
-    // this call's score tag and the gate_up arrivals of earlier calls (both advanced by CTA 0
-    // of the previous call)
+    // this call's tag and the CTA starts of earlier calls (both advanced by CTA 0 of the
+    // previous call)
     const uint32_t epoch = *(volatile uint32_t*)&a.hdr->dec_epoch;
     const uint32_t tag = epoch + 1u;
-    const uint32_t ubase = *(volatile uint32_t*)&a.hdr->dec_u_base;
+    const uint32_t sbase = *(volatile uint32_t*)&a.hdr->dec_start_base;
     const int o0 = c * H / G, ro = (c + 1) * H / G - o0;  // this CTA's output rows
 
     if (threadIdx.x == 0) {
@@ -364,11 +405,11 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
             mbar_init(&empty[s], kWarps);
         }
         mbar_init(xbar, 1);
-        mbar_init(hbar, 1);
         mbar_init(routed, 1);
         fence_mbar_init();
     }
-    __syncthreads();
+    __syncthreads();  // also orders every thread's reads of the tag before the count below
+    if (threadIdx.x == 0) red_release_add(&a.hdr->dec_start, 1u);
 
     if (warp == kProducerWarp) {
         // ================= producer: fills the stages in the order the consumers take them
@@ -438,32 +479,13 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
             }
         }
         // 2. shared gate_up: features [c*Is/G, (c+1)*Is/G), all tokens, h rows P..P+T-1
-        const int fs0 = c * a.Is / G, fs1 = (c + 1) * a.Is / G;
+        const int fs0 = even_split(a.Is, c, G), fs1 = even_split(a.Is, c + 1, G);
         for (int f = fs0; f < fs1 && ok; f += g.sf)
             issue_up(a.sgu, a.Is, f, min(g.sf, fs1 - f), P, T, 0x76543210u);
-        // 3. the consumers compute the routing and hand the tables over through `routed`
-        if (ok) post(kStTopK);
-        if (ok && !warp_wait(routed, 0, lane)) ok = false;
-        // 4. routed gate_up: (expert, feature) pairs [c*F/G, (c+1)*F/G) of the F = n_act * I
-        const int n_act = ok ? rt.n_act : 0;
-        const int F = n_act * a.I;
-        const int g1 = (int)((long long)(c + 1) * F / G);
-        for (int gi = (int)((long long)c * F / G); gi < g1 && ok;) {
-            const int j = gi / a.I, f = gi - j * a.I;
-            const int n = min(g.sf, min(g1 - gi, a.I - f));
-            const int e = rt.act[j];
-            const int row0 = rt.aoff[j], mt = rt.acnt[j];
-            uint32_t toks = 0;
-            for (int q = 0; q < mt; ++q) toks |= (uint32_t)(rt.perm[row0 + q] / K) << (4 * q);
-            issue_up(a.gate_up + (size_t)e * 2 * a.I * H, a.I, f, n, row0, mt, toks);
-            gi += n;
-        }
-        if (ok) post(kStUpDone);
-        // 5. down rows o0..o0+ro-1 of the shared expert (slot 0) and of each used expert
-        for (int j0 = 0; ro > 0 && j0 <= n_act && ok; j0 += g.nbs) {
-            const int nb = min(g.nbs, n_act + 1 - j0);
+        // down rows o0..o0+ro-1 of block j0.. (nb blocks) into the next stage
+        auto issue_down = [&](int j0, int nb) {
             const int s = claim();
-            if (!ok) break;
+            if (!ok) return;
             uint8_t* st = stg + (size_t)s * g.stage;
             if (lane == 0) {
                 uint32_t bytes = 0;
@@ -484,7 +506,28 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
                 bulk_load(st + (size_t)(b * g.ro + r) * g.dp, W + (size_t)(o0 + r) * inner, inner * 2, &full[s]);
             }
             ++it;
+        };
+        // 3. the consumers compute the routing and hand the tables over through `routed`; the
+        //    shared expert's down rows stream in meanwhile
+        if (ok) post(kStTopK);
+        if (ok && ro > 0) issue_down(0, 1);
+        if (ok && !warp_wait(routed, 0, lane)) ok = false;
+        // 4. routed gate_up: (expert, feature) pairs [c*F/G, (c+1)*F/G) of the F = n_act * I
+        const int n_act = ok ? rt.n_act : 0;
+        const int F = n_act * a.I;
+        const int g1 = even_split(F, c + 1, G);
+        for (int gi = even_split(F, c, G); gi < g1 && ok;) {
+            const int j = gi / a.I, f = gi - j * a.I;
+            const int n = min(g.sf, min(g1 - gi, a.I - f));
+            const int e = rt.act[j];
+            const int row0 = rt.aoff[j], mt = rt.acnt[j];
+            uint32_t toks = 0;
+            for (int q = 0; q < mt; ++q) toks |= (uint32_t)(rt.perm[row0 + q] / K) << (4 * q);
+            issue_up(a.gate_up + (size_t)e * 2 * a.I * H, a.I, f, n, row0, mt, toks);
+            gi += n;
         }
+        // 5. down rows o0..o0+ro-1 of each used expert (slots 1..n_act)
+        for (int j0 = 1; ro > 0 && j0 <= n_act && ok; j0 += g.nbs) issue_down(j0, min(g.nbs, n_act + 1 - j0));
         if (!ok && lane == 0) atomicOr(err, ERR_TIMEOUT);
         // every copy issued must land before the CTA can exit
         if (lane == 0) {
@@ -499,30 +542,17 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
         return;
     }
 
-    if (warp == kHWarp) {
-        // ================= h loader: all h rows of this call, once every CTA has written its own
-        if (lane == 0) {
-            if (!wait_count(&a.hdr->dec_u_cnt, ubase, (uint32_t)G)) atomicOr(err, ERR_TIMEOUT);
-            if (c == 0) {
-                // every CTA has passed both exchanges of this call: advance the tag and the base
-                a.hdr->dec_epoch = tag == 0xffffffffu ? 0u : tag;
-                a.hdr->dec_u_base = ubase + (uint32_t)G;
-            }
-            mbar_arrive_expect_tx(hbar, (uint32_t)(P * a.I * 2 + T * a.Is * 2));
-        }
-        __syncwarp();  // orders the lanes' copies after lane 0's acquire
-        fence_proxy_async_global();
-        for (int i = lane; i < P + T; i += 32)
-            bulk_load(hs + (size_t)i * g.dp, a.h + (size_t)i * a.Imax, (i < P ? a.I : a.Is) * 2, hbar);
-        if (lane == 0 && !mbar_wait(hbar, 0)) atomicOr(err, ERR_TIMEOUT);
-        return;
-    }
-
     // ================= consumers
     const int tid = threadIdx.x;
+    // router bias of this warp's router row (if any), requested before the first wait
+    float bias = 0.f;
+    {
+        const int row = c * g.rr + warp;
+        if (warp < g.rr && row < E && a.router_b) bias = __bfloat162float(a.router_b[row]);
+    }
     if (!consumers_all(warp_wait(xbar, 0, lane)) && tid == 0) atomicOr(err, ERR_TIMEOUT);
     int rb = 0;  // reduction buffer in use (alternates between the stages that reduce)
-    bool hready = false;
+    bool have_sh = false, have_rh = false;  // shared / routed h rows gathered
     const uint32_t xs_a = smem_u32(xs), hs_a = smem_u32(hs);
     for (int it = 0;; ++it) {
         const int s = it % g.nst;
@@ -557,6 +587,13 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
                 }
                 a.out[(size_t)t * H + o] = __float2bfloat16_rn(acc);
             }
+            if (c == 0 && tid == 0) {
+                // every CTA has read this call's tag once all have counted themselves in: move
+                // the tag and the base on for the next call
+                if (!wait_count(&a.hdr->dec_start, sbase, (uint32_t)G)) atomicOr(err, ERR_TIMEOUT);
+                a.hdr->dec_epoch = tag == 0xffffffffu ? 0u : tag;
+                a.hdr->dec_start_base = sbase + (uint32_t)G;
+            }
             break;
         }
 
@@ -590,21 +627,10 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
             continue;
         }
 
-        if (m.type == kStUpDone) {
-            release();
-            // every h value of this CTA was written by warp 0
-            if (warp == 0) {
-                __syncwarp();
-                if (lane == 0) red_release_add(&a.hdr->dec_u_cnt, 1u);
-            }
-            continue;
-        }
-
         if (m.type == kStRoute) {
             // warp w < n: router row row0 + w for every token; lane l takes elements 8l + 256i
             if (warp < m.n) {
                 const int row = m.row0 + warp;
-                const float bias = (row < E && a.router_b) ? __bfloat162float(a.router_b[row]) : 0.f;
                 const uint8_t* wr = stp + (size_t)warp * g.xp;
                 float acc[kDTT];
 #pragma unroll
@@ -653,20 +679,35 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
                     const float4 q4 = *reinterpret_cast<const float4*>(rbuf + (w * 32 + lane) * 4);
                     v[0] += q4.x; v[1] += q4.y; v[2] += q4.z; v[3] += q4.w;
                 }
+                // feature f0+rl for tokens t, t+1: the plain bf16 h (workspace tap) and, from the
+                // lanes of even features, tagged pairs (f, f+1) for the other CTAs
                 const int rl = lane >> 2, t = 2 * (lane & 3);
+                const bf16 h0 = __float2bfloat16_rn(silu(v[0]) * v[2]);
+                const bf16 h1 = __float2bfloat16_rn(silu(v[1]) * v[3]);
+                const uint32_t u0 = __bfloat16_as_ushort(h0), u1 = __bfloat16_as_ushort(h1);
+                const uint32_t n0 = __shfl_down_sync(0xffffffffu, u0, 4), n1 = __shfl_down_sync(0xffffffffu, u1, 4);
                 if (rl < m.n) {
                     bf16* hrow = a.h + (size_t)(m.row0 + t) * a.Imax + m.f0 + rl;
-                    if (t < m.mt) hrow[0] = __float2bfloat16_rn(silu(v[0]) * v[2]);
-                    if (t + 1 < m.mt) hrow[a.Imax] = __float2bfloat16_rn(silu(v[1]) * v[3]);
+                    if (t < m.mt) hrow[0] = h0;
+                    if (t + 1 < m.mt) hrow[a.Imax] = h1;
+                    if (!(rl & 1)) {
+                        uint64_t* w = a.dh + (size_t)(m.row0 + t) * (a.Imax / 2) + (m.f0 + rl) / 2;
+                        const uint64_t hi = (uint64_t)tag << 32;
+                        if (t < m.mt) st_relaxed_u64(w, hi | (n0 << 16) | u0);
+                        if (t + 1 < m.mt) st_relaxed_u64(w + a.Imax / 2, hi | (n1 << 16) | u1);
+                    }
                 }
             }
             continue;
         }
 
-        // kStDown: block b of this stage by warps b*wpb .. b*wpb+wpb-1, each one K slice
-        if (!hready) {
-            if (!warp_wait(hbar, 0, lane) && lane == 0) atomicOr(err, ERR_TIMEOUT);
-            hready = true;
+        // kStDown: block b of this stage by warps b*wpb .. b*wpb+wpb-1, each one K slice; the h
+        // rows it needs are gathered first (all consumers)
+        if (meta[s].blk[0] == 0 ? !have_sh : !have_rh) {
+            const bool sh = meta[s].blk[0] == 0;
+            const bool got = sh ? gather_h(a, hs, g.dp, P, T, a.Is, tag, tid) : gather_h(a, hs, g.dp, 0, P, a.I, tag, tid);
+            if (!consumers_all(got) && tid == 0) atomicOr(err, ERR_TIMEOUT);
+            (sh ? have_sh : have_rh) = true;
         }
         const int wpb = min(4, kWarps / g.nbs);
         const int b = warp / wpb, kq = warp - b * wpb;
@@ -733,7 +774,7 @@ static int dynamic_smem_cap() {
 
 bool decode_fused_supported(const LayerArgs& a) {
     if (!(a.T >= 1 && a.T <= kDTT && a.K <= 8 && a.H <= kDMaxH && a.H % 128 == 0 && a.Imax <= kDMaxI &&
-          a.I % 64 == 0 && a.Is % 64 == 0 && a.E <= 256 && a.num_sms >= 1 && a.dlog))
+          a.I % 64 == 0 && a.Is % 64 == 0 && a.E <= 256 && a.num_sms >= 1 && a.dlog && a.dh))
         return false;
     DGeom g;
     return pick_geom(a, dynamic_smem_cap(), &g);

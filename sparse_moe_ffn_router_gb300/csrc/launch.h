@@ -41,6 +41,7 @@ struct LayerArgs {
     int32_t* n_groups;
     UpRec* uprec;     // routed gate_up records (few-token path), nullptr when not produced
     uint64_t* dlog;   // [T, E+1] router scores tagged with their call (fused few-token kernel)
+    uint64_t* dh;     // [P+T, Imax/2] gated activation pairs tagged with their call (same kernel)
     WsHeader* hdr;
     bool gemm;
     int T, H, E, K, I, Is, Imax, ldl, nb;
