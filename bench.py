@@ -27,6 +27,7 @@ independent; no collective on the data path): value = tokens of all ranks / max 
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -106,6 +107,27 @@ def max_over_ranks(v: float) -> float:
 
 # ---------------------------------------------------------------------------------------
 # peaks, clocks
+
+
+# Source file of each kernel whose DRAM traffic a committed ncu summary records; a recorded
+# figure is used only while the file still hashes to the value stored with it.
+KERNEL_SOURCES = {"decode_fused": "sparse_moe_ffn_router_gb300/csrc/decode.cu",
+                  "gate_up": "sparse_moe_ffn_router_gb300/csrc/gemm.cu"}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) of `kernel` on `workload` from profiles/
+    ncu_traffic.json, or None when absent or recorded for another version of the source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            rec = json.load(f).get(kernel, {}).get(workload)
+        with open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()
+    except (OSError, KeyError, ValueError, AttributeError):
+        return None
+    if not rec or rec.get("source_sha1") != sha:
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 def load_peaks() -> dict:
@@ -239,7 +261,8 @@ def algorithmic(dims, groups: list[int]) -> dict:
 
     gate_up reads each touched expert's [2I, H] block and the shared [2Is, H] once, the
     dispatched x rows once and writes h; down reads each touched [H, I] block and the shared
-    [H, Is] once, reads h and writes Y; the layer adds the router [E+1, H], x and out."""
+    [H, Is] once, reads h and writes Y; the layer adds the router [E+1, H], x and out. The
+    single-kernel few-token path moves the whole layer's bytes."""
     T, H, E, K, I, Is = dims
     P = T * K
     n = len(groups)
@@ -248,7 +271,8 @@ def algorithmic(dims, groups: list[int]) -> dict:
     router = 2 * (E + 1) * H + 2 * T * H
     layer_bytes = 2 * ((E + 1) * H + n * 3 * I * H + 3 * Is * H) + 2 * 2 * T * H
     flops = 2 * T * (E + 1) * H + 2 * P * 3 * I * H + 2 * T * 3 * Is * H
-    return dict(gate_up=gate_up, down=down, router_scores=router, layer=layer_bytes, flops=flops)
+    return dict(gate_up=gate_up, down=down, router_scores=router, decode_fused=layer_bytes, layer=layer_bytes,
+                flops=flops)
 
 
 def trace_kernels(moe, names, n):
@@ -279,8 +303,10 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
                    graph: bool = False):
     """Warm-up (all kernels traced, to find the dominant one), then the timed region (only
     the dominant kernel traced). With graph=True the timed steps are replays of a CUDA graph
-    that holds G steps (and the dominant kernel's trace events); launch overhead on the host
-    is then out of the measurement. Returns a result dict."""
+    that holds G steps, so launch overhead on the host is out of the measurement; the dominant
+    kernel's duration then comes from a second graph of the same steps with its trace events,
+    replayed once after the timed region (event nodes stay out of the timed graph). Returns a
+    result dict."""
     moe = ls.moe
     ev = trace_kernels(moe, KERNEL_NAMES, warmup)
     for i in range(warmup):
@@ -303,14 +329,19 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
         reps = max(1, -(-steps // G))
         steps = G * reps
         ev = trace_kernels(moe, [dominant], G)
+        g_trace = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_trace):
+            for i in range(G):
+                ls.step(i)
+        clear_traces(moe)
         g = torch.cuda.CUDAGraph()
         n0 = moe.moe_launch_count()
         with torch.cuda.graph(g):
             for i in range(G):
                 ls.step(i)
         per_graph = moe.moe_launch_count() - n0
-        clear_traces(moe)
         g.replay()
+        g_trace.replay()
         torch.cuda.synchronize()
         run = lambda: [g.replay() for _ in range(reps)]  # noqa: E731
         n_ev = G
@@ -338,7 +369,17 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
     if sampler:
         sampler.__exit__(None, None, None)
     ms = max_over_ranks(start.elapsed_time(stop))
-    dom_ms = kernel_ms(ev, n_ev)[dominant]
+    if graph and per_graph == G:
+        # one launch per step: the kernel's average duration is the timed region's elapsed
+        # time over its launches (timed-region events, no event nodes between the launches)
+        dom_ms = ms / steps
+        dom_src = "timed-region events / launches"
+    else:
+        if graph:
+            g_trace.replay()
+            torch.cuda.synchronize()
+        dom_ms = kernel_ms(ev, n_ev)[dominant]
+        dom_src = "per-launch events"
     clear_traces(moe)
     groups = ls.routed_groups()
     first = 0 if graph else warmup
@@ -347,8 +388,11 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
     layer_bytes = sum(p["layer"] for p in per_step) / n_ev
     flops = per_step[0]["flops"]
     T = ls.dims[0]
+    # the device error word of the workspace (0: no non-finite score, no timed-out wait)
+    dev_err = moe.moe_last_device_error(ls.ws)
     res = dict(steps=steps, ms_per_step=ms / steps, tokens_per_s=T * steps / (ms / 1e3), launches=launches,
-               dominant=dominant, dominant_ms=dom_ms, warm_kernel_ms=warm, graph=graph,
+               device_error=dev_err,
+               dominant=dominant, dominant_ms=dom_ms, dominant_ms_source=dom_src, warm_kernel_ms=warm, graph=graph,
                unique_experts=sum(len(groups[(first + i) % nl]) for i in range(n_ev)) / n_ev,
                layer_bytes=layer_bytes, layer_flops=flops)
     if alg_bytes:
@@ -356,6 +400,7 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
         res["roofline"] = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1),
                            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
                            "traffic": None, "bytes_per_launch": int(alg_bytes),
+                           "duration_us": round(dom_ms * 1e3, 3), "duration_source": dom_src,
                            "peak_source": peaks["source"]}
     layer_gbs = layer_bytes / (ms / steps * 1e-3) / 1e9
     res["layer_hbm_frac"] = round(layer_gbs / peaks["hbm_gbs"], 4)
@@ -501,6 +546,8 @@ def main():
     ls = LayerSet(wl, n_rot, device)
     main_res = time_layer_set(ls, args.steps, args.warmup, peaks, clocks_index=torch.cuda.current_device(),
                               graph=not args.no_graph)
+    if main_res.get("roofline"):
+        main_res["roofline"]["traffic"] = ncu_traffic(main_res["roofline"]["kernel"], wl.name)
     e2e = time_e2e(ls, min(main_res["steps"], 20000), args.warmup)
     value = main_res["tokens_per_s"] * world
     line = {
@@ -519,6 +566,7 @@ def main():
         "e2e": {"value": round(e2e["value"] * world, 3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["ms_per_step"], 6)},
         "gpu_launches": main_res["launches"],
+        "device_error": main_res["device_error"],
         "clocks": main_res.get("clocks"),
         "layer": {"unique_experts_per_step": main_res["unique_experts"],
                   "hbm_frac_of_layer_bytes": main_res["layer_hbm_frac"],
@@ -541,7 +589,10 @@ def main():
             ls2 = LayerSet(w2, ROTATE if w2.T <= 32 else 1, device)
             r = time_layer_set(ls2, 0 if args.steps <= 0 else max(5, min(args.steps, 50)), 3, peaks,
                                auto=(1.0, 5, 500), graph=not args.no_graph and w2.T <= 64)
+            if r.get("roofline"):
+                r["roofline"]["traffic"] = ncu_traffic(r["roofline"]["kernel"], w2.name)
             also[name] = {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 5),
+                          "device_error": r["device_error"],
                           "roofline": r.get("roofline"), "hbm_frac_of_layer_bytes": r["layer_hbm_frac"],
                           "tensor_frac": r["layer_tensor_frac"], "unique_experts_per_step": r["unique_experts"],
                           "kernel_ms_warmup": {k: round(v, 5) for k, v in r["warm_kernel_ms"].items()}}
