@@ -48,7 +48,6 @@ struct StageMeta {
     int f0;          // up: first feature / down: first output row
     int inner;       // down: length of a weight row (I or Is)
     int block;       // down: output block
-    int expect;      // down: items of that block over all groups
     int tok[kTT], slot[kTT];
     float sc[kTT];
 };
@@ -193,6 +192,14 @@ __device__ __forceinline__ int routed_tiles(const LayerArgs& a, int lane) {
     return tot;
 }
 
+// Work of CTA c of G: shared-expert items c, c+G, ... below n_shared (they need no routing),
+// then routed items [c*R/G, (c+1)*R/G) -- a contiguous run, so consecutive items mostly share
+// their expert and token tile and the producer looks the routing up once per change.
+__device__ __forceinline__ int shared_items_of(int n_shared, int c, int G) {
+    return n_shared > c ? (n_shared - c + G - 1) / G : 0;
+}
+__device__ __forceinline__ int routed_split(int R, int c, int G) { return (int)((long long)c * R / G); }
+
 // Largest g with tiles[g] <= i (tiles ascending, tiles[0] = 0).
 __device__ __forceinline__ int find_group(const int* tiles, int n, int i) {
     int lo = 0, hi = n - 1;
@@ -228,48 +235,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up(LayerArgs a) {
     if (warp == kWarps) {
         // ---------------- producer
         int* tiles = r.misc + 4;
-        int it = 0, n_items = -1, n_act = 0;
-        for (int i = blockIdx.x;; i += gridDim.x) {
-            if (i >= n_shared && n_items < 0) {
-                grid_dep_wait();
-                n_act = a.hdr->n_act;
-                build_tiles(a, tiles, fb_r);
-                n_items = n_shared + tiles[n_act];
-            }
-            if (n_items >= 0 && i >= n_items) break;
-            if (__shfl_sync(0xffffffffu, *(volatile int*)&r.misc[0], 0)) break;
-            const bf16* W;
-            int inner, row0, f0, mt, t0;
-            bool shared;
-            if (i < n_shared) {
-                const int tile = i / fb_s, fb = i - tile * fb_s;
-                W = a.sgu;
-                inner = a.Is;
-                t0 = tile * kTT;
-                mt = min(kTT, a.T - t0);
-                row0 = (int)a.P;
-                f0 = fb * kFps;
-                shared = true;
-            } else {
-                const int k = i - n_shared;
-                const int g = find_group(tiles, n_act, k);
-                const int local = k - tiles[g];
-                const int tile = local / fb_r, fb = local - tile * fb_r;
-                const int e = a.act[g];
-                W = a.gate_up + (size_t)e * 2 * a.I * a.H;
-                inner = a.I;
-                row0 = a.offsets[e];
-                t0 = tile * kTT;
-                mt = min(kTT, a.offsets[e + 1] - row0 - t0);
-                f0 = fb * kFps;
-                shared = false;
-            }
+        const int G = gridDim.x, c = blockIdx.x;
+        int it = 0;
+        // stage it: 8 gate rows f0.. and the matching up rows of W, and the x rows of the mt
+        // tokens (lane < mt holds its token in tok)
+        auto issue = [&](const bf16* W, int inner, int f0, int hrow, int mt, int tok) -> bool {
+            if (__shfl_sync(0xffffffffu, *(volatile int*)&r.misc[0], 0)) return false;  // consumers gave up
             const int s = it % kSt;
-            if (!acquire_stage(r, it, err)) break;
+            if (!acquire_stage(r, it, err)) return false;
             if (lane == 0) {
                 StageMeta& m = r.meta[s];
                 m.mt = mt;
-                m.row0 = row0 + t0;
+                m.row0 = hrow;
                 m.f0 = f0;
                 mbar_arrive_expect_tx(&r.full[s], (uint32_t)((2 * kFps + mt) * a.H * 2));
             }
@@ -277,12 +254,36 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up(LayerArgs a) {
             uint8_t* st = r.st[s];
             copy_rows(st, pitch, W + (size_t)f0 * a.H, a.H, kFps, a.H * 2, &r.full[s], lane);
             copy_rows(st + kFps * pitch, pitch, W + (size_t)(inner + f0) * a.H, a.H, kFps, a.H * 2, &r.full[s], lane);
-            if (lane < mt) {
-                const int j = row0 + t0 + lane;
-                const int t = shared ? j - (int)a.P : a.perm[j] / a.K;
-                bulk_load(st + (size_t)(2 * kFps + lane) * pitch, a.x + (size_t)t * a.H, a.H * 2, &r.full[s]);
-            }
+            if (lane < mt) bulk_load(st + (size_t)(2 * kFps + lane) * pitch, a.x + (size_t)tok * a.H, a.H * 2, &r.full[s]);
             ++it;
+            return true;
+        };
+        bool ok = true;
+        const int my_shared = shared_items_of(n_shared, c, G);
+        for (int k = 0; k < my_shared && ok; ++k) {
+            const int i = c + k * G, tile = i / fb_s, fb = i - tile * fb_s, t0 = tile * kTT;
+            ok = issue(a.sgu, a.Is, fb * kFps, (int)a.P + t0, min(kTT, a.T - t0), t0 + lane);
+        }
+        grid_dep_wait();
+        const int n_act = a.hdr->n_act;
+        build_tiles(a, tiles, fb_r);
+        const int q1 = routed_split(tiles[n_act], c + 1, G);
+        int g = -1, e = 0, off = 0, cnt = 0, ctile = -1, mt = 0, tok = 0;
+        for (int q = routed_split(tiles[n_act], c, G); q < q1 && ok; ++q) {
+            if (g < 0 || q >= tiles[g + 1]) {
+                g = find_group(tiles, n_act, q);
+                e = a.act[g];
+                off = a.offsets[e];
+                cnt = a.offsets[e + 1] - off;
+                ctile = -1;
+            }
+            const int local = q - tiles[g], tile = local / fb_r, fb = local - tile * fb_r;
+            if (tile != ctile) {
+                ctile = tile;
+                mt = min(kTT, cnt - tile * kTT);
+                tok = lane < mt ? a.perm[off + tile * kTT + lane] / a.K : 0;
+            }
+            ok = issue(a.gate_up + (size_t)e * 2 * a.I * a.H, a.I, fb * kFps, off + tile * kTT, mt, tok);
         }
         if (lane == 0) drain(r, it, err);
         return;
@@ -290,13 +291,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up(LayerArgs a) {
 
     // ---------------- consumers: warp w takes K range [w*H/8, (w+1)*H/8) of all 16 rows
     const int kw = a.H / kWarps;
-    int it = 0, n_items = -1;
-    for (int i = blockIdx.x;; i += gridDim.x, ++it) {
-        if (i >= n_shared && n_items < 0) {
+    const int my_shared = shared_items_of(n_shared, blockIdx.x, gridDim.x);
+    int n_items = -1;
+    for (int it = 0;; ++it) {
+        if (it == my_shared && n_items < 0) {
             grid_dep_wait();
-            n_items = n_shared + routed_tiles(a, lane) * fb_r;
+            const int R = routed_tiles(a, lane) * fb_r;
+            n_items = my_shared + routed_split(R, blockIdx.x + 1, gridDim.x) - routed_split(R, blockIdx.x, gridDim.x);
         }
-        if (n_items >= 0 && i >= n_items) break;
+        if (n_items >= 0 && it >= n_items) break;
         const bool ok = wait_stage(r, it, err);
         if (!consumers_all(ok)) break;
         const int s = it % kSt;
@@ -535,17 +538,23 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
     const int n_blocks = a.H / kRows;
 
     if (warp == kWarps) {
-        // ---------------- producer: items ordered block-major: (block, group, token tile)
+        // ---------------- producer: shared items (block, token tile) strided over the CTAs,
+        // then this CTA's run of routed items (group, token tile, block)
         int* tiles = r.misc + 4;
-        build_tiles(a, tiles, 1);
-        const int per_block = tiles[n_act] + tiles_s;
-        const int n_items = per_block * n_blocks;
+        build_tiles(a, tiles, n_blocks);
+        const int G = gridDim.x, c = blockIdx.x;
+        const int my_shared = shared_items_of(n_blocks * tiles_s, c, G);
+        const int q0 = routed_split(tiles[n_act], c, G), q1 = routed_split(tiles[n_act], c + 1, G);
+        const int n_mine = my_shared + q1 - q0;
         int it = 0;
-        bool waited = false;
+        bool waited = false, ok = true;
         int pend_row[kSt], pend_mt[kSt], pend_inner[kSt];
-        for (int i = blockIdx.x;; i += gridDim.x) {
-            // after the first kSt stages (or at the end), wait for h and copy the pending rows
-            if (!waited && (it == kSt || i >= n_items)) {
+        int g = -1, e = 0, off = 0, cnt = 0, ctile = -1;
+        int tok = 0, slot = 0;
+        float sc = 0.f;
+        for (int k = 0; k < n_mine && ok; ++k) {
+            // after the first kSt stages, wait for h and copy the pending rows
+            if (!waited && it == kSt) {
                 grid_dep_wait();
                 waited = true;
                 for (int q = 0; q < it; ++q)
@@ -553,44 +562,54 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
                         bulk_load(r.st[q] + (size_t)(kRows + lane) * (2 * pend_inner[q] + kPad),
                                   a.h + (size_t)(pend_row[q] + lane) * a.Imax, pend_inner[q] * 2, &r.full[q]);
             }
-            if (i >= n_items) break;
             if (__shfl_sync(0xffffffffu, *(volatile int*)&r.misc[0], 0)) break;
-            const int blk = i / per_block, k = i - blk * per_block;
             const bf16* W;
-            int inner, hrow0, mt;
-            bool shared;
-            if (k >= tiles[n_act]) {
-                const int t0 = (k - tiles[n_act]) * kTT;
+            int inner, hrow0, mt, blk;
+            if (k < my_shared) {
+                const int i = c + k * G, tile = i % tiles_s, t0 = tile * kTT;
+                blk = i / tiles_s;
                 W = a.sd;
                 inner = a.Is;
                 hrow0 = (int)a.P + t0;
                 mt = min(kTT, a.T - t0);
-                shared = true;
+                if (lane < mt) {
+                    tok = t0 + lane;
+                    slot = a.K;
+                    sc = a.sgate[t0 + lane];
+                }
+                ctile = -1;  // the routed token cache no longer matches
             } else {
-                const int g = find_group(tiles, n_act, k);
-                const int t0 = (k - tiles[g]) * kTT;
-                const int e = a.act[g];
+                const int q = q0 + (k - my_shared);
+                if (g < 0 || q >= tiles[g + 1]) {
+                    g = find_group(tiles, n_act, q);
+                    e = a.act[g];
+                    off = a.offsets[e];
+                    cnt = a.offsets[e + 1] - off;
+                    ctile = -1;
+                }
+                const int local = q - tiles[g], tile = local / n_blocks;
+                blk = local - tile * n_blocks;
                 W = a.down + (size_t)e * a.H * a.I;
                 inner = a.I;
-                hrow0 = a.offsets[e] + t0;
-                mt = min(kTT, a.offsets[e + 1] - a.offsets[e] - t0);
-                shared = false;
+                hrow0 = off + tile * kTT;
+                mt = min(kTT, cnt - tile * kTT);
+                if (tile != ctile) {
+                    ctile = tile;
+                    if (lane < mt) {
+                        const int pv = a.perm[hrow0 + lane];
+                        tok = pv / a.K;
+                        slot = pv - tok * a.K;
+                        sc = a.topw[pv];
+                    }
+                }
             }
             const int s = it % kSt;
             if (!acquire_stage(r, it, err)) break;
             StageMeta& m = r.meta[s];
             if (lane < mt) {
-                const int j = hrow0 + lane;
-                if (shared) {
-                    m.tok[lane] = j - (int)a.P;
-                    m.slot[lane] = a.K;
-                    m.sc[lane] = a.sgate[j - (int)a.P];
-                } else {
-                    const int pv = a.perm[j];
-                    m.tok[lane] = pv / a.K;
-                    m.slot[lane] = pv - (pv / a.K) * a.K;
-                    m.sc[lane] = a.topw[pv];
-                }
+                m.tok[lane] = tok;
+                m.slot[lane] = slot;
+                m.sc[lane] = sc;
             }
             const int pitch = 2 * inner + kPad;
             if (lane == 0) {
@@ -598,7 +617,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
                 m.f0 = blk * kRows;
                 m.inner = inner;
                 m.block = blk;
-                m.expect = per_block;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_expect_tx(&r.full[s], (uint32_t)((kRows + mt) * inner * 2));
@@ -616,20 +634,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
             }
             ++it;
         }
+        if (!waited) {
+            // fewer than kSt items: their h rows are still pending
+            grid_dep_wait();
+            for (int q = 0; q < it; ++q)
+                if (lane < pend_mt[q])
+                    bulk_load(r.st[q] + (size_t)(kRows + lane) * (2 * pend_inner[q] + kPad),
+                              a.h + (size_t)(pend_row[q] + lane) * a.Imax, pend_inner[q] * 2, &r.full[q]);
+        }
         if (lane == 0) drain(r, it, err);
         return;
     }
 
     // ---------------- consumers: warp w takes M tile (w % 4) and K half (w / 4)
-    const int per_block = routed_tiles(a, lane) + tiles_s;
-    const int n_items = per_block * n_blocks;
-    int it = 0;
-    for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++it) {
+    const int R = routed_tiles(a, lane) * n_blocks;
+    const int n_items = shared_items_of(n_blocks * tiles_s, blockIdx.x, gridDim.x) +
+                        routed_split(R, blockIdx.x + 1, gridDim.x) - routed_split(R, blockIdx.x, gridDim.x);
+    for (int it = 0; it < n_items; ++it) {
         const bool ok = wait_stage(r, it, err);
         if (!consumers_all(ok)) break;
         const int s = it % kSt;
         const StageMeta& m = r.meta[s];  // read in place: rewritten only after the stage is released
-        const int mt = m.mt, inner = m.inner, f0 = m.f0, blk = m.block, expect = m.expect;
+        const int mt = m.mt, inner = m.inner, f0 = m.f0;
         const int pitch = 2 * inner + kPad;
         const int mtile = warp & 3, khalf = warp >> 2;
         const int kh = inner / 2;
