@@ -6,8 +6,9 @@
 //
 // Both kernels are persistent (one CTA per SM). A producer warp walks the CTA's work items and,
 // for each, fills one stage of a 2-stage shared-memory ring with 1-D TMA bulk copies
-// (cp.async.bulk, one per row so rows land 16 bytes apart modulo 128 and ldmatrix is free of
-// bank conflicts): the item's weight rows plus its activation rows (up to 8 tokens), and writes
+// (cp.async.bulk; gate/up one per 4 KB row, down one per group of 4 consecutive 1 KB rows, with
+// 16 bytes of padding per row or group so ldmatrix is free of bank conflicts): the item's
+// weight rows plus its activation rows (up to 8 tokens), and writes
 // the item's metadata into the stage before arming its mbarrier. Eight consumer warps multiply
 // the staged rows with warp-level bf16 MMAs (m16n8k16, fp32 accumulate: 16 weight rows by
 // the item's tokens, padded to 8), each warp over a fixed K range, and sum the warps' partial
@@ -40,7 +41,15 @@ constexpr int kPad = 16;                // row padding: rows start 16 B apart mo
 constexpr int kMaxH = 2048, kMaxInner = 512;
 constexpr int kPitchH = 2 * kMaxH + kPad, kPitchI = 2 * kMaxInner + kPad;
 constexpr int kStageBytes = 2 * kFps * kPitchH + kTT * kPitchH;  // the larger of the up and down layouts
-static_assert(kRows * kPitchI + kTT * kPitchI <= kStageBytes, "down stage must fit");
+static_assert((kRows / 4) * (8 * kMaxInner + kPad) + kTT * kPitchI <= kStageBytes, "down stage must fit");
+
+// Down stage layout: kRows/4 groups of 4 consecutive Wd rows, each group one 1-D bulk copy
+// (4 KB at inner = 512: copies of 1 KB rows stream markedly slower than 4 KB ones), groups
+// 8*inner + 16 bytes apart so any 8 consecutive groups start in 8 different 16-byte bank
+// slots; then kTT h rows, 2*inner + 16 bytes apart. An MMA tile of 16 rows takes rows j and
+// j+1 of 8 consecutive groups, so each 8x8 ldmatrix fetch reads 8 different bank slots.
+__host__ __device__ constexpr int dn_gpitch(int inner) { return 8 * inner + kPad; }
+__host__ __device__ constexpr int dn_hoff(int inner) { return (kRows / 4) * dn_gpitch(inner); }
 
 struct StageMeta {
     int mt;          // tokens in this item
@@ -91,6 +100,21 @@ __device__ __forceinline__ void mma_rows(float (&d)[4], uint32_t a_base, uint32_
                                          int ksteps, int lane) {
     const uint32_t a = a_base + (uint32_t)((lane & 15) * pitch + (k0 + 8 * (lane >> 4)) * 2);
     const uint32_t b = b_base + (uint32_t)((lane & 7) * pitch + (k0 + 8 * ((lane >> 3) & 1)) * 2);
+#pragma unroll 4
+    for (int k = 0; k < ksteps; ++k) {
+        uint32_t a0, a1, a2, a3, b0, b1;
+        ldsm_x4(a + k * 32, a0, a1, a2, a3);
+        ldsm_x2(b + k * 32, b0, b1);
+        mma16816(d, a0, a1, a2, a3, b0, b1);
+    }
+}
+
+// The same MMA with per-lane row addresses: a_row is the A row this lane feeds to ldmatrix
+// (tile row lane % 16), b_row the B row (token row lane % 8), K from element k0.
+__device__ __forceinline__ void mma_rows_at(float (&d)[4], uint32_t a_row, uint32_t b_row, int k0, int ksteps,
+                                            int lane) {
+    const uint32_t a = a_row + (uint32_t)((k0 + 8 * (lane >> 4)) * 2);
+    const uint32_t b = b_row + (uint32_t)((k0 + 8 * ((lane >> 3) & 1)) * 2);
 #pragma unroll 4
     for (int k = 0; k < ksteps; ++k) {
         uint32_t a0, a1, a2, a3, b0, b1;
@@ -220,7 +244,8 @@ __device__ __forceinline__ void copy_rows(uint8_t* dst, int dst_pitch, const bf1
 // ---------------------------------------------------------------------------------------
 // Stage layout, up:   rows 0..7 gate features f0..f0+7, rows 8..15 the matching up rows
 //                     (pitch 2H + 16), then kTT activation rows (same pitch).
-//           down:     kRows rows of Wd (pitch 2*inner + 16), then kTT h rows (same pitch).
+//           down:     kRows/4 groups of 4 Wd rows (one copy each, see dn_gpitch), then kTT
+//                     h rows (pitch 2*inner + 16).
 
 __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up(LayerArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -559,7 +584,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
                 waited = true;
                 for (int q = 0; q < it; ++q)
                     if (lane < pend_mt[q])
-                        bulk_load(r.st[q] + (size_t)(kRows + lane) * (2 * pend_inner[q] + kPad),
+                        bulk_load(r.st[q] + dn_hoff(pend_inner[q]) + (size_t)lane * (2 * pend_inner[q] + kPad),
                                   a.h + (size_t)(pend_row[q] + lane) * a.Imax, pend_inner[q] * 2, &r.full[q]);
             }
             if (__shfl_sync(0xffffffffu, *(volatile int*)&r.misc[0], 0)) break;
@@ -622,11 +647,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
             if (lane == 0) mbar_arrive_expect_tx(&r.full[s], (uint32_t)((kRows + mt) * inner * 2));
             __syncwarp();
             uint8_t* st = r.st[s];
-            copy_rows(st, pitch, W + (size_t)blk * kRows * inner, inner, kRows, inner * 2, &r.full[s], lane);
+            copy_rows(st, dn_gpitch(inner), W + (size_t)blk * kRows * inner, 4 * (size_t)inner, kRows / 4, inner * 8,
+                      &r.full[s], lane);
             if (waited) {
                 if (lane < mt)
-                    bulk_load(st + (size_t)(kRows + lane) * pitch, a.h + (size_t)(hrow0 + lane) * a.Imax, inner * 2,
-                              &r.full[s]);
+                    bulk_load(st + dn_hoff(inner) + (size_t)lane * pitch, a.h + (size_t)(hrow0 + lane) * a.Imax,
+                              inner * 2, &r.full[s]);
             } else {
                 pend_row[it] = hrow0;
                 pend_mt[it] = mt;
@@ -639,7 +665,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
             grid_dep_wait();
             for (int q = 0; q < it; ++q)
                 if (lane < pend_mt[q])
-                    bulk_load(r.st[q] + (size_t)(kRows + lane) * (2 * pend_inner[q] + kPad),
+                    bulk_load(r.st[q] + dn_hoff(pend_inner[q]) + (size_t)lane * (2 * pend_inner[q] + kPad),
                               a.h + (size_t)(pend_row[q] + lane) * a.Imax, pend_inner[q] * 2, &r.full[q]);
         }
         if (lane == 0) drain(r, it, err);
@@ -660,9 +686,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
         const int mtile = warp & 3, khalf = warp >> 2;
         const int kh = inner / 2;
         const uint32_t sa = smem_u32(r.st[s]);
+        // M tile mtile: rows j, j+1 (j = 2*(mtile & 1)) of groups 8*(mtile >> 1) .. +7
+        const int gbase = 8 * (mtile >> 1), jbase = 2 * (mtile & 1);
+        const int tr = lane & 15;
+        const uint32_t a_row = sa + (uint32_t)((gbase + (tr & 7)) * dn_gpitch(inner) + (jbase + (tr >> 3)) * inner * 2);
+        const uint32_t b_row = sa + (uint32_t)(dn_hoff(inner) + (lane & 7) * pitch);
         float d[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_rows(d, sa + (uint32_t)(mtile * 16 * pitch), sa + (uint32_t)(kRows * pitch), pitch, khalf * kh, kh / 16,
-                 lane);
+        mma_rows_at(d, a_row, b_row, khalf * kh, kh / 16, lane);
         // tokens of this lane's accumulator columns
         const int t0 = 2 * (lane & 3);
         size_t y0 = 0, y1 = 0;
@@ -676,21 +706,21 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
             s1 = m.sc[t0 + 1];
         }
         release_stage(r, it);
-        // fixed-order sum of the two K halves, then scale and store: lane l holds rows l/4 and
-        // l/4 + 8 of the M tile for tokens t0, t0 + 1
+        // fixed-order sum of the two K halves, then scale and store: lane l holds tile rows l/4
+        // and l/4 + 8 (Wd rows 4*(gbase + l/4) + jbase and the next one) for tokens t0, t0 + 1
         float* red = r.red + (size_t)s * kWarps * 128;
         if (khalf == 1) *reinterpret_cast<float4*>(red + (mtile * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
         consumers_sync();
         if (khalf == 0) {
             const float4 v = *reinterpret_cast<const float4*>(red + (mtile * 32 + lane) * 4);
-            const int row = mtile * 16 + (lane >> 2);
+            const int row = 4 * (gbase + (lane >> 2)) + jbase;
             if (t0 < mt) {
                 a.Y[y0 + row] = s0 * (d[0] + v.x);
-                a.Y[y0 + row + 8] = s0 * (d[2] + v.z);
+                a.Y[y0 + row + 1] = s0 * (d[2] + v.z);
             }
             if (t0 + 1 < mt) {
                 a.Y[y1 + row] = s1 * (d[1] + v.y);
-                a.Y[y1 + row + 8] = s1 * (d[3] + v.w);
+                a.Y[y1 + row + 1] = s1 * (d[3] + v.w);
             }
         }
     }
