@@ -17,11 +17,10 @@
 //   4. routed gate_up: CTA c's even share of the n_act x I (expert, feature) pairs. Like the
 //      scores, its h values are stored as tagged 64-bit words (two bf16 values and the tag);
 //   5. down + combine: CTA c owns output rows [c*H/G, (c+1)*H/G) of every expert, shared and
-//      routed. The shared expert's block comes right after the routing (its h values were
-//      written in step 2), the routed blocks stream in behind step 4; the CTA gathers the
-//      tagged h rows into shared memory as soon as they carry this call's tag, multiplies, and
-//      sums residual + gated shared output + weighted slots 0..K-1 of its rows in that fixed
-//      order.
+//      routed. The shared expert's block comes right after step 3 (its h values were written in
+//      step 2), the routed blocks stream in behind step 4; the CTA gathers the tagged h rows
+//      into shared memory as soon as they carry this call's tag, multiplies, and sums residual
+//      + gated shared output + weighted slots 0..K-1 of its rows in that fixed order.
 //
 // Roles: a producer warp streams each stage's rows into a ring of shared-memory stages with 1-D
 // TMA bulk copies (one per row; rows 16 bytes apart modulo 128 so ldmatrix is conflict-free);
@@ -478,10 +477,6 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
                 ++it;
             }
         }
-        // 2. shared gate_up: features [c*Is/G, (c+1)*Is/G), all tokens, h rows P..P+T-1
-        const int fs0 = even_split(a.Is, c, G), fs1 = even_split(a.Is, c + 1, G);
-        for (int f = fs0; f < fs1 && ok; f += g.sf)
-            issue_up(a.sgu, a.Is, f, min(g.sf, fs1 - f), P, T, 0x76543210u);
         // down rows o0..o0+ro-1 of block j0.. (nb blocks) into the next stage
         auto issue_down = [&](int j0, int nb) {
             const int s = claim();
@@ -507,8 +502,14 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
             }
             ++it;
         };
+        // 2. shared gate_up: features [c*Is/G, (c+1)*Is/G), all tokens, h rows P..P+T-1
+        //    (computed while the other CTAs' scores arrive)
+        const int fs0 = even_split(a.Is, c, G), fs1 = even_split(a.Is, c + 1, G);
+        for (int f = fs0; f < fs1 && ok; f += g.sf)
+            issue_up(a.sgu, a.Is, f, min(g.sf, fs1 - f), P, T, 0x76543210u);
         // 3. the consumers compute the routing and hand the tables over through `routed`; the
-        //    shared expert's down rows stream in meanwhile
+        //    shared expert's down rows (output rows o0..o0+ro-1, slot 0) stream in meanwhile and
+        //    are multiplied while the first routed weights are in flight
         if (ok) post(kStTopK);
         if (ok && ro > 0) issue_down(0, 1);
         if (ok && !warp_wait(routed, 0, lane)) ok = false;
@@ -544,11 +545,14 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
 
     // ================= consumers
     const int tid = threadIdx.x;
-    // router bias of this warp's router row (if any), requested before the first wait
+    // router bias of the router row whose slices this warp sums (router stage with up to 8
+    // rows, see there), requested before the first wait
     float bias = 0.f;
     {
-        const int row = c * g.rr + warp;
-        if (warp < g.rr && row < E && a.router_b) bias = __bfloat162float(a.router_b[row]);
+        const int nrr = max(0, min(E + 1, c * g.rr + g.rr) - c * g.rr);
+        const int wpr = nrr <= 1 ? 8 : nrr <= 2 ? 4 : nrr <= 4 ? 2 : 1;
+        const int row = c * g.rr + warp / wpr;
+        if (warp / wpr < nrr && row < E && a.router_b) bias = __bfloat162float(a.router_b[row]);
     }
     if (!consumers_all(warp_wait(xbar, 0, lane)) && tid == 0) atomicOr(err, ERR_TIMEOUT);
     int rb = 0;  // reduction buffer in use (alternates between the stages that reduce)
@@ -628,14 +632,18 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
         }
 
         if (m.type == kStRoute) {
-            // warp w < n: router row row0 + w for every token; lane l takes elements 8l + 256i
-            if (warp < m.n) {
-                const int row = m.row0 + warp;
-                const uint8_t* wr = stp + (size_t)warp * g.xp;
+            // rows row0 .. row0+n-1 for every token: wpr warps per row, each a K slice of H/wpr
+            // (lane l takes elements 8l + 256i of it); the slices' sums are added in a fixed
+            // order by the row's first warp. Beyond 8 rows, warps loop over rows.
+            const int wpr = m.n <= 1 ? 8 : m.n <= 2 ? 4 : m.n <= 4 ? 2 : 1;
+            const int kl = H / wpr, q = warp % wpr;
+            float* part = rbuf;  // [warp][kDTT] slice sums
+            for (int rl = warp / wpr; rl < m.n; rl += kWarps / wpr) {
+                const uint8_t* wr = stp + (size_t)rl * g.xp;
                 float acc[kDTT];
 #pragma unroll
                 for (int t = 0; t < kDTT; ++t) acc[t] = 0.f;
-                for (int k = lane * 8; k < H; k += 256) {
+                for (int k = q * kl + lane * 8; k < (q + 1) * kl; k += 256) {
                     const uint4 wv = *reinterpret_cast<const uint4*>(wr + k * 2);
 #pragma unroll
                     for (int t = 0; t < kDTT; ++t)
@@ -650,13 +658,31 @@ __global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeo
                 for (int t = 0; t < kDTT; ++t)
                     if (t < T) {
                         const float v = warp_sum(acc[t]);
-                        if (lane == t) mine = v + bias;
+                        if (lane == t) mine = v;
                     }
-                if (lane < T)
-                    st_relaxed_u64(a.dlog + (size_t)lane * (E + 1) + row,
-                                   ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(mine));
+                if (wpr == 1) {
+                    if (lane < T) {
+                        const int row = m.row0 + rl;
+                        const float b = (row < E && a.router_b) ? __bfloat162float(a.router_b[row]) : 0.f;
+                        st_relaxed_u64(a.dlog + (size_t)lane * (E + 1) + row,
+                                       ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(mine + b));
+                    }
+                } else if (lane < T) {
+                    part[warp * kDTT + lane] = mine;
+                }
             }
             release();
+            if (wpr > 1) {
+                consumers_sync();
+                rb ^= 1;
+                if (q == 0 && warp / wpr < m.n && lane < T) {
+                    float v = 0.f;
+                    for (int w = warp; w < warp + wpr; ++w) v += part[w * kDTT + lane];
+                    const int row = m.row0 + warp / wpr;
+                    st_relaxed_u64(a.dlog + (size_t)lane * (E + 1) + row,
+                                   ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v + bias));
+                }
+            }
             continue;
         }
 
