@@ -109,23 +109,20 @@ def max_over_ranks(v: float) -> float:
 # peaks, clocks
 
 
-# Source file of each kernel whose DRAM traffic a committed ncu summary records; a recorded
-# figure is used only while the file still hashes to the value stored with it.
-KERNEL_SOURCES = {"decode_fused": "sparse_moe_ffn_router_gb300/csrc/decode.cu",
-                  "gate_up": "sparse_moe_ffn_router_gb300/csrc/gemm.cu"}
-
-
 def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch (read + write) of `kernel` on `workload` from profiles/
-    ncu_traffic.json, or None when absent or recorded for another version of the source."""
+    ncu_traffic.json, or None when absent or recorded for another version of the kernel's
+    source file (each record names the file and its SHA-1)."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             rec = json.load(f).get(kernel, {}).get(workload)
-        with open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb") as f:
+        if not rec:
+            return None
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
             sha = hashlib.sha1(f.read()).hexdigest()
-    except (OSError, KeyError, ValueError, AttributeError):
+    except (OSError, KeyError, ValueError, AttributeError, TypeError):
         return None
-    if not rec or rec.get("source_sha1") != sha:
+    if rec.get("source_sha1") != sha:
         return None
     return rec.get("dram_bytes_per_launch")
 
