@@ -129,12 +129,13 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // Router scores, top-K and dispatch: one fused launch for few tokens, else separate kernels.
-// Routing: up to 8 tokens on one thread-block cluster; beyond, scores over (E+1)/8 x T/8 CTAs,
-// top-K one warp per token, then the three dispatch kernels. (The single-kernel routing of
-// up to 64 tokens scores on only (E+1)/8 CTAs and routes all tokens in its last CTA; measured
-// at 16-64 tokens it is as fast or slower, so only the fixed-scratch entry point uses it.)
+// Routing: up to 8 tokens on one thread-block cluster; 9..255 tokens in two kernels (tensor-
+// pipe scores, then top-K and the whole dispatch in one CTA); from 256 tokens the scores as a
+// tcgen05 GEMM, top-K one warp per token and the three block-parallel dispatch kernels. (The
+// single-kernel routing of up to 64 tokens is used only by the fixed-scratch entry point.)
 cudaError_t launch_routing(const LayerArgs& a, cudaStream_t s) {
     if (route_cluster_supported(a)) return launch_route_cluster(a, s);
+    if (route_small_supported(a)) return launch_route_small(a, s);
     cudaError_t e = launch_router(a, s);
     if (e == cudaSuccess) e = launch_dispatch(a, s);
     return e;

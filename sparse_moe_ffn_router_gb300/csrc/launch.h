@@ -75,6 +75,8 @@ struct GemmPlan {
 
 cudaError_t launch_router(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_route_fused(const LayerArgs& a, cudaStream_t s);
+bool route_small_supported(const LayerArgs& a);
+cudaError_t launch_route_small(const LayerArgs& a, cudaStream_t s);
 bool route_cluster_supported(const LayerArgs& a);
 cudaError_t launch_route_cluster(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_router_gemm(const LayerArgs& a, cudaStream_t s);
