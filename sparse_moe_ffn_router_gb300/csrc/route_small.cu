@@ -15,6 +15,9 @@
 //   shared gate; then the dispatch as one stable counting sort of the T*K (token, slot) pairs in
 //   chunks of 1024: within a warp, pairs of one expert are ranked by lane (match_any), across
 //   the warps of a chunk by a prefix of per-warp counts, across chunks by running counts.
+// Both launch early (programmatic dependent launch): k_route_small waits for the scores
+// (griddepcontrol.wait) and at once lets the expert kernel after it start the shared expert's
+// work, which needs no routing; that kernel waits for the routing before its routed work.
 #include <math.h>
 
 #include "launch.h"
@@ -34,6 +37,7 @@ __global__ void __launch_bounds__(256) k_router_mma(LayerArgs a) {
     __shared__ __align__(8) uint64_t full[2];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* base = smem_raw + (((raw + 127u) & ~127u) - raw);
+    grid_dep_launch();  // the routing kernel may launch; it waits for this grid's scores
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = blockIdx.x * kRmRows, t0 = blockIdx.y * kRmTok;
     const int nr = min(kRmRows, a.E + 1 - row0), nt = min(kRmTok, a.T - t0);
@@ -120,6 +124,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) k_route_small(LayerArgs a) {
     __shared__ int n_act_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, E = a.E, K = a.K, P = T * K;
+    grid_dep_wait();    // the scores of k_router_mma
+    grid_dep_launch();  // the expert kernel may start its shared-expert work
 
     // 1. top-K, weights and shared gate of every token
     for (int t = warp; t < T; t += kRsWarps) {
@@ -270,7 +276,18 @@ cudaError_t launch_route_small(const LayerArgs& a, cudaStream_t s) {
     }
     const dim3 g1((a.E + 1 + kRmRows - 1) / kRmRows, (a.T + kRmTok - 1) / kRmTok);
     MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (k_router_mma<<<g1, 256, kRmSmem, s>>>(a)));
-    MOE_LAUNCH(MOE_KERNEL_ROUTER_TOPK, s, (k_route_small<<<1, kRsThreads, 0, s>>>(a)));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kRsThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaSuccess;
+    MOE_LAUNCH(MOE_KERNEL_ROUTER_TOPK, s, (e = cudaLaunchKernelEx(&cfg, k_route_small, a)));
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
