@@ -362,17 +362,20 @@ cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, const CUte
 
 // Router scores of all T tokens on the tensor cores: logits[:, 0:E] = x . Wr^T (+ br).
 cudaError_t launch_router_gemm(const LayerArgs& a, cudaStream_t s) {
+    // 64-wide N tiles: the E <= 256 score columns of T/128 token tiles would otherwise give
+    // only T/128 tiles for 152 SMs
+    constexpr int kBNr = 64;
     CUtensorMap mx, mw;
-    if (!make_map(&mx, a.x, a.T, a.H, a.H, kBM) || !make_map(&mw, a.router_w, a.E, a.H, a.H, 256))
+    if (!make_map(&mx, a.x, a.T, a.H, a.H, kBM) || !make_map(&mw, a.router_w, a.E, a.H, a.H, kBNr))
         return cudaErrorInvalidValue;
     GemmPlan p{};
     p.dense_rows = a.T;
-    p.dense_tiles = (a.T + kBM - 1) / kBM;
+    p.dense_tiles = ((a.T + kBM - 1) / kBM) * ((a.E + kBNr - 1) / kBNr);
     p.k_routed = p.k_shared = a.H;
     p.err = &a.hdr->err;
     const int grid = min(p.dense_tiles, a.num_sms);
     cudaError_t e;
-    MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (e = launch_gemm<kLogits, 256>(mx, mx, mw, mw, p, a, grid, s)));
+    MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (e = launch_gemm<kLogits, kBNr>(mx, mx, mw, mw, p, a, grid, s)));
     return e;
 }
 
