@@ -133,7 +133,7 @@ enum {
     /* (from T >= 256 the router scores, gate_up and down run as tensor-core GEMMs) */
     MOE_KERNEL_COMBINE = 7,         /* fixed-order sum into the residual           */
     MOE_KERNEL_RMSNORM = 8,
-    MOE_KERNEL_SHARED_GATE = 9,     /* shared-expert gate scores (many-token path)  */
+    MOE_KERNEL_SHARED_GATE = 9,     /* not launched: the top-K kernel scores the shared gate */
     MOE_KERNEL_GATHER = 10,         /* token rows in dispatch order (many-token path) */
     MOE_KERNEL_GEMM_PLAN = 11,      /* group/tile tables of the expert GEMMs        */
     MOE_KERNEL_DECODE_FUSED = 12,   /* whole layer in one persistent kernel (T <= 8) */

@@ -104,6 +104,21 @@ __global__ void __launch_bounds__(256) k_router_topk(LayerArgs a) {
             sel_e[k] = be;
         }
     }
+    // shared-expert gate score: from the score kernel (column E), or, when the E router columns
+    // came from the tensor-core GEMM, one more dot product x[t] . ws here
+    float z;
+    if (a.gemm) {
+        float acc = 0.f;
+        for (int c = lane; c < a.H / 8; c += 32) {
+            float xf[8];
+            unpack8(ld_ro(a.x + (size_t)t * a.H + (size_t)c * 8), xf);
+            acc = dot8(ld_ro(a.sg + (size_t)c * 8), xf, acc);
+        }
+        z = warp_sum(acc);
+        if (lane == 0) a.logits[(size_t)t * a.ldl + a.E] = z;
+    } else {
+        z = l[a.E];
+    }
     if (lane == 0) {
         float ex[8], s = 0.f;
 #pragma unroll
@@ -118,34 +133,16 @@ __global__ void __launch_bounds__(256) k_router_topk(LayerArgs a) {
                 a.ids[(size_t)t * a.K + k] = sel_e[k];
                 a.topw[(size_t)t * a.K + k] = ex[k] / s;
             }
-        const float z = l[a.E];
         if (!isfinite(z)) bad = true;
         a.sgate[t] = 1.0f / (1.0f + expf(-z));
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&a.hdr->err, ERR_NONFINITE_SCORE);
 }
 
-// Shared-expert gate score of every token, logits[t, E] = x[t] . ws (one warp per token);
-// the many-token path scores the E router columns on the tensor cores.
-__global__ void __launch_bounds__(256) k_shared_gate_scores(LayerArgs a) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= a.T) return;
-    float acc = 0.f;
-    for (int c = lane; c < a.H / 8; c += 32) {
-        float xf[8];
-        unpack8(ld_ro(a.x + (size_t)t * a.H + (size_t)c * 8), xf);
-        acc = dot8(ld_ro(a.sg + (size_t)c * 8), xf, acc);
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) a.logits[(size_t)t * a.ldl + a.E] = acc;
-}
-
 cudaError_t launch_router(const LayerArgs& a, cudaStream_t s) {
     if (a.gemm) {
         cudaError_t e = launch_router_gemm(a, s);
         if (e != cudaSuccess) return e;
-        MOE_LAUNCH(MOE_KERNEL_SHARED_GATE, s, (k_shared_gate_scores<<<(a.T + 7) / 8, 256, 0, s>>>(a)));
     } else {
         dim3 g1((a.E + 1 + 7) / 8, (a.T + kRouterTokens - 1) / kRouterTokens);
         MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (k_router_scores<<<g1, 256, 0, s>>>(a)));
