@@ -61,6 +61,7 @@ def _load():
             lib.oracle_forward.restype = ctypes.c_int
             lib.oracle_forward.argtypes = [ctypes.POINTER(Dims)] + [P] * 16
             lib.oracle_rmsnorm.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, ctypes.c_double, P]
+            lib.oracle_router_stats.argtypes = [ctypes.POINTER(Dims)] + [P] * 6
             _lib = lib
     return _lib
 
@@ -120,6 +121,20 @@ def route(dims, x, router_w, router_b=None, want_probs=False) -> dict:
     if want_probs:
         r["probs"] = probs
     return r
+
+
+def router_stats(dims, x, router_w, router_b=None) -> dict:
+    """Load-balancing statistics: P [E] (mean router probability), f [E] (share of the
+    (token, slot) assignments) and loss = 0.001 * E * sum(f * P), all fp64."""
+    lib = _load()
+    d = Dims(*dims)
+    x, wr, br = _u16(x), _u16(router_w), _u16(router_b)
+    P = np.zeros(d.E, np.float64)
+    f = np.zeros(d.E, np.float64)
+    loss = np.zeros(1, np.float64)
+    if lib.oracle_router_stats(ctypes.byref(d), _p(x), _p(wr), _p(br), _p(P), _p(f), _p(loss)) != 0:
+        raise ValueError(f"oracle_router_stats rejected dims {dims}")
+    return dict(P=P, f=f, loss=float(loss[0]))
 
 
 def permute(dims, ids) -> dict:

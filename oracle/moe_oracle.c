@@ -203,6 +203,55 @@ int oracle_route(const oracle_dims* d, const uint16_t* x, const uint16_t* router
     return 0;
 }
 
+/* Load-balancing statistics ("Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256
+ * Experts, Load Balancing: an auxiliary loss with coefficient 0.001 penalises uneven expert
+ * utilisation across the batch). The page names the loss but gives no formula; this oracle
+ * computes the two per-expert quantities such a loss is built from, and the product form
+ * that is smallest when routing is uniform:
+ *   P_e  = (1/T) sum_t softmax(l_t)_e      mean router probability of expert e,
+ *   f_e  = count_e / (T K)                 share of the T*K (token, slot) assignments,
+ *   loss = 0.001 * E * sum_e f_e * P_e     (exactly 0.001 for uniform routing).
+ * Sums run over t ascending and then e ascending. T = 0 gives zeros. Returns 0, or -1 when
+ * the dims are unusable. */
+int oracle_router_stats(const oracle_dims* d, const uint16_t* x, const uint16_t* router_w, const uint16_t* router_b,
+                        double* P, double* f, double* loss) {
+    const int T = d->T, E = d->E, K = d->K;
+    if (T < 0 || E <= 0 || K <= 0 || K > E || d->H <= 0) return -1;
+    for (int e = 0; e < E; ++e) P[e] = f[e] = 0.0;
+    *loss = 0.0;
+    if (T == 0) return 0;
+    const size_t P_ = (size_t)T * K;
+    int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * P_);
+    double* w = (double*)malloc(sizeof(double) * P_);
+    double* probs = (double*)malloc(sizeof(double) * (size_t)T * E);
+    int32_t* counts = (int32_t*)malloc(sizeof(int32_t) * E);
+    int32_t* offsets = (int32_t*)malloc(sizeof(int32_t) * (E + 1));
+    int32_t* perm = (int32_t*)malloc(sizeof(int32_t) * P_);
+    int32_t* inv = (int32_t*)malloc(sizeof(int32_t) * P_);
+    int rc = -1;
+    if (ids && w && probs && counts && offsets && perm && inv &&
+        oracle_route(d, x, router_w, router_b, ids, w, probs, counts, offsets, perm, inv) == 0) {
+        for (int e = 0; e < E; ++e) {
+            double s = 0.0;
+            for (int t = 0; t < T; ++t) s += probs[(size_t)t * E + e];
+            P[e] = s / T;
+            f[e] = (double)counts[e] / (double)P_;
+        }
+        double acc = 0.0;
+        for (int e = 0; e < E; ++e) acc += f[e] * P[e];
+        *loss = 0.001 * E * acc;
+        rc = 0;
+    }
+    free(ids);
+    free(w);
+    free(probs);
+    free(counts);
+    free(offsets);
+    free(perm);
+    free(inv);
+    return rc;
+}
+
 /* One SwiGLU feed-forward network applied to one token:
  *   expert(x) = SiLU(x . W_gate) (elementwise *) (x . W_up) . W_down
  * ("Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256 Experts, Experts; the same

@@ -346,3 +346,58 @@ def test_gap_control_separates_scores():
     g = top_gaps(oracle.router_logits(wl.dims, x, wr), wl.K)
     assert (g >= 1e-3).all()
     print(f"rows redrawn: {(attempts > 0).sum()} of {wl.T}")
+
+
+# ---------------------------------------------------------------------------------------
+# Load-balancing statistics (inputs of the auxiliary loss): closed forms and invariants
+
+
+def test_stats_uniform_scores_closed_form():
+    """All scores equal: every expert has probability 1/E and every token picks experts
+    0..K-1, so P = 1/E, f = 1/K on the first K experts and 0 elsewhere, and the loss is the
+    coefficient itself."""
+    H, E, K, T = 8, 32, 4, 5
+    w = _zero_layer(H, E, 4, 4)
+    s = oracle.router_stats((T, H, E, K, 4, 4), synth.make_x(T, H, 1), w["router_w"])
+    np.testing.assert_array_equal(s["P"], np.full(E, 1.0 / E))
+    np.testing.assert_array_equal(s["f"], np.r_[np.full(K, 1.0 / K), np.zeros(E - K)])
+    assert s["loss"] == pytest.approx(0.001, rel=1e-15)
+
+
+def test_stats_two_experts_reduce_to_the_logistic_function():
+    """E = 2, K = 1, one-hot tokens: the softmax of two scores is the logistic function of
+    their difference, so P_0 is the mean of sig(l_t0 - l_t1) over the tokens."""
+    H, E, K = 16, 2, 1
+    wr = torch.zeros(E, H, dtype=torch.bfloat16)
+    wr[0, 0] = 1.0  # expert 0 scores x[0]
+    wr[1, 1] = 1.0  # expert 1 scores x[1]
+    x = torch.zeros(3, H, dtype=torch.bfloat16)
+    x[0, 0] = 2.0  # scores (2, 0): expert 0
+    x[1, 0] = 4.0  # scores (4, 0): expert 0
+    x[2, 0], x[2, 1] = 0.5, 1.0  # scores (0.5, 1): expert 1
+    s = oracle.router_stats((3, H, E, K, 4, 4), x, wr)
+    p0 = (sig(2.0) + sig(4.0) + sig(-0.5)) / 3
+    np.testing.assert_allclose(s["P"], [p0, 1.0 - p0], rtol=1e-14)
+    np.testing.assert_array_equal(s["f"], [2 / 3, 1 / 3])
+    assert s["loss"] == pytest.approx(0.002 * (2 / 3 * p0 + 1 / 3 * (1 - p0)), rel=1e-14)
+
+
+def test_stats_invariants_and_expert_relabelling():
+    """Random layers: P and f are distributions over the experts, f * T * K are the routing
+    counts, and relabelling the experts (permuting the router rows and the bias) permutes P
+    and f and leaves the loss unchanged."""
+    T, H, E, K = 24, 128, 32, 4
+    dims = (T, H, E, K, 64, 64)
+    w = _rand_layer(H, E, 64, 64, 9, router_std=0.5)
+    br = synth.zipf_bias(E, 1.1, 9)
+    x = synth.make_x(T, H, 9)
+    s = oracle.router_stats(dims, x, w["router_w"], br)
+    assert s["P"].sum() == pytest.approx(1.0, abs=1e-13) and s["f"].sum() == pytest.approx(1.0, abs=1e-13)
+    assert (s["P"] > 0).all() and (s["f"] >= 0).all()
+    counts = oracle.route(dims, x, w["router_w"], br)["counts"]
+    np.testing.assert_array_equal(np.rint(s["f"] * T * K).astype(np.int64), counts)
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(E))
+    s2 = oracle.router_stats(dims, x, w["router_w"][perm], br[perm])
+    np.testing.assert_allclose(s2["P"], s["P"][perm.numpy()], rtol=1e-12, atol=1e-18)
+    np.testing.assert_array_equal(s2["f"], s["f"][perm.numpy()])
+    assert s2["loss"] == pytest.approx(s["loss"], rel=1e-12)
