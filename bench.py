@@ -407,6 +407,41 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
     return res
 
 
+def time_stats(ls: LayerSet, peaks: dict, n: int = 20, reps: int = 10) -> dict:
+    """moe_router_stats (load-balancing statistics) on one layer: a CUDA graph of n calls,
+    replayed reps times. Bytes: router weights and x read, the score matrix written and read
+    back, the ids read."""
+    moe = ls.moe
+    T, H, E, K = ls.dims[:4]
+    dev = ls.out.device
+    P = torch.empty(E, dtype=torch.float32, device=dev)
+    f = torch.empty(E, dtype=torch.float32, device=dev)
+    loss = torch.empty(4, dtype=torch.float32, device=dev)
+    W, x = ls.layers[0]
+    for _ in range(3):
+        moe.moe_router_stats(ls.dims, x, W, P, f, loss, ls.ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(n):
+            moe.moe_router_stats(ls.dims, x, W, P, f, loss, ls.ws)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / (n * reps)
+    nbytes = 2 * (E + 1) * H + 2 * T * H + 2 * 4 * T * (E + 1) + 4 * T * K
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_call": round(us, 2), "tokens_per_s": round(T / (us * 1e-6), 1),
+            "device_error": moe.moe_last_device_error(ls.ws),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_call": nbytes}}
+
+
 def time_e2e(ls: LayerSet, steps: int, warmup: int) -> dict:
     """Same metric through the public call with host buffers: per step, x is copied from
     pinned host memory, the layer runs, and the output is copied back to pinned memory."""
@@ -588,11 +623,13 @@ def main():
                                auto=(1.0, 5, 500), graph=not args.no_graph and w2.T <= 64)
             if r.get("roofline"):
                 r["roofline"]["traffic"] = ncu_traffic(r["roofline"]["kernel"], w2.name)
+            stats = time_stats(ls2, peaks)
             also[name] = {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 5),
                           "device_error": r["device_error"],
                           "roofline": r.get("roofline"), "hbm_frac_of_layer_bytes": r["layer_hbm_frac"],
                           "tensor_frac": r["layer_tensor_frac"], "unique_experts_per_step": r["unique_experts"],
-                          "kernel_ms_warmup": {k: round(v, 5) for k, v in r["warm_kernel_ms"].items()}}
+                          "kernel_ms_warmup": {k: round(v, 5) for k, v in r["warm_kernel_ms"].items()},
+                          "router_stats": stats}
             del ls2
         torch.cuda.empty_cache()
     line["also"] = also

@@ -121,6 +121,21 @@ moe_status moe_last_device_error(void* workspace, void* stream);
  * Row strides are the widths given. Returns MOE_ERR_INVALID_ARG for an unknown tap. */
 moe_status moe_workspace_tap(const moe_dims* d, int tap, size_t* offset, size_t* bytes);
 
+/* Load-balancing statistics of one routing call ("Qwen3.6-35B-A3B -- Architecture Overview",
+ * MoE FFN: 256 Experts, Load Balancing: an auxiliary loss, coefficient 0.001, penalises uneven
+ * expert utilisation across the batch). The page gives no formula; this computes, for the T
+ * tokens of x, the quantities such a loss is built from and the product form that is
+ * smallest under uniform routing:
+ *   P[e] = (1/T) sum_t softmax(router scores of token t)[e]   (full softmax over the E scores)
+ *   f[e] = (tokens routed to expert e) / (T*K)
+ *   loss = 0.001 * E * sum_e f[e] * P[e]
+ * P, f: [E] fp32; loss: one fp32; all device pointers (P and f 16-byte aligned), owned by the
+ * caller. The routing is the same as moe_route's (and it leaves the same results in the
+ * workspace). Every sum runs in a fixed order, so repeated calls give identical bits.
+ * T = 0 writes zeros. Errors as moe_route. */
+moe_status moe_router_stats(const moe_dims* d, const void* x, const moe_weights* w, float* P, float* f, float* loss,
+                            void* workspace, size_t ws_bytes, void* stream);
+
 /* Kernels of the layer, for moe_set_trace. */
 enum {
     MOE_KERNEL_ROUTER_SCORES = 0,   /* router + shared-gate scores                 */
@@ -137,7 +152,8 @@ enum {
     MOE_KERNEL_GATHER = 10,         /* token rows in dispatch order (many-token path) */
     MOE_KERNEL_GEMM_PLAN = 11,      /* group/tile tables of the expert GEMMs        */
     MOE_KERNEL_DECODE_FUSED = 12,   /* whole layer in one persistent kernel (T <= 8) */
-    MOE_KERNEL_COUNT = 13
+    MOE_KERNEL_ROUTER_STATS = 13,   /* load-balancing statistics (moe_router_stats) */
+    MOE_KERNEL_COUNT = 14
 };
 
 /* Benchmarking aid. While set, every launch of `kernel` made by this library records

@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     moe_set_trace,
     moe_rmsnorm,
     moe_route,
+    moe_router_stats,
     moe_workspace_init,
     moe_workspace_size,
     moe_workspace_tap,

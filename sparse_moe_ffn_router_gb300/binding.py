@@ -18,10 +18,11 @@ from . import build as _build
 MOE_STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_MISALIGNED",
               4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE"}
 EXPORTED = ["moe_workspace_size", "moe_workspace_init", "moe_route", "moe_forward", "moe_rmsnorm",
-            "moe_last_device_error", "moe_workspace_tap", "moe_set_trace", "moe_launch_count", "moe_route_noalloc", "moe_status_string"]
+            "moe_last_device_error", "moe_workspace_tap", "moe_set_trace", "moe_launch_count", "moe_route_noalloc", "moe_status_string",
+            "moe_router_stats"]
 KERNELS = {"router_scores": 0, "router_topk": 1, "dispatch_local": 2, "dispatch_scan": 3, "dispatch_scatter": 4,
            "gate_up": 5, "down": 6, "combine": 7, "rmsnorm": 8, "shared_gate": 9, "gather": 10, "gemm_plan": 11,
-           "decode_fused": 12}
+           "decode_fused": 12, "router_stats": 13}
 
 
 class Dims(ctypes.Structure):
@@ -100,6 +101,8 @@ def load_library(build_if_missing: bool = True):
             lib.moe_launch_count.argtypes = []
             lib.moe_route_noalloc.restype = st
             lib.moe_route_noalloc.argtypes = [D, P, W, P, P, P, P, P, P]
+            lib.moe_router_stats.restype = st
+            lib.moe_router_stats.argtypes = [D, P, W, P, P, P, P, S, P]
             lib.moe_status_string.restype = ctypes.c_char_p
             lib.moe_status_string.argtypes = [ctypes.c_int]
             _lib = lib
@@ -170,6 +173,15 @@ def moe_route_noalloc(dims, x, weights: Weights, ids, topk_w, counts, offsets, p
     _check(load_library().moe_route_noalloc(ctypes.byref(_dims(dims)), _ptr(x), ctypes.byref(w), _ptr(ids),
                                             _ptr(topk_w), _ptr(counts), _ptr(offsets), _ptr(perm), _stream(stream)),
            "moe_route_noalloc")
+
+
+def moe_router_stats(dims, x, weights: Weights, P, f, loss, workspace, stream=None):
+    """Load-balancing statistics: P [E] and f [E] fp32 (mean router probability, share of the
+    assignments) and loss [1] fp32 = 0.001 * E * sum(f * P)."""
+    w = weights.to_c()
+    _check(load_library().moe_router_stats(ctypes.byref(_dims(dims)), _ptr(x), ctypes.byref(w), _ptr(P), _ptr(f),
+                                           _ptr(loss), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                           _stream(stream)), "moe_router_stats")
 
 
 def moe_forward(dims, x, weights: Weights, residual, out, workspace, stream=None):

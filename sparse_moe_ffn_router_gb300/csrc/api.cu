@@ -179,6 +179,28 @@ extern "C" moe_status moe_route(const moe_dims* d, const void* x, const moe_weig
     return cuda_status(launch_routing(a, s));
 }
 
+extern "C" moe_status moe_router_stats(const moe_dims* d, const void* x, const moe_weights* w, float* P, float* f,
+                                       float* loss, void* workspace, size_t ws_bytes, void* stream) {
+    Plan p;
+    LayerArgs a;
+    moe_status st = prepare(d, x, w, workspace, ws_bytes, &p, &a);
+    if (st != MOE_OK) return st;
+    if (!P || !f || !loss) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(P) || !aligned16(f) || ((uintptr_t)loss & 3u)) return MOE_ERR_MISALIGNED;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (d->T == 0) {
+        cudaError_t e = cudaMemsetAsync(P, 0, sizeof(float) * d->E, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(f, 0, sizeof(float) * d->E, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(loss, 0, sizeof(float), s);
+        return cuda_status(e);
+    }
+    // every score column must be in the workspace: below 256 tokens the tensor-pipe score
+    // kernel and the one-CTA routing, from 256 the score GEMM and the top-K kernel
+    cudaError_t e = route_small_supported(a) ? launch_route_small(a, s) : launch_router(a, s);
+    if (e == cudaSuccess) e = launch_router_stats(a, P, f, loss, s);
+    return cuda_status(e);
+}
+
 extern "C" moe_status moe_forward(const moe_dims* d, const void* x, const moe_weights* w, const void* residual,
                                   void* out, void* workspace, size_t ws_bytes, void* stream) {
     Plan p;

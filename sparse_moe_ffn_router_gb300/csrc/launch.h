@@ -76,6 +76,7 @@ struct GemmPlan {
 cudaError_t launch_router(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_route_fused(const LayerArgs& a, cudaStream_t s);
 bool route_small_supported(const LayerArgs& a);
+cudaError_t launch_router_stats(const LayerArgs& a, float* P, float* f, float* loss, cudaStream_t s);
 cudaError_t launch_route_small(const LayerArgs& a, cudaStream_t s);
 bool route_cluster_supported(const LayerArgs& a);
 cudaError_t launch_route_cluster(const LayerArgs& a, cudaStream_t s);
