@@ -5,16 +5,19 @@
 // expert at the full shape, "Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256 Experts).
 //
 // Both kernels are persistent (one CTA per SM). A producer warp walks the CTA's work items and,
-// for each, fills one stage of a 2-stage shared-memory ring with 1-D TMA bulk copies
-// (cp.async.bulk; gate/up one per 4 KB row, down one per group of 4 consecutive 1 KB rows, with
-// 16 bytes of padding per row or group so ldmatrix is free of bank conflicts): the item's
-// weight rows plus its activation rows (up to 8 tokens), and writes
-// the item's metadata into the stage before arming its mbarrier. Eight consumer warps multiply
-// the staged rows with warp-level bf16 MMAs (m16n8k16, fp32 accumulate: 16 weight rows by
-// the item's tokens, padded to 8), each warp over a fixed K range, and sum the warps' partial
-// results in a fixed order. A stage is 16 (gate/up) or 64 (down) weight rows, too few rows for
-// the 64/128-row tcgen05 MMA without four times larger stages; the tensor-core work is small
-// either way, the kernels are bound by HBM.
+// for each, fills one stage of a 3-stage shared-memory ring with the item's weight rows only,
+// by 1-D TMA bulk copies (cp.async.bulk; gate/up one per 4 KB row, down one per group of 4
+// consecutive 1 KB rows, with 16 bytes of padding per row or group so ldmatrix is free of bank
+// conflicts), and writes the item's metadata into the stage before arming its mbarrier. The
+// ring is sized for bytes in flight: at the full-GPU HBM rate a loaded SM needs close to
+// 200 KB of copies outstanding, so the activation rows (x for gate_up, h for down) are kept
+// out of it. Eight consumer warps multiply the staged rows with warp-level bf16 MMAs
+// (m16n8k16, fp32 accumulate: 16 weight rows by the item's tokens, padded to 8), each warp over
+// a fixed K range whose token-row fragments it holds in registers, loaded from L2 when the
+// item's token set changes; the warps' partial results are summed in a fixed order. A stage
+// is 16 (gate/up) or 64 (down) weight rows, too few rows for the 64/128-row tcgen05 MMA without
+// four times larger stages; the tensor-core work is small either way, the kernels are bound by
+// HBM.
 //
 // k_stream_up:   h = bf16(SiLU(x . Wg^T) * (x . Wu^T)); a stage holds 8 gate rows and the 8
 //                matching up rows of one group, so the 16 x 8 MMA tile gives g and u of the same
@@ -30,39 +33,39 @@
 
 namespace moe {
 
-constexpr int kSt = 2;                  // ring stages
+constexpr int kSt = 3;                  // ring stages
 constexpr int kTT = 8;                  // tokens per item (the MMA's N)
 constexpr int kFps = 8;                 // up: features per stage (16 rows: 8 gate + 8 up)
 constexpr int kRows = 64;               // down: output rows per stage (= combine block)
-
-
-
 constexpr int kPad = 16;                // row padding: rows start 16 B apart modulo 128 B
 constexpr int kMaxH = 2048, kMaxInner = 512;
-constexpr int kPitchH = 2 * kMaxH + kPad, kPitchI = 2 * kMaxInner + kPad;
-constexpr int kStageBytes = 2 * kFps * kPitchH + kTT * kPitchH;  // the larger of the up and down layouts
-static_assert((kRows / 4) * (8 * kMaxInner + kPad) + kTT * kPitchI <= kStageBytes, "down stage must fit");
+constexpr int kPitchH = 2 * kMaxH + kPad;
+constexpr int kMaxSteps = 16;           // MMA k-steps of one consumer warp per stage, at most
+// A stage holds weight rows only: 16 gate/up rows of up to 2048 elements, or 16 groups of 4
+// down rows of up to 512 -- the same 65,792 bytes.
+constexpr int kStageBytes = 2 * kFps * kPitchH;
+static_assert((kRows / 4) * (8 * kMaxInner + kPad) <= kStageBytes, "down stage must fit");
+static_assert(kMaxH / kWarps / 16 <= kMaxSteps && kMaxInner / 2 / 16 <= kMaxSteps, "k-steps per warp");
 
 // Down stage layout: kRows/4 groups of 4 consecutive Wd rows, each group one 1-D bulk copy
 // (4 KB at inner = 512: copies of 1 KB rows stream markedly slower than 4 KB ones), groups
 // 8*inner + 16 bytes apart so any 8 consecutive groups start in 8 different 16-byte bank
-// slots; then kTT h rows, 2*inner + 16 bytes apart. An MMA tile of 16 rows takes rows j and
-// j+1 of 8 consecutive groups, so each 8x8 ldmatrix fetch reads 8 different bank slots.
+// slots. An MMA tile of 16 rows takes rows j and j+1 of 8 consecutive groups, so each 8x8
+// ldmatrix fetch reads 8 different bank slots.
 __host__ __device__ constexpr int dn_gpitch(int inner) { return 8 * inner + kPad; }
-__host__ __device__ constexpr int dn_hoff(int inner) { return (kRows / 4) * dn_gpitch(inner); }
 
 struct StageMeta {
     int mt;          // tokens in this item
-    int row0;        // up: h row of token 0
+    int row0;        // h row of the item's token 0 (up: written, down: read)
     int f0;          // up: first feature / down: first output row
     int inner;       // down: length of a weight row (I or Is)
-    int block;       // down: output block
+    int key;         // the item's token set: consecutive items with one key use the same rows
     int tok[kTT], slot[kTT];
     float sc[kTT];
 };
 
 struct Ring {
-    uint8_t* st[kSt];
+    uint8_t* st0;    // stage s at st0 + s * kStageBytes
     StageMeta* meta;
     float* red;      // [kSt][kWarps][32][4] per-warp partial accumulators
     uint64_t* full;
@@ -79,10 +82,8 @@ __device__ __forceinline__ Ring carve(uint8_t* raw) {
     const uint32_t base = smem_u32(raw);
     uint8_t* p = raw + (((base + 127u) & ~127u) - base);
     Ring r;
-    for (int s = 0; s < kSt; ++s) {
-        r.st[s] = p;
-        p += kStageBytes;
-    }
+    r.st0 = p;
+    p += kSt * kStageBytes;
     r.red = reinterpret_cast<float*>(p);
     p += kRedBytes;
     r.meta = reinterpret_cast<StageMeta*>(p);
@@ -92,36 +93,6 @@ __device__ __forceinline__ Ring carve(uint8_t* raw) {
     r.empty = r.full + kSt;
     r.misc = reinterpret_cast<int*>(r.empty + kSt);
     return r;
-}
-
-// D[16 x 8] += A[16 rows, k0 .. k0+16*ksteps) . B[8 rows, same k]^T, rows `pitch` bytes apart.
-// lane l addresses A row (l % 16) at k + 8*(l / 16) and B row (l % 8) at k + 8*((l / 8) % 2).
-__device__ __forceinline__ void mma_rows(float (&d)[4], uint32_t a_base, uint32_t b_base, int pitch, int k0,
-                                         int ksteps, int lane) {
-    const uint32_t a = a_base + (uint32_t)((lane & 15) * pitch + (k0 + 8 * (lane >> 4)) * 2);
-    const uint32_t b = b_base + (uint32_t)((lane & 7) * pitch + (k0 + 8 * ((lane >> 3) & 1)) * 2);
-#pragma unroll 4
-    for (int k = 0; k < ksteps; ++k) {
-        uint32_t a0, a1, a2, a3, b0, b1;
-        ldsm_x4(a + k * 32, a0, a1, a2, a3);
-        ldsm_x2(b + k * 32, b0, b1);
-        mma16816(d, a0, a1, a2, a3, b0, b1);
-    }
-}
-
-// The same MMA with per-lane row addresses: a_row is the A row this lane feeds to ldmatrix
-// (tile row lane % 16), b_row the B row (token row lane % 8), K from element k0.
-__device__ __forceinline__ void mma_rows_at(float (&d)[4], uint32_t a_row, uint32_t b_row, int k0, int ksteps,
-                                            int lane) {
-    const uint32_t a = a_row + (uint32_t)((k0 + 8 * (lane >> 4)) * 2);
-    const uint32_t b = b_row + (uint32_t)((k0 + 8 * ((lane >> 3) & 1)) * 2);
-#pragma unroll 4
-    for (int k = 0; k < ksteps; ++k) {
-        uint32_t a0, a1, a2, a3, b0, b1;
-        ldsm_x4(a + k * 32, a0, a1, a2, a3);
-        ldsm_x2(b + k * 32, b0, b1);
-        mma16816(d, a0, a1, a2, a3, b0, b1);
-    }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -216,12 +187,10 @@ __device__ __forceinline__ int routed_tiles(const LayerArgs& a, int lane) {
     return tot;
 }
 
-// Work of CTA c of G: shared-expert items c, c+G, ... below n_shared (they need no routing),
-// then routed items [c*R/G, (c+1)*R/G) -- a contiguous run, so consecutive items mostly share
-// their expert and token tile and the producer looks the routing up once per change.
-__device__ __forceinline__ int shared_items_of(int n_shared, int c, int G) {
-    return n_shared > c ? (n_shared - c + G - 1) / G : 0;
-}
+// Work of CTA c of G: shared-expert items [c*S/G, (c+1)*S/G) (they need no routing), then
+// routed items [c*R/G, (c+1)*R/G) -- contiguous runs, so consecutive items mostly share their
+// token tile (and expert): the producer looks the routing up, and the consumers load the token
+// rows, once per change.
 __device__ __forceinline__ int routed_split(int R, int c, int G) { return (int)((long long)c * R / G); }
 
 // Largest g with tiles[g] <= i (tiles ascending, tiles[0] = 0).
@@ -243,9 +212,26 @@ __device__ __forceinline__ void copy_rows(uint8_t* dst, int dst_pitch, const bf1
 
 // ---------------------------------------------------------------------------------------
 // Stage layout, up:   rows 0..7 gate features f0..f0+7, rows 8..15 the matching up rows
-//                     (pitch 2H + 16), then kTT activation rows (same pitch).
-//           down:     kRows/4 groups of 4 Wd rows (one copy each, see dn_gpitch), then kTT
-//                     h rows (pitch 2*inner + 16).
+//                     (pitch 2H + 16).
+//           down:     kRows/4 groups of 4 Wd rows (one copy each, see dn_gpitch).
+// The activation rows (x for up, h for down) are not staged: each consumer warp holds its K
+// range of the item's token rows as MMA operand fragments in registers and reloads them from
+// L2 only when the token set changes (the items of one expert and token tile are consecutive),
+// so the ring's shared memory carries weight bytes alone.
+
+// B operand fragments of one consumer warp: token row `row` (lane l takes row l/4 of the tile)
+// from element 0 over `ksteps` k-steps, in the m16n8k16 layout -- lane l holds elements
+// 16s + 2(l%4) + {0, 1} and 16s + 8 + 2(l%4) + {0, 1} of k-step s. L2 loads (the rows were
+// written by an earlier kernel).
+__device__ __forceinline__ void load_bfrag(uint32_t (&b)[kMaxSteps][2], const bf16* row, int ksteps, int lane) {
+    const unsigned int* p = reinterpret_cast<const unsigned int*>(row + 2 * (lane & 3));
+#pragma unroll
+    for (int k = 0; k < kMaxSteps; ++k)
+        if (k < ksteps) {
+            b[k][0] = __ldcg(p + 8 * k);
+            b[k][1] = __ldcg(p + 8 * k + 4);
+        }
+}
 
 __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up(LayerArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -256,38 +242,42 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up(LayerArgs a) {
     const int fb_s = a.Is / kFps, fb_r = a.I / kFps;          // feature blocks per group
     const int n_shared = fb_s * ((a.T + kTT - 1) / kTT);       // shared items first
     const int pitch = 2 * a.H + kPad;
+    const int G = gridDim.x, c = blockIdx.x;
+    // this CTA's shared items: a contiguous run in (token tile, feature block) order
+    const int s0 = routed_split(n_shared, c, G), my_shared = routed_split(n_shared, c + 1, G) - s0;
 
     if (warp == kWarps) {
         // ---------------- producer
         int* tiles = r.misc + 4;
-        const int G = gridDim.x, c = blockIdx.x;
         int it = 0;
-        // stage it: 8 gate rows f0.. and the matching up rows of W, and the x rows of the mt
-        // tokens (lane < mt holds its token in tok)
-        auto issue = [&](const bf16* W, int inner, int f0, int hrow, int mt, int tok) -> bool {
+        // stage it: 8 gate rows f0.. and the matching up rows of W; lane < kTT holds the x row
+        // of token lane of the item (a valid row for lanes past mt)
+        auto issue = [&](const bf16* W, int inner, int f0, int hrow, int mt, int key, int tok) -> bool {
             if (__shfl_sync(0xffffffffu, *(volatile int*)&r.misc[0], 0)) return false;  // consumers gave up
             const int s = it % kSt;
             if (!acquire_stage(r, it, err)) return false;
+            StageMeta& m = r.meta[s];
+            if (lane < kTT) m.tok[lane] = tok;
             if (lane == 0) {
-                StageMeta& m = r.meta[s];
                 m.mt = mt;
                 m.row0 = hrow;
                 m.f0 = f0;
-                mbar_arrive_expect_tx(&r.full[s], (uint32_t)((2 * kFps + mt) * a.H * 2));
+                m.key = key;
             }
             __syncwarp();
-            uint8_t* st = r.st[s];
+            if (lane == 0) mbar_arrive_expect_tx(&r.full[s], (uint32_t)(2 * kFps * a.H * 2));
+            __syncwarp();
+            uint8_t* st = r.st0 + (size_t)s * kStageBytes;
             copy_rows(st, pitch, W + (size_t)f0 * a.H, a.H, kFps, a.H * 2, &r.full[s], lane);
             copy_rows(st + kFps * pitch, pitch, W + (size_t)(inner + f0) * a.H, a.H, kFps, a.H * 2, &r.full[s], lane);
-            if (lane < mt) bulk_load(st + (size_t)(2 * kFps + lane) * pitch, a.x + (size_t)tok * a.H, a.H * 2, &r.full[s]);
             ++it;
             return true;
         };
         bool ok = true;
-        const int my_shared = shared_items_of(n_shared, c, G);
         for (int k = 0; k < my_shared && ok; ++k) {
-            const int i = c + k * G, tile = i / fb_s, fb = i - tile * fb_s, t0 = tile * kTT;
-            ok = issue(a.sgu, a.Is, fb * kFps, (int)a.P + t0, min(kTT, a.T - t0), t0 + lane);
+            const int i = s0 + k, tile = i / fb_s, fb = i - tile * fb_s, t0 = tile * kTT;
+            const int mt = min(kTT, a.T - t0);
+            ok = issue(a.sgu, a.Is, fb * kFps, (int)a.P + t0, mt, -1 - t0, t0 + (lane < mt ? lane : 0));
         }
         grid_dep_wait();
         const int n_act = a.hdr->n_act;
@@ -308,31 +298,43 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up(LayerArgs a) {
                 mt = min(kTT, cnt - tile * kTT);
                 tok = lane < mt ? a.perm[off + tile * kTT + lane] / a.K : 0;
             }
-            ok = issue(a.gate_up + (size_t)e * 2 * a.I * a.H, a.I, fb * kFps, off + tile * kTT, mt, tok);
+            const int hrow = off + tile * kTT;
+            ok = issue(a.gate_up + (size_t)e * 2 * a.I * a.H, a.I, fb * kFps, hrow, mt, hrow, tok);
         }
         if (lane == 0) drain(r, it, err);
         return;
     }
 
     // ---------------- consumers: warp w takes K range [w*H/8, (w+1)*H/8) of all 16 rows
-    const int kw = a.H / kWarps;
-    const int my_shared = shared_items_of(n_shared, blockIdx.x, gridDim.x);
-    int n_items = -1;
+    const int kw = a.H / kWarps, ksteps = kw / 16;
+    int n_items = -1, ckey = 0x7fffffff;  // no item has this key
+    uint32_t bfr[kMaxSteps][2];
     for (int it = 0;; ++it) {
         if (it == my_shared && n_items < 0) {
             grid_dep_wait();
             const int R = routed_tiles(a, lane) * fb_r;
-            n_items = my_shared + routed_split(R, blockIdx.x + 1, gridDim.x) - routed_split(R, blockIdx.x, gridDim.x);
+            n_items = my_shared + routed_split(R, c + 1, G) - routed_split(R, c, G);
         }
         if (n_items >= 0 && it >= n_items) break;
         const bool ok = wait_stage(r, it, err);
         if (!consumers_all(ok)) break;
         const int s = it % kSt;
         const StageMeta& m = r.meta[s];  // read in place: rewritten only after the stage is released
-        const int mt = m.mt, row0 = m.row0, f0 = m.f0;
-        const uint32_t sa = smem_u32(r.st[s]);
+        const int mt = m.mt, row0 = m.row0, f0 = m.f0, key = m.key;
+        if (key != ckey) {
+            ckey = key;
+            load_bfrag(bfr, a.x + (size_t)m.tok[lane >> 2] * a.H + warp * kw, ksteps, lane);
+        }
+        const uint32_t a_lane =
+            smem_u32(r.st0 + (size_t)s * kStageBytes) + (uint32_t)((lane & 15) * pitch + (warp * kw + 8 * (lane >> 4)) * 2);
         float d[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_rows(d, sa, sa + 2 * kFps * pitch, pitch, warp * kw, kw / 16, lane);
+#pragma unroll
+        for (int k = 0; k < kMaxSteps; ++k)
+            if (k < ksteps) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(a_lane + k * 32, a0, a1, a2, a3);
+                mma16816(d, a0, a1, a2, a3, bfr[k][0], bfr[k][1]);
+            }
         release_stage(r, it);
         // fixed-order sum of the 8 warps' K ranges: lane l holds gate (d0, d1) and up (d2, d3)
         // of feature l/4 for tokens 2*(l%4) and 2*(l%4)+1
@@ -554,45 +556,35 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
     Ring r = carve(smem_raw);
     ring_init(r);
     // The routing is complete (the gate_up kernel waited for it before it let this kernel
-    // launch); only the h rows come from the gate_up kernel: the producer streams the weights
-    // of its first stages, then waits for that kernel before copying any h row.
+    // launch); only the h rows come from the gate_up kernel. The producer streams weights from
+    // the start; the consumers wait for that kernel before they load any h row.
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint32_t* err = &a.hdr->err;
     const int n_act = a.hdr->n_act;
     const int tiles_s = (a.T + kTT - 1) / kTT;
     const int n_blocks = a.H / kRows;
+    const int G = gridDim.x, c = blockIdx.x;
+    // this CTA's shared items: a contiguous run in (token tile, output block) order
+    const int s0 = routed_split(n_blocks * tiles_s, c, G), my_shared = routed_split(n_blocks * tiles_s, c + 1, G) - s0;
 
     if (warp == kWarps) {
-        // ---------------- producer: shared items (block, token tile) strided over the CTAs,
-        // then this CTA's run of routed items (group, token tile, block)
+        // ---------------- producer: the shared items, then this CTA's run of routed items
+        // (group, token tile, block)
         int* tiles = r.misc + 4;
         build_tiles(a, tiles, n_blocks);
-        const int G = gridDim.x, c = blockIdx.x;
-        const int my_shared = shared_items_of(n_blocks * tiles_s, c, G);
         const int q0 = routed_split(tiles[n_act], c, G), q1 = routed_split(tiles[n_act], c + 1, G);
         const int n_mine = my_shared + q1 - q0;
         int it = 0;
-        bool waited = false, ok = true;
-        int pend_row[kSt], pend_mt[kSt], pend_inner[kSt];
         int g = -1, e = 0, off = 0, cnt = 0, ctile = -1;
         int tok = 0, slot = 0;
         float sc = 0.f;
-        for (int k = 0; k < n_mine && ok; ++k) {
-            // after the first kSt stages, wait for h and copy the pending rows
-            if (!waited && it == kSt) {
-                grid_dep_wait();
-                waited = true;
-                for (int q = 0; q < it; ++q)
-                    if (lane < pend_mt[q])
-                        bulk_load(r.st[q] + dn_hoff(pend_inner[q]) + (size_t)lane * (2 * pend_inner[q] + kPad),
-                                  a.h + (size_t)(pend_row[q] + lane) * a.Imax, pend_inner[q] * 2, &r.full[q]);
-            }
+        for (int k = 0; k < n_mine; ++k) {
             if (__shfl_sync(0xffffffffu, *(volatile int*)&r.misc[0], 0)) break;
             const bf16* W;
             int inner, hrow0, mt, blk;
             if (k < my_shared) {
-                const int i = c + k * G, tile = i % tiles_s, t0 = tile * kTT;
-                blk = i / tiles_s;
+                const int i = s0 + k, tile = i / n_blocks, t0 = tile * kTT;
+                blk = i - tile * n_blocks;
                 W = a.sd;
                 inner = a.Is;
                 hrow0 = (int)a.P + t0;
@@ -636,37 +628,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
                 m.slot[lane] = slot;
                 m.sc[lane] = sc;
             }
-            const int pitch = 2 * inner + kPad;
             if (lane == 0) {
                 m.mt = mt;
+                m.row0 = hrow0;
                 m.f0 = blk * kRows;
                 m.inner = inner;
-                m.block = blk;
+                m.key = hrow0;  // the h rows of the item
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&r.full[s], (uint32_t)((kRows + mt) * inner * 2));
+            if (lane == 0) mbar_arrive_expect_tx(&r.full[s], (uint32_t)(kRows * inner * 2));
             __syncwarp();
-            uint8_t* st = r.st[s];
-            copy_rows(st, dn_gpitch(inner), W + (size_t)blk * kRows * inner, 4 * (size_t)inner, kRows / 4, inner * 8,
-                      &r.full[s], lane);
-            if (waited) {
-                if (lane < mt)
-                    bulk_load(st + dn_hoff(inner) + (size_t)lane * pitch, a.h + (size_t)(hrow0 + lane) * a.Imax,
-                              inner * 2, &r.full[s]);
-            } else {
-                pend_row[it] = hrow0;
-                pend_mt[it] = mt;
-                pend_inner[it] = inner;
-            }
+            copy_rows(r.st0 + (size_t)s * kStageBytes, dn_gpitch(inner), W + (size_t)blk * kRows * inner, 4 * (size_t)inner, kRows / 4,
+                      inner * 8, &r.full[s], lane);
             ++it;
-        }
-        if (!waited) {
-            // fewer than kSt items: their h rows are still pending
-            grid_dep_wait();
-            for (int q = 0; q < it; ++q)
-                if (lane < pend_mt[q])
-                    bulk_load(r.st[q] + dn_hoff(pend_inner[q]) + (size_t)lane * (2 * pend_inner[q] + kPad),
-                              a.h + (size_t)(pend_row[q] + lane) * a.Imax, pend_inner[q] * 2, &r.full[q]);
         }
         if (lane == 0) drain(r, it, err);
         return;
@@ -674,36 +648,48 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
 
     // ---------------- consumers: warp w takes M tile (w % 4) and K half (w / 4)
     const int R = routed_tiles(a, lane) * n_blocks;
-    const int n_items = shared_items_of(n_blocks * tiles_s, blockIdx.x, gridDim.x) +
-                        routed_split(R, blockIdx.x + 1, gridDim.x) - routed_split(R, blockIdx.x, gridDim.x);
+    const int n_items = my_shared + routed_split(R, c + 1, G) - routed_split(R, c, G);
+    const int mtile = warp & 3, khalf = warp >> 2;
+    int ckey = -1;  // h rows are never negative
+    uint32_t bfr[kMaxSteps][2];
+    grid_dep_wait();  // the h rows of the gate_up kernel
     for (int it = 0; it < n_items; ++it) {
         const bool ok = wait_stage(r, it, err);
         if (!consumers_all(ok)) break;
         const int s = it % kSt;
         const StageMeta& m = r.meta[s];  // read in place: rewritten only after the stage is released
-        const int mt = m.mt, inner = m.inner, f0 = m.f0;
-        const int pitch = 2 * inner + kPad;
-        const int mtile = warp & 3, khalf = warp >> 2;
-        const int kh = inner / 2;
-        const uint32_t sa = smem_u32(r.st[s]);
+        const int mt = m.mt, inner = m.inner, f0 = m.f0, key = m.key;
+        const int kh = inner / 2, ksteps = kh / 16;
+        if (key != ckey) {
+            ckey = key;
+            const int n = lane >> 2;
+            load_bfrag(bfr, a.h + (size_t)(m.row0 + (n < mt ? n : 0)) * a.Imax + khalf * kh, ksteps, lane);
+        }
+        const uint32_t sa = smem_u32(r.st0 + (size_t)s * kStageBytes);
         // M tile mtile: rows j, j+1 (j = 2*(mtile & 1)) of groups 8*(mtile >> 1) .. +7
         const int gbase = 8 * (mtile >> 1), jbase = 2 * (mtile & 1);
         const int tr = lane & 15;
-        const uint32_t a_row = sa + (uint32_t)((gbase + (tr & 7)) * dn_gpitch(inner) + (jbase + (tr >> 3)) * inner * 2);
-        const uint32_t b_row = sa + (uint32_t)(dn_hoff(inner) + (lane & 7) * pitch);
+        const uint32_t a_lane = sa + (uint32_t)((gbase + (tr & 7)) * dn_gpitch(inner) + (jbase + (tr >> 3)) * inner * 2 +
+                                                (khalf * kh + 8 * (lane >> 4)) * 2);
         float d[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_rows_at(d, a_row, b_row, khalf * kh, kh / 16, lane);
+#pragma unroll
+        for (int k = 0; k < kMaxSteps; ++k)
+            if (k < ksteps) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(a_lane + k * 32, a0, a1, a2, a3);
+                mma16816(d, a0, a1, a2, a3, bfr[k][0], bfr[k][1]);
+            }
         // tokens of this lane's accumulator columns
         const int t0 = 2 * (lane & 3);
         size_t y0 = 0, y1 = 0;
-        float s0 = 0.f, s1 = 0.f;
+        float s0v = 0.f, s1v = 0.f;
         if (t0 < mt) {
             y0 = ((size_t)m.tok[t0] * (a.K + 1) + m.slot[t0]) * a.H + f0;
-            s0 = m.sc[t0];
+            s0v = m.sc[t0];
         }
         if (t0 + 1 < mt) {
             y1 = ((size_t)m.tok[t0 + 1] * (a.K + 1) + m.slot[t0 + 1]) * a.H + f0;
-            s1 = m.sc[t0 + 1];
+            s1v = m.sc[t0 + 1];
         }
         release_stage(r, it);
         // fixed-order sum of the two K halves, then scale and store: lane l holds tile rows l/4
@@ -715,12 +701,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
             const float4 v = *reinterpret_cast<const float4*>(red + (mtile * 32 + lane) * 4);
             const int row = 4 * (gbase + (lane >> 2)) + jbase;
             if (t0 < mt) {
-                a.Y[y0 + row] = s0 * (d[0] + v.x);
-                a.Y[y0 + row + 1] = s0 * (d[2] + v.z);
+                a.Y[y0 + row] = s0v * (d[0] + v.x);
+                a.Y[y0 + row + 1] = s0v * (d[2] + v.z);
             }
             if (t0 + 1 < mt) {
-                a.Y[y1 + row] = s1 * (d[1] + v.y);
-                a.Y[y1 + row + 1] = s1 * (d[3] + v.w);
+                a.Y[y1 + row] = s1v * (d[1] + v.y);
+                a.Y[y1 + row + 1] = s1v * (d[3] + v.w);
             }
         }
     }
