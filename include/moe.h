@@ -149,8 +149,8 @@ enum {
     MOE_KERNEL_COMBINE = 7,         /* fixed-order sum into the residual           */
     MOE_KERNEL_RMSNORM = 8,
     MOE_KERNEL_SHARED_GATE = 9,     /* not launched: the top-K kernel scores the shared gate */
-    MOE_KERNEL_GATHER = 10,         /* token rows in dispatch order (many-token path) */
-    MOE_KERNEL_GEMM_PLAN = 11,      /* group/tile tables of the expert GEMMs        */
+    MOE_KERNEL_GATHER = 10,         /* not launched: the dispatch scatter copies the token rows */
+    MOE_KERNEL_GEMM_PLAN = 11,      /* not launched: the dispatch scan writes the GEMM tables */
     MOE_KERNEL_DECODE_FUSED = 12,   /* whole layer in one persistent kernel (T <= 8) */
     MOE_KERNEL_ROUTER_STATS = 13,   /* load-balancing statistics (moe_router_stats) */
     MOE_KERNEL_COUNT = 14

@@ -106,11 +106,11 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
     a->lr = (int32_t*)(base + p->o_lr);
     a->cntb = (int32_t*)(base + p->o_cntb);
     a->base = (int32_t*)(base + p->o_base);
+    a->xperm = p->gemm ? (bf16*)(base + p->o_xperm) : nullptr;
     a->act = (int32_t*)(base + p->o_act);
     a->h = (bf16*)(base + p->o_h);
     a->Y = (float*)(base + p->o_y);
     a->Yb = (bf16*)(base + p->o_y);
-    a->xperm = (bf16*)(base + p->o_xperm);
     a->up_groups = (GemmGroup*)(base + p->o_upg);
     a->dn_groups = (GemmGroup*)(base + p->o_dng);
     a->up_tiles = (int32_t*)(base + p->o_upt);
@@ -218,7 +218,6 @@ extern "C" moe_status moe_forward(const moe_dims* d, const void* x, const moe_we
     if (decode_fused_supported(a)) return cuda_status(launch_decode_fused(a, s));  // whole layer, one launch
     cudaError_t e = launch_routing(a, s);
     if (a.gemm) {
-        if (e == cudaSuccess) e = launch_gemm_prep(a, s);
         if (e == cudaSuccess) e = launch_expert_gemms(a, s);
         if (e == cudaSuccess) e = launch_combine(a, s);
     } else if (e == cudaSuccess && stream_supported(a)) {

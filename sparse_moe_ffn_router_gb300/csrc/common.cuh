@@ -156,6 +156,50 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// Order-preserving unsigned key of a router score: larger score, larger key; -0 is taken as
+// +0. Key 0 lies below every score (an empty candidate).
+__device__ __forceinline__ uint32_t score_key(float v) {
+    if (v == 0.f) v = 0.f;
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Top-K of one token by a warp ("Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256
+// Experts, Router: the 8 highest scores; ties go to the lower expert index). Lane l holds the
+// keys of experts l + 32j in key[j]. Each of K rounds takes the largest remaining key by a warp
+// max and, among equal keys, the lowest expert by a warp min. Lane k < K receives slot k: its
+// score (myv) and expert (mye); every lane receives the slot-0 score (v0).
+__device__ __forceinline__ void warp_topk(const uint32_t (&key)[8], int K, int lane, float& v0, float& myv, int& mye) {
+    uint32_t taken = 0;
+    v0 = 0.f;
+    myv = 0.f;
+    mye = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (k < K) {
+            uint32_t bk = 0;
+            int bj = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (!((taken >> j) & 1u) && key[j] > bk) {
+                    bk = key[j];
+                    bj = j;
+                }
+            const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t win = __reduce_min_sync(0xffffffffu, bk == m ? (uint32_t)(lane + 32 * bj) : 0xffffffffu);
+            if ((int)(win & 31u) == lane) taken |= 1u << (win >> 5);
+            if (k == 0) v0 = key_score(m);
+            if (k == lane) {
+                myv = key_score(m);
+                mye = (int)win;
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&v);

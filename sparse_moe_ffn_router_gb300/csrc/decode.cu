@@ -113,16 +113,6 @@ inline bool decode_geom(const LayerArgs& a, int G, int sf, int nst, DGeom* g) {
     return true;
 }
 
-// Order-preserving unsigned key of a score: larger score, larger key; -0 is taken as +0.
-__device__ __forceinline__ uint32_t score_key(float v) {
-    if (v == 0.f) v = 0.f;
-    const uint32_t b = __float_as_uint(v);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key_score(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
@@ -252,30 +242,9 @@ __device__ void route_token(const LayerArgs& a, DRoute& rt, int t, int lane, uin
             key[j] = score_key(v);
         }
     }
-    uint32_t taken = 0;
-    float v0 = 0.f, myv = 0.f;
-    int mye = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        if (k < a.K) {
-            uint32_t bk = 0;
-            int bj = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (!((taken >> j) & 1u) && key[j] > bk) {
-                    bk = key[j];
-                    bj = j;
-                }
-            const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-            const uint32_t win = __reduce_min_sync(0xffffffffu, bk == m ? (uint32_t)(lane + 32 * bj) : 0xffffffffu);
-            if ((int)(win & 31u) == lane) taken |= 1u << (win >> 5);
-            if (k == 0) v0 = key_score(m);
-            if (k == lane) {
-                myv = key_score(m);
-                mye = (int)win;
-            }
-        }
-    }
+    float v0, myv;
+    int mye;
+    warp_topk(key, a.K, lane, v0, myv, mye);
     const float ex = lane < a.K ? expf(myv - v0) : 0.f;
     const float s = warp_sum(ex);
     if (lane < a.K) {

@@ -381,13 +381,13 @@ cudaError_t launch_router_gemm(const LayerArgs& a, cudaStream_t s) {
 
 // Expert GEMMs over the dispatched groups (routed experts + the shared expert).
 cudaError_t launch_expert_gemms(const LayerArgs& a, cudaStream_t s) {
-    const int fh = (a.I % 128 == 0 && a.Is % 128 == 0) ? 128 : 64;
+    const int fh = gemm_up_half(a);
     CUtensorMap mxp, mx, mgu, msgu, mh, mdn, msd;
     bool ok = make_map(&mxp, a.xperm, a.P, a.H, a.H, kBM) && make_map(&mx, a.x, a.T, a.H, a.H, kBM) &&
               make_map(&mgu, a.gate_up, (uint64_t)a.E * 2 * a.I, a.H, a.H, fh) &&
               make_map(&msgu, a.sgu, (uint64_t)2 * a.Is, a.H, a.H, fh) &&
               make_map(&mh, a.h, a.P + a.T, a.Imax, a.Imax, kBM);
-    const int bn_dn = (a.H % 256 == 0) ? 256 : 128;
+    const int bn_dn = gemm_down_bn(a);
     ok = ok && make_map(&mdn, a.down, (uint64_t)a.E * a.H, a.I, a.I, bn_dn) &&
          make_map(&msd, a.sd, a.H, a.Is, a.Is, bn_dn);
     if (!ok) return cudaErrorInvalidValue;

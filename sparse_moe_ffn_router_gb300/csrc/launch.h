@@ -30,10 +30,10 @@ struct LayerArgs {
     int32_t* cntb;    // [nb, E] pairs per expert per token block
     int32_t* base;    // [nb, E] first perm position of each (block, expert)
     int32_t* act;     // experts with pairs, ascending; count in hdr->n_act
+    bf16* xperm;      // [P, H] x rows in dispatch order (tensor-core path)
     bf16* h;          // [P + T, Imax] gated activations
     float* Y;         // [T, K+1, H] weighted expert outputs, slot K = shared expert (fp32 path)
     bf16* Yb;         // the same in bf16 (tensor-core path)
-    bf16* xperm;      // [P, H] x rows in dispatch order (tensor-core path)
     GemmGroup* up_groups;
     GemmGroup* dn_groups;
     int32_t* up_tiles;  // [n_groups + 1] first tile of each gate_up group
@@ -63,6 +63,11 @@ void trace_end(int kernel, cudaStream_t s);
 
 // Grouped-GEMM description consumed by the tensor-core kernel. With dense_rows > 0 there is a
 // single group of dense_rows rows (the router) and the tables are not read.
+// N tiles of the grouped GEMMs: gate_up takes FH gate rows and the FH matching up rows
+// (FH = 128, else 64), down takes 256 output rows (else 128).
+inline int gemm_up_half(const LayerArgs& a) { return (a.I % 128 == 0 && a.Is % 128 == 0) ? 128 : 64; }
+inline int gemm_down_bn(const LayerArgs& a) { return (a.H % 256 == 0) ? 256 : 128; }
+
 struct GemmPlan {
     const GemmGroup* groups;
     const int32_t* tile_start;
@@ -82,7 +87,6 @@ bool route_cluster_supported(const LayerArgs& a);
 cudaError_t launch_route_cluster(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_router_gemm(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_expert_gemms(const LayerArgs& a, cudaStream_t s);
-cudaError_t launch_gemm_prep(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_combine_pdl(const LayerArgs& a, cudaStream_t s);
 bool stream_supported(const LayerArgs& a);

@@ -15,12 +15,12 @@
 //   arrive in about one memory latency, where a few CTAs streaming the whole matrix were held
 //   to the per-SM copy rate.
 // k_route_small: ceil(T/8) CTAs of 1024 threads. Warp w of CTA c takes token 8c + w: top-K
-//   (each of K rounds takes the largest remaining order-preserving score key by a warp max and,
-//   among equal keys, the lowest expert index by a warp min), the renormalised weights and the
-//   shared gate. The last CTA to finish (a ticket counter in the workspace header, re-armed by
-//   that CTA) runs the dispatch: one stable counting sort of the T*K (token, slot) pairs in
-//   chunks of 1024; within a warp, pairs of one expert are ranked by lane (match_any), across
-//   the warps of a chunk by a prefix of per-warp counts, across chunks by running counts.
+//   (warp_topk: K rounds of a warp max over order-preserving score keys and, among equal keys,
+//   a warp min over expert indices), the renormalised weights and the shared gate. The last
+//   CTA to finish (a ticket counter in the workspace header, re-armed by that CTA) runs the
+//   dispatch: one stable counting sort of the T*K (token, slot) pairs in chunks of 1024;
+//   within a warp, pairs of one expert are ranked by lane (match_any), across the warps of a
+//   chunk by a prefix of per-warp counts, across chunks by running counts.
 // Both launch early (programmatic dependent launch): k_route_small waits for the scores
 // (griddepcontrol.wait) and at once lets the expert kernel after it start the shared expert's
 // work, which needs no routing; that kernel waits for the routing before its routed work.
@@ -148,16 +148,6 @@ __global__ void __launch_bounds__(256) k_router_mma(LayerArgs a, int S) {
     rm_cluster_sync();  // the other slices read this CTA's tile up to here
 }
 
-// Order-preserving unsigned key of a score: larger score, larger key; -0 is taken as +0.
-__device__ __forceinline__ uint32_t rs_key(float v) {
-    if (v == 0.f) v = 0.f;
-    const uint32_t b = __float_as_uint(v);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float rs_score(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 // Top-K of token t by one warp: ids in slot order, renormalised weights, shared gate.
 __device__ __forceinline__ void rs_topk_token(const LayerArgs& a, int t, int lane) {
     const float* l = a.logits + (size_t)t * a.ldl;
@@ -173,33 +163,12 @@ __device__ __forceinline__ void rs_topk_token(const LayerArgs& a, int t, int lan
                 bad = true;
                 v = -INFINITY;
             }
-            key[j] = rs_key(v);
+            key[j] = score_key(v);
         }
     }
-    uint32_t taken = 0;
-    float v0 = 0.f, myv = 0.f;
-    int mye = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        if (k < K) {
-            uint32_t bk = 0;
-            int bj = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (!((taken >> j) & 1u) && key[j] > bk) {
-                    bk = key[j];
-                    bj = j;
-                }
-            const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-            const uint32_t win = __reduce_min_sync(0xffffffffu, bk == m ? (uint32_t)(lane + 32 * bj) : 0xffffffffu);
-            if ((int)(win & 31u) == lane) taken |= 1u << (win >> 5);
-            if (k == 0) v0 = rs_score(m);
-            if (k == lane) {
-                myv = rs_score(m);
-                mye = (int)win;
-            }
-        }
-    }
+    float v0, myv;
+    int mye;
+    warp_topk(key, K, lane, v0, myv, mye);
     const float ex = lane < K ? expf(myv - v0) : 0.f;
     const float s = warp_sum(ex);
     if (lane < K) {

@@ -60,50 +60,23 @@ __global__ void __launch_bounds__(256) k_router_topk(LayerArgs a) {
     const int t = blockIdx.x * 8 + warp;
     if (t >= a.T) return;
     const float* l = a.logits + (size_t)t * a.ldl;
-    float v[8];
+    uint32_t key[8];
     bool bad = false;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const int e = lane + 32 * j;
-        v[j] = -INFINITY;
-        if (e < a.E) {
-            v[j] = l[e];
-            if (!isfinite(v[j])) {
+        key[j] = 0u;
+        if (lane + 32 * j < a.E) {
+            float v = l[lane + 32 * j];
+            if (!isfinite(v)) {
                 bad = true;
-                v[j] = -INFINITY;
+                v = -INFINITY;
             }
+            key[j] = score_key(v);
         }
     }
-    uint32_t taken = 0;
-    float sel_v[8];
-    int sel_e[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        if (k < a.K) {
-            float bv = -INFINITY;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = lane + 32 * j;
-                if (e < a.E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
-                    bv = v[j];
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            sel_v[k] = bv;
-            sel_e[k] = be;
-        }
-    }
+    float v0, myv;
+    int mye;
+    warp_topk(key, a.K, lane, v0, myv, mye);
     // shared-expert gate score: from the score kernel (column E), or, when the E router columns
     // came from the tensor-core GEMM, one more dot product x[t] . ws here
     float z;
@@ -119,20 +92,13 @@ __global__ void __launch_bounds__(256) k_router_topk(LayerArgs a) {
     } else {
         z = l[a.E];
     }
+    const float ex = lane < a.K ? expf(myv - v0) : 0.f;
+    const float s = warp_sum(ex);
+    if (lane < a.K) {
+        a.ids[(size_t)t * a.K + lane] = mye;
+        a.topw[(size_t)t * a.K + lane] = ex / s;
+    }
     if (lane == 0) {
-        float ex[8], s = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            if (k < a.K) {
-                ex[k] = expf(sel_v[k] - sel_v[0]);
-                s += ex[k];
-            }
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            if (k < a.K) {
-                a.ids[(size_t)t * a.K + k] = sel_e[k];
-                a.topw[(size_t)t * a.K + k] = ex[k] / s;
-            }
         if (!isfinite(z)) bad = true;
         a.sgate[t] = 1.0f / (1.0f + expf(-z));
     }
@@ -204,64 +170,30 @@ namespace moe {
 // ticket. No CTA ever waits on another.
 
 __device__ void topk_one_token(const LayerArgs& a, const float* l, int t, int lane) {
-    float v[8];
+    uint32_t key[8];
     bool bad = false;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const int e = lane + 32 * j;
-        v[j] = -INFINITY;
-        if (e < a.E) {
-            v[j] = __ldcg(l + e);
-            if (!isfinite(v[j])) {
+        key[j] = 0u;
+        if (lane + 32 * j < a.E) {
+            float v = __ldcg(l + lane + 32 * j);
+            if (!isfinite(v)) {
                 bad = true;
-                v[j] = -INFINITY;
+                v = -INFINITY;
             }
+            key[j] = score_key(v);
         }
     }
-    uint32_t taken = 0;
-    float sel_v[8];
-    int sel_e[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        if (k < a.K) {
-            float bv = -INFINITY;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = lane + 32 * j;
-                if (e < a.E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
-                    bv = v[j];
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            sel_v[k] = bv;
-            sel_e[k] = be;
-        }
+    float v0, myv;
+    int mye;
+    warp_topk(key, a.K, lane, v0, myv, mye);
+    const float ex = lane < a.K ? expf(myv - v0) : 0.f;
+    const float s = warp_sum(ex);
+    if (lane < a.K) {
+        a.ids[(size_t)t * a.K + lane] = mye;
+        a.topw[(size_t)t * a.K + lane] = ex / s;
     }
     if (lane == 0) {
-        float ex[8], s = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            if (k < a.K) {
-                ex[k] = expf(sel_v[k] - sel_v[0]);
-                s += ex[k];
-            }
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            if (k < a.K) {
-                a.ids[(size_t)t * a.K + k] = sel_e[k];
-                a.topw[(size_t)t * a.K + k] = ex[k] / s;
-            }
         const float z = __ldcg(l + a.E);
         if (!isfinite(z)) bad = true;
         a.sgate[t] = 1.0f / (1.0f + expf(-z));
@@ -551,65 +483,31 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
     // 3. CTA 0: top-K of every token from shared memory, then the dispatch
     for (int t = warp; t < a.T; t += 8) {
         const float* l = lg + (size_t)t * a.ldl;
-        float v[8];
+        uint32_t key[8];
         bool bad = false;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int e = lane + 32 * j;
-            v[j] = -INFINITY;
-            if (e < a.E) {
-                v[j] = l[e];
-                if (!isfinite(v[j])) {
+            key[j] = 0u;
+            if (lane + 32 * j < a.E) {
+                float v = l[lane + 32 * j];
+                if (!isfinite(v)) {
                     bad = true;
-                    v[j] = -INFINITY;
+                    v = -INFINITY;
                 }
+                key[j] = score_key(v);
             }
         }
-        uint32_t taken = 0;
-        float sel_v[8];
-        int sel_e[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            if (k < a.K) {
-                float bv = -INFINITY;
-                int be = 0x7fffffff;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int e = lane + 32 * j;
-                    if (e < a.E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
-                        bv = v[j];
-                        be = e;
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                    if (ov > bv || (ov == bv && oe < be)) {
-                        bv = ov;
-                        be = oe;
-                    }
-                }
-                if ((be & 31) == lane) taken |= 1u << (be >> 5);
-                sel_v[k] = bv;
-                sel_e[k] = be;
-            }
+        float v0, myv;
+        int mye;
+        warp_topk(key, a.K, lane, v0, myv, mye);
+        const float ex = lane < a.K ? expf(myv - v0) : 0.f;
+        const float s = warp_sum(ex);
+        if (lane < a.K) {
+            sids[t * a.K + lane] = mye;
+            a.ids[(size_t)t * a.K + lane] = mye;
+            a.topw[(size_t)t * a.K + lane] = ex / s;
         }
         if (lane == 0) {
-            float ex[8], s = 0.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k < a.K) {
-                    ex[k] = expf(sel_v[k] - sel_v[0]);
-                    s += ex[k];
-                }
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k < a.K) {
-                    sids[t * a.K + k] = sel_e[k];
-                    a.ids[(size_t)t * a.K + k] = sel_e[k];
-                    a.topw[(size_t)t * a.K + k] = ex[k] / s;
-                }
             const float z = l[a.E];
             if (!isfinite(z)) bad = true;
             a.sgate[t] = 1.0f / (1.0f + expf(-z));
