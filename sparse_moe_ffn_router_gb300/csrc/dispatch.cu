@@ -102,18 +102,31 @@ __device__ void gemm_plan_warp(const LayerArgs& a, const int* act, int n, const 
     }
 }
 
-__global__ void __launch_bounds__(256) k_dispatch_scan(LayerArgs a, int fh, int bn_dn) {
+constexpr int kScanParts = 4, kScanRegs = 16;  // threads per expert, block counts kept in registers
+
+__global__ void __launch_bounds__(256 * kScanParts) k_dispatch_scan(LayerArgs a, int fh, int bn_dn) {
+    __shared__ int part[kScanParts][256];
     __shared__ int tot[256];
     __shared__ int off[257];
     __shared__ int sact[256];
     __shared__ int n_act_s;
-    const int e = threadIdx.x, warp = e >> 5, lane = e & 31;
+    // thread (q, e) takes blocks [q*nb/4, (q+1)*nb/4) of expert e: its counts in one round of
+    // loads (up to kScanRegs of them kept for the bases), then their sum
+    const int e = threadIdx.x & 255, q = threadIdx.x >> 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b0 = q * a.nb / kScanParts, b1 = (q + 1) * a.nb / kScanParts;
+    int c[kScanRegs];
     int sum = 0;
-    if (e < a.E) {
-#pragma unroll 8
-        for (int b = 0; b < a.nb; ++b) sum += a.cntb[(size_t)b * a.E + e];
+#pragma unroll
+    for (int i = 0; i < kScanRegs; ++i) {
+        c[i] = (e < a.E && b0 + i < b1) ? a.cntb[(size_t)(b0 + i) * a.E + e] : 0;
+        sum += c[i];
     }
-    tot[e] = sum;
+    if (e < a.E)
+        for (int b = b0 + kScanRegs; b < b1; ++b) sum += a.cntb[(size_t)b * a.E + e];
+    part[q][e] = sum;
+    __syncthreads();
+    if (q == 0) tot[e] = part[0][e] + part[1][e] + part[2][e] + part[3][e];
     __syncthreads();
     if (warp == 0) {
         // exclusive scan of the counts and the ascending list of experts with pairs: lane
@@ -157,16 +170,24 @@ __global__ void __launch_bounds__(256) k_dispatch_scan(LayerArgs a, int fh, int 
     }
     __syncthreads();
     if (e < a.E) {
-        a.counts[e] = tot[e];
-        a.offsets[e] = off[e];
+        if (q == 0) {
+            a.counts[e] = tot[e];
+            a.offsets[e] = off[e];
+        }
         int run = off[e];
-#pragma unroll 8
-        for (int b = 0; b < a.nb; ++b) {
+        for (int p = 0; p < q; ++p) run += part[p][e];
+#pragma unroll
+        for (int i = 0; i < kScanRegs; ++i)
+            if (b0 + i < b1) {
+                a.base[(size_t)(b0 + i) * a.E + e] = run;
+                run += c[i];
+            }
+        for (int b = b0 + kScanRegs; b < b1; ++b) {
             a.base[(size_t)b * a.E + e] = run;
             run += a.cntb[(size_t)b * a.E + e];
         }
     }
-    if (e == 0) a.offsets[a.E] = off[a.E];
+    if (threadIdx.x == 0) a.offsets[a.E] = off[a.E];
     if (a.gemm && warp == 1) gemm_plan_warp(a, sact, n_act_s, off, tot, fh, bn_dn);
 }
 
@@ -204,7 +225,7 @@ __global__ void __launch_bounds__(256) k_dispatch_scatter_rows(LayerArgs a) {
 cudaError_t launch_dispatch(const LayerArgs& a, cudaStream_t s) {
     const int fh = gemm_up_half(a), bn_dn = gemm_down_bn(a);
     MOE_LAUNCH(MOE_KERNEL_DISPATCH_LOCAL, s, (k_dispatch_local<<<a.nb, 32, 0, s>>>(a)));
-    MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCAN, s, (k_dispatch_scan<<<1, 256, 0, s>>>(a, fh, bn_dn)));
+    MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCAN, s, (k_dispatch_scan<<<1, 256 * kScanParts, 0, s>>>(a, fh, bn_dn)));
     if (a.gemm)
         MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCATTER, s,
                    (k_dispatch_scatter_rows<<<(unsigned)((a.P + 7) / 8), 256, 0, s>>>(a)));

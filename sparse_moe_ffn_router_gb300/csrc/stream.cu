@@ -700,14 +700,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
         if (khalf == 0) {
             const float4 v = *reinterpret_cast<const float4*>(red + (mtile * 32 + lane) * 4);
             const int row = 4 * (gbase + (lane >> 2)) + jbase;
-            if (t0 < mt) {
-                a.Y[y0 + row] = s0v * (d[0] + v.x);
-                a.Y[y0 + row + 1] = s0v * (d[2] + v.z);
-            }
-            if (t0 + 1 < mt) {
-                a.Y[y1 + row] = s1v * (d[1] + v.y);
-                a.Y[y1 + row + 1] = s1v * (d[3] + v.w);
-            }
+            // rows row and row + 1 are adjacent in Y (row is even): one 8-byte store per token
+            if (t0 < mt) *reinterpret_cast<float2*>(a.Y + y0 + row) = make_float2(s0v * (d[0] + v.x), s0v * (d[2] + v.z));
+            if (t0 + 1 < mt)
+                *reinterpret_cast<float2*>(a.Y + y1 + row) = make_float2(s1v * (d[1] + v.y), s1v * (d[3] + v.w));
         }
     }
     grid_dep_launch();
