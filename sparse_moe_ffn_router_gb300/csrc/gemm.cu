@@ -24,15 +24,17 @@
 
 namespace moe {
 
-constexpr int kBM = 128, kBK = 64, kStages = 4;
+constexpr int kBM = 128, kBK = 64;
 constexpr int kThreads = 192;
 constexpr uint32_t kAStage = kBM * kBK * 2;
 
 enum { kLogits = 0, kSwiGLU = 1, kScaleY = 2 };
 
+// Ring stages: as many as keep about 192 KB of A and B tiles in flight per SM.
 template <int BN>
 struct GemmSmem {
     static constexpr uint32_t kBStage = BN * kBK * 2;
+    static constexpr int kStages = (int)((192u * 1024u) / (kAStage + kBStage));
     static constexpr uint32_t kTiles = kStages * (kAStage + kBStage);
     static constexpr uint32_t kBytes = 1024 + kTiles + 256;  // alignment slack + tiles + barriers
 };
@@ -74,6 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
            const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1, const GemmPlan p,
            const LayerArgs a) {
+    constexpr int kStages = GemmSmem<BN>::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);

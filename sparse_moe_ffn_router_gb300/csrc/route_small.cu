@@ -7,7 +7,7 @@
 // k_router_mma: scores[t, r] = x[t] . W[r] (+ br[r]) on the tensor pipe. A cluster of S CTAs
 //   takes 16 score rows and up to 64 tokens; CTA s of the cluster multiplies K slice s (H/S
 //   columns) with warp-level bf16 MMAs (m16n8k16, fp32 accumulate, K in order; warp w takes
-//   tokens 8w..8w+7). Its operand rows come in with 16-byte loads, eight per thread in flight,
+//   tokens 8w..8w+7). Its operand rows come in with 16-byte loads, sixteen per thread in flight,
 //   into rows 16 bytes apart modulo 128 so ldmatrix is conflict-free. The S partial 16 x 64
 //   tiles are then added in slice order through distributed shared memory, so a score does not
 //   depend on which CTA finished first. S (1..8) is the smallest count that fits shared memory,
@@ -34,6 +34,7 @@ namespace moe {
 constexpr int kRmRows = 16, kRmTok = 64;  // score rows and tokens per cluster
 constexpr int kRmMaxSplit = 8;            // K slices, one CTA each
 constexpr int kRmSmemMax = 200 * 1024;    // dynamic shared memory of one CTA, at most
+constexpr int kRmBatch = 16;              // 16-byte loads per thread in flight
 constexpr int kRsThreads = 1024, kRsWarps = kRsThreads / 32;
 constexpr int kRsTok = 8;  // tokens per routing CTA, one per warp
 constexpr int kRsMaxP = 255 * 8;
@@ -74,10 +75,10 @@ __global__ void __launch_bounds__(256) k_router_mma(LayerArgs a, int S) {
     const int total = (nr + nt) * cpr;  // 16-byte pieces of this slice's operand rows
 
     // 1. the nr score rows, then the nt token rows, of K slice s into shared memory
-    for (int b = tid; b < total; b += 8 * 256) {
-        uint4 v[8];
+    for (int b = tid; b < total; b += kRmBatch * 256) {
+        uint4 v[kRmBatch];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < kRmBatch; ++u) {
             const int i = b + u * 256;
             v[u] = make_uint4(0u, 0u, 0u, 0u);
             if (i < total) {
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(256) k_router_mma(LayerArgs a, int S) {
             }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < kRmBatch; ++u) {
             const int i = b + u * 256;
             if (i < total) {
                 const int row = i / cpr, c = i - row * cpr;
@@ -199,13 +200,13 @@ __global__ void __launch_bounds__(kRsThreads, 1) k_route_small(LayerArgs a) {
     const int t = blockIdx.x * kRsTok + warp;
     if (warp < kRsTok && t < T) rs_topk_token(a, t, lane);
 
-    // 2. the last CTA to get here sorts the pairs of every token
-    __threadfence();
+    // 2. the last CTA to get here sorts the pairs of every token: thread 0 counts the CTA in
+    //    with one acquire-release atomic after the CTA barrier (the release covers the ids
+    //    the CTA's warps wrote, the acquire the other CTAs' ids)
     __syncthreads();
-    if (tid == 0) ticket = atomicAdd(&a.hdr->route_ticket, 1u);
+    if (tid == 0) ticket = atom_acq_rel_add(&a.hdr->route_ticket, 1u);
     __syncthreads();
     if (ticket != gridDim.x - 1) return;
-    __threadfence();
     for (int p = tid; p < P; p += kRsThreads) sid[p] = __ldcg(a.ids + p);
     for (int e = tid; e < 256; e += kRsThreads) running[e] = 0;
     __syncthreads();
