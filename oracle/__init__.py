@@ -25,9 +25,13 @@ _lock = threading.Lock()
 _lib = None
 
 
+# dims tuples are (T, H, E, K, I, Is) or (T, H, E, K, I, Is, flags)
+BF16_SCORES = 1  # router and shared-gate scores typed bf16 (rounded before ranking and sigmoid)
+
+
 class Dims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
-                ("K", ctypes.c_int32), ("I", ctypes.c_int32), ("Is", ctypes.c_int32)]
+                ("K", ctypes.c_int32), ("I", ctypes.c_int32), ("Is", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 def build(force: bool = False) -> str:

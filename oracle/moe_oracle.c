@@ -17,6 +17,13 @@
  *     SparseMoe; "Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256 Experts). The pages
  *     do not say how the two halves are placed; this oracle reads rows [0, I) as the gate
  *     projection and rows [I, 2I) as the up projection (name order, not interleaved).
+ *   - Router outputs: by default the router and shared-gate scores are kept exact (fp64).
+ *     With ORACLE_BF16_SCORES in dims.flags they are typed T = bf16 as the pages' interface
+ *     types them (`gate: Linear<H, Experts, T>`, `shared_expert_gate: Linear<H, 1, T>` and
+ *     `ranks(logits: Tensor[R, Experts; T])` in "Qwen3.6 35B-A3B", Blocks: SparseMoe): each
+ *     score, bias included, is rounded to the nearest bf16 (ties to even) before the softmax,
+ *     the ranking and the sigmoid. Equal rounded scores are then common; the rank rule puts
+ *     the lower expert index first.
  *
  * Each function follows one step of the pages and cites it. Work is split over tokens with
  * OpenMP only; tokens are independent, so the split changes no result.
@@ -36,7 +43,10 @@ typedef struct {
     int32_t K;  /* experts chosen per token */
     int32_t I;  /* routed expert inner width */
     int32_t Is; /* shared expert inner width */
+    int32_t flags; /* ORACLE_BF16_SCORES: router and shared-gate scores typed bf16 */
 } oracle_dims;
+
+#define ORACLE_BF16_SCORES 1
 
 /* Exact widening of a bf16 bit pattern: bf16 is the top half of an IEEE binary32. */
 static double bf(uint16_t b) {
@@ -77,11 +87,16 @@ uint16_t oracle_round_bf16(double v) {
     return (uint16_t)hi;
 }
 
+/* A score as the following steps see it: exact, or rounded to bf16 under ORACLE_BF16_SCORES. */
+static double score_as_typed(const oracle_dims* d, double s) {
+    return (d->flags & ORACLE_BF16_SCORES) ? bf(oracle_round_bf16(s)) : s;
+}
+
 /* Router projection: "A learned linear layer 2048 -> 256 scores all 256 experts for each
  * token" ("Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256 Experts, Router; the
  * router is `gate: Linear<H, Experts>` in "Qwen3.6 35B-A3B", Blocks: SparseMoe, with the
  * optional `bias: Tensor[Out; T]?` of Blocks: Linear).
- * logits[t*E + e] = sum_h x[t,h] * Wr[e,h] (+ br[e]). */
+ * logits[t*E + e] = sum_h x[t,h] * Wr[e,h] (+ br[e]), then typed (score_as_typed). */
 void oracle_router_logits(const oracle_dims* d, const uint16_t* x, const uint16_t* router_w,
                           const uint16_t* router_b, double* logits) {
     const int T = d->T, H = d->H, E = d->E;
@@ -91,7 +106,7 @@ void oracle_router_logits(const oracle_dims* d, const uint16_t* x, const uint16_
             double s = 0.0;
             for (int h = 0; h < H; ++h) s += bf(x[(size_t)t * H + h]) * bf(router_w[(size_t)e * H + h]);
             if (router_b) s += bf(router_b[e]);
-            logits[(size_t)t * E + e] = s;
+            logits[(size_t)t * E + e] = score_as_typed(d, s);
         }
     }
 }
@@ -328,6 +343,7 @@ int oracle_forward(const oracle_dims* d, const uint16_t* x, const uint16_t* rout
                 /* Shared expert, always active, scaled by sigmoid(Linear(x, 1)). */
                 double z = 0.0;
                 for (int h = 0; h < H; ++h) z += xrow[h] * bf(shared_gate[h]);
+                z = score_as_typed(d, z);
                 double sg = 1.0 / (1.0 + exp(-z));
                 swiglu_token(H, Is, xrow, shared_gate_up, shared_down, hb, y);
                 for (int h = 0; h < H; ++h) acc[h] += sg * y[h];

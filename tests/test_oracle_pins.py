@@ -401,3 +401,72 @@ def test_stats_invariants_and_expert_relabelling():
     np.testing.assert_allclose(s2["P"], s["P"][perm.numpy()], rtol=1e-12, atol=1e-18)
     np.testing.assert_array_equal(s2["f"], s["f"][perm.numpy()])
     assert s2["loss"] == pytest.approx(s["loss"], rel=1e-12)
+
+
+# ---------------------------------------------------------------------------------------
+# bf16-typed router outputs: the pages' interface types the router and the shared gate as
+# Linear<..., T> with T = bf16 and ranks bf16 logits ("Qwen3.6 35B-A3B", Blocks: SparseMoe).
+# Under this reading each score, bias included, is rounded to the nearest bf16 before the
+# softmax, the ranking and the sigmoid. The cases below are worked by hand; H = 2 tokens with
+# x = (1, 1) make every score the sum of a row's two entries (plus the bias).
+
+BF16 = oracle.BF16_SCORES
+
+
+def _two_column_router(rows):
+    """Router weight [E, 2] with the given (w0, w1) rows and x = (1, 1): score_e = w0 + w1."""
+    return bf16(np.array(rows, np.float64)), bf16(np.ones((1, 2)))
+
+
+def test_bf16_scores_rounding_makes_a_tie_broken_by_the_lower_index():
+    # exact scores 1, 1 + 2^-10, 1/2, 1 + 2^-9: bf16 has 8 significant bits, so the three
+    # near 1 all round to 1.0 and tie; the tie goes to the lower indices 0 and 1
+    wr, x = _two_column_router([[1.0, 0.0], [1.0, 2.0 ** -10], [0.5, 0.0], [1.0, 2.0 ** -9]])
+    exact = oracle.route((1, 2, 4, 2, 4, 4), x, wr)
+    typed = oracle.route((1, 2, 4, 2, 4, 4, BF16), x, wr)
+    assert exact["ids"].tolist() == [[3, 1]]
+    assert typed["ids"].tolist() == [[0, 1]]
+    np.testing.assert_array_equal(typed["w"], [[0.5, 0.5]])  # equal scores, equal weights
+    # K = 3 takes all three tied experts in index order; their weights stay equal
+    typed3 = oracle.route((1, 2, 4, 3, 4, 4, BF16), x, wr)
+    assert typed3["ids"].tolist() == [[0, 1, 3]]
+    np.testing.assert_allclose(typed3["w"], [[1 / 3, 1 / 3, 1 / 3]], rtol=1e-15)
+
+
+def test_bf16_scores_round_after_the_bias_to_even():
+    # expert 1 scores 1 + 2^-8 only through its bias: the exact midpoint between 1 and the next
+    # bf16 (1 + 2^-7), which rounds to the even neighbour 1.0 and ties with expert 0. Rounding
+    # before adding the bias would leave 1 + 2^-8 and pick expert 1.
+    wr, x = _two_column_router([[1.0, 0.0], [1.0, 0.0], [0.25, 0.0]])
+    br = bf16([0.0, 2.0 ** -8, 0.0])
+    assert oracle.route((1, 2, 3, 1, 4, 4), x, wr, br)["ids"].tolist() == [[1]]
+    assert oracle.route((1, 2, 3, 1, 4, 4, BF16), x, wr, br)["ids"].tolist() == [[0]]
+    # above the midpoint (1 + 3 * 2^-9) it rounds up to 1 + 2^-7 and wins again
+    br_up = bf16([0.0, 3 * 2.0 ** -9, 0.0])
+    assert oracle.route((1, 2, 3, 1, 4, 4, BF16), x, wr, br_up)["ids"].tolist() == [[1]]
+
+
+def test_bf16_scores_shared_gate_is_rounded_before_the_sigmoid():
+    H, E, I, Is = 2, 4, 4, 4
+    w = _zero_layer(H, E, I, Is)
+    w["shared_gate"] = bf16([[1.0, 2.0 ** -10]])  # z = 1 + 2^-10 exactly, 1.0 in bf16
+    x = bf16(np.ones((1, H)))
+    exact = oracle.forward((1, H, E, 2, I, Is), x, w, taps=True)
+    typed = oracle.forward((1, H, E, 2, I, Is, BF16), x, w, taps=True)
+    assert exact["sg"][0] == pytest.approx(sig(1.0 + 2.0 ** -10), rel=1e-15)
+    assert typed["sg"][0] == pytest.approx(sig(1.0), rel=1e-15)
+
+
+def test_bf16_scores_change_nothing_when_every_score_is_a_bf16_value():
+    # one-hot tokens: every score is one bf16 weight, already representable, so both readings
+    # route identically (ids, weights and dispatch)
+    H, E, K, T = 16, 64, 6, 16
+    wr = synth.normal_bf16((E, H), 0.02, synth.stream_key(9, 0, "router_w"))
+    x = torch.zeros(T, H, dtype=torch.bfloat16)
+    for t in range(T):
+        x[t, (3 * t) % H] = 1.0
+    a = oracle.route((T, H, E, K, 4, 4), x, wr)
+    b = oracle.route((T, H, E, K, 4, 4, BF16), x, wr)
+    for k in ("ids", "counts", "offsets", "perm", "inv"):
+        np.testing.assert_array_equal(a[k], b[k])
+    np.testing.assert_array_equal(a["w"], b["w"])
