@@ -442,6 +442,47 @@ def time_stats(ls: LayerSet, peaks: dict, n: int = 20, reps: int = 10) -> dict:
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_call": nbytes}}
 
 
+def time_variant(ls: LayerSet, flags: int, n: int = 32, reps: int = 5) -> dict:
+    """moe_forward with the dims flags (MOE_FLAG_BF16_SCORES: bf16-typed router and shared-gate
+    scores) and without them, over the same rotating layers: n steps, a CUDA graph replayed
+    reps times up to 64 tokens, plain launches above."""
+    moe = ls.moe
+    T = ls.dims[0]
+
+    def run(dims) -> float:
+        def step(i):
+            W, x = ls.layers[i % len(ls.layers)]
+            moe.moe_forward(dims, x, W, None, ls.out, ls.ws)
+
+        for i in range(3):
+            step(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if T <= 64:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    step(i)
+            g.replay()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(reps):
+                g.replay()
+            b.record()
+        else:
+            a.record()
+            for i in range(n * reps):
+                step(i)
+            b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (n * reps)
+
+    base = run(tuple(ls.dims))
+    var = run(tuple(ls.dims) + (flags,))
+    return {"ms_per_step": round(var, 5), "tokens_per_s": round(T / (var * 1e-3), 1),
+            "default_ms_per_step": round(base, 5), "device_error": moe.moe_last_device_error(ls.ws)}
+
+
 def time_e2e(ls: LayerSet, steps: int, warmup: int) -> dict:
     """Same metric through the public call with host buffers: per step, x is copied from
     pinned host memory, the layer runs, and the output is copied back to pinned memory."""
@@ -624,12 +665,13 @@ def main():
             if r.get("roofline"):
                 r["roofline"]["traffic"] = ncu_traffic(r["roofline"]["kernel"], w2.name)
             stats = time_stats(ls2, peaks)
+            bf16s = time_variant(ls2, ls2.moe.FLAG_BF16_SCORES)
             also[name] = {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 5),
                           "device_error": r["device_error"],
                           "roofline": r.get("roofline"), "hbm_frac_of_layer_bytes": r["layer_hbm_frac"],
                           "tensor_frac": r["layer_tensor_frac"], "unique_experts_per_step": r["unique_experts"],
                           "kernel_ms_warmup": {k: round(v, 5) for k, v in r["warm_kernel_ms"].items()},
-                          "router_stats": stats}
+                          "router_stats": stats, "bf16_scores": bf16s}
             del ls2
         torch.cuda.empty_cache()
     line["also"] = also

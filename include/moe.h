@@ -44,10 +44,21 @@ extern "C" {
  * [B, S, H]), H hidden width, E routed experts, K experts per token, I routed inner width,
  * Is shared inner width. Supported: T >= 0, 128 <= H <= 8192 with H % 128 == 0,
  * 1 <= K <= 8, K <= E <= 256, 64 <= I, Is <= 2048 with I % 64 == 0 and Is % 64 == 0,
- * T * (K + 1) < 2^31. T == 0 is a valid no-op. */
+ * T * (K + 1) < 2^31. T == 0 is a valid no-op.
+ * flags: 0, or MOE_FLAG_BF16_SCORES; any other bit is rejected with MOE_ERR_INVALID_ARG
+ * before anything runs (moe_workspace_size ignores flags). */
 typedef struct {
     int32_t T, H, E, K, I, Is;
+    int32_t flags;
 } moe_dims;
+
+/* bf16-typed router outputs ("Qwen3.6 35B-A3B", Blocks: SparseMoe types `gate:
+ * Linear<H, Experts, T>`, `shared_expert_gate: Linear<H, 1, T>` and `ranks(logits: Tensor[R,
+ * Experts; T])` with T = bf16): each router score and the shared-gate score, accumulated in
+ * fp32 with the bias added, is rounded to the nearest bf16 (ties to even) before the softmax,
+ * the ranking and the sigmoid. Equal rounded scores rank the lower expert index first.
+ * Without the flag the fp32 scores are used unrounded. */
+#define MOE_FLAG_BF16_SCORES 1
 
 /* Device pointers to one layer's weights; router_b may be NULL. */
 typedef struct {

@@ -8,6 +8,7 @@ behind the C ABI of ``include/moe.h``; this package only marshals torch tensors 
 ABI. There is no CPU path: a call fails loudly when the library or a GPU is missing.
 """
 from .binding import (  # noqa: F401
+    FLAG_BF16_SCORES,
     MoEError,
     Weights,
     library_path,
@@ -18,6 +19,7 @@ from .binding import (  # noqa: F401
     moe_set_trace,
     moe_rmsnorm,
     moe_route,
+    moe_route_noalloc,
     moe_router_stats,
     moe_workspace_init,
     moe_workspace_size,

@@ -25,9 +25,14 @@ KERNELS = {"router_scores": 0, "router_topk": 1, "dispatch_local": 2, "dispatch_
            "decode_fused": 12, "router_stats": 13}
 
 
+# moe_dims.flags: router and shared-gate scores rounded to bf16 before ranking and sigmoid
+FLAG_BF16_SCORES = 1
+
+
 class Dims(ctypes.Structure):
+    """moe_dims; a dims tuple is (T, H, E, K, I, Is) or (T, H, E, K, I, Is, flags)."""
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
-                ("K", ctypes.c_int32), ("I", ctypes.c_int32), ("Is", ctypes.c_int32)]
+                ("K", ctypes.c_int32), ("I", ctypes.c_int32), ("Is", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class CWeights(ctypes.Structure):

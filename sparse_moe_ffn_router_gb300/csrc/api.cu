@@ -73,7 +73,7 @@ int sm_count() {
 // workspace-backed fields of the argument block.
 moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void* ws, size_t ws_bytes, Plan* p,
                    LayerArgs* a) {
-    if (!d) return MOE_ERR_INVALID_ARG;
+    if (!d || (d->flags & ~MOE_FLAG_BF16_SCORES)) return MOE_ERR_INVALID_ARG;
     if (!make_plan(*d, p)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (d->T == 0) return MOE_OK;
     if (!x || !w || !ws || !w->router_w || !w->gate_up || !w->down || !w->shared_gate_up || !w->shared_down ||
@@ -86,6 +86,7 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
     if (ws_bytes < p->total) return MOE_ERR_WORKSPACE_TOO_SMALL;
     memset(a, 0, sizeof *a);
     char* base = (char*)ws;
+    a->flags = d->flags;
     a->x = (const bf16*)x;
     a->router_w = (const bf16*)w->router_w;
     a->router_b = (const bf16*)w->router_b;

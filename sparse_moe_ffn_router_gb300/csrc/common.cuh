@@ -156,6 +156,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// A router or shared-gate score as the routing uses it: the fp32 value, or that value rounded
+// to the nearest bf16 under MOE_FLAG_BF16_SCORES.
+__device__ __forceinline__ float router_score(float v, int flags) {
+    return (flags & MOE_FLAG_BF16_SCORES) ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+}
+
 // Order-preserving unsigned key of a router score: larger score, larger key; -0 is taken as
 // +0. Key 0 lies below every score (an empty candidate).
 __device__ __forceinline__ uint32_t score_key(float v) {

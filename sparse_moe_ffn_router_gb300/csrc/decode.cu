@@ -234,7 +234,7 @@ __device__ void route_token(const LayerArgs& a, DRoute& rt, int t, int lane, uin
     for (int j = 0; j < 8; ++j) {
         key[j] = 0u;  // below every score: never taken while a real expert remains
         if (lane + 32 * j < a.E) {
-            float v = __uint_as_float(val[j]);
+            float v = router_score(__uint_as_float(val[j]), a.flags);
             if (!isfinite(v)) {
                 bad = true;
                 v = -INFINITY;
@@ -252,7 +252,7 @@ __device__ void route_token(const LayerArgs& a, DRoute& rt, int t, int lane, uin
         rt.sw[t * a.K + lane] = ex / s;
     }
     if (lane == 0) {
-        const float z = __uint_as_float(val[8]);
+        const float z = router_score(__uint_as_float(val[8]), a.flags);
         if (!isfinite(z)) bad = true;
         rt.sgate[t] = 1.0f / (1.0f + expf(-z));
         if (timed_out) atomicOr(&a.hdr->err, ERR_TIMEOUT);

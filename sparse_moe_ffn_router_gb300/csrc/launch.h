@@ -44,6 +44,7 @@ struct LayerArgs {
     uint64_t* dh;     // [P+T, Imax/2] gated activation pairs tagged with their call (same kernel)
     WsHeader* hdr;
     bool gemm;
+    int flags;        // moe_dims.flags (MOE_FLAG_BF16_SCORES)
     int T, H, E, K, I, Is, Imax, ldl, nb;
     int64_t P;
     int num_sms;

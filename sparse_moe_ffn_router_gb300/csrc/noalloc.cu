@@ -74,7 +74,7 @@ using namespace moe;
 extern "C" moe_status moe_route_noalloc(const moe_dims* d, const void* x, const moe_weights* w, int32_t* ids,
                                         float* topk_w, int32_t* counts, int32_t* offsets, int32_t* perm,
                                         void* stream) {
-    if (!d) return MOE_ERR_INVALID_ARG;
+    if (!d || (d->flags & ~MOE_FLAG_BF16_SCORES)) return MOE_ERR_INVALID_ARG;
     Plan p;
     if (!make_plan(*d, &p)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (d->T > kFusedRouteTokens) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -114,6 +114,7 @@ extern "C" moe_status moe_route_noalloc(const moe_dims* d, const void* x, const 
     a.counts = counts;
     a.offsets = offsets;
     a.perm = perm;
+    a.flags = d->flags;
     a.T = p.T; a.H = p.H; a.E = p.E; a.K = p.K; a.I = p.I; a.Is = p.Is;
     a.Imax = p.Imax; a.ldl = p.ldl; a.nb = p.nb; a.P = p.P;
     // the array keeps the previous call's contents: the header (completion ticket, error word)

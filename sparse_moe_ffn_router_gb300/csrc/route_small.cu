@@ -159,7 +159,7 @@ __device__ __forceinline__ void rs_topk_token(const LayerArgs& a, int t, int lan
     for (int j = 0; j < 8; ++j) {
         key[j] = 0u;  // below every score: never taken while a real expert remains
         if (lane + 32 * j < E) {
-            float v = l[lane + 32 * j];
+            float v = router_score(l[lane + 32 * j], a.flags);
             if (!isfinite(v)) {
                 bad = true;
                 v = -INFINITY;
@@ -177,7 +177,7 @@ __device__ __forceinline__ void rs_topk_token(const LayerArgs& a, int t, int lan
         a.topw[(size_t)t * K + lane] = ex / s;
     }
     if (lane == 0) {
-        const float z = l[E];
+        const float z = router_score(l[E], a.flags);
         if (!isfinite(z)) bad = true;
         a.sgate[t] = 1.0f / (1.0f + expf(-z));
     }

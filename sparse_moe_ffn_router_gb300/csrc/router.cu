@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(256) k_router_topk(LayerArgs a) {
     for (int j = 0; j < 8; ++j) {
         key[j] = 0u;
         if (lane + 32 * j < a.E) {
-            float v = l[lane + 32 * j];
+            float v = router_score(l[lane + 32 * j], a.flags);
             if (!isfinite(v)) {
                 bad = true;
                 v = -INFINITY;
@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(256) k_router_topk(LayerArgs a) {
     } else {
         z = l[a.E];
     }
+    z = router_score(z, a.flags);
     const float ex = lane < a.K ? expf(myv - v0) : 0.f;
     const float s = warp_sum(ex);
     if (lane < a.K) {
@@ -176,7 +177,7 @@ __device__ void topk_one_token(const LayerArgs& a, const float* l, int t, int la
     for (int j = 0; j < 8; ++j) {
         key[j] = 0u;
         if (lane + 32 * j < a.E) {
-            float v = __ldcg(l + lane + 32 * j);
+            float v = router_score(__ldcg(l + lane + 32 * j), a.flags);
             if (!isfinite(v)) {
                 bad = true;
                 v = -INFINITY;
@@ -194,7 +195,7 @@ __device__ void topk_one_token(const LayerArgs& a, const float* l, int t, int la
         a.topw[(size_t)t * a.K + lane] = ex / s;
     }
     if (lane == 0) {
-        const float z = __ldcg(l + a.E);
+        const float z = router_score(__ldcg(l + a.E), a.flags);
         if (!isfinite(z)) bad = true;
         a.sgate[t] = 1.0f / (1.0f + expf(-z));
     }
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
         for (int j = 0; j < 8; ++j) {
             key[j] = 0u;
             if (lane + 32 * j < a.E) {
-                float v = l[lane + 32 * j];
+                float v = router_score(l[lane + 32 * j], a.flags);
                 if (!isfinite(v)) {
                     bad = true;
                     v = -INFINITY;
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
             a.topw[(size_t)t * a.K + lane] = ex / s;
         }
         if (lane == 0) {
-            const float z = l[a.E];
+            const float z = router_score(l[a.E], a.flags);
             if (!isfinite(z)) bad = true;
             a.sgate[t] = 1.0f / (1.0f + expf(-z));
         }

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(256) k_stats_partial(LayerArgs a, float* part_
             const int e = lane + 32 * j;
             v[j] = -INFINITY;
             if (e < a.E) {
-                const float s = l[e];
+                const float s = router_score(l[e], a.flags);
                 v[j] = isfinite(s) ? s : -INFINITY;
             }
             m = fmaxf(m, v[j]);

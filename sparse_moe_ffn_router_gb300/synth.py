@@ -30,7 +30,9 @@ _CHUNK = 1 << 25
 
 # Tensor tags of the key derivation.
 TAGS = {"x": 1, "router_w": 2, "router_b": 3, "gate_up": 4, "down": 5, "shared_gate_up": 6,
-        "shared_down": 7, "shared_gate": 8, "zipf_rank": 9, "x_stack": 10}
+        "shared_down": 7, "shared_gate": 8, "zipf_rank": 9, "x_stack": 10,
+        # streams of the exact-score test inputs (small-integer values, see tests/inputs.py)
+        "x_exact": 11, "router_w_exact": 12, "shared_gate_exact": 13, "router_b_exact": 14}
 
 
 def _signed(v: int) -> int:

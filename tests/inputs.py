@@ -60,3 +60,26 @@ def to_host(w: dict) -> dict:
 
 def bf16(a) -> torch.Tensor:
     return torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def exact_score_inputs(dims, seed: int, with_bias: bool = False, layer: int = 0) -> dict:
+    """Router inputs whose fp32 scores are exact in any summation order, for comparing the
+    bf16-typed scores bit for bit: x in {-1, 0, 1}; router and shared-gate weights integer
+    multiples of 2^-7 up to 40/128 (6 significant bits, exact in bf16); the bias (when asked)
+    a multiple of 2^-5 up to 3 (7 bits). Every score is then an integer multiple of 2^-7 below
+    2^17 * 2^-7, exact in fp32 whatever the order of the additions, and mostly needs more than
+    bf16's 8 significant bits, so the rounding and its ties are exercised. Drawn from the
+    seeded synthetic streams (N(0, 1) token values and N(0, 16^2) weights, clamped and
+    rounded)."""
+    T, H, E = dims[:3]
+    z = synth.make_x(T, H, seed, layer, tag="x_exact").float()
+    x = torch.round(torch.clamp(z, -1.4, 1.4)).to(torch.bfloat16)
+    wr = synth.normal_bf16((E, H), 16.0, synth.stream_key(seed, layer, "router_w_exact")).float()
+    wr = (torch.round(torch.clamp(wr, -40, 40)) / 128).to(torch.bfloat16)
+    sg = synth.normal_bf16((1, H), 16.0, synth.stream_key(seed, layer, "shared_gate_exact")).float()
+    sg = (torch.round(torch.clamp(sg, -40, 40)) / 128).to(torch.bfloat16)
+    br = None
+    if with_bias:
+        b = synth.normal_bf16((E,), 1.0, synth.stream_key(seed, layer, "router_b_exact")).float()
+        br = (torch.round(torch.clamp(b, -3, 3) * 32) / 32).to(torch.bfloat16)
+    return dict(x=x, router_w=wr, shared_gate=sg, router_b=br)

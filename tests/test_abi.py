@@ -114,3 +114,19 @@ def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError, match="GPU only"):
         binding._ptr(torch.zeros(4))
+
+
+def test_unknown_flag_bits_are_rejected_before_any_launch(lib):
+    # MOE_FLAG_BF16_SCORES (1) is the only flag; every entry point that routes refuses others
+    w = _weights()
+    for flags in (2, 1 << 30, -1):
+        dims = FULL + (flags,)
+        d = Dims(*dims)
+        assert _forward(lib, dims=dims) == 1
+        wsb = lib.moe_workspace_size(ctypes.byref(d))
+        assert wsb == lib.moe_workspace_size(ctypes.byref(Dims(*FULL)))  # the size ignores flags
+        assert lib.moe_route(ctypes.byref(d), A, ctypes.byref(w), A, A, A, A, A, A, wsb, None) == 1
+        assert lib.moe_router_stats(ctypes.byref(d), A, ctypes.byref(w), A, A, A, A, wsb, None) == 1
+        assert lib.moe_route_noalloc(ctypes.byref(d), A, ctypes.byref(w), A, A, A, A, A, None) == 1
+    # the defined flag passes host validation (the call then stops at a misaligned output)
+    assert _forward(lib, dims=FULL + (binding.FLAG_BF16_SCORES,), out=A + 0x200002) == 3
