@@ -50,7 +50,8 @@ UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "decode_T1"
 ROTATE = 8
 KERNEL_NAMES = ["router_scores", "router_topk", "dispatch_local", "dispatch_scan", "dispatch_scatter", "gate_up",
-                "down", "combine", "rmsnorm", "shared_gate", "gather", "gemm_plan", "decode_fused"]
+                "down", "combine", "rmsnorm", "shared_gate", "gather", "gemm_plan", "decode_fused", "fetch_experts"]
+HOST_LAYERS = 4  # layers cycled through with host-resident experts (their touched experts exceed L2)
 
 
 def parse_args():
@@ -483,6 +484,74 @@ def time_variant(ls: LayerSet, flags: int, n: int = 32, reps: int = 5) -> dict:
             "default_ms_per_step": round(base, 5), "device_error": moe.moe_last_device_error(ls.ws)}
 
 
+def time_host_experts(wl, device, n: int = 32, reps: int = 5) -> dict:
+    """moe_forward_host_experts: the routed experts (gate_up, down) of HOST_LAYERS layers in
+    pinned host memory, router and shared expert in HBM, one device shadow for all layers.
+    Step time over the rotating layers (a CUDA graph of n steps replayed reps times), and the
+    fetch kernel's share: the touched experts' bytes over its event-timed duration (the host
+    link's achieved rate)."""
+    import sparse_moe_ffn_router_gb300 as moe
+    T, H, E, K, I, Is = wl.dims
+    layers, nbytes = [], []
+    for l in range(HOST_LAYERS):
+        w = synth.make_weights(H, E, I, Is, wl.seed, l, wl.zipf_s)
+        x = synth.make_x(T, H, wl.seed, l, device=device)
+        dev = {k: (None if v is None else v.to(device)) for k, v in w.items()}
+        dev["gate_up"], dev["down"] = w["gate_up"].pin_memory(), w["down"].pin_memory()
+        layers.append((moe.Weights.from_dict(dev), x))
+    ws = moe.new_workspace(wl.dims, device)
+    shadow = torch.zeros(moe.moe_expert_shadow_size(wl.dims), dtype=torch.uint8, device=device)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    # experts each layer touches (the bytes its fetch copies)
+    for W, x in layers:
+        ids = torch.empty(T, K, dtype=torch.int32, device=device)
+        tw = torch.empty(T, K, dtype=torch.float32, device=device)
+        counts = torch.empty(E, dtype=torch.int32, device=device)
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=device)
+        perm = torch.empty(T * K, dtype=torch.int32, device=device)
+        Wd = moe.Weights(W.router_w, W.router_b, W.shared_gate_up, W.shared_gate_up, W.shared_gate_up, W.shared_down,
+                         W.shared_gate)  # routing reads the router and the shared gate only
+        moe.moe_route(wl.dims, x, Wd, ids, tw, counts, offsets, perm, ws)
+        nbytes.append(int((counts > 0).sum().item()) * (2 * I * H + H * I) * 2)
+
+    def step(i):
+        W, x = layers[i % HOST_LAYERS]
+        moe.moe_forward_host_experts(wl.dims, x, W, None, out, shadow, ws)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            step(i)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (n * reps)
+    ev = trace_kernels(moe, ["fetch_experts"], n)
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2):
+        for i in range(n):
+            step(i)
+    g2.replay()
+    torch.cuda.synchronize()
+    clear_traces(moe)
+    fetch_ms = kernel_ms(ev, n)["fetch_experts"]
+    fetched = sum(nbytes[i % HOST_LAYERS] for i in range(n)) / n
+    err = moe.moe_last_device_error(ws)
+    del layers, shadow
+    return {"tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_step": round(ms, 5),
+            "expert_bytes_per_step": int(fetched), "fetch_ms": round(fetch_ms, 5),
+            "host_link_gbs": round(fetched / (fetch_ms * 1e-3) / 1e9, 1), "layers": HOST_LAYERS,
+            "device_error": err}
+
+
 def time_e2e(ls: LayerSet, steps: int, warmup: int) -> dict:
     """Same metric through the public call with host buffers: per step, x is copied from
     pinned host memory, the layer runs, and the output is copied back to pinned memory."""
@@ -675,6 +744,13 @@ def main():
             del ls2
         torch.cuda.empty_cache()
     line["also"] = also
+    # routed experts resident in host memory, fetched over the host link per step
+    host = {}
+    for name in ("decode_T1", "decode_T64"):
+        if name == wl.name or name in names:
+            host[name] = time_host_experts(WORKLOADS[name], device)
+            torch.cuda.empty_cache()
+    line["host_experts"] = host
     if rank == 0 and world == 1:
         r = oracle_steps(wl, 10 ** 6, 1, budget_s=args.cpu_budget, device=device)
         line["cpu_baseline"] = {"value": round(r["value"], 3), "unit": UNIT, "cores": r["cores"], "kind": "oracle",

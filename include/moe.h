@@ -111,6 +111,25 @@ moe_status moe_route(const moe_dims* d, const void* x, const moe_weights* w, int
 moe_status moe_forward(const moe_dims* d, const void* x, const moe_weights* w, const void* residual, void* out,
                        void* workspace, size_t ws_bytes, void* stream);
 
+/* Routed experts resident in host memory ("One Token Through Qwen3.6", Where the Weights
+ * Live: checkpoint on disk, system RAM, GPU memory, kernels; the routing decides which expert
+ * weights a layer needs). Same layer as moe_forward, but w->gate_up and w->down point to HOST
+ * memory that is pinned and mapped into the device address space (cudaHostAlloc, or
+ * cudaHostRegister with mapping); every other weight, x, out, residual and the workspace are
+ * device memory as for moe_forward. After the routing, one kernel copies the gate_up and down
+ * rows of the experts this call touches over the host link into `shadow`, device memory of
+ * moe_expert_shadow_size(d) bytes laid out like [E, 2I, H] followed by [E, H, I] bf16 (only
+ * the touched experts' rows are written; the rest is left as it was), and the experts run
+ * from there. One shadow can serve every layer of a model in turn.
+ * Errors: MOE_ERR_INVALID_ARG when gate_up or down is not registered host memory mapped into
+ * the device (checked with cudaPointerGetAttributes before any launch) or shadow is NULL,
+ * MOE_ERR_MISALIGNED when shadow is not 16-byte aligned, MOE_ERR_WORKSPACE_TOO_SMALL when
+ * shadow_bytes < moe_expert_shadow_size(d); otherwise as moe_forward. */
+size_t moe_expert_shadow_size(const moe_dims* d);
+moe_status moe_forward_host_experts(const moe_dims* d, const void* x, const moe_weights* w, const void* residual,
+                                    void* out, void* shadow, size_t shadow_bytes, void* workspace, size_t ws_bytes,
+                                    void* stream);
+
 /* RMSNorm of the pre-MoE norm ("RMSNorm -> MoE FFN -> +residual", "Qwen3.6-35B-A3B --
  * Architecture Overview", Stage 2; "Qwen3.6 35B-A3B", Blocks: RmsNorm):
  *   xn[t,h] = bf16( x[t,h] / sqrt(mean_h x[t,h]^2 + eps) * gamma[h] )   (fp32 arithmetic)
@@ -164,7 +183,8 @@ enum {
     MOE_KERNEL_GEMM_PLAN = 11,      /* not launched: the dispatch scan writes the GEMM tables */
     MOE_KERNEL_DECODE_FUSED = 12,   /* whole layer in one persistent kernel (T <= 8) */
     MOE_KERNEL_ROUTER_STATS = 13,   /* load-balancing statistics (moe_router_stats) */
-    MOE_KERNEL_COUNT = 14
+    MOE_KERNEL_FETCH_EXPERTS = 14,  /* touched experts copied from host memory (moe_forward_host_experts) */
+    MOE_KERNEL_COUNT = 15
 };
 
 /* Benchmarking aid. While set, every launch of `kernel` made by this library records

@@ -13,7 +13,9 @@ from .binding import (  # noqa: F401
     Weights,
     library_path,
     load_library,
+    moe_expert_shadow_size,
     moe_forward,
+    moe_forward_host_experts,
     moe_last_device_error,
     moe_launch_count,
     moe_set_trace,

@@ -19,10 +19,10 @@ MOE_STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHA
               4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE"}
 EXPORTED = ["moe_workspace_size", "moe_workspace_init", "moe_route", "moe_forward", "moe_rmsnorm",
             "moe_last_device_error", "moe_workspace_tap", "moe_set_trace", "moe_launch_count", "moe_route_noalloc", "moe_status_string",
-            "moe_router_stats"]
+            "moe_router_stats", "moe_expert_shadow_size", "moe_forward_host_experts"]
 KERNELS = {"router_scores": 0, "router_topk": 1, "dispatch_local": 2, "dispatch_scan": 3, "dispatch_scatter": 4,
            "gate_up": 5, "down": 6, "combine": 7, "rmsnorm": 8, "shared_gate": 9, "gather": 10, "gemm_plan": 11,
-           "decode_fused": 12, "router_stats": 13}
+           "decode_fused": 12, "router_stats": 13, "fetch_experts": 14}
 
 
 # moe_dims.flags: router and shared-gate scores rounded to bf16 before ranking and sigmoid
@@ -108,6 +108,10 @@ def load_library(build_if_missing: bool = True):
             lib.moe_route_noalloc.argtypes = [D, P, W, P, P, P, P, P, P]
             lib.moe_router_stats.restype = st
             lib.moe_router_stats.argtypes = [D, P, W, P, P, P, P, S, P]
+            lib.moe_expert_shadow_size.restype = S
+            lib.moe_expert_shadow_size.argtypes = [D]
+            lib.moe_forward_host_experts.restype = st
+            lib.moe_forward_host_experts.argtypes = [D, P, W, P, P, P, S, P, S, P]
             lib.moe_status_string.restype = ctypes.c_char_p
             lib.moe_status_string.argtypes = [ctypes.c_int]
             _lib = lib
@@ -194,6 +198,33 @@ def moe_forward(dims, x, weights: Weights, residual, out, workspace, stream=None
     _check(load_library().moe_forward(ctypes.byref(_dims(dims)), _ptr(x), ctypes.byref(w), _ptr(residual), _ptr(out),
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(stream)), "moe_forward")
+
+
+def _ptr_host(t) -> int:
+    """Address of a pinned (page-locked) host tensor, for the host-resident expert weights."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("host-resident expert weights must be pinned CPU tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def moe_expert_shadow_size(dims) -> int:
+    return int(load_library().moe_expert_shadow_size(ctypes.byref(_dims(dims))))
+
+
+def moe_forward_host_experts(dims, x, weights: Weights, residual, out, shadow, workspace, stream=None):
+    """moe_forward with weights.gate_up and weights.down in pinned host memory: the experts
+    each call touches are copied over the host link into `shadow` (a uint8 CUDA tensor of
+    moe_expert_shadow_size(dims) bytes) and run from there."""
+    w = CWeights(*[(_ptr_host(getattr(weights, f.name)) if f.name in ("gate_up", "down") else _ptr(getattr(weights, f.name)))
+                   for f in fields(weights)])
+    _check(load_library().moe_forward_host_experts(ctypes.byref(_dims(dims)), _ptr(x), ctypes.byref(w), _ptr(residual),
+                                                   _ptr(out), _ptr(shadow), shadow.numel() * shadow.element_size(),
+                                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                                   _stream(stream)), "moe_forward_host_experts")
 
 
 def moe_rmsnorm(dims, x, gamma, eps: float, xn, stream=None):

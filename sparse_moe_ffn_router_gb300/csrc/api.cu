@@ -134,11 +134,50 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 // pipe scores, then top-K and the whole dispatch in one CTA); from 256 tokens the scores as a
 // tcgen05 GEMM, top-K one warp per token and the three block-parallel dispatch kernels. (The
 // single-kernel routing of up to 64 tokens is used only by the fixed-scratch entry point.)
+// The output buffers of a layer call: out given, 16-byte aligned, not overlapping x, and
+// either equal to the residual or apart from it.
+moe_status check_output(const moe_dims* d, const void* x, const void* residual, const void* out) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(out) || (residual && !aligned16(residual))) return MOE_ERR_MISALIGNED;
+    const size_t act_bytes = (size_t)d->T * d->H * 2;
+    if (overlap(out, act_bytes, x, act_bytes)) return MOE_ERR_INVALID_ARG;
+    if (residual && residual != out && overlap(out, act_bytes, residual, act_bytes)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+// Host memory that is pinned and mapped into the device address space; dev receives the
+// address kernels use.
+bool host_mapped(const void* p, const void** dev) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the error this query left
+        return false;
+    }
+    if (at.type != cudaMemoryTypeHost || !at.devicePointer) return false;
+    *dev = at.devicePointer;
+    return true;
+}
+
 cudaError_t launch_routing(const LayerArgs& a, cudaStream_t s) {
     if (route_cluster_supported(a)) return launch_route_cluster(a, s);
     if (route_small_supported(a)) return launch_route_small(a, s);
     cudaError_t e = launch_router(a, s);
     if (e == cudaSuccess) e = launch_dispatch(a, s);
+    return e;
+}
+
+// The experts and the combine, once the routing tables are in the workspace.
+cudaError_t launch_after_routing(const LayerArgs& a, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    if (a.gemm) {
+        e = launch_expert_gemms(a, s);
+        if (e == cudaSuccess) e = launch_combine(a, s);
+    } else if (stream_supported(a)) {
+        e = launch_stream_experts(a, s);  // the combine runs as its programmatic dependent
+    } else {
+        e = launch_experts(a, s);
+        if (e == cudaSuccess) e = launch_combine(a, s);
+    }
     return e;
 }
 
@@ -208,25 +247,48 @@ extern "C" moe_status moe_forward(const moe_dims* d, const void* x, const moe_we
     LayerArgs a;
     moe_status st = prepare(d, x, w, workspace, ws_bytes, &p, &a);
     if (st != MOE_OK || d->T == 0) return st;
-    if (!out) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(out) || (residual && !aligned16(residual))) return MOE_ERR_MISALIGNED;
-    const size_t act_bytes = (size_t)d->T * d->H * 2;
-    if (overlap(out, act_bytes, x, act_bytes)) return MOE_ERR_INVALID_ARG;
-    if (residual && residual != out && overlap(out, act_bytes, residual, act_bytes)) return MOE_ERR_INVALID_ARG;
+    st = check_output(d, x, residual, out);
+    if (st != MOE_OK) return st;
     a.residual = (const bf16*)residual;
     a.out = (bf16*)out;
     cudaStream_t s = (cudaStream_t)stream;
     if (decode_fused_supported(a)) return cuda_status(launch_decode_fused(a, s));  // whole layer, one launch
     cudaError_t e = launch_routing(a, s);
-    if (a.gemm) {
-        if (e == cudaSuccess) e = launch_expert_gemms(a, s);
-        if (e == cudaSuccess) e = launch_combine(a, s);
-    } else if (e == cudaSuccess && stream_supported(a)) {
-        e = launch_stream_experts(a, s);  // the combine is fused into its down kernel
-    } else if (e == cudaSuccess) {
-        e = launch_experts(a, s);
-        if (e == cudaSuccess) e = launch_combine(a, s);
-    }
+    if (e == cudaSuccess) e = launch_after_routing(a, s);
+    return cuda_status(e);
+}
+
+extern "C" size_t moe_expert_shadow_size(const moe_dims* d) {
+    Plan p;
+    if (!d || !make_plan(*d, &p)) return 0;
+    return ((size_t)d->E * 2 * d->I * d->H + (size_t)d->E * d->H * d->I) * 2;
+}
+
+extern "C" moe_status moe_forward_host_experts(const moe_dims* d, const void* x, const moe_weights* w,
+                                               const void* residual, void* out, void* shadow, size_t shadow_bytes,
+                                               void* workspace, size_t ws_bytes, void* stream) {
+    Plan p;
+    LayerArgs a;
+    moe_status st = prepare(d, x, w, workspace, ws_bytes, &p, &a);
+    if (st != MOE_OK || d->T == 0) return st;
+    st = check_output(d, x, residual, out);
+    if (st != MOE_OK) return st;
+    if (!shadow) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(shadow)) return MOE_ERR_MISALIGNED;
+    if (shadow_bytes < moe_expert_shadow_size(d)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    const void* hgu = nullptr;
+    const void* hdn = nullptr;
+    if (!host_mapped(w->gate_up, &hgu) || !host_mapped(w->down, &hdn)) return MOE_ERR_INVALID_ARG;
+    a.residual = (const bf16*)residual;
+    a.out = (bf16*)out;
+    bf16* sgu = (bf16*)shadow;
+    bf16* sdn = sgu + (size_t)d->E * 2 * d->I * d->H;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_routing(a, s);
+    if (e == cudaSuccess) e = launch_fetch_experts(a, (const bf16*)hgu, (const bf16*)hdn, sgu, sdn, s);
+    a.gate_up = sgu;
+    a.down = sdn;
+    if (e == cudaSuccess) e = launch_after_routing(a, s);
     return cuda_status(e);
 }
 

@@ -130,3 +130,18 @@ def test_unknown_flag_bits_are_rejected_before_any_launch(lib):
         assert lib.moe_route_noalloc(ctypes.byref(d), A, ctypes.byref(w), A, A, A, A, A, None) == 1
     # the defined flag passes host validation (the call then stops at a misaligned output)
     assert _forward(lib, dims=FULL + (binding.FLAG_BF16_SCORES,), out=A + 0x200002) == 3
+
+
+def test_host_experts_shadow_size_and_host_checks(lib):
+    T, H, E, K, I, Is = FULL
+    assert binding.moe_expert_shadow_size(FULL) == E * (2 * I * H + H * I) * 2
+    assert binding.moe_expert_shadow_size((1, 2048, 256, 9, 512, 512)) == 0  # K > 8
+    d = Dims(*FULL)
+    w = _weights()
+    wsb = lib.moe_workspace_size(ctypes.byref(d))
+    sb = binding.moe_expert_shadow_size(FULL)
+    call = lambda shadow, nb: lib.moe_forward_host_experts(  # noqa: E731
+        ctypes.byref(d), A + 0x100000, ctypes.byref(w), None, A + 0x200000, shadow, nb, A + 0x400000, wsb, None)
+    assert call(None, sb) == 1
+    assert call(A + 0x800008, sb) == 3
+    assert call(A + 0x800000, sb - 16) == 4
