@@ -9,7 +9,8 @@
 // rows of the experts this call touches over the host link into a device shadow laid out like
 // the full [E, 2I, H] and [E, H, I] tensors, and the expert kernels run from the shadow
 // unchanged. The copy uses plain 16-byte loads of the mapped host memory (eight per thread in
-// flight), the ordinary way a kernel reads mapped pinned memory.
+// flight, each warp on one 4 KB stretch at a time), the ordinary way a kernel reads mapped
+// pinned memory.
 #include "launch.h"
 
 namespace moe {
@@ -20,26 +21,24 @@ __global__ void __launch_bounds__(256) k_fetch_experts(LayerArgs a, const uint4*
                                                        uint4* sdn) {
     const int n = a.hdr->n_act;  // experts with pairs, from the routing kernels
     const size_t gu = (size_t)2 * a.I * a.H / 8, dn = (size_t)a.H * a.I / 8, per = gu + dn;  // 16-byte units
-    const size_t total = (size_t)n * per;
-    const size_t stride = (size_t)gridDim.x * blockDim.x;
-    for (size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += stride * kFetchUnroll) {
+    // warp w copies runs of 32 * kFetchUnroll consecutive units (4 KB), runs w, w + warps, ...:
+    // each load instruction reads 512 contiguous bytes and a warp's loads in flight share
+    // one 4 KB stretch of host memory (per is a multiple of the run, so no run spans experts
+    // or the gate_up / down boundary)
+    constexpr size_t kRun = 32 * kFetchUnroll;
+    const int lane = threadIdx.x & 31;
+    const size_t warps = (size_t)gridDim.x * (blockDim.x >> 5);
+    const size_t runs = (size_t)n * per / kRun;
+    for (size_t q = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); q < runs; q += warps) {
+        const size_t i0 = q * kRun, j = i0 / per, r0 = i0 - j * per;
+        const size_t e = (size_t)a.act[j];
+        const uint4* src = r0 < gu ? hgu + e * gu + r0 : hdn + e * dn + (r0 - gu);
+        uint4* dst = r0 < gu ? sgu + e * gu + r0 : sdn + e * dn + (r0 - gu);
         uint4 v[kFetchUnroll];
-        uint4* dst[kFetchUnroll];
 #pragma unroll
-        for (int u = 0; u < kFetchUnroll; ++u) {
-            const size_t i = i0 + u * stride;
-            dst[u] = nullptr;
-            if (i < total) {
-                const size_t j = i / per, r = i - j * per;
-                const size_t e = (size_t)a.act[j];
-                const uint4* src = r < gu ? hgu + e * gu + r : hdn + e * dn + (r - gu);
-                dst[u] = r < gu ? sgu + e * gu + r : sdn + e * dn + (r - gu);
-                v[u] = __ldcg(src);
-            }
-        }
+        for (int u = 0; u < kFetchUnroll; ++u) v[u] = __ldcg(src + u * 32 + lane);
 #pragma unroll
-        for (int u = 0; u < kFetchUnroll; ++u)
-            if (dst[u]) *dst[u] = v[u];
+        for (int u = 0; u < kFetchUnroll; ++u) dst[u * 32 + lane] = v[u];
     }
 }
 
