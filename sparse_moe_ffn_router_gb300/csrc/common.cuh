@@ -70,6 +70,7 @@ struct Plan {
         o_act, o_h, o_y, o_xperm, o_upg, o_dng, o_upt, o_dnt, o_uprec, o_dlog, o_dh, total;
 };
 
+constexpr int kStatsTokens = 32;     // tokens per block of the load-balancing statistics
 constexpr int kDispatchTokens = 64;  // tokens per block of the dispatch (counting-sort) kernels
 
 inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -103,7 +104,10 @@ inline bool make_plan(const moe_dims& d, Plan* p) {
     p->o_act = take((size_t)(d.E + 1) * 4);
     p->o_h = take((P + T) * p->Imax * 2);
     p->gemm = d.T >= kGemmMinTokens;
-    p->o_y = take(T * (d.K + 1) * d.H * (p->gemm ? 2 : 4));
+    // Y, which a statistics call borrows for its per-block partial sums (fp32 + int per expert)
+    const size_t ybytes = T * (d.K + 1) * d.H * (p->gemm ? 2 : 4);
+    const size_t sbytes = (size_t)((d.T + kStatsTokens - 1) / kStatsTokens) * d.E * 8;
+    p->o_y = take(ybytes > sbytes ? ybytes : sbytes);
     p->o_xperm = take(p->gemm ? P * d.H * 2 : 0);
     p->o_upg = take((size_t)(d.E + 1) * sizeof(GemmGroup));
     p->o_dng = take((size_t)(d.E + 1) * sizeof(GemmGroup));

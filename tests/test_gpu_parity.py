@@ -92,6 +92,9 @@ EDGE = [
     (5, 1024, 64, 6, 256, 128),   # one persistent kernel: odd T, I > Is
     (8, 2048, 256, 8, 512, 512),  # one persistent kernel: full shape, 64 (token, slot) pairs
     (9, 2048, 256, 8, 512, 512),  # full shape, ragged token tile
+    (65, 1024, 128, 8, 256, 256),   # split router: two token blocks, the second with one token
+    (129, 2048, 256, 2, 512, 512),  # split router in 2 K slices of 1024 (165 KB of operands per CTA)
+    (255, 512, 64, 8, 128, 128),    # largest few-token case: 2040 (token, slot) pairs, 4 token blocks
     # from T = 256 on, the tensor-core path
     (256, 256, 16, 4, 64, 128),     # smallest tensor-core case: one 64-feature SwiGLU tile, E < 256
     (300, 384, 40, 3, 192, 64),     # 128-wide tiles, ragged M tiles, I > Is

@@ -54,7 +54,8 @@ def test_router_stats_parity(name):
     check_stats(Layer(wl.dims, wl.seed, wl.zipf_s))
 
 
-@pytest.mark.parametrize("dims", [(1, 128, 8, 1, 64, 64), (67, 256, 8, 8, 64, 128), (300, 384, 40, 3, 192, 64)],
+@pytest.mark.parametrize("dims", [(1, 128, 8, 1, 64, 64), (1, 128, 256, 2, 64, 64), (67, 256, 8, 8, 64, 128),
+                                  (300, 384, 40, 3, 192, 64)],
                          ids=lambda d: "x".join(map(str, d)))
 def test_router_stats_edge_shapes(dims):
     check_stats(Layer(dims, seed=200 + dims[0], router_std=0.1))
