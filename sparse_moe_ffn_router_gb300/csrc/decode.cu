@@ -1,4 +1,6 @@
-// decode.cu -- the whole MoE layer for a few tokens (T <= 8) in one persistent kernel.
+// decode.cu -- the whole MoE layer for a few tokens (T <= 8) in one persistent kernel;
+// moe_forward runs it for a single token (from two tokens on the router and streaming expert
+// kernels, with their larger ring, are faster).
 //
 // At decode the layer streams ~55 MB of weights per token ("Qwen3.6-35B-A3B -- Architecture
 // Overview", MoE FFN: router 2048 -> 256 plus the shared-expert gate, 8 routed SwiGLU experts

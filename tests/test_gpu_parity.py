@@ -89,8 +89,8 @@ EDGE = [
     (67, 256, 8, 8, 64, 128),     # K = E (dense mixture), ragged T, Is > I
     (129, 384, 40, 3, 192, 64),   # odd E and K, ragged T, I > Is
     (200, 128, 256, 8, 64, 64),   # most experts receive no rows
-    (5, 1024, 64, 6, 256, 128),   # one persistent kernel: odd T, I > Is
-    (8, 2048, 256, 8, 512, 512),  # one persistent kernel: full shape, 64 (token, slot) pairs
+    (5, 1024, 64, 6, 256, 128),   # one-cluster router + streaming experts: odd T, I > Is
+    (8, 2048, 256, 8, 512, 512),  # one-cluster router + streaming experts: full shape, 64 pairs
     (9, 2048, 256, 8, 512, 512),  # full shape, ragged token tile
     (65, 1024, 128, 8, 256, 256),   # split router: two token blocks, the second with one token
     (129, 2048, 256, 2, 512, 512),  # split router in 2 K slices of 1024 (165 KB of operands per CTA)
