@@ -11,44 +11,7 @@
 
 namespace moe {
 
-constexpr int kRouterTokens = 8;  // tokens per warp in the score kernel
-
-// logits[t, r] = sum_h x[t,h] * W[r,h] (+ br[r]) for r < E, and x[t] . ws at r = E.
-// One warp per (score row r, block of 8 tokens); fp32 products and sums in a fixed order
-// (16-byte chunks lane-strided, then a butterfly across the warp).
-__global__ void __launch_bounds__(256) k_router_scores(LayerArgs a) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x * 8 + warp;
-    if (r > a.E) return;
-    const bf16* wrow = r < a.E ? a.router_w + (size_t)r * a.H : a.sg;
-    const int t0 = blockIdx.y * kRouterTokens;
-    const int mt = min(kRouterTokens, a.T - t0);
-    float acc[kRouterTokens];
-#pragma unroll
-    for (int i = 0; i < kRouterTokens; ++i) acc[i] = 0.f;
-#pragma unroll 8
-    for (int c = lane; c < a.H / 8; c += 32) {
-        const uint4 wv = ld_ro(wrow + (size_t)c * 8);
-#pragma unroll
-        for (int tt = 0; tt < kRouterTokens; ++tt) {
-            if (tt < mt) {
-                float xf[8];
-                unpack8(ld_ro(a.x + (size_t)(t0 + tt) * a.H + (size_t)c * 8), xf);
-                acc[tt] = dot8(wv, xf, acc[tt]);
-            }
-        }
-    }
-#pragma unroll
-    for (int tt = 0; tt < kRouterTokens; ++tt) {
-        if (tt < mt) {
-            float s = warp_sum(acc[tt]);
-            if (lane == 0) {
-                if (r < a.E && a.router_b) s += __bfloat162float(a.router_b[r]);
-                a.logits[(size_t)(t0 + tt) * a.ldl + r] = s;
-            }
-        }
-    }
-}
+constexpr int kRouterTokens = 8;  // tokens per warp in the fused routing kernel's scoring loop
 
 // One warp per token: top-K of the E scores under the total order (score descending, index
 // ascending), renormalised weights, and the shared-expert gate.
@@ -77,21 +40,16 @@ __global__ void __launch_bounds__(256) k_router_topk(LayerArgs a) {
     float v0, myv;
     int mye;
     warp_topk(key, a.K, lane, v0, myv, mye);
-    // shared-expert gate score: from the score kernel (column E), or, when the E router columns
-    // came from the tensor-core GEMM, one more dot product x[t] . ws here
-    float z;
-    if (a.gemm) {
-        float acc = 0.f;
-        for (int c = lane; c < a.H / 8; c += 32) {
-            float xf[8];
-            unpack8(ld_ro(a.x + (size_t)t * a.H + (size_t)c * 8), xf);
-            acc = dot8(ld_ro(a.sg + (size_t)c * 8), xf, acc);
-        }
-        z = warp_sum(acc);
-        if (lane == 0) a.logits[(size_t)t * a.ldl + a.E] = z;
-    } else {
-        z = l[a.E];
+    // shared-expert gate score: the E router columns came from the tensor-core GEMM, the gate
+    // is one more dot product x[t] . ws here (kept in column E for the workspace taps)
+    float acc = 0.f;
+    for (int c = lane; c < a.H / 8; c += 32) {
+        float xf[8];
+        unpack8(ld_ro(a.x + (size_t)t * a.H + (size_t)c * 8), xf);
+        acc = dot8(ld_ro(a.sg + (size_t)c * 8), xf, acc);
     }
+    float z = warp_sum(acc);
+    if (lane == 0) a.logits[(size_t)t * a.ldl + a.E] = z;
     z = router_score(z, a.flags);
     const float ex = lane < a.K ? expf(myv - v0) : 0.f;
     const float s = warp_sum(ex);
@@ -106,14 +64,12 @@ __global__ void __launch_bounds__(256) k_router_topk(LayerArgs a) {
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&a.hdr->err, ERR_NONFINITE_SCORE);
 }
 
+// Routing of T >= 256 tokens: router GEMM on the tensor cores, then top-K (fewer tokens are
+// routed by the one-cluster or the split router, which cover every supported shape).
 cudaError_t launch_router(const LayerArgs& a, cudaStream_t s) {
-    if (a.gemm) {
-        cudaError_t e = launch_router_gemm(a, s);
-        if (e != cudaSuccess) return e;
-    } else {
-        dim3 g1((a.E + 1 + 7) / 8, (a.T + kRouterTokens - 1) / kRouterTokens);
-        MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (k_router_scores<<<g1, 256, 0, s>>>(a)));
-    }
+    if (!a.gemm) return cudaErrorNotSupported;
+    cudaError_t e = launch_router_gemm(a, s);
+    if (e != cudaSuccess) return e;
     MOE_LAUNCH(MOE_KERNEL_ROUTER_TOPK, s, (k_router_topk<<<(a.T + 7) / 8, 256, 0, s>>>(a)));
     return cudaGetLastError();
 }

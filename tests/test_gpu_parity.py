@@ -95,7 +95,12 @@ EDGE = [
     (65, 1024, 128, 8, 256, 256),   # split router: two token blocks, the second with one token
     (129, 2048, 256, 2, 512, 512),  # split router in 2 K slices of 1024 (165 KB of operands per CTA)
     (255, 512, 64, 8, 128, 128),    # largest few-token case: 2040 (token, slot) pairs, 4 token blocks
+    # hidden widths above 2048 and experts wider than 512: the generic expert kernels
+    (1, 2048, 64, 8, 1024, 512),    # one token with 1024-wide experts (not the fused kernel)
+    (3, 1024, 32, 4, 1024, 640),    # one-cluster router, wide experts, Is != I
+    (16, 4096, 64, 4, 256, 256),    # split router over H = 4096 (8 slices of 512)
     # from T = 256 on, the tensor-core path
+    (300, 4096, 16, 2, 128, 256),   # GEMMs over H = 4096, Is > I
     (256, 256, 16, 4, 64, 128),     # smallest tensor-core case: one 64-feature SwiGLU tile, E < 256
     (300, 384, 40, 3, 192, 64),     # 128-wide tiles, ragged M tiles, I > Is
     (1000, 2048, 256, 8, 512, 512), # full shape, many partly filled M tiles
