@@ -745,9 +745,10 @@ def main():
         torch.cuda.empty_cache()
     line["also"] = also
     # routed experts resident in host memory, fetched over the host link per step
+    # (with the extra workloads only: the short runs behind the ncu launch lists skip it)
     host = {}
     for name in ("decode_T1", "decode_T64"):
-        if name == wl.name or name in names:
+        if names and (name == wl.name or name in names):
             host[name] = time_host_experts(WORKLOADS[name], device)
             torch.cuda.empty_cache()
     line["host_experts"] = host
