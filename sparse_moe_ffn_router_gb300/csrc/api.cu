@@ -160,11 +160,12 @@ bool host_mapped(const void* p, const void** dev) {
     return true;
 }
 
-cudaError_t launch_routing(const LayerArgs& a, cudaStream_t s) {
+// experts: the experts run next (from T >= 256 the dispatch then also lays out their token rows)
+cudaError_t launch_routing(const LayerArgs& a, bool experts, cudaStream_t s) {
     if (route_cluster_supported(a)) return launch_route_cluster(a, s);
     if (route_small_supported(a)) return launch_route_small(a, s);
     cudaError_t e = launch_router(a, s);
-    if (e == cudaSuccess) e = launch_dispatch(a, s);
+    if (e == cudaSuccess) e = launch_dispatch(a, experts, s);
     return e;
 }
 
@@ -218,7 +219,7 @@ extern "C" moe_status moe_route(const moe_dims* d, const void* x, const moe_weig
     a.counts = counts;
     a.offsets = offsets;
     a.perm = perm;
-    return cuda_status(launch_routing(a, s));
+    return cuda_status(launch_routing(a, false, s));
 }
 
 extern "C" moe_status moe_router_stats(const moe_dims* d, const void* x, const moe_weights* w, float* P, float* f,
@@ -259,7 +260,7 @@ extern "C" moe_status moe_forward(const moe_dims* d, const void* x, const moe_we
     // router kernel + streaming expert kernels are faster (measured per layer: T=2 37.7 vs
     // 44.7 us, T=4 55.8 vs 85.7 us, T=8 84.8 vs 168.3 us).
     if (a.T <= kFusedMaxTokens && decode_fused_supported(a)) return cuda_status(launch_decode_fused(a, s));
-    cudaError_t e = launch_routing(a, s);
+    cudaError_t e = launch_routing(a, true, s);
     if (e == cudaSuccess) e = launch_after_routing(a, s);
     return cuda_status(e);
 }
@@ -290,7 +291,7 @@ extern "C" moe_status moe_forward_host_experts(const moe_dims* d, const void* x,
     bf16* sgu = (bf16*)shadow;
     bf16* sdn = sgu + (size_t)d->E * 2 * d->I * d->H;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = launch_routing(a, s);
+    cudaError_t e = launch_routing(a, true, s);
     if (e == cudaSuccess) e = launch_fetch_experts(a, (const bf16*)hgu, (const bf16*)hdn, sgu, sdn, s);
     a.gate_up = sgu;
     a.down = sdn;

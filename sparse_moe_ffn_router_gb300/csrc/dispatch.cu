@@ -222,11 +222,11 @@ __global__ void __launch_bounds__(256) k_dispatch_scatter_rows(LayerArgs a) {
     for (int c = lane; c < a.H / 8; c += 32) dst[c] = ld_ro(src + c);
 }
 
-cudaError_t launch_dispatch(const LayerArgs& a, cudaStream_t s) {
+cudaError_t launch_dispatch(const LayerArgs& a, bool with_rows, cudaStream_t s) {
     const int fh = gemm_up_half(a), bn_dn = gemm_down_bn(a);
     MOE_LAUNCH(MOE_KERNEL_DISPATCH_LOCAL, s, (k_dispatch_local<<<a.nb, 32, 0, s>>>(a)));
     MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCAN, s, (k_dispatch_scan<<<1, 256 * kScanParts, 0, s>>>(a, fh, bn_dn)));
-    if (a.gemm)
+    if (a.gemm && with_rows)
         MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCATTER, s,
                    (k_dispatch_scatter_rows<<<(unsigned)((a.P + 7) / 8), 256, 0, s>>>(a)));
     else

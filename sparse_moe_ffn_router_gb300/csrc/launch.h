@@ -96,7 +96,8 @@ bool stream_supported(const LayerArgs& a);
 bool decode_fused_supported(const LayerArgs& a);
 cudaError_t launch_decode_fused(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_stream_experts(const LayerArgs& a, cudaStream_t s);
-cudaError_t launch_dispatch(const LayerArgs& a, cudaStream_t s);
+// with_rows: also copy each pair's token row into xperm (the gate_up GEMM's A operand)
+cudaError_t launch_dispatch(const LayerArgs& a, bool with_rows, cudaStream_t s);
 cudaError_t launch_experts(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_rmsnorm(const bf16* x, const bf16* gamma, float eps, bf16* xn, int T, int H, cudaStream_t s);
 
