@@ -403,6 +403,8 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
     layer_gbs = layer_bytes / (ms / steps * 1e-3) / 1e9
     res["layer_hbm_frac"] = round(layer_gbs / peaks["hbm_gbs"], 4)
     res["layer_tensor_frac"] = round(flops / (ms / steps * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)
+    # the layer against its binding roofline: max(bytes / HBM peak, flops / tensor peak) / time
+    res["layer_binding_frac"] = max(res["layer_hbm_frac"], res["layer_tensor_frac"])
     if sampler:
         res["clocks"] = sampler.summary()
     return res
@@ -713,6 +715,7 @@ def main():
         "layer": {"unique_experts_per_step": main_res["unique_experts"],
                   "hbm_frac_of_layer_bytes": main_res["layer_hbm_frac"],
                   "tensor_frac": main_res["layer_tensor_frac"],
+                  "binding_frac": main_res["layer_binding_frac"],
                   "kernel_ms_warmup": {k: round(v, 5) for k, v in main_res["warm_kernel_ms"].items()}},
     }
     del ls
@@ -738,7 +741,8 @@ def main():
             also[name] = {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 5),
                           "device_error": r["device_error"],
                           "roofline": r.get("roofline"), "hbm_frac_of_layer_bytes": r["layer_hbm_frac"],
-                          "tensor_frac": r["layer_tensor_frac"], "unique_experts_per_step": r["unique_experts"],
+                          "tensor_frac": r["layer_tensor_frac"], "binding_frac": r["layer_binding_frac"],
+                          "unique_experts_per_step": r["unique_experts"],
                           "kernel_ms_warmup": {k: round(v, 5) for k, v in r["warm_kernel_ms"].items()},
                           "router_stats": stats, "bf16_scores": bf16s}
             del ls2
