@@ -60,7 +60,8 @@ typedef struct {
  * Without the flag the fp32 scores are used unrounded. */
 #define MOE_FLAG_BF16_SCORES 1
 
-/* Device pointers to one layer's weights; router_b may be NULL. */
+/* Pointers to one layer's weights, in device memory (moe_forward_host_experts takes gate_up
+ * and down in mapped host memory instead); router_b may be NULL. */
 typedef struct {
     const void* router_w;
     const void* router_b;
