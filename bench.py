@@ -15,8 +15,12 @@ Extra keys: `roofline` (dominant kernel: algorithmic bytes per launch over its C
 duration inside the timed region, against the measured HBM copy bandwidth), `e2e` (the same
 metric with x copied from pinned host memory and the output copied back inside the timed
 region), `cpu_baseline` (the fp64 C oracle on the host cores on a bounded sample of the same
-workload), `clocks` (nvidia-smi samples taken during the timed region), `also` (the decode
-T=64, prefill T=4096 and 40-layer stack workloads, shorter runs of the same measurement).
+workload), `clocks` (nvidia-smi samples taken during the timed region), `layer` (the whole
+layer's fractions of the HBM and tensor peaks and of its binding roofline), `also` (the
+decode T=64, prefill T=4096 and 40-layer stack workloads, shorter runs of the same
+measurement, each with the load-balancing statistics call and the bf16-score variant timed
+beside it), `host_experts` (decode with the routed experts in pinned host memory, fetched
+over the host link per step).
 
 `--impl reference` times the oracle (the only reference implementation: the pages publish
 no code) on the host cores for the same workload and metric.
