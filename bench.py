@@ -13,8 +13,8 @@ from the 129 MB L2. Weights and inputs are resident in HBM before timing starts.
 
 Extra keys: `roofline` (dominant kernel: algorithmic bytes per launch over its CUDA-event
 duration inside the timed region, against the measured HBM copy bandwidth), `e2e` (the same
-metric with x copied from pinned host memory and the output copied back inside the timed
-region), `cpu_baseline` (the fp64 C oracle on the host cores on a bounded sample of the same
+metric through moe_forward_host_io: x copied from pinned host memory and the output copied
+back by the library, inside the timed region), `cpu_baseline` (the fp64 C oracle on the host cores on a bounded sample of the same
 workload), `clocks` (nvidia-smi samples taken during the timed region), `layer` (the whole
 layer's fractions of the HBM and tensor peaks and of its binding roofline), `also` (the
 decode T=64, prefill T=4096 and 40-layer stack workloads, shorter runs of the same
@@ -559,8 +559,9 @@ def time_host_experts(wl, device, n: int = 32, reps: int = 5) -> dict:
 
 
 def time_e2e(ls: LayerSet, steps: int, warmup: int) -> dict:
-    """Same metric through the public call with host buffers: per step, x is copied from
-    pinned host memory, the layer runs, and the output is copied back to pinned memory."""
+    """Same metric through the public call with host buffers (moe_forward_host_io): per step,
+    the library copies x from pinned host memory into device staging, runs the layer, and
+    copies the output back to pinned host memory."""
     moe = ls.moe
     T, H = ls.dims[:2]
     hx = [x.cpu().pin_memory() for _, x in ls.layers]
@@ -569,9 +570,7 @@ def time_e2e(ls: LayerSet, steps: int, warmup: int) -> dict:
 
     def step(i):
         W, _ = ls.layers[i % len(ls.layers)]
-        xd.copy_(hx[i % len(hx)], non_blocking=True)
-        moe.moe_forward(ls.dims, xd, W, None, ls.out, ls.ws)
-        hout.copy_(ls.out, non_blocking=True)
+        moe.moe_forward_host_io(ls.dims, hx[i % len(hx)], W, None, hout, xd, ls.out, ls.ws)
 
     for i in range(warmup):
         step(i)

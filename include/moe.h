@@ -112,6 +112,23 @@ moe_status moe_route(const moe_dims* d, const void* x, const moe_weights* w, int
 moe_status moe_forward(const moe_dims* d, const void* x, const moe_weights* w, const void* residual, void* out,
                        void* workspace, size_t ws_bytes, void* stream);
 
+/* The layer with its token rows in HOST memory (the decode loop's view: a token's hidden
+ * state arrives from the host and the layer's output goes back to it). On `stream`, in this
+ * order: host_x is copied into dev_x, host_residual (when not NULL) into dev_out, moe_forward
+ * runs on (dev_x, dev_out as residual or none, dev_out), and dev_out is copied into host_out
+ * (cudaMemcpyAsync each; pinned host buffers keep the copies asynchronous, pageable ones work
+ * but the driver stages them and may block the calling thread). host_out holds the result
+ * once `stream` has passed the call.
+ *   host_x, host_residual, host_out  [T, H] bf16, host memory (pinned or pageable);
+ *                                    host_out may be the same buffer as host_x or host_residual
+ *   dev_x, dev_out                   [T, H] bf16, device memory, 16-byte aligned, disjoint
+ * Errors: MOE_ERR_INVALID_ARG when host_x or host_out is NULL, a host buffer is device memory
+ * or dev_x / dev_out is not device memory (cudaPointerGetAttributes, before any copy);
+ * otherwise as moe_forward with x = dev_x and out = dev_out. */
+moe_status moe_forward_host_io(const moe_dims* d, const void* host_x, const moe_weights* w, const void* host_residual,
+                               void* host_out, void* dev_x, void* dev_out, void* workspace, size_t ws_bytes,
+                               void* stream);
+
 /* Routed experts resident in host memory ("One Token Through Qwen3.6", Where the Weights
  * Live: checkpoint on disk, system RAM, GPU memory, kernels; the routing decides which expert
  * weights a layer needs). Same layer as moe_forward, but w->gate_up and w->down point to HOST

@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     moe_expert_shadow_size,
     moe_forward,
     moe_forward_host_experts,
+    moe_forward_host_io,
     moe_last_device_error,
     moe_launch_count,
     moe_set_trace,

@@ -19,7 +19,7 @@ MOE_STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHA
               4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE"}
 EXPORTED = ["moe_workspace_size", "moe_workspace_init", "moe_route", "moe_forward", "moe_rmsnorm",
             "moe_last_device_error", "moe_workspace_tap", "moe_set_trace", "moe_launch_count", "moe_route_noalloc", "moe_status_string",
-            "moe_router_stats", "moe_expert_shadow_size", "moe_forward_host_experts"]
+            "moe_router_stats", "moe_expert_shadow_size", "moe_forward_host_experts", "moe_forward_host_io"]
 KERNELS = {"router_scores": 0, "router_topk": 1, "dispatch_local": 2, "dispatch_scan": 3, "dispatch_scatter": 4,
            "gate_up": 5, "down": 6, "combine": 7, "rmsnorm": 8, "shared_gate": 9, "gather": 10, "gemm_plan": 11,
            "decode_fused": 12, "router_stats": 13, "fetch_experts": 14}
@@ -112,6 +112,8 @@ def load_library(build_if_missing: bool = True):
             lib.moe_expert_shadow_size.argtypes = [D]
             lib.moe_forward_host_experts.restype = st
             lib.moe_forward_host_experts.argtypes = [D, P, W, P, P, P, S, P, S, P]
+            lib.moe_forward_host_io.restype = st
+            lib.moe_forward_host_io.argtypes = [D, P, W, P, P, P, P, P, S, P]
             lib.moe_status_string.restype = ctypes.c_char_p
             lib.moe_status_string.argtypes = [ctypes.c_int]
             _lib = lib
@@ -225,6 +227,39 @@ def moe_forward_host_experts(dims, x, weights: Weights, residual, out, shadow, w
                                                    _ptr(out), _ptr(shadow), shadow.numel() * shadow.element_size(),
                                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
                                                    _stream(stream)), "moe_forward_host_experts")
+
+
+def _ptr_cpu(t, nbytes: int) -> int | None:
+    """Address of a contiguous CPU tensor (pinned or pageable) of at least nbytes bytes."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError("host-side token rows must be CPU tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"host tensor holds {t.numel() * t.element_size()} bytes, the layer needs {nbytes}")
+    return t.data_ptr()
+
+
+def moe_forward_host_io(dims, x, weights: Weights, residual, out, x_dev, out_dev, workspace, stream=None):
+    """moe_forward with the token rows in host memory: x (and residual, when given) are CPU
+    tensors copied into the device staging tensors x_dev (and out_dev), the layer runs, and
+    out_dev is copied back into the CPU tensor out, all in order on `stream`. Pinned host
+    tensors keep the copies asynchronous; out holds the result once the stream has passed
+    the call."""
+    d = _dims(dims)
+    nbytes = d.T * d.H * 2
+    for t in (x_dev, out_dev):
+        if t is not None and t.numel() * t.element_size() < nbytes:
+            raise ValueError("device staging tensors must hold [T, H] bf16")
+    _check(load_library().moe_forward_host_io(ctypes.byref(d), _ptr_cpu(x, nbytes), ctypes.byref(weights.to_c()),
+                                              _ptr_cpu(residual, nbytes), _ptr_cpu(out, nbytes), _ptr(x_dev),
+                                              _ptr(out_dev), _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_forward_host_io")
 
 
 def moe_rmsnorm(dims, x, gamma, eps: float, xn, stream=None):

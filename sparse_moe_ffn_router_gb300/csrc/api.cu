@@ -160,6 +160,23 @@ bool host_mapped(const void* p, const void** dev) {
     return true;
 }
 
+// The kind of memory p points to (cudaMemoryTypeUnregistered for pageable host memory), or
+// -1 when the query fails.
+int memory_type(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the error this query left
+        return -1;
+    }
+    return (int)at.type;
+}
+
+// Host memory, pinned or pageable: what the host-side token rows may live in.
+bool host_side(const void* p) {
+    const int t = memory_type(p);
+    return t == cudaMemoryTypeHost || t == cudaMemoryTypeUnregistered;
+}
+
 // experts: the experts run next (from T >= 256 the dispatch then also lays out their token rows)
 cudaError_t launch_routing(const LayerArgs& a, bool experts, cudaStream_t s) {
     if (route_cluster_supported(a)) return launch_route_cluster(a, s);
@@ -181,6 +198,17 @@ cudaError_t launch_after_routing(const LayerArgs& a, cudaStream_t s) {
         e = launch_experts(a, s);
         if (e == cudaSuccess) e = launch_combine(a, s);
     }
+    return e;
+}
+
+// The whole layer, once its arguments are checked. One token: one persistent launch. From two
+// tokens on the fused kernel's shared memory holds a smaller ring (the token rows and h rows
+// grow with T) and the router kernel + streaming expert kernels are faster (measured per
+// layer: T=2 37.7 vs 44.7 us, T=4 55.8 vs 85.7 us, T=8 84.8 vs 168.3 us).
+cudaError_t launch_layer(const LayerArgs& a, cudaStream_t s) {
+    if (a.T <= kFusedMaxTokens && decode_fused_supported(a)) return launch_decode_fused(a, s);
+    cudaError_t e = launch_routing(a, true, s);
+    if (e == cudaSuccess) e = launch_after_routing(a, s);
     return e;
 }
 
@@ -254,14 +282,31 @@ extern "C" moe_status moe_forward(const moe_dims* d, const void* x, const moe_we
     if (st != MOE_OK) return st;
     a.residual = (const bf16*)residual;
     a.out = (bf16*)out;
+    return cuda_status(launch_layer(a, (cudaStream_t)stream));
+}
+
+extern "C" moe_status moe_forward_host_io(const moe_dims* d, const void* host_x, const moe_weights* w,
+                                          const void* host_residual, void* host_out, void* dev_x, void* dev_out,
+                                          void* workspace, size_t ws_bytes, void* stream) {
+    Plan p;
+    LayerArgs a;
+    moe_status st = prepare(d, dev_x, w, workspace, ws_bytes, &p, &a);
+    if (st != MOE_OK || d->T == 0) return st;
+    st = check_output(d, dev_x, host_residual ? dev_out : nullptr, dev_out);
+    if (st != MOE_OK) return st;
+    if (!host_x || !host_out) return MOE_ERR_INVALID_ARG;
+    if (!host_side(host_x) || !host_side(host_out) || (host_residual && !host_side(host_residual)) ||
+        memory_type(dev_x) != cudaMemoryTypeDevice || memory_type(dev_out) != cudaMemoryTypeDevice)
+        return MOE_ERR_INVALID_ARG;
+    a.residual = host_residual ? (const bf16*)dev_out : nullptr;
+    a.out = (bf16*)dev_out;
+    const size_t act_bytes = (size_t)d->T * d->H * 2;
     cudaStream_t s = (cudaStream_t)stream;
-    // One token: the whole layer in one persistent launch. From two tokens on the fused kernel's
-    // shared memory holds a smaller ring (the token rows and h rows grow with T) and the
-    // router kernel + streaming expert kernels are faster (measured per layer: T=2 37.7 vs
-    // 44.7 us, T=4 55.8 vs 85.7 us, T=8 84.8 vs 168.3 us).
-    if (a.T <= kFusedMaxTokens && decode_fused_supported(a)) return cuda_status(launch_decode_fused(a, s));
-    cudaError_t e = launch_routing(a, true, s);
-    if (e == cudaSuccess) e = launch_after_routing(a, s);
+    cudaError_t e = cudaMemcpyAsync(dev_x, host_x, act_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && host_residual)
+        e = cudaMemcpyAsync(dev_out, host_residual, act_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = launch_layer(a, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(host_out, dev_out, act_bytes, cudaMemcpyDeviceToHost, s);
     return cuda_status(e);
 }
 

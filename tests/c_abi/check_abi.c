@@ -46,6 +46,8 @@ int main(void) {
     CHECK(moe_route(&full, A, &w, NULL, A, A, A, A, A, ws, NULL) == MOE_ERR_INVALID_ARG);
     CHECK(moe_forward_host_experts(&full, A, &w, NULL, A + 0x100000, NULL, 0, A + 0x200000, ws, NULL) ==
           MOE_ERR_INVALID_ARG);
+    CHECK(moe_forward_host_io(&full, NULL, &w, NULL, A, A + 0x100000, A + 0x200000, A + 0x400000, ws, NULL) ==
+          MOE_ERR_INVALID_ARG); /* no host x */
 
     CHECK(strncmp(moe_status_string(MOE_OK), "MOE_OK", 6) == 0);
     CHECK(strncmp(moe_status_string(MOE_ERR_MISALIGNED), "MOE_ERR_MISALIGNED", 18) == 0);

@@ -10,6 +10,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from sparse_moe_ffn_router_gb300 import binding
 from sparse_moe_ffn_router_gb300.binding import CWeights, Dims
@@ -145,3 +146,25 @@ def test_host_experts_shadow_size_and_host_checks(lib):
     assert call(None, sb) == 1
     assert call(A + 0x800008, sb) == 3
     assert call(A + 0x800000, sb - 16) == 4
+
+
+def test_host_io_host_checks(lib):
+    d = Dims(*FULL)
+    w = _weights()
+    wsb = lib.moe_workspace_size(ctypes.byref(d))
+    act = FULL[0] * FULL[1] * 2
+    call = lambda hx, hout, xd, od, nb=wsb: lib.moe_forward_host_io(  # noqa: E731
+        ctypes.byref(d), hx, ctypes.byref(w), None, hout, xd, od, A + 0x400000, nb, None)
+    xd, od = A + 0x100000, A + 0x200000
+    assert call(None, A, xd, od) == 1  # no host x
+    assert call(A, None, xd, od) == 1  # no host out
+    assert call(A, A, xd, None) == 1  # no device staging for out
+    assert call(A, A, xd + 8, od) == 3
+    assert call(A, A, xd, od + 8) == 3
+    assert call(A, A, xd, xd + act - 16) == 1  # staging buffers overlap
+    assert call(A, A, xd, od, wsb - 256) == 4
+    # T = 0 is a no-op before any pointer is looked at
+    assert lib.moe_forward_host_io(ctypes.byref(Dims(0, 2048, 256, 8, 512, 512)), None, None, None, None, None,
+                                   None, None, 0, None) == 0
+    with pytest.raises(ValueError, match="the layer needs"):  # a host x shorter than [T, H] bf16
+        binding.moe_forward_host_io(FULL, torch.empty(4, dtype=torch.bfloat16), None, None, None, None, None, None)
