@@ -559,18 +559,21 @@ def time_host_experts(wl, device, n: int = 32, reps: int = 5) -> dict:
 
 
 def time_e2e(ls: LayerSet, steps: int, warmup: int) -> dict:
-    """Same metric through the public call with host buffers (moe_forward_host_io): per step,
-    the library copies x from pinned host memory into device staging, runs the layer, and
-    copies the output back to pinned host memory."""
+    """Same metric through the public call with host buffers (moe_forward_host_io, prepared
+    once per layer as a ForwardHostIO): per step, the library copies x from pinned host
+    memory into device staging, runs the layer, and copies the output back to pinned host
+    memory. Also reports the host time to issue one step, taken over the first steps of the
+    timed loop while the launch queue is still short (a host time close to the step time
+    means the loop is issue-bound)."""
     moe = ls.moe
     T, H = ls.dims[:2]
     hx = [x.cpu().pin_memory() for _, x in ls.layers]
     hout = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
     xd = torch.empty(T, H, dtype=torch.bfloat16, device=ls.device)
+    calls = [moe.ForwardHostIO(ls.dims, W, xd, ls.out, ls.ws) for W, _ in ls.layers]
 
     def step(i):
-        W, _ = ls.layers[i % len(ls.layers)]
-        moe.moe_forward_host_io(ls.dims, hx[i % len(hx)], W, None, hout, xd, ls.out, ls.ws)
+        calls[i % len(calls)](hx[i % len(hx)], hout)
 
     for i in range(warmup):
         step(i)
@@ -578,13 +581,19 @@ def time_e2e(ls: LayerSet, steps: int, warmup: int) -> dict:
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
-    for i in range(steps):
+    n_host = min(steps, 64)
+    t0 = time.perf_counter()
+    for i in range(n_host):
+        step(warmup + i)
+    t1 = time.perf_counter()
+    for i in range(n_host, steps):
         step(warmup + i)
     stop.record()
     torch.cuda.synchronize()
     barrier()
     ms = max_over_ranks(start.elapsed_time(stop))
-    return dict(value=T * steps / (ms / 1e3), ms_per_step=ms / steps, h2d=T * H * 2, d2h=T * H * 2)
+    return dict(value=T * steps / (ms / 1e3), ms_per_step=ms / steps, h2d=T * H * 2, d2h=T * H * 2,
+                host_us_per_step=(t1 - t0) / n_host * 1e6)
 
 
 class StackSet:
@@ -711,7 +720,8 @@ def main():
                    "cuda_graph": main_res["graph"]},
         "roofline": main_res.get("roofline"),
         "e2e": {"value": round(e2e["value"] * world, 3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
-                "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["ms_per_step"], 6)},
+                "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["ms_per_step"], 6),
+                "host_us_per_step": round(e2e["host_us_per_step"], 2)},
         "gpu_launches": main_res["launches"],
         "device_error": main_res["device_error"],
         "clocks": main_res.get("clocks"),

@@ -9,6 +9,7 @@ ABI. There is no CPU path: a call fails loudly when the library or a GPU is miss
 """
 from .binding import (  # noqa: F401
     FLAG_BF16_SCORES,
+    ForwardHostIO,
     MoEError,
     Weights,
     library_path,

@@ -262,6 +262,34 @@ def moe_forward_host_io(dims, x, weights: Weights, residual, out, x_dev, out_dev
            "moe_forward_host_io")
 
 
+class ForwardHostIO:
+    """moe_forward_host_io with everything but the host buffers marshalled once.
+
+    A decode loop calls the same layer with the same weights, staging tensors and workspace
+    on every step; this object converts those (and the stream, the current one when none is
+    given) into C arguments at construction and keeps references to the tensors, so each
+    call only checks and passes the host tensors. The tensors must not be resized or
+    re-pointed (``set_``) while the object is in use."""
+
+    def __init__(self, dims, weights: Weights, x_dev, out_dev, workspace, stream=None):
+        self._d = _dims(dims)
+        self._nbytes = self._d.T * self._d.H * 2
+        for t in (x_dev, out_dev):
+            if t is not None and t.numel() * t.element_size() < self._nbytes:
+                raise ValueError("device staging tensors must hold [T, H] bf16")
+        self._w = weights.to_c()
+        self._keep = (weights, x_dev, out_dev, workspace)
+        self._fixed = (ctypes.byref(self._d), ctypes.byref(self._w))
+        self._staging = (_ptr(x_dev), _ptr(out_dev), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                         _stream(stream))
+        self._fn = load_library().moe_forward_host_io
+
+    def __call__(self, x, out, residual=None):
+        n = self._nbytes
+        _check(self._fn(self._fixed[0], _ptr_cpu(x, n), self._fixed[1], _ptr_cpu(residual, n), _ptr_cpu(out, n),
+                        *self._staging), "moe_forward_host_io")
+
+
 def moe_rmsnorm(dims, x, gamma, eps: float, xn, stream=None):
     _check(load_library().moe_rmsnorm(ctypes.byref(_dims(dims)), _ptr(x), _ptr(gamma), float(eps), _ptr(xn),
                                       _stream(stream)), "moe_rmsnorm")

@@ -2,8 +2,8 @@
 copied from host buffers into device staging, the layer runs, and the output is copied back.
 Compared with the oracle, and bit for bit with moe_forward on the same device inputs, in each
 regime the entry point reaches (the fused one-token kernel, the streaming experts, the
-tensor-core GEMMs), with pinned and pageable host buffers, with and without a residual, and
-with the output written over the host x."""
+tensor-core GEMMs), with pinned and pageable host buffers, with and without a residual, with
+the output written over the host x, and through the prepared call (ForwardHostIO)."""
 from __future__ import annotations
 
 import ctypes
@@ -97,3 +97,26 @@ def test_host_io_refuses_device_buffers_as_host_rows():
     assert call(hx.data_ptr(), host_out.data_ptr(), x_dev.data_ptr(), host_out.data_ptr()) == 1
     assert call(hx.data_ptr(), host_out.data_ptr(), hx.data_ptr(), out_dev.data_ptr()) == 1
     torch.cuda.synchronize()
+
+
+def test_prepared_call_matches_the_entry():
+    dims = CASES[0]
+    x, residual, w, W = _layer(dims, 17)
+    T, H = dims[:2]
+    ws = moe.new_workspace(dims)
+    x_dev = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    out_dev = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    call = moe.ForwardHostIO(dims, W, x_dev, out_dev, ws)
+    hx, hr = x.pin_memory(), residual.pin_memory()
+    outs = []
+    for r in (None, hr, None):  # the same prepared call, with and without a residual
+        out = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+        call(hx, out, r)
+        torch.cuda.synchronize()
+        outs.append(out)
+    assert moe.moe_last_device_error(ws) == 0
+    assert torch.equal(outs[0], _device_forward(dims, x, None, W))
+    assert torch.equal(outs[1], _device_forward(dims, x, residual, W))
+    assert torch.equal(outs[2], outs[0])
+    with pytest.raises(ValueError, match="the layer needs"):
+        call(hx[:, :8].contiguous(), outs[0])
