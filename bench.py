@@ -54,7 +54,8 @@ UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "decode_T1"
 ROTATE = 8
 KERNEL_NAMES = ["router_scores", "router_topk", "dispatch_local", "dispatch_scan", "dispatch_scatter", "gate_up",
-                "down", "combine", "rmsnorm", "shared_gate", "gather", "gemm_plan", "decode_fused", "fetch_experts"]
+                "down", "combine", "rmsnorm", "shared_gate", "gather", "gemm_plan", "decode_fused", "fetch_experts",
+                "copy_rows"]
 HOST_LAYERS = 4  # layers cycled through with host-resident experts (their touched experts exceed L2)
 
 

@@ -202,7 +202,8 @@ enum {
     MOE_KERNEL_DECODE_FUSED = 12,   /* whole layer in one persistent kernel (T <= 8) */
     MOE_KERNEL_ROUTER_STATS = 13,   /* load-balancing statistics (moe_router_stats) */
     MOE_KERNEL_FETCH_EXPERTS = 14,  /* touched experts copied from host memory (moe_forward_host_experts) */
-    MOE_KERNEL_COUNT = 15
+    MOE_KERNEL_COPY_ROWS = 15,      /* token rows to or from mapped host memory (moe_forward_host_io) */
+    MOE_KERNEL_COUNT = 16
 };
 
 /* Benchmarking aid. While set, every launch of `kernel` made by this library records

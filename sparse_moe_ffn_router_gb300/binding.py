@@ -22,7 +22,8 @@ EXPORTED = ["moe_workspace_size", "moe_workspace_init", "moe_route", "moe_forwar
             "moe_router_stats", "moe_expert_shadow_size", "moe_forward_host_experts", "moe_forward_host_io"]
 KERNELS = {"router_scores": 0, "router_topk": 1, "dispatch_local": 2, "dispatch_scan": 3, "dispatch_scatter": 4,
            "gate_up": 5, "down": 6, "combine": 7, "rmsnorm": 8, "shared_gate": 9, "gather": 10, "gemm_plan": 11,
-           "decode_fused": 12, "router_stats": 13, "fetch_experts": 14}
+           "decode_fused": 12, "router_stats": 13, "fetch_experts": 14,
+           "copy_rows": 15}
 
 
 # moe_dims.flags: router and shared-gate scores rounded to bf16 before ranking and sigmoid

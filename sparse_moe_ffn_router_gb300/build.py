@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe_gb300.so")
 SOURCES = ["api.cu", "router.cu", "route_small.cu", "dispatch.cu", "experts.cu", "gemm.cu", "stream.cu", "decode.cu",
-           "noalloc.cu", "stats.cu", "host_experts.cu"]
+           "noalloc.cu", "stats.cu", "host_experts.cu", "host_io.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v", "--expt-relaxed-constexpr"]
 

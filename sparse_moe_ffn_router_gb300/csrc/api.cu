@@ -135,6 +135,7 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 // tcgen05 GEMM, top-K one warp per token and the three block-parallel dispatch kernels. (The
 // single-kernel routing of up to 64 tokens is used only by the fixed-scratch entry point.)
 constexpr int kFusedMaxTokens = 1;  // largest T that moe_forward runs in the fused decode kernel
+constexpr size_t kKernelCopyBytes = 1 << 20;  // largest host-row transfer moe_forward_host_io gives k_copy_rows
 
 // The output buffers of a layer call: out given, 16-byte aligned, not overlapping x, and
 // either equal to the residual or apart from it.
@@ -302,11 +303,22 @@ extern "C" moe_status moe_forward_host_io(const moe_dims* d, const void* host_x,
     a.out = (bf16*)dev_out;
     const size_t act_bytes = (size_t)d->T * d->H * 2;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = cudaMemcpyAsync(dev_x, host_x, act_bytes, cudaMemcpyHostToDevice, s);
+    // Up to kKernelCopyBytes, rows in pinned mapped host memory move by k_copy_rows (a copy-engine
+    // transfer would expose its own latency and the layer's launch behind it); pageable or
+    // larger buffers by cudaMemcpyAsync.
+    auto mapped = [&](const void* host, const void** dev) {
+        return act_bytes <= kKernelCopyBytes && aligned16(host) && host_mapped(host, dev);
+    };
+    const void* m = nullptr;
+    cudaError_t e = mapped(host_x, &m) ? launch_copy_rows(m, dev_x, act_bytes, a.num_sms, s)
+                                       : cudaMemcpyAsync(dev_x, host_x, act_bytes, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess && host_residual)
-        e = cudaMemcpyAsync(dev_out, host_residual, act_bytes, cudaMemcpyHostToDevice, s);
+        e = mapped(host_residual, &m) ? launch_copy_rows(m, dev_out, act_bytes, a.num_sms, s)
+                                      : cudaMemcpyAsync(dev_out, host_residual, act_bytes, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = launch_layer(a, s);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(host_out, dev_out, act_bytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = mapped(host_out, &m) ? launch_copy_rows(dev_out, const_cast<void*>(m), act_bytes, a.num_sms, s)
+                                 : cudaMemcpyAsync(host_out, dev_out, act_bytes, cudaMemcpyDeviceToHost, s);
     return cuda_status(e);
 }
 

@@ -84,6 +84,8 @@ cudaError_t launch_route_fused(const LayerArgs& a, cudaStream_t s);
 bool route_small_supported(const LayerArgs& a);
 cudaError_t launch_fetch_experts(const LayerArgs& a, const bf16* host_gate_up, const bf16* host_down,
                                  bf16* shadow_gate_up, bf16* shadow_down, cudaStream_t s);
+// dst = src, bytes a multiple of 16; one side pinned host memory mapped into the device.
+cudaError_t launch_copy_rows(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t s);
 cudaError_t launch_router_stats(const LayerArgs& a, float* P, float* f, float* loss, cudaStream_t s);
 cudaError_t launch_route_small(const LayerArgs& a, cudaStream_t s);
 bool route_cluster_supported(const LayerArgs& a);
