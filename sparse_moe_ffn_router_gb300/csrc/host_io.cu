@@ -1,11 +1,12 @@
 // host_io.cu -- token rows moved between host memory and the device by a kernel.
 //
-// A decode step's hidden state comes from the host and its output goes back ("One Token
-// Through Qwen3.6", One Complete Decode Step). For a few rows a copy-engine transfer costs more
-// than the bytes: the copy's own latency, and the layer's launch exposed behind it. When the host
-// buffer is pinned and mapped into the device address space, k_copy_rows moves the rows with
-// plain 16-byte loads and stores over the host link instead, so the layer's launch follows a
-// kernel on the same stream.
+// A decode step carries one token's hidden state through every layer ("One Token Through
+// Qwen3.6", One Complete Decode Step). A caller that keeps the token rows in host memory hands
+// the layer a few rows and takes a few rows back per step, and for so few rows a copy-engine
+// transfer costs more than its bytes: the copy's own latency, and the layer's launch exposed
+// behind it. When the host buffer is pinned and mapped into the device address space,
+// k_copy_rows moves the rows with plain 16-byte loads and stores over the host link instead,
+// so the layer's launch follows a kernel on the same stream.
 #include "launch.h"
 
 namespace moe {
