@@ -168,3 +168,14 @@ def test_host_io_host_checks(lib):
                                    None, None, 0, None) == 0
     with pytest.raises(ValueError, match="the layer needs"):  # a host x shorter than [T, H] bf16
         binding.moe_forward_host_io(FULL, torch.empty(4, dtype=torch.bfloat16), None, None, None, None, None, None)
+
+
+def test_prepared_host_io_checks_its_tensors():
+    T, H = FULL[:2]
+    cpu = lambda *shape: torch.empty(*shape, dtype=torch.bfloat16)  # noqa: E731
+    W = binding.Weights(router_w=cpu(4), router_b=None, gate_up=cpu(4), down=cpu(4), shared_gate_up=cpu(4),
+                        shared_down=cpu(4), shared_gate=cpu(4))
+    with pytest.raises(ValueError, match=r"\[T, H\]"):  # staging shorter than [T, H] bf16
+        binding.ForwardHostIO(FULL, W, cpu(T, H // 2), cpu(T, H), torch.empty(16, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="GPU only"):  # the weights and staging must be CUDA tensors
+        binding.ForwardHostIO(FULL, W, cpu(T, H), cpu(T, H), torch.empty(16, dtype=torch.uint8))
