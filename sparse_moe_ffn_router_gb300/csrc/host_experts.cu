@@ -23,8 +23,9 @@ __global__ void __launch_bounds__(256) k_fetch_experts(LayerArgs a, const uint4*
     const size_t gu = (size_t)2 * a.I * a.H / 8, dn = (size_t)a.H * a.I / 8, per = gu + dn;  // 16-byte units
     // warp w copies runs of 32 * kFetchUnroll consecutive units (4 KB), runs w, w + warps, ...:
     // each load instruction reads 512 contiguous bytes and a warp's loads in flight share
-    // one 4 KB stretch of host memory (per is a multiple of the run, so no run spans experts
-    // or the gate_up / down boundary)
+    // one 4 KB stretch of host memory. No run spans experts or the gate_up / down boundary:
+    // with H % 128 == 0 and I % 64 == 0 (checked on the host), gu = H*I/4 and dn = H*I/8 are
+    // multiples of 1024 units, so both are multiples of the run.
     constexpr size_t kRun = 32 * kFetchUnroll;
     const int lane = threadIdx.x & 31;
     const size_t warps = (size_t)gridDim.x * (blockDim.x >> 5);
