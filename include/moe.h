@@ -115,10 +115,11 @@ moe_status moe_forward(const moe_dims* d, const void* x, const moe_weights* w, c
 /* The layer with its token rows in HOST memory (the decode loop's view: a token's hidden
  * state arrives from the host and the layer's output goes back to it). On `stream`, in this
  * order: host_x is copied into dev_x, host_residual (when not NULL) into dev_out, moe_forward
- * runs on (dev_x, dev_out as residual or none, dev_out), and dev_out is copied into host_out
- * (cudaMemcpyAsync each; pinned host buffers keep the copies asynchronous, pageable ones work
- * but the driver stages them and may block the calling thread). host_out holds the result
- * once `stream` has passed the call.
+ * runs on (dev_x, dev_out as residual or none, dev_out), and dev_out is copied into host_out.
+ * Up to 1 MB of rows (T*H*2 bytes) in pinned host memory mapped into the device move by a
+ * small copy kernel (MOE_KERNEL_COPY_ROWS) over the host link; pageable or larger buffers by
+ * cudaMemcpyAsync (pageable ones work, but the driver stages them and may block the calling
+ * thread). host_out holds the result once `stream` has passed the call.
  *   host_x, host_residual, host_out  [T, H] bf16, host memory (pinned or pageable);
  *                                    host_out may be the same buffer as host_x or host_residual
  *   dev_x, dev_out                   [T, H] bf16, device memory, 16-byte aligned, disjoint
