@@ -63,11 +63,13 @@ def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=0,
-                   help="timed steps (default: enough for about 2 s of timed work, at least 200)")
+                   help="steps per timed repeat (default 512); the repeat runs until --min-seconds of timed work")
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    p.add_argument("--also", default="decode_T64,prefill_T4096_zipf,stack40_decode_T32",
+    p.add_argument("--min-seconds", type=float, default=1.0, help="timed work of the headline workload, in seconds")
+    p.add_argument("--also-seconds", type=float, default=0.5, help="timed work of each extra workload, in seconds")
+    p.add_argument("--also", default="decode_T8,decode_T64,prefill_T4096_zipf,stack40_decode_T32",
                    help="comma-separated extra workloads reported under 'also' ('none' to skip)")
     p.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--no-graph", action="store_true", help="time plain calls instead of CUDA-graph replays")
@@ -238,44 +240,56 @@ class LayerSet:
         self.out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=device)
         self._groups = None
 
-    def step(self, i: int):
-        W, x = self.layers[i % len(self.layers)]
+    def step(self, layer: int):
+        W, x = self.layers[layer % len(self.layers)]
         self.moe.moe_forward(self.dims, x, W, None, self.out, self.ws)
 
     def routed_groups(self) -> list[list[int]]:
         """Per layer: rows of each touched expert (for the algorithmic byte count)."""
         if self._groups is None:
-            T, H, E, K = self.dims[:4]
-            g = []
-            for W, x in self.layers:
-                ids = torch.empty(T, K, dtype=torch.int32, device=self.device)
-                tw = torch.empty(T, K, dtype=torch.float32, device=self.device)
-                counts = torch.empty(E, dtype=torch.int32, device=self.device)
-                offsets = torch.empty(E + 1, dtype=torch.int32, device=self.device)
-                perm = torch.empty(T * K, dtype=torch.int32, device=self.device)
-                self.moe.moe_route(self.dims, x, W, ids, tw, counts, offsets, perm, self.ws)
-                g.append([int(c) for c in counts.cpu().tolist() if c > 0])
-            self._groups = g
+            self._groups = [route_counts(self.moe, self.dims, x, W, self.device) for W, x in self.layers]
         return self._groups
 
 
-def algorithmic(dims, groups: list[int]) -> dict:
-    """Bytes each kernel must move at least, and the layer's flops, for one call.
+def route_counts(moe, dims, x, W, device) -> list[int]:
+    """Rows routed to each touched expert for one call (moe_route on its own workspace)."""
+    T, H, E, K = dims[:4]
+    ws = moe.new_workspace(dims, device)
+    ids = torch.empty(T, K, dtype=torch.int32, device=device)
+    tw = torch.empty(T, K, dtype=torch.float32, device=device)
+    counts = torch.empty(E, dtype=torch.int32, device=device)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=device)
+    perm = torch.empty(T * K, dtype=torch.int32, device=device)
+    moe.moe_route(dims, x, W, ids, tw, counts, offsets, perm, ws)
+    return [int(c) for c in counts.cpu().tolist() if c > 0]
 
-    gate_up reads each touched expert's [2I, H] block and the shared [2Is, H] once, the
-    dispatched x rows once and writes h; down reads each touched [H, I] block and the shared
-    [H, Is] once, reads h and writes Y; the layer adds the router [E+1, H], x and out. The
-    single-kernel few-token path moves the whole layer's bytes."""
-    T, H, E, K, I, Is = dims
+
+def algorithmic(dims, groups: list[int]) -> dict:
+    """Bytes each kernel must move at least (the method's bytes), and the layer's flops, for
+    one call; `impl_*` adds what this implementation stages on top.
+
+    Method bytes: gate_up reads each touched expert's [2I, H] block and the shared [2Is, H]
+    once, x once, and writes h; down reads each touched [H, I] block and the shared [H, Is]
+    once and reads h; the layer adds the router [E+1, H], x and out. Implementation bytes:
+    from 256 tokens gate_up reads the token rows in dispatch order (written by the dispatch
+    scatter) instead of x, and down writes Y (bf16 from 256 tokens, fp32 below) for the
+    fixed-order combine, which reads it back."""
+    T, H, E, K, I, Is = dims[:6]
     P = T * K
     n = len(groups)
-    gate_up = 2 * (n * 2 * I * H + 2 * Is * H) + 2 * (P + T) * H + 2 * (P * I + T * Is)
-    down = 2 * (n * H * I + H * Is) + 2 * (P * I + T * Is) + 4 * (P + T) * H
+    ysz = 2 if T >= 256 else 4
+    h_bytes = 2 * (P * I + T * Is)
+    gate_up = 2 * (n * 2 * I * H + 2 * Is * H) + 2 * T * H + h_bytes
+    down = 2 * (n * H * I + H * Is) + h_bytes
     router = 2 * (E + 1) * H + 2 * T * H
     layer_bytes = 2 * ((E + 1) * H + n * 3 * I * H + 3 * Is * H) + 2 * 2 * T * H
     flops = 2 * T * (E + 1) * H + 2 * P * 3 * I * H + 2 * T * 3 * Is * H
+    impl_gate_up = gate_up + (2 * P * H if T >= 256 else 0)
+    impl_down = down + ysz * (P + T) * H
+    combine = ysz * (P + T) * H + 2 * T * H
     return dict(gate_up=gate_up, down=down, router_scores=router, decode_fused=layer_bytes, layer=layer_bytes,
-                flops=flops)
+                flops=flops, impl_gate_up=impl_gate_up, impl_down=impl_down, impl_combine=combine,
+                impl_decode_fused=layer_bytes)
 
 
 def trace_kernels(moe, names, n):
@@ -302,15 +316,72 @@ def kernel_ms(ev, n) -> dict:
     return {k: sum(a[i].elapsed_time(b[i]) for i in range(n)) / n for k, (a, b) in ev.items()}
 
 
-def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_index=None, auto=(2.0, 200, 100000),
-                   graph: bool = False):
-    """Warm-up (all kernels traced, to find the dominant one), then the timed region (only
-    the dominant kernel traced). With graph=True the timed steps are replays of a CUDA graph
-    that holds G steps, so launch overhead on the host is out of the measurement; the dominant
-    kernel's duration then comes from a second graph of the same steps with its trace events,
-    replayed once after the timed region (event nodes stay out of the timed graph). Returns a
-    result dict."""
+def graph_plan(steps: int, n_layers: int, gmax: int) -> tuple[int, list[int]]:
+    """A CUDA graph of G steps (G divides the requested step count, G <= gmax) and the layer
+    each of its steps runs. Consecutive steps never run the same layer, also across the
+    boundary between two replays (then the last step takes the next layer instead)."""
+    G = max(d for d in range(1, min(steps, gmax) + 1) if steps % d == 0)
+    layers = [i % n_layers for i in range(G)]
+    if n_layers > 2 and G > 1 and layers[-1] == layers[0]:
+        layers[-1] = (layers[-1] + 1) % n_layers
+    return G, layers
+
+
+def percentile(v: list[float], q: float) -> float:
+    s = sorted(v)
+    if len(s) == 1:
+        return s[0]
+    x = q * (len(s) - 1)
+    i = int(math.floor(x))
+    j = min(i + 1, len(s) - 1)
+    return s[i] + (s[j] - s[i]) * (x - i)
+
+
+def timed_regions(run_region, min_total_s: float, min_repeats: int, sampler=None) -> list[float]:
+    """Repeat one timed region (exactly the requested steps) until about min_total_s of timed
+    work, each repeat between CUDA events on the launching stream, with a barrier and a
+    synchronize on both sides of the whole timed span; milliseconds of each repeat (max over
+    ranks)."""
+    # one untimed region sizes the repeat count
+    t0 = time.perf_counter()
+    run_region()
+    torch.cuda.synchronize()
+    one = max(time.perf_counter() - t0, 1e-6)
+    reps = int(min(100000, max(min_repeats, math.ceil(min_total_s / one))))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(True)
+    ev[0].record()
+    for r in range(reps):
+        run_region()
+        ev[r + 1].record()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(False)
+    barrier()
+    return [max_over_ranks(ev[r].elapsed_time(ev[r + 1])) for r in range(reps)]
+
+
+def spread(ms_regions: list[float], steps: int) -> dict:
+    per = [m / steps for m in ms_regions]
+    return {"repeats": len(per), "median_ms_per_step": round(statistics.median(per), 6),
+            "p10_ms_per_step": round(percentile(per, 0.1), 6), "p90_ms_per_step": round(percentile(per, 0.9), 6),
+            "timed_s_total": round(sum(ms_regions) / 1e3, 3)}
+
+
+def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_index=None, min_total_s: float = 1.0,
+                   graph: bool = True, gmax: int = 4096, auto_steps: int = 512):
+    """Warm-up (all kernels traced, to find the dominant one), then the timed region: exactly
+    `steps` steps (a CUDA graph of G steps, G dividing `steps`, replayed steps/G times; plain
+    calls without graph), repeated until about min_total_s of timed work. Reported: the
+    median repeat (tokens/s, ms per step) with p10/p90 over the repeats. The dominant
+    kernel's duration: for one launch per step, the timed repeats over their launches; else
+    per-launch CUDA events from a second graph of the same steps, replayed once after the
+    timed region (no event node inside the timed graph). Returns a result dict."""
     moe = ls.moe
+    nl = len(ls.layers)
     ev = trace_kernels(moe, KERNEL_NAMES, warmup)
     for i in range(warmup):
         ls.step(i)
@@ -318,91 +389,77 @@ def time_layer_set(ls: LayerSet, steps: int, warmup: int, peaks: dict, clocks_in
     warm = kernel_ms(ev, warmup)
     clear_traces(moe)
     dominant = max(warm, key=warm.get)
-    if steps <= 0:  # auto: about `auto[0]` s of timed work
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for i in range(3):
-            ls.step(i)
-        torch.cuda.synchronize()
-        per = (time.perf_counter() - t0) / 3
-        steps = int(min(auto[2], max(auto[1], auto[0] / max(per, 1e-6))))
-    nl = len(ls.layers)
+    if steps <= 0:
+        steps = auto_steps
+    G, order = graph_plan(steps, nl, gmax) if graph else (steps, [i % nl for i in range(steps)])
     if graph:
-        G = max(nl, min(512, steps) // nl * nl)
-        reps = max(1, -(-steps // G))
-        steps = G * reps
-        ev = trace_kernels(moe, [dominant], G)
-        g_trace = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_trace):
-            for i in range(G):
-                ls.step(i)
-        clear_traces(moe)
         g = torch.cuda.CUDAGraph()
         n0 = moe.moe_launch_count()
         with torch.cuda.graph(g):
-            for i in range(G):
-                ls.step(i)
+            for l in order:
+                ls.step(l)
         per_graph = moe.moe_launch_count() - n0
         g.replay()
-        g_trace.replay()
         torch.cuda.synchronize()
-        run = lambda: [g.replay() for _ in range(reps)]  # noqa: E731
-        n_ev = G
+        run = lambda: [g.replay() for _ in range(steps // G)]  # noqa: E731
+        launches_per_region = per_graph * (steps // G)
     else:
-        ev = trace_kernels(moe, [dominant], steps)
-        run = lambda: [ls.step(warmup + i) for i in range(steps)]  # noqa: E731
-        n_ev = steps
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = moe.moe_launch_count()
+        for l in order:
+            ls.step(l)
+        torch.cuda.synchronize()
+        launches_per_region = moe.moe_launch_count() - n0
+        run = lambda: [ls.step(l) for l in order]  # noqa: E731
     sampler = ClockSampler(clocks_index) if clocks_index is not None else None
     if sampler:
         sampler.__enter__()
-    barrier()
-    torch.cuda.synchronize()
-    n0 = moe.moe_launch_count()
-    if sampler:
-        sampler.mark(True)
-    start.record()
-    run()
-    stop.record()
-    torch.cuda.synchronize()
-    launches = per_graph * reps if graph else moe.moe_launch_count() - n0
-    if sampler:
-        sampler.mark(False)
-    barrier()
+    regions = timed_regions(run, min_total_s, 5, sampler)
     if sampler:
         sampler.__exit__(None, None, None)
-    ms = max_over_ranks(start.elapsed_time(stop))
-    if graph and per_graph == G:
-        # one launch per step: the kernel's average duration is the timed region's elapsed
-        # time over its launches (timed-region events, no event nodes between the launches)
+    sp = spread(regions, steps)
+    ms = sp["median_ms_per_step"] * steps  # the median repeat
+    one_launch = launches_per_region == steps
+    if one_launch:
         dom_ms = ms / steps
-        dom_src = "timed-region events / launches"
+        dom_src = "median timed repeat / launches"
     else:
+        ev = trace_kernels(moe, [dominant], G)
         if graph:
+            g_trace = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_trace):
+                for l in order:
+                    ls.step(l)
+            clear_traces(moe)
             g_trace.replay()
             torch.cuda.synchronize()
-        dom_ms = kernel_ms(ev, n_ev)[dominant]
+        else:
+            for l in order[:G]:
+                ls.step(l)
+            torch.cuda.synchronize()
+        dom_ms = kernel_ms(ev, G)[dominant]
         dom_src = "per-launch events"
-    clear_traces(moe)
+        clear_traces(moe)
     groups = ls.routed_groups()
-    first = 0 if graph else warmup
-    per_step = [algorithmic(ls.dims, groups[(first + i) % nl]) for i in range(n_ev)]
-    alg_bytes = sum(p[dominant] if dominant in p else 0 for p in per_step) / n_ev
-    layer_bytes = sum(p["layer"] for p in per_step) / n_ev
+    per_step = [algorithmic(ls.dims, groups[l % nl]) for l in order]
+    alg_bytes = sum(p.get(dominant, 0) for p in per_step) / len(order)
+    impl_bytes = sum(p.get("impl_" + dominant, 0) for p in per_step) / len(order)
+    layer_bytes = sum(p["layer"] for p in per_step) / len(order)
     flops = per_step[0]["flops"]
     T = ls.dims[0]
     # the device error word of the workspace (0: no non-finite score, no timed-out wait)
     dev_err = moe.moe_last_device_error(ls.ws)
-    res = dict(steps=steps, ms_per_step=ms / steps, tokens_per_s=T * steps / (ms / 1e3), launches=launches,
-               device_error=dev_err,
+    res = dict(steps=steps, ms_per_step=ms / steps, tokens_per_s=T * steps / (ms / 1e3),
+               launches=launches_per_region * sp["repeats"], launches_per_step=launches_per_region / steps,
+               spread=sp, device_error=dev_err, graph_steps=G if graph else None,
                dominant=dominant, dominant_ms=dom_ms, dominant_ms_source=dom_src, warm_kernel_ms=warm, graph=graph,
-               unique_experts=sum(len(groups[(first + i) % nl]) for i in range(n_ev)) / n_ev,
+               unique_experts=sum(len(groups[l % nl]) for l in order) / len(order),
                layer_bytes=layer_bytes, layer_flops=flops)
     if alg_bytes:
         ach = alg_bytes / (dom_ms * 1e-3) / 1e9
         res["roofline"] = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1),
                            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
                            "traffic": None, "bytes_per_launch": int(alg_bytes),
+                           "impl_bytes_per_launch": int(impl_bytes),
                            "duration_us": round(dom_ms * 1e3, 3), "duration_source": dom_src,
                            "peak_source": peaks["source"]}
     layer_gbs = layer_bytes / (ms / steps * 1e-3) / 1e9
@@ -598,69 +655,114 @@ def time_e2e(ls: LayerSet, steps: int, warmup: int) -> dict:
 
 
 class StackSet:
-    """The 40-layer stack: x_{l+1} = x_l + MoE_l(RMSNorm(x_l)), one distinct layer each."""
+    """The 40-layer stack: x_{l+1} = x_l + MoE_l(RMSNorm(x_l)), one distinct layer each. The
+    residual stream ping-pongs between two buffers (layer l reads one and writes the other),
+    so a step is only the layers' own launches."""
 
     def __init__(self, wl, device):
         import sparse_moe_ffn_router_gb300 as moe
         self.moe = moe
         self.wl = wl
         self.dims = wl.dims
+        self.device = device
         self.layers = [moe.Weights.from_dict(synth.make_weights(wl.H, wl.E, wl.I, wl.Is, wl.seed, l, None,
                                                                 device=device)) for l in range(wl.layers)]
         self.x0 = synth.make_x(wl.T, wl.H, wl.seed, 0, device=device, tag="x_stack")
-        self.x = torch.empty_like(self.x0)
+        self.buf = [torch.empty_like(self.x0), torch.empty_like(self.x0)]
         self.xn = torch.empty_like(self.x0)
         self.ws = moe.new_workspace(self.dims, device)
+        self._groups = None
 
-    def step(self, i: int):
-        self.x.copy_(self.x0)
-        for W in self.layers:
-            self.moe.moe_rmsnorm(self.dims, self.x, None, RMSNORM_EPS, self.xn)
-            self.moe.moe_forward(self.dims, self.xn, W, self.x, self.x, self.ws)
+    def step(self, i: int = 0, groups: list | None = None):
+        x = self.x0
+        for l, W in enumerate(self.layers):
+            out = self.buf[l % 2]
+            self.moe.moe_rmsnorm(self.dims, x, None, RMSNORM_EPS, self.xn)
+            if groups is not None:
+                groups.append(route_counts(self.moe, self.dims, self.xn, W, self.device))
+            self.moe.moe_forward(self.dims, self.xn, W, x, out, self.ws)
+            x = out
+
+    def routed_groups(self) -> list[list[int]]:
+        """Per layer: rows of each touched expert of one step (all steps route alike)."""
+        if self._groups is None:
+            g = []
+            self.step(0, g)
+            torch.cuda.synchronize()
+            self._groups = g
+        return self._groups
 
 
-def time_stack(ss: StackSet, steps: int, warmup: int) -> dict:
+def time_stack(ss: StackSet, steps: int, warmup: int, peaks: dict, min_total_s: float = 0.5) -> dict:
+    """The stack's step as one CUDA graph (40 x (RMSNorm + layer)), replayed `steps` times per
+    timed repeat; bytes per step: every layer's router, touched experts, shared expert, its
+    input, residual and output rows, and the RMSNorm's read and write."""
+    moe = ss.moe
     for i in range(warmup):
         ss.step(i)
-    barrier()
     torch.cuda.synchronize()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for i in range(steps):
-        ss.step(i)
-    stop.record()
+    g = torch.cuda.CUDAGraph()
+    n0 = moe.moe_launch_count()
+    with torch.cuda.graph(g):
+        ss.step(0)
+    per_step = moe.moe_launch_count() - n0
+    g.replay()
     torch.cuda.synchronize()
-    barrier()
-    ms = max_over_ranks(start.elapsed_time(stop))
-    T = ss.dims[0]
-    return dict(ms_per_step=ms / steps, tokens_per_s=T * steps / (ms / 1e3), layers=len(ss.layers))
+    regions = timed_regions(lambda: [g.replay() for _ in range(steps)], min_total_s, 3)
+    sp = spread(regions, steps)
+    ms = sp["median_ms_per_step"]
+    T, H = ss.dims[:2]
+    groups = ss.routed_groups()
+    nbytes = sum(algorithmic(ss.dims, gr)["layer"] + 2 * T * H + 4 * T * H for gr in groups)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return dict(ms_per_step=ms, tokens_per_s=T / (ms * 1e-3), layers=len(ss.layers), steps=steps, spread=sp,
+                launches_per_step=per_step, device_error=moe.moe_last_device_error(ss.ws),
+                unique_experts_per_layer=round(sum(len(gr) for gr in groups) / len(groups), 2),
+                roofline={"bound": "hbm", "kernel": "whole step (40 layers)", "achieved": round(gbs, 1),
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                          "bytes_per_step": int(nbytes), "peak_source": peaks["source"]})
 
 
 # ---------------------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline and --impl reference)
 
 
-def oracle_steps(wl, steps: int, warmup: int, budget_s=None, device=None) -> dict:
-    """Time the fp64 C oracle on decode-shaped steps of the workload (layer 0 weights)."""
+def oracle_steps(wl, steps: int, warmup: int, budget_s=None, device=None, tokens=None) -> dict:
+    """Time the fp64 C oracle (OpenMP over tokens on the host's threads) on steps of the
+    workload with its layer-0 weights: each step is the whole layer for the first `tokens`
+    tokens of the workload's x (all T by default). For the layer stack one layer stands for
+    each of its layers (all cost the same), so a step takes layers x one layer's time."""
     import oracle
     dev = device if device is not None else "cpu"
     w = synth.make_weights(wl.H, wl.E, wl.I, wl.Is, wl.seed, 0, wl.zipf_s, device=dev)
     hw = {k: (None if v is None else v.cpu()) for k, v in w.items()}
     del w
-    x = synth.make_x(wl.T, wl.H, wl.seed, 0)
+    T = wl.T if tokens is None else max(1, min(tokens, wl.T))
+    x = synth.make_x(wl.T, wl.H, wl.seed, 0)[:T].contiguous()
+    dims = (T,) + tuple(wl.dims[1:])
     for _ in range(warmup):
-        oracle.forward(wl.dims, x, hw)
+        oracle.forward(dims, x, hw)
     if budget_s is not None:
         t0 = time.perf_counter()
-        oracle.forward(wl.dims, x, hw)
+        oracle.forward(dims, x, hw)
         one = time.perf_counter() - t0
         steps = max(1, min(steps, int(budget_s / max(one, 1e-6))))
     t0 = time.perf_counter()
     for _ in range(steps):
-        oracle.forward(wl.dims, x, hw)
+        oracle.forward(dims, x, hw)
     dt = time.perf_counter() - t0
-    cores = min(wl.T, oracle.num_threads())
-    return dict(value=wl.T * steps / dt, steps=steps, seconds=dt, cores=cores)
+    cores = min(T, oracle.num_threads())
+    return dict(value=T * steps / (dt * wl.layers), steps=steps, seconds=dt, cores=cores, tokens=T,
+                host_cores=os.cpu_count())
+
+
+def cpu_baseline(wl, budget_s: float, device, tokens=None) -> dict:
+    r = oracle_steps(wl, 10 ** 6, 1, budget_s=budget_s, device=device, tokens=tokens)
+    what = f"{r['steps']} oracle steps of {r['tokens']} of the workload's {wl.T} token(s), layer-0 weights"
+    if wl.layers > 1:
+        what += f", one layer standing for each of the {wl.layers}"
+    return {"value": round(r["value"], 3), "unit": UNIT, "cores": r["cores"], "host_cores": r["host_cores"],
+            "kind": "oracle", "sample": f"{what}; {r['seconds']:.1f} s of fp64 C oracle work"}
 
 
 def run_reference(args, rank, world):
@@ -675,13 +777,22 @@ def run_reference(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded SplitMix64 + Box-Muller, bf16)",
             "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "E": wl.E, "K": wl.K, "I": wl.I, "Is": wl.Is},
-            "cpu_baseline": {"value": round(r["value"], 3), "unit": UNIT, "cores": r["cores"], "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": round(r["value"], 3), "unit": UNIT, "cores": r["cores"],
+                             "host_cores": r["host_cores"], "kind": "oracle", "sample": sample},
             "e2e": {"value": round(r["value"], 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ---------------------------------------------------------------------------------------
+
+
+def also_entry(r: dict, world: int) -> dict:
+    return {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 5),
+            "steps": r["steps"], "timing": r["spread"], "device_error": r["device_error"],
+            "roofline": r.get("roofline"), "hbm_frac_of_layer_bytes": r["layer_hbm_frac"],
+            "tensor_frac": r["layer_tensor_frac"], "binding_frac": r["layer_binding_frac"],
+            "unique_experts_per_step": r["unique_experts"], "launches_per_step": r["launches_per_step"],
+            "kernel_ms_warmup": {k: round(v, 5) for k, v in r["warm_kernel_ms"].items()}}
 
 
 def main():
@@ -702,10 +813,11 @@ def main():
     n_rot = max(1, args.rotate) if wl.T <= 32 else 1
     ls = LayerSet(wl, n_rot, device)
     main_res = time_layer_set(ls, args.steps, args.warmup, peaks, clocks_index=torch.cuda.current_device(),
-                              graph=not args.no_graph)
+                              graph=not args.no_graph, min_total_s=args.min_seconds)
     if main_res.get("roofline"):
         main_res["roofline"]["traffic"] = ncu_traffic(main_res["roofline"]["kernel"], wl.name)
-    e2e = time_e2e(ls, min(main_res["steps"], 20000), args.warmup)
+    e2e_steps = int(min(50000, max(main_res["steps"], 0.5 / (main_res["ms_per_step"] * 1e-3))))
+    e2e = time_e2e(ls, e2e_steps, args.warmup)
     value = main_res["tokens_per_s"] * world
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": main_res["steps"],
@@ -719,9 +831,11 @@ def main():
                    "inputs larger than L2 (%.2f GB of weights touched per step)" % (main_res["layer_bytes"] / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "cuda_graph": main_res["graph"]},
+        "timing": dict(main_res["spread"], graph_steps=main_res["graph_steps"],
+                       note="value and ms_per_step: the median of the timed repeats, each exactly `steps` steps"),
         "roofline": main_res.get("roofline"),
         "e2e": {"value": round(e2e["value"] * world, 3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
-                "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["ms_per_step"], 6),
+                "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e["ms_per_step"], 6), "steps": e2e_steps,
                 "host_us_per_step": round(e2e["host_us_per_step"], 2)},
         "gpu_launches": main_res["launches"],
         "device_error": main_res["device_error"],
@@ -730,37 +844,40 @@ def main():
                   "hbm_frac_of_layer_bytes": main_res["layer_hbm_frac"],
                   "tensor_frac": main_res["layer_tensor_frac"],
                   "binding_frac": main_res["layer_binding_frac"],
+                  "launches_per_step": main_res["launches_per_step"],
                   "kernel_ms_warmup": {k: round(v, 5) for k, v in main_res["warm_kernel_ms"].items()}},
     }
     del ls
     torch.cuda.empty_cache()
     also = {}
     names = [] if args.also in ("", "none") else [n for n in args.also.split(",") if n]
+    cpu_also = rank == 0 and world == 1 and args.cpu_budget > 0
     for name in names:
         w2 = WORKLOADS[name]
         if w2.layers > 1:
             ss = StackSet(w2, device)
-            r = time_stack(ss, 10 if args.steps <= 0 else max(3, min(args.steps, 10)), 3)
+            r = time_stack(ss, 3, 2, peaks, min_total_s=args.also_seconds)
             also[name] = {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 4),
-                          "layers": r["layers"]}
+                          "steps": r["steps"], "timing": r["spread"], "layers": r["layers"],
+                          "launches_per_step": r["launches_per_step"], "device_error": r["device_error"],
+                          "unique_experts_per_layer": r["unique_experts_per_layer"], "roofline": r["roofline"],
+                          "cuda_graph": True}
             del ss
         else:
             ls2 = LayerSet(w2, ROTATE if w2.T <= 32 else 1, device)
-            r = time_layer_set(ls2, 0 if args.steps <= 0 else max(5, min(args.steps, 50)), 3, peaks,
-                               auto=(1.0, 5, 500), graph=not args.no_graph and w2.T <= 64)
+            r = time_layer_set(ls2, 0, 3, peaks, graph=not args.no_graph, min_total_s=args.also_seconds,
+                               auto_steps=64 if w2.T >= 256 else 512)
             if r.get("roofline"):
                 r["roofline"]["traffic"] = ncu_traffic(r["roofline"]["kernel"], w2.name)
-            stats = time_stats(ls2, peaks)
-            bf16s = time_variant(ls2, ls2.moe.FLAG_BF16_SCORES)
-            also[name] = {"tokens_per_s": round(r["tokens_per_s"] * world, 2), "ms_per_step": round(r["ms_per_step"], 5),
-                          "device_error": r["device_error"],
-                          "roofline": r.get("roofline"), "hbm_frac_of_layer_bytes": r["layer_hbm_frac"],
-                          "tensor_frac": r["layer_tensor_frac"], "binding_frac": r["layer_binding_frac"],
-                          "unique_experts_per_step": r["unique_experts"],
-                          "kernel_ms_warmup": {k: round(v, 5) for k, v in r["warm_kernel_ms"].items()},
-                          "router_stats": stats, "bf16_scores": bf16s}
+            also[name] = also_entry(r, world)
+            if name != "decode_T8":
+                also[name]["router_stats"] = time_stats(ls2, peaks)
+                also[name]["bf16_scores"] = time_variant(ls2, ls2.moe.FLAG_BF16_SCORES)
             del ls2
         torch.cuda.empty_cache()
+        if cpu_also:
+            also[name]["cpu_baseline"] = cpu_baseline(w2, args.cpu_budget / 2, device,
+                                                      tokens=256 if w2.T > 256 else None)
     line["also"] = also
     # routed experts resident in host memory, fetched over the host link per step
     # (with the extra workloads only: the short runs behind the ncu launch lists skip it)
@@ -771,10 +888,7 @@ def main():
             torch.cuda.empty_cache()
     line["host_experts"] = host
     if rank == 0 and world == 1:
-        r = oracle_steps(wl, 10 ** 6, 1, budget_s=args.cpu_budget, device=device)
-        line["cpu_baseline"] = {"value": round(r["value"], 3), "unit": UNIT, "cores": r["cores"], "kind": "oracle",
-                                "sample": f"{r['steps']} steps of {wl.name} ({wl.T} token(s) each, layer-0 weights), "
-                                          f"{r['seconds']:.1f} s of fp64 C oracle work"}
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget, device)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

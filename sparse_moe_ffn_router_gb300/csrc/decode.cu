@@ -1,118 +1,107 @@
-// decode.cu -- the whole MoE layer for a few tokens (T <= 8) in one persistent kernel;
-// moe_forward runs it for a single token (from two tokens on the router and streaming expert
-// kernels, with their larger ring, are faster).
+// decode.cu -- the whole MoE layer for one token (decode) in one persistent kernel.
 //
-// At decode the layer streams ~55 MB of weights per token ("Qwen3.6-35B-A3B -- Architecture
-// Overview", MoE FFN: router 2048 -> 256 plus the shared-expert gate, 8 routed SwiGLU experts
-// with merged gate_up [1024 x 2048] and down [2048 x 512], one always-on shared expert of the
-// same shape), and every step depends on the one before. One CTA per SM runs the whole layer
-// with two grid-wide exchanges:
+// At decode a layer streams ~55 MB of weights per token ("Qwen3.6-35B-A3B -- Architecture
+// Overview", MoE FFN: 256 Experts: router 2048 -> 256 plus the shared-expert gate, 8 routed
+// SwiGLU experts with merged gate_up [1024 x 2048] and down [2048 x 512], one always-on
+// shared expert of the same shape; "One Token Through Qwen3.6", The Router), and only the
+// router and the shared expert (7 MB) are known before the routing. So the kernel's job is
+// to start the routed stream as early as possible and then keep HBM busy until the end.
+// It is built for that layer shape (H = 2048, expert widths 512); other shapes and more
+// tokens take the routing and streaming kernels.
 //
-//   1. router rows: CTA c scores its ceil((E+1)/G) rows of the router (the shared-gate row is
-//      row E) for every token and stores each score as one 64-bit word together with the tag
-//      of this call, so a reader recognises fresh scores by their tag (no flag, no fence);
-//   2. shared gate_up: CTA c's even share of the shared expert's features (no routing needed),
-//      computed while the other CTAs' scores arrive;
-//   3. routing: EVERY CTA reads the T x (E+1) tagged scores and computes top-K, the
-//      renormalised weights, the shared gate and the dispatch (counts, offsets, permutation)
-//      itself. All CTAs derive the same tables, so no second exchange is needed for them;
-//   4. routed gate_up: CTA c's even share of the n_act x I (expert, feature) pairs. Like the
-//      scores, its h values are stored as tagged 64-bit words (two bf16 values and the tag);
-//   5. down + combine: CTA c owns output rows [c*H/G, (c+1)*H/G) of every expert, shared and
-//      routed. The shared expert's block comes right after step 3 (its h values were written in
-//      step 2), the routed blocks stream in behind step 4; the CTA gathers the tagged h rows
-//      into shared memory as soon as they carry this call's tag, multiplies, and sums residual
-//      + gated shared output + weighted slots 0..K-1 of its rows in that fixed order.
+// One CTA per SM (G CTAs). CTA c owns:
+//   - router rows c, c+G, ... (row E is the shared-expert gate);
+//   - shared-expert features [c*Is/G, (c+1)*Is/G) and routed (slot, feature) pairs
+//     [c*F/G, (c+1)*F/G) of the F = K*I: the gate row and the up row of each, giving h;
+//   - output rows [c*H/G, (c+1)*H/G) of the shared and of every routed expert's down
+//     projection, and their fixed-order combine (residual + gated shared + slots 0..K-1).
+// Its work is a fixed sequence of items, one per 8 KB ring slot: router rows, shared
+// features, routed features, then down rows (shared first, then slots 0..K-1, 8 rows per
+// item). One producer lane copies items into the ring with 1-D TMA bulk copies: the token row
+// and the router rows first, then the shared features, and the rest as soon as the routing
+// is known and a slot is free. Consumer warp w takes items w, w+8, ... in order, so the warps
+// never wait for one another; a warp's dot products read the weights from shared memory with
+// x held in registers (one token: an MMA would use one column of eight).
 //
-// Roles: a producer warp streams each stage's rows into a ring of shared-memory stages with 1-D
-// TMA bulk copies (one per row; rows 16 bytes apart modulo 128 so ldmatrix is conflict-free);
-// 8 consumer warps compute (router rows as warp dot products; gate_up and down with warp-level
-// bf16 MMAs, m16n8k16, fp32 accumulate, partial sums added in a fixed order), the routing and
-// the gathers. No exchange needs a flag or a fence: a word is fresh when it carries this
-// call's tag. Every wait is bounded (~1 s): a timeout sets MOE_ERR_TIMEOUT and the kernel still
-// runs to its end with in-range indices. Each CTA counts itself in when it starts; CTA 0 moves
-// the tag on at its end once all are in, so nothing has to be re-armed between calls.
+// Exchanges between CTAs carry a tag of the call instead of a flag: router scores are 64-bit
+// words (tag, fp32 score), h values 32-bit words (16-bit tag, bf16 h). A reader polls the
+// words it needs until all carry this call's tag; every word is rewritten by every call, so
+// a stale word always carries the previous call's tag. A relaxed store alone can take
+// microseconds to reach the other SMs, so the writer of a router score, and each warp after
+// its last routed h value, issues a fence. Warp 0 of every CTA ranks the E scores itself
+// (top-K with ties to the lower index, renormalised weights, the shared gate) right after its
+// own router row; the producer then issues the routed rows. Down items come last and wait
+// only for the h words of their own expert slot.
+//
+// Every wait is bounded (~1 s): a timeout sets MOE_ERR_TIMEOUT in the workspace and the
+// kernel still runs to its end with in-range indices. Each CTA counts itself in when it
+// starts; CTA 0 moves the call's tag on at its end once all are in.
 #include "launch.h"
 #include "ring.cuh"
 
 namespace moe {
 
-constexpr int kDTT = 8;                     // max tokens
-constexpr int kDMaxH = 2048, kDMaxI = 512;  // largest hidden size / expert width
-constexpr int kDMaxP = kDTT * 8;            // max (token, slot) pairs
-constexpr int kDBlk = 4;                    // max down blocks per ring stage
-constexpr int kDThreads = kConsumers + 32;  // 8 consumer warps and the producer
-constexpr int kProducerWarp = kWarps;
-constexpr uint32_t kPollNs = 128;           // longest sleep between two polls
+constexpr int kOWarps = 8;                     // consumer warps
+constexpr int kOThreads = (kOWarps + 1) * 32;  // + the producer warp
+constexpr int kOH = 2048;                      // hidden width (the page's layer shape)
+constexpr int kOI = 512;                       // routed and shared expert widths
+constexpr int kONch = kOH / 256;               // 16-byte chunks of an H-long row per lane
+constexpr int kOIch = kOI / 256;               // 16-byte chunks of an I-long row per lane
+constexpr int kOMaxK = 8;                      // experts per token
+constexpr int kOSlot = 8192;                   // ring slot: one feature's gate and up rows
+constexpr int kOMaxSlots = 28;
+constexpr int kOMaxRo = kOSlot / (kOI * 2);    // down rows per item
+constexpr int kOMaxOut = 16;                   // output rows per CTA
+constexpr int kOProducer = kOWarps;
 
-enum { kStRoute = 0, kStUp = 1, kStTopK = 2, kStDown = 3, kStEnd = 4 };
+enum : int { kOkRouter = 0, kOkSharedUp = 1, kOkSharedDown = 2, kOkUp = 3, kOkDown = 4 };
 
-// What one ring stage holds (written by the producer before the stage's barrier completes).
-struct DMeta {
-    int type;
-    int n;           // route: rows; up: features; down: blocks
-    int row0;        // route: first router row; up: first h row
-    int f0;          // up: first feature
-    int mt;          // up: tokens
-    uint32_t toks;   // up: token of each of its mt h rows, 4 bits each
-    int blk[kDBlk];  // down: expert slot of each block (0: shared expert, j >= 1: act[j - 1]);
-                     // a stage holds the shared block alone or routed blocks only
+// What one ring slot holds (written by the producer before the slot's copies).
+struct OMeta {
+    int kind;
+    int k;  // expert slot 0..K-1, or K for the shared expert
+    int a;  // router row / feature / first output row
+    int n;  // rows (down items)
 };
 
-// Shared-memory geometry of one launch, fixed on the host.
-struct DGeom {
-    int sf;     // features per gate_up stage (8 or 4); a stage holds 2 * sf rows of H
-    int nst;    // ring stages
-    int xp;     // pitch of x rows and H-long weight rows (2H + 16 bytes)
-    int dp;     // pitch of h rows and down rows (2 Imax + 16 bytes)
-    int rr;     // router rows per CTA
-    int ro;     // output rows per CTA (at most)
-    int nbs;    // down blocks per ring stage (1, 2 or 4); a block holds ro rows
-    int stage;  // stage bytes
-    int o_xs, o_hs, o_ys, o_red, o_st, o_meta, o_bar, smem;
+// The routing of the token as every CTA derives it, and the routed experts' weight blocks.
+struct ORoute {
+    const bf16* gu[kOMaxK];
+    const bf16* dn[kOMaxK];
+    int ids[kOMaxK];
+    float w[kOMaxK];
+    int inv[kOMaxK];
+    float sg;
 };
 
-// Routing tables, identical in every CTA.
-struct DRoute {
-    int sid[kDMaxP];    // expert of pair p = t*K + k
-    float sw[kDMaxP];   // renormalised weight of pair p
-    int less[kDMaxP];   // pairs whose expert is lower than pair p's
-    int rank[kDMaxP];   // earlier pairs with pair p's expert
-    int pcnt[kDMaxP];   // pairs with pair p's expert
-    int perm[kDMaxP];   // pair at each dispatch position
-    int inv[kDMaxP];    // dispatch position of each pair
-    int act[kDMaxP];    // used experts, ascending
-    int aoff[kDMaxP];   // first dispatch position of act[j]
-    int acnt[kDMaxP];   // pairs of act[j]
-    float sgate[kDTT];
-    int n_act;
+// Per-CTA share of the work; identical in every thread (32-bit arithmetic only).
+struct OPlan {
+    int nr;        // router rows: c, c + G, ...
+    int fs0, nsf;  // shared features
+    int o0, ro;    // output rows
+    int dpk;       // down items per expert (kOMaxRo rows each)
+    int f0, nf;    // routed (slot, feature) pairs
+    int n;         // items
 };
 
-inline int round_up128(int b) { return (b + 127) & ~127; }
+struct OGeom {
+    int nslot;
+    int o_x, o_slot, o_meta, o_bar, o_ys, o_rt, smem;
+};
 
-// Geometry for sf features per stage and nst stages; false if the layer does not fit it.
-inline bool decode_geom(const LayerArgs& a, int G, int sf, int nst, DGeom* g) {
-    g->sf = sf;
-    g->nst = nst;
-    g->xp = 2 * a.H + 16;
-    g->dp = 2 * a.Imax + 16;
-    g->rr = (a.E + 1 + G - 1) / G;
-    g->ro = (a.H + G - 1) / G;
-    g->stage = 2 * sf * g->xp;
-    const int nb = g->stage / (g->ro * g->dp);
-    g->nbs = nb >= 4 ? 4 : nb >= 2 ? 2 : nb;
-    if (g->rr > 2 * sf || g->ro > 16 || g->nbs < 1 || (a.I | a.Is) & 1) return false;
-    const int P = a.T * a.K;
-    int o = 0;
-    g->o_xs = o; o += round_up128(a.T * g->xp);
-    g->o_hs = o; o += round_up128((P + a.T) * g->dp);
-    g->o_ys = o; o += round_up128((P + a.T) * 16 * 4);
-    g->o_red = o; o += 2 * kWarps * 32 * 16;
-    g->o_st = o; o += nst * g->stage;
-    g->o_meta = o; o += round_up128(nst * (int)sizeof(DMeta));
-    g->o_bar = o; o += round_up128((2 * nst + 2) * 8);
-    g->smem = o + 128;  // room to align the dynamic base to 128 bytes
-    return true;
+__device__ __forceinline__ OPlan oplan(const LayerArgs& a, int c, int G) {
+    OPlan p;
+    p.nr = c < a.E + 1 ? (a.E + 1 - c + G - 1) / G : 0;
+    p.fs0 = c * kOI / G;
+    p.nsf = (c + 1) * kOI / G - p.fs0;
+    p.o0 = c * kOH / G;
+    p.ro = (c + 1) * kOH / G - p.o0;
+    const int F = a.K * kOI;
+    p.f0 = c * F / G;
+    p.nf = (c + 1) * F / G - p.f0;
+    p.dpk = (p.ro + kOMaxRo - 1) / kOMaxRo;
+    p.n = p.nr + p.nsf + p.nf + (a.K + 1) * p.dpk;
+    return p;
 }
 
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
@@ -123,23 +112,26 @@ __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
-
-// Poll until *p - base >= n (unsigned, acquire), sleeping up to kPollNs between polls; false
-// after ~1 s.
-__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t base, uint32_t n) {
-    if (ld_acquire(p) - base >= n) return true;
-    const uint64_t t0 = global_ns();
-    uint32_t ns = 32;
-    for (;;) {
-        __nanosleep(ns);
-        if (ld_acquire(p) - base >= n) return true;
-        if (ns < kPollNs) ns <<= 1;
-        if (global_ns() - t0 > 1000000000ull) return false;
-    }
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4(const uint32_t* p) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+// 16 bytes from shared memory at a shared-window address (an explicit shared load; a generic
+// load through a pointer into dynamic shared memory is several times slower here).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
 }
 
-// Lane 0 waits for a barrier phase (bounded); the warp shares the outcome and, through the
-// warp barrier, the visibility of what completed the phase.
+// Lane 0 waits for a barrier phase (bounded); the warp shares the verdict.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane) {
     bool ok = lane == 0 ? mbar_wait(bar, parity) : true;
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -147,59 +139,81 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int la
     return ok;
 }
 
-// Barrier of the consumer warps that also counts the threads whose predicate is true.
-__device__ __forceinline__ int consumers_count(bool p) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.popc.u32 %0, 1, %2, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)p), "n"(kConsumers)
-        : "memory");
-    return (int)r;
+// Poll until *p - base >= n (unsigned, acquire); false after ~1 s.
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t base, uint32_t n) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (ld_acquire(p) - base >= n) return true;
+        if (global_ns() - t0 > 1000000000ull) return false;
+        __nanosleep(64);
+    }
 }
 
-// D[16 x 8] += A[16 x 16 ksteps] B for this lane's A row (a_row: byte address of the row the
-// lane feeds to ldmatrix, i.e. tile row lane % 16) and B row (token row of lane % 8), K range
-// starting at element k0. Even and odd K steps go to two accumulators (two short dependency
-// chains), added at the end.
-__device__ __forceinline__ void mma_rows(float (&d)[4], uint32_t a_row, uint32_t b_row, int k0, int ksteps, int lane) {
-    const uint32_t a = a_row + (uint32_t)((k0 + 8 * (lane >> 4)) * 2);
-    const uint32_t b = b_row + (uint32_t)((k0 + 8 * ((lane >> 3) & 1)) * 2);
-    float e[4] = {0.f, 0.f, 0.f, 0.f};
-    int k = 0;
-#pragma unroll 2
-    for (; k + 1 < ksteps; k += 2) {
-        uint32_t a0, a1, a2, a3, b0, b1, c0, c1, c2, c3, f0, f1;
-        ldsm_x4(a + k * 32, a0, a1, a2, a3);
-        ldsm_x2(b + k * 32, b0, b1);
-        ldsm_x4(a + k * 32 + 32, c0, c1, c2, c3);
-        ldsm_x2(b + k * 32 + 32, f0, f1);
-        mma16816(d, a0, a1, a2, a3, b0, b1);
-        mma16816(e, c0, c1, c2, c3, f0, f1);
-    }
-    if (k < ksteps) {
-        uint32_t a0, a1, a2, a3, b0, b1;
-        ldsm_x4(a + k * 32, a0, a1, a2, a3);
-        ldsm_x2(b + k * 32, b0, b1);
-        mma16816(d, a0, a1, a2, a3, b0, b1);
+// Dot products of x (this lane's chunks in registers) with R H-long bf16 rows in shared
+// memory; lane l takes the 16-byte chunks l, l+32, ... into two partial sums per row (short
+// dependency chains), added in a fixed order, then the warp sums in a fixed order.
+template <int R>
+__device__ __forceinline__ void dot_rows(const uint32_t (&rows)[R], const float (&xr)[kONch][8], int lane,
+                                         float (&out)[R]) {
+    float acc[R][2];
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r][0] = acc[r][1] = 0.f;
+    // loads run two chunks ahead of the multiplies (shared-memory loads wait behind the ring's
+    // incoming copies)
+    uint4 w[3][R];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int r = 0; r < R; ++r) w[q][r] = lds128(rows[r] + 16u * (lane + 32 * q));
+#pragma unroll
+    for (int q = 0; q < kONch; ++q) {
+        if (q + 2 < kONch)
+#pragma unroll
+            for (int r = 0; r < R; ++r) w[(q + 2) % 3][r] = lds128(rows[r] + 16u * (lane + 32 * (q + 2)));
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[r][q & 1] = dot8(w[q % 3][r], xr[q], acc[r][q & 1]);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] += e[i];
+    for (int r = 0; r < R; ++r) out[r] = warp_sum(acc[r][0] + acc[r][1]);
 }
 
-// ---------------------------------------------------------------------------------------
-// Routing ("Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: softmax over the 256 router
-// scores, the 8 highest kept and renormalised; ties go to the lower expert index).
+// The h values of expert slot k that this lane multiplies (chunks lane, lane+32, ... of the
+// inner width: 8 values each), polled from their tagged words until all carry `tag16`. False
+// after ~1 s (the values are then taken as they are).
+__device__ bool poll_h(const uint32_t* words, uint32_t tag16, float (&hv)[kOIch][8], int lane) {
+    uint32_t need = (1u << kOIch) - 1u;
+    const uint64_t t0 = global_ns();
+    bool ok = true;
+    for (;;) {
+        const bool give_up = !ok;
+#pragma unroll
+        for (int q = 0; q < kOIch; ++q)
+            if ((need >> q) & 1u) {
+                const uint32_t* p = words + 8 * (lane + 32 * q);
+                const uint4 v0 = ld_relaxed_v4(p), v1 = ld_relaxed_v4(p + 4);
+                const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                bool fresh = true;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) fresh &= (w[i] >> 16) == tag16;
+                if (fresh || give_up) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) hv[q][i] = __uint_as_float(w[i] << 16);
+                    need &= ~(1u << q);
+                }
+            }
+        if (!__any_sync(0xffffffffu, need != 0)) return ok;
+        if (global_ns() - t0 > 1000000000ull) ok = false;
+        __nanosleep(32);
+    }
+}
 
-// Top-K of token t by one warp. Lane l polls the tagged scores of experts l, l+32, ... (lane 0
-// also the shared-gate score) until all carry this call's tag; each of K rounds then takes the
-// largest remaining key (warp max) and, among equal keys, the lowest expert index (warp min).
-// The weights are the softmax over the kept scores, which equals the full softmax renormalised
-// over them; lane k holds slot k.
-__device__ void route_token(const LayerArgs& a, DRoute& rt, int t, int lane, uint32_t tag) {
-    const uint64_t* l = a.dlog + (size_t)t * (a.E + 1);
+// Top-K of the token by warp 0 from the E + 1 tagged scores (expert scores, then the shared
+// gate): lane l polls experts l, l+32, ... (lane 0 also the gate) until all carry this call's
+// tag; each of K rounds takes the largest remaining key and, among equal keys, the lowest
+// expert ("Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256 Experts, Router). The
+// weights are the softmax over the kept scores (the full softmax renormalised over them).
+__device__ void route_one(const LayerArgs& a, ORoute& rt, uint32_t tag, int lane) {
+    const uint64_t* l = a.dlog;
     uint32_t val[9];
     uint32_t need = 0;
 #pragma unroll
@@ -211,7 +225,6 @@ __device__ void route_token(const LayerArgs& a, DRoute& rt, int t, int lane, uin
     const uint64_t t0 = global_ns();
     bool timed_out = false;
     for (;;) {
-        // all pending words are requested before any is examined (one round trip per poll)
         uint64_t w[9];
 #pragma unroll
         for (int j = 0; j < 9; ++j) w[j] = ((need >> j) & 1u) ? ld_relaxed_u64(l + (j < 8 ? lane + 32 * j : a.E)) : 0ull;
@@ -228,7 +241,7 @@ __device__ void route_token(const LayerArgs& a, DRoute& rt, int t, int lane, uin
             timed_out = true;
             break;
         }
-        __nanosleep(64);
+        __nanosleep(32);
     }
     bool bad = false;
     uint32_t key[8];
@@ -249,503 +262,275 @@ __device__ void route_token(const LayerArgs& a, DRoute& rt, int t, int lane, uin
     warp_topk(key, a.K, lane, v0, myv, mye);
     const float ex = lane < a.K ? expf(myv - v0) : 0.f;
     const float s = warp_sum(ex);
+    // dispatch position of slot `lane`: the slots whose expert is lower (the K experts differ)
+    int pos = 0;
+    for (int j = 0; j < a.K; ++j) pos += __shfl_sync(0xffffffffu, mye, j) < mye;
     if (lane < a.K) {
-        rt.sid[t * a.K + lane] = mye;
-        rt.sw[t * a.K + lane] = ex / s;
+        rt.ids[lane] = mye;
+        rt.w[lane] = ex / s;
+        rt.inv[lane] = pos;
+        rt.gu[lane] = a.gate_up + (size_t)mye * 2 * kOI * kOH;
+        rt.dn[lane] = a.down + (size_t)mye * kOH * kOI;
     }
     if (lane == 0) {
         const float z = router_score(__uint_as_float(val[8]), a.flags);
         if (!isfinite(z)) bad = true;
-        rt.sgate[t] = 1.0f / (1.0f + expf(-z));
+        rt.sg = 1.0f / (1.0f + expf(-z));
         if (timed_out) atomicOr(&a.hdr->err, ERR_TIMEOUT);
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&a.hdr->err, ERR_NONFINITE_SCORE);
+    __syncwarp();
 }
 
-// Dispatch of the P pairs by the consumer threads (thread p takes pair p): a stable counting
-// sort by expert -- pair p goes to position #{pairs with a lower expert} + #{earlier pairs with
-// its expert} -- and the ascending list of used experts with their first position and count.
-// Starts and ends with a barrier of the consumers.
-__device__ void route_dispatch(DRoute& rt, int P, int tid) {
-    if (tid < P) {
-        const int e = rt.sid[tid];
-        int less = 0, cnt = 0, rank = 0;
-        for (int q = 0; q < P; ++q) {
-            const int eq = rt.sid[q];
-            less += eq < e;
-            cnt += eq == e;
-            rank += (eq == e) & (q < tid);
-        }
-        rt.less[tid] = less;
-        rt.rank[tid] = rank;
-        rt.pcnt[tid] = cnt;
+// The routing results of the call in the workspace (ids, weights, counts, offsets, dispatch
+// permutation, used experts, shared gate), written by warp 0 of CTA 0.
+__device__ void write_routing(const LayerArgs& a, const ORoute& rt, int lane) {
+    const int K = a.K;
+    if (lane < K) {
+        a.ids[lane] = rt.ids[lane];
+        a.topw[lane] = rt.w[lane];
+        a.perm[rt.inv[lane]] = lane;
+        a.inv[lane] = rt.inv[lane];
+        a.act[rt.inv[lane]] = rt.ids[lane];
     }
-    consumers_count(false);  // barrier: pass 1 complete
-    int first = 0;
-    if (tid < P) {
-        const int e = rt.sid[tid], pos = rt.less[tid] + rt.rank[tid];
-        rt.perm[pos] = tid;
-        rt.inv[tid] = pos;
-        if (rt.rank[tid] == 0) {
-            first = 1;
-            int j = 0;
-            for (int q = 0; q < P; ++q) j += (rt.rank[q] == 0) & (rt.sid[q] < e);
-            rt.act[j] = e;
-            rt.aoff[j] = rt.less[tid];
-            rt.acnt[j] = rt.pcnt[tid];
+    for (int e = lane; e <= a.E; e += 32) {
+        int less = 0, cnt = 0;
+        for (int j = 0; j < K; ++j) {
+            less += rt.ids[j] < e;
+            cnt += rt.ids[j] == e;
         }
+        a.offsets[e] = less;
+        if (e < a.E) a.counts[e] = cnt;
     }
-    const int na = consumers_count(first != 0);  // barrier: tables complete
-    if (tid == 0) rt.n_act = na;
-    consumers_sync();
+    if (lane == 0) {
+        a.sgate[0] = rt.sg;
+        a.hdr->n_act = K;
+    }
 }
 
-// Even split of n items over G CTAs, boundaries rounded down to even (h values travel in pairs).
-__device__ __forceinline__ int even_split(int n, int c, int G) { return (int)((long long)c * n / G) & ~1; }
-
-// Copies h rows r0 .. r0+nr-1 (features 0 .. inner-1) of this call from their tagged words into
-// shared memory (pitch dp), each consumer thread polling its words until they carry `tag`.
-// False after ~1 s; the words not yet fresh are then copied as they are.
-__device__ bool gather_h(const LayerArgs& a, uint8_t* hs, int dp, int r0, int nr, int inner, uint32_t tag, int tid) {
-    constexpr int kB = 16;  // words in flight per thread
-    const int wpr = inner / 2, ldw = a.Imax / 2, n = nr * wpr;
-    const uint64_t t0 = global_ns();
-    bool ok = true;
-    for (int base = 0; base < n; base += kConsumers * kB) {
-        uint32_t need = 0;
-#pragma unroll
-        for (int q = 0; q < kB; ++q)
-            if (base + q * kConsumers + tid < n) need |= 1u << q;
-        while (need) {
-            uint64_t w[kB];
-#pragma unroll
-            for (int q = 0; q < kB; ++q) {
-                const int idx = base + q * kConsumers + tid, r = idx / wpr;
-                w[q] = ((need >> q) & 1u) ? ld_relaxed_u64(a.dh + (size_t)(r0 + r) * ldw + (idx - r * wpr)) : 0ull;
-            }
-            const bool give_up = !ok || global_ns() - t0 > 1000000000ull;
-            uint32_t still = need;
-#pragma unroll
-            for (int q = 0; q < kB; ++q)
-                if (((need >> q) & 1u) && ((uint32_t)(w[q] >> 32) == tag || give_up)) {
-                    const int idx = base + q * kConsumers + tid, r = idx / wpr;
-                    *reinterpret_cast<uint32_t*>(hs + (size_t)(r0 + r) * dp + (idx - r * wpr) * 4) = (uint32_t)w[q];
-                    still &= ~(1u << q);
-                }
-            if (give_up) ok = false;
-            need = still;
-            if (need) __nanosleep(64);
-        }
-    }
-    return ok;
-}
-
-// ---------------------------------------------------------------------------------------
-
-__global__ void __launch_bounds__(kDThreads, 1) k_decode_fused(LayerArgs a, DGeom g) {
+__global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeom g) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ DRoute rt;
     const uint32_t raw = smem_u32(smem_raw);
-    uint8_t* base = smem_raw + (((raw + 127u) & ~127u) - raw);
-    uint8_t* xs = base + g.o_xs;
-    uint8_t* hs = base + g.o_hs;
-    float* Ys = reinterpret_cast<float*>(base + g.o_ys);  // [P + T][16] unscaled down outputs
-    float* red = reinterpret_cast<float*>(base + g.o_red);
-    uint8_t* stg = base + g.o_st;
-    DMeta* meta = reinterpret_cast<DMeta*>(base + g.o_meta);
+    uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* xs = base + g.o_x;
+    uint8_t* slots = base + g.o_slot;
+    OMeta* meta = reinterpret_cast<OMeta*>(base + g.o_meta);
     uint64_t* full = reinterpret_cast<uint64_t*>(base + g.o_bar);
-    uint64_t* empty = full + g.nst;
-    uint64_t* xbar = empty + g.nst;
+    uint64_t* empty = full + kOMaxSlots;
+    uint64_t* xbar = empty + kOMaxSlots;
     uint64_t* routed = xbar + 1;
+    float* ys = reinterpret_cast<float*>(base + g.o_ys);  // [K + 1][kOMaxOut] down outputs, unscaled
+    ORoute& rt = *reinterpret_cast<ORoute*>(base + g.o_rt);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
-    const int T = a.T, H = a.H, E = a.E, K = a.K, P = T * K;
+    const int K = a.K, nslot = g.nslot;
     uint32_t* err = &a.hdr->err;
-    // this call's tag and the CTA starts of earlier calls (both advanced by CTA 0 of the
-    // previous call)
-    const uint32_t epoch = *(volatile uint32_t*)&a.hdr->dec_epoch;
-    const uint32_t tag = epoch + 1u;
-    const uint32_t sbase = *(volatile uint32_t*)&a.hdr->dec_start_base;
-    const int o0 = c * H / G, ro = (c + 1) * H / G - o0;  // this CTA's output rows
+    const OPlan p = oplan(a, c, G);
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < g.nst; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kWarps);
+    // ---- producer lane: barriers, then the token row and the router rows before anything else
+    int ps = 0;          // producer's slot cursor
+    uint32_t pround = 0;
+    auto issue = [&](int kind, int k, int a_, int n, const void* src0, uint32_t b0, const void* src1, uint32_t b1) {
+        meta[ps] = OMeta{kind, k, a_, n};
+        uint8_t* dst = slots + (size_t)ps * kOSlot;
+        mbar_arrive_expect_tx(&full[ps], b0 + b1);
+        bulk_load(dst, src0, b0, &full[ps]);
+        if (b1) bulk_load(dst + b0, src1, b1, &full[ps]);
+        if (++ps == nslot) {
+            ps = 0;
+            ++pround;
+        }
+    };
+    // the next slot, once the consumers have released it (false after ~1 s)
+    auto slot_free = [&]() { return pround == 0 || mbar_wait(&empty[ps], (pround - 1u) & 1u); };
+    bool pok = true;
+    if (warp == kOProducer && lane == 0) {
+        for (int i = 0; i < nslot; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
         }
         mbar_init(xbar, 1);
         mbar_init(routed, 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(xbar, (uint32_t)(kOH * 2));
+        bulk_load(xs, a.x, (uint32_t)(kOH * 2), xbar);
+        for (int j = 0; j < p.nr && pok; ++j) {
+            const int row = c + j * G;
+            pok = slot_free();
+            if (pok) issue(kOkRouter, K, row, 1, row < a.E ? a.router_w + (size_t)row * kOH : a.sg, kOH * 2, nullptr, 0);
+        }
+        // the shared expert's features: no routing needed
+        for (int f = p.fs0; f < p.fs0 + p.nsf && pok; ++f) {
+            pok = slot_free();
+            if (pok) issue(kOkSharedUp, K, f, 1, a.sgu + (size_t)f * kOH, kOH * 2, a.sgu + (size_t)(kOI + f) * kOH, kOH * 2);
+        }
     }
-    __syncthreads();  // also orders every thread's reads of the tag before the count below
+    // this call's tags and the CTA starts of earlier calls (both advanced by CTA 0 of the
+    // previous call)
+    const uint32_t epoch = *(volatile uint32_t*)&a.hdr->dec_epoch;
+    const uint32_t sbase = *(volatile uint32_t*)&a.hdr->dec_start_base;
+    __syncthreads();  // barriers initialised; every thread has read the tags before the count below
     if (threadIdx.x == 0) red_release_add(&a.hdr->dec_start, 1u);
+    const uint32_t tag = epoch + 1u;
+    const uint32_t tag16 = (tag - 1u) % 65535u + 1u;
+    uint32_t* hw = reinterpret_cast<uint32_t*>(a.dh);  // [K + 1][I] tagged h words
 
-    if (warp == kProducerWarp) {
-        // ================= producer: fills the stages in the order the consumers take them
-        if (lane == 0) mbar_arrive_expect_tx(xbar, (uint32_t)(T * H * 2));
-        __syncwarp();
-        if (lane < T) bulk_load(xs + (size_t)lane * g.xp, a.x + (size_t)lane * H, H * 2, xbar);
-        int it = 0;
-        bool ok = true;
-        auto claim = [&]() -> int {  // next stage, once the consumers have released it
-            const int s = it % g.nst;
-            if (!warp_wait(&empty[s], (((uint32_t)(it / g.nst)) & 1u) ^ 1u, lane)) ok = false;
-            return s;
-        };
-        auto post = [&](int type) {  // a stage without copies
-            const int s = claim();
-            if (!ok) return;
-            if (lane == 0) {
-                meta[s].type = type;
-                mbar_arrive(&full[s]);
-            }
-            __syncwarp();
-            ++it;
-        };
-        // gate rows f0.. to stage rows 0.., up rows (inner + f0).. to stage rows sf..
-        auto issue_up = [&](const bf16* W, int inner, int f0, int n, int row0, int mt, uint32_t toks) {
-            const int s = claim();
-            if (!ok) return;
-            uint8_t* st = stg + (size_t)s * g.stage;
-            if (lane == 0) {
-                DMeta& m = meta[s];
-                m.type = kStUp;
-                m.n = n;
-                m.row0 = row0;
-                m.f0 = f0;
-                m.mt = mt;
-                m.toks = toks;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * n * H * 2));
-            }
-            __syncwarp();
-            if (lane < n)
-                bulk_load(st + (size_t)lane * g.xp, W + (size_t)(f0 + lane) * H, H * 2, &full[s]);
-            else if (lane >= 16 && lane < 16 + n)
-                bulk_load(st + (size_t)(g.sf + lane - 16) * g.xp, W + (size_t)(inner + f0 + lane - 16) * H, H * 2,
-                          &full[s]);
-            ++it;
-        };
-
-        // 1. router rows (row E is the shared-expert gate)
-        const int r0 = c * g.rr, nrr = max(0, min(E + 1, r0 + g.rr) - r0);
-        if (nrr > 0) {
-            const int s = claim();
-            if (ok) {
-                uint8_t* st = stg + (size_t)s * g.stage;
-                if (lane == 0) {
-                    meta[s].type = kStRoute;
-                    meta[s].n = nrr;
-                    meta[s].row0 = r0;
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nrr * H * 2));
-                }
-                __syncwarp();
-                if (lane < nrr) {
-                    const int row = r0 + lane;
-                    bulk_load(st + (size_t)lane * g.xp, row < E ? a.router_w + (size_t)row * H : a.sg, H * 2,
-                              &full[s]);
-                }
-                ++it;
-            }
-        }
-        // down rows o0..o0+ro-1 of block j0.. (nb blocks) into the next stage
-        auto issue_down = [&](int j0, int nb) {
-            const int s = claim();
-            if (!ok) return;
-            uint8_t* st = stg + (size_t)s * g.stage;
-            if (lane == 0) {
-                uint32_t bytes = 0;
-                DMeta& m = meta[s];
-                m.type = kStDown;
-                m.n = nb;
-                for (int b = 0; b < nb; ++b) {
-                    m.blk[b] = j0 + b;
-                    bytes += (uint32_t)(ro * (j0 + b == 0 ? a.Is : a.I) * 2);
-                }
-                mbar_arrive_expect_tx(&full[s], bytes);
-            }
-            __syncwarp();
-            for (int idx = lane; idx < nb * ro; idx += 32) {
-                const int b = idx / ro, r = idx - b * ro, j = j0 + b;
-                const int inner = j == 0 ? a.Is : a.I;
-                const bf16* W = j == 0 ? a.sd : a.down + (size_t)rt.act[j - 1] * H * a.I;
-                bulk_load(st + (size_t)(b * g.ro + r) * g.dp, W + (size_t)(o0 + r) * inner, inner * 2, &full[s]);
-            }
-            ++it;
-        };
-        // 2. shared gate_up: features [c*Is/G, (c+1)*Is/G), all tokens, h rows P..P+T-1
-        //    (computed while the other CTAs' scores arrive)
-        const int fs0 = even_split(a.Is, c, G), fs1 = even_split(a.Is, c + 1, G);
-        for (int f = fs0; f < fs1 && ok; f += g.sf)
-            issue_up(a.sgu, a.Is, f, min(g.sf, fs1 - f), P, T, 0x76543210u);
-        // 3. the consumers compute the routing and hand the tables over through `routed`; the
-        //    shared expert's down rows (output rows o0..o0+ro-1, slot 0) stream in meanwhile and
-        //    are multiplied while the first routed weights are in flight
-        if (ok) post(kStTopK);
-        if (ok && ro > 0) issue_down(0, 1);
-        if (ok && !warp_wait(routed, 0, lane)) ok = false;
-        // 4. routed gate_up: (expert, feature) pairs [c*F/G, (c+1)*F/G) of the F = n_act * I
-        const int n_act = ok ? rt.n_act : 0;
-        const int F = n_act * a.I;
-        const int g1 = even_split(F, c + 1, G);
-        for (int gi = even_split(F, c, G); gi < g1 && ok;) {
-            const int j = gi / a.I, f = gi - j * a.I;
-            const int n = min(g.sf, min(g1 - gi, a.I - f));
-            const int e = rt.act[j];
-            const int row0 = rt.aoff[j], mt = rt.acnt[j];
-            uint32_t toks = 0;
-            for (int q = 0; q < mt; ++q) toks |= (uint32_t)(rt.perm[row0 + q] / K) << (4 * q);
-            issue_up(a.gate_up + (size_t)e * 2 * a.I * H, a.I, f, n, row0, mt, toks);
-            gi += n;
-        }
-        // 5. down rows o0..o0+ro-1 of each used expert (slots 1..n_act)
-        for (int j0 = 1; ro > 0 && j0 <= n_act && ok; j0 += g.nbs) issue_down(j0, min(g.nbs, n_act + 1 - j0));
-        if (!ok && lane == 0) atomicOr(err, ERR_TIMEOUT);
-        // every copy issued must land before the CTA can exit
+    if (warp == kOProducer) {
+        // ================= producer lane: the routed items once the routing is known
         if (lane == 0) {
-            for (int k = 0; k < g.nst && it - 1 - k >= 0; ++k) {
-                const int j = it - 1 - k;
-                if (!mbar_wait(&full[j % g.nst], ((uint32_t)(j / g.nst)) & 1u)) atomicOr(err, ERR_TIMEOUT);
+            if (pok && !mbar_wait(routed, 0)) pok = false;
+            // routed (slot, feature) pairs [f0, f0 + nf): slot k = pair / I
+            for (int fi = p.f0; fi < p.f0 + p.nf && pok; ++fi) {
+                pok = slot_free();
+                if (!pok) break;
+                const int k = fi / kOI, f = fi - k * kOI;
+                const bf16* W = rt.gu[k];
+                issue(kOkUp, k, f, 1, W + (size_t)f * kOH, kOH * 2, W + (size_t)(kOI + f) * kOH, kOH * 2);
             }
+            // down rows [o0, o0 + ro) in runs of kOMaxRo: the shared expert's, then each routed slot's
+            for (int kk = 0; kk <= K && pok; ++kk)
+                for (int r0 = p.o0; r0 < p.o0 + p.ro && pok; r0 += kOMaxRo) {
+                    const int n = min(kOMaxRo, p.o0 + p.ro - r0);
+                    pok = slot_free();
+                    if (!pok) break;
+                    const bf16* W = kk == 0 ? a.sd : rt.dn[kk - 1];
+                    issue(kk == 0 ? kOkSharedDown : kOkDown, kk == 0 ? K : kk - 1, r0, n, W + (size_t)r0 * kOI,
+                          (uint32_t)(n * kOI * 2), nullptr, 0);
+                }
+            if (!pok) atomicOr(err, ERR_TIMEOUT);
+            // every copy issued must land before the CTA can exit
+            const int issued = (int)pround * nslot + ps;
+            for (int j = max(0, issued - nslot); j < issued; ++j)
+                if (!mbar_wait(&full[j % nslot], ((uint32_t)(j / nslot)) & 1u)) atomicOr(err, ERR_TIMEOUT);
             if (!mbar_wait(xbar, 0)) atomicOr(err, ERR_TIMEOUT);
         }
-        __syncwarp();
-        if (ok) post(kStEnd);
         return;
     }
 
-    // ================= consumers
-    const int tid = threadIdx.x;
-    // router bias of the router row whose slices this warp sums (router stage with up to 8
-    // rows, see there), requested before the first wait
-    float bias = 0.f;
-    {
-        const int nrr = max(0, min(E + 1, c * g.rr + g.rr) - c * g.rr);
-        const int wpr = nrr <= 1 ? 8 : nrr <= 2 ? 4 : nrr <= 4 ? 2 : 1;
-        const int row = c * g.rr + warp / wpr;
-        if (warp / wpr < nrr && row < E && a.router_b) bias = __bfloat162float(a.router_b[row]);
-    }
-    if (!consumers_all(warp_wait(xbar, 0, lane)) && tid == 0) atomicOr(err, ERR_TIMEOUT);
-    int rb = 0;  // reduction buffer in use (alternates between the stages that reduce)
-    bool have_sh = false, have_rh = false;  // shared / routed h rows gathered
-    const uint32_t xs_a = smem_u32(xs), hs_a = smem_u32(hs);
-    for (int it = 0;; ++it) {
-        const int s = it % g.nst;
-        if (!consumers_all(warp_wait(&full[s], ((uint32_t)(it / g.nst)) & 1u, lane))) {
-            if (tid == 0) atomicOr(err, ERR_TIMEOUT);
+    // ================= consumers: warp w takes items w, w + 8, ...
+    float xr[kONch][8];
+    if (!warp_wait(xbar, 0, lane) && lane == 0) atomicOr(err, ERR_TIMEOUT);
+#pragma unroll
+    for (int q = 0; q < kONch; ++q) unpack8(lds128(smem_u32(xs) + 16u * (lane + 32 * q)), xr[q]);
+    const int up_end = p.n - (K + 1) * p.dpk;  // the down items come last
+    int s = warp % nslot;
+    uint32_t round = warp / nslot;
+    for (int j = warp; j < p.n; j += kOWarps) {
+        if (!warp_wait(&full[s], round & 1u, lane)) {
+            if (lane == 0) atomicOr(err, ERR_TIMEOUT);
             break;
         }
-        const DMeta m = meta[s];
-        const uint8_t* stp = stg + (size_t)s * g.stage;
-        const uint32_t sa = smem_u32(stp);
-        float* rbuf = red + rb * kWarps * 32 * 4;
-        auto release = [&]() {
+        const OMeta m = meta[s];
+        const uint32_t d = smem_u32(slots) + (uint32_t)(s * kOSlot);
+        if (m.kind == kOkRouter) {
+            const uint32_t rows[1] = {d};
+            float v[1];
+            dot_rows<1>(rows, xr, lane, v);
+            if (lane == 0) {
+                float sc = v[0];
+                if (m.a < a.E && a.router_b) sc += __bfloat162float(a.router_b[m.a]);
+                st_relaxed_u64(a.dlog + m.a, ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(sc));
+                __threadfence();  // a relaxed store alone can take microseconds to reach the other SMs
+            }
+        } else if (m.kind == kOkSharedUp || m.kind == kOkUp) {
+            // feature a: its gate row, then its up row
+            const uint32_t rows[2] = {d, d + kOH * 2};
+            float v[2];
+            dot_rows<2>(rows, xr, lane, v);
+            if (lane == 0) {
+                const bf16 h = __float2bfloat16_rn(silu(v[0]) * v[1]);
+                const int row = m.kind == kOkSharedUp ? K : rt.inv[m.k];  // h tap: routed rows in dispatch order, then the shared row
+                a.h[(size_t)row * kOI + m.a] = h;
+                st_relaxed_u32(hw + (size_t)m.k * kOI + m.a, (tag16 << 16) | (uint32_t)__bfloat16_as_ushort(h));
+                if (m.kind == kOkUp && j + kOWarps >= up_end) __threadfence();  // this warp's last h word
+            }
+        } else {
+            float hv[kOIch][8];
+            if (!poll_h(hw + (size_t)m.k * kOI, tag16, hv, lane) && lane == 0) atomicOr(err, ERR_TIMEOUT);
+            float acc[kOMaxRo];
+#pragma unroll
+            for (int r0 = 0; r0 < kOMaxRo; r0 += 4) {
+                // four rows' loads in flight before their multiplies
+                uint4 w[4][kOIch];
+#pragma unroll
+                for (int r = r0; r < r0 + 4; ++r)
+#pragma unroll
+                    for (int q = 0; q < kOIch; ++q)
+                        w[r - r0][q] = lds128(d + (uint32_t)(min(r, m.n - 1) * kOI * 2) + 16u * (lane + 32 * q));
+#pragma unroll
+                for (int r = r0; r < r0 + 4; ++r) {
+                    acc[r] = 0.f;
+#pragma unroll
+                    for (int q = 0; q < kOIch; ++q) acc[r] = dot8(w[r - r0][q], hv[q], acc[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kOMaxRo; ++r) {
+                const float v = warp_sum(acc[r]);
+                if (lane == r && r < m.n) ys[m.k * kOMaxOut + (m.a - p.o0) + r] = v;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (j == 0) {
+            // warp 0 after its first item: the routing, then the producer may issue the
+            // routed items
+            route_one(a, rt, tag, lane);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-        };
-
-        if (m.type == kStEnd) {
-            consumers_sync();  // every block's Ys rows are written
-            // residual + gated shared output + weighted slots 0..K-1, in that order
-            for (int idx = tid; idx < T * ro; idx += kConsumers) {
-                const int t = idx / ro, r = idx - t * ro, o = o0 + r;
-                float acc = a.residual ? __bfloat162float(a.residual[(size_t)t * H + o]) : 0.f;
-                float* yt = a.Y + (size_t)t * (K + 1) * H + o;
-                const float sh = rt.sgate[t] * Ys[(P + t) * 16 + r];
-                yt[(size_t)K * H] = sh;
-                acc += sh;
-                for (int k = 0; k < K; ++k) {
-                    const int p = t * K + k;
-                    const float v = rt.sw[p] * Ys[p * 16 + r];
-                    yt[(size_t)k * H] = v;
-                    acc += v;
-                }
-                a.out[(size_t)t * H + o] = __float2bfloat16_rn(acc);
-            }
-            if (c == 0 && tid == 0) {
-                // every CTA has read this call's tag once all have counted themselves in: move
-                // the tag and the base on for the next call
-                if (!wait_count(&a.hdr->dec_start, sbase, (uint32_t)G)) atomicOr(err, ERR_TIMEOUT);
-                a.hdr->dec_epoch = tag == 0xffffffffu ? 0u : tag;
-                a.hdr->dec_start_base = sbase + (uint32_t)G;
-            }
-            break;
+            if (lane == 0) mbar_arrive(routed);
+            if (c == 0) write_routing(a, rt, lane);
         }
-
-        if (m.type == kStTopK) {
-            release();
-            if (warp < T) route_token(a, rt, warp, lane, tag);
-            consumers_sync();
-            route_dispatch(rt, P, tid);
-            if (tid == 0) mbar_arrive(routed);
-            if (c == 0) {
-                // the routing results of this call, for the caller and the workspace taps
-                for (int p = tid; p < P; p += kConsumers) {
-                    a.ids[p] = rt.sid[p];
-                    a.topw[p] = rt.sw[p];
-                    a.perm[p] = rt.perm[p];
-                    a.inv[p] = rt.inv[p];
-                }
-                for (int e = tid; e <= E; e += kConsumers) {
-                    int less = 0, cnt = 0;
-                    for (int q = 0; q < P; ++q) {
-                        less += rt.sid[q] < e;
-                        cnt += rt.sid[q] == e;
-                    }
-                    a.offsets[e] = less;
-                    if (e < E) a.counts[e] = cnt;
-                }
-                for (int j = tid; j < rt.n_act; j += kConsumers) a.act[j] = rt.act[j];
-                if (tid < T) a.sgate[tid] = rt.sgate[tid];
-                if (tid == 0) a.hdr->n_act = rt.n_act;
-            }
-            continue;
+        s += kOWarps;
+        if (s >= nslot) {
+            s -= nslot;
+            ++round;
         }
-
-        if (m.type == kStRoute) {
-            // rows row0 .. row0+n-1 for every token: wpr warps per row, each a K slice of H/wpr
-            // (lane l takes elements 8l + 256i of it); the slices' sums are added in a fixed
-            // order by the row's first warp. Beyond 8 rows, warps loop over rows.
-            const int wpr = m.n <= 1 ? 8 : m.n <= 2 ? 4 : m.n <= 4 ? 2 : 1;
-            const int kl = H / wpr, q = warp % wpr;
-            float* part = rbuf;  // [warp][kDTT] slice sums
-            for (int rl = warp / wpr; rl < m.n; rl += kWarps / wpr) {
-                const uint8_t* wr = stp + (size_t)rl * g.xp;
-                float acc[kDTT];
-#pragma unroll
-                for (int t = 0; t < kDTT; ++t) acc[t] = 0.f;
-                for (int k = q * kl + lane * 8; k < (q + 1) * kl; k += 256) {
-                    const uint4 wv = *reinterpret_cast<const uint4*>(wr + k * 2);
-#pragma unroll
-                    for (int t = 0; t < kDTT; ++t)
-                        if (t < T) {
-                            float xf[8];
-                            unpack8(*reinterpret_cast<const uint4*>(xs + (size_t)t * g.xp + k * 2), xf);
-                            acc[t] = dot8(wv, xf, acc[t]);
-                        }
-                }
-                float mine = 0.f;
-#pragma unroll
-                for (int t = 0; t < kDTT; ++t)
-                    if (t < T) {
-                        const float v = warp_sum(acc[t]);
-                        if (lane == t) mine = v;
-                    }
-                if (wpr == 1) {
-                    if (lane < T) {
-                        const int row = m.row0 + rl;
-                        const float b = (row < E && a.router_b) ? __bfloat162float(a.router_b[row]) : 0.f;
-                        st_relaxed_u64(a.dlog + (size_t)lane * (E + 1) + row,
-                                       ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(mine + b));
-                    }
-                } else if (lane < T) {
-                    part[warp * kDTT + lane] = mine;
-                }
-            }
-            release();
-            if (wpr > 1) {
-                consumers_sync();
-                rb ^= 1;
-                if (q == 0 && warp / wpr < m.n && lane < T) {
-                    float v = 0.f;
-                    for (int w = warp; w < warp + wpr; ++w) v += part[w * kDTT + lane];
-                    const int row = m.row0 + warp / wpr;
-                    st_relaxed_u64(a.dlog + (size_t)lane * (E + 1) + row,
-                                   ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v + bias));
-                }
-            }
-            continue;
+    }
+    if (warp == 0 && p.n == 0) {  // no item at all: still route, so the producer is released
+        route_one(a, rt, tag, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(routed);
+        if (c == 0) write_routing(a, rt, lane);
+    }
+    consumers_sync();  // every item's down outputs are in ys
+    // residual + gated shared output + weighted slots 0..K-1, in that order
+    const int tid = threadIdx.x;
+    if (tid < p.ro) {
+        const int o = p.o0 + tid;
+        float acc = a.residual ? __bfloat162float(a.residual[o]) : 0.f;
+        const float sh = rt.sg * ys[K * kOMaxOut + tid];
+        a.Y[(size_t)K * kOH + o] = sh;
+        acc += sh;
+        for (int k = 0; k < K; ++k) {
+            const float v = rt.w[k] * ys[k * kOMaxOut + tid];
+            a.Y[(size_t)k * kOH + o] = v;
+            acc += v;
         }
-
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        if (m.type == kStUp) {
-            const int r = lane & 15, gi = r & 7;  // tile rows 0-7: gate of feature f0+gi, 8-15: its up row
-            const int srow = gi < m.n ? (r >> 3) * g.sf + gi : 0;
-            const int tt = lane & 7;
-            const int tok = tt < m.mt ? (int)((m.toks >> (4 * tt)) & 15u) : 0;
-            mma_rows(d, sa + (uint32_t)(srow * g.xp), xs_a + (uint32_t)(tok * g.xp), warp * (H / kWarps),
-                     H / kWarps / 16, lane);
-            release();
-            *reinterpret_cast<float4*>(rbuf + (warp * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
-            consumers_sync();
-            rb ^= 1;
-            if (warp == 0) {
-                float v[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float4 q4 = *reinterpret_cast<const float4*>(rbuf + (w * 32 + lane) * 4);
-                    v[0] += q4.x; v[1] += q4.y; v[2] += q4.z; v[3] += q4.w;
-                }
-                // feature f0+rl for tokens t, t+1: the plain bf16 h (workspace tap) and, from the
-                // lanes of even features, tagged pairs (f, f+1) for the other CTAs
-                const int rl = lane >> 2, t = 2 * (lane & 3);
-                const bf16 h0 = __float2bfloat16_rn(silu(v[0]) * v[2]);
-                const bf16 h1 = __float2bfloat16_rn(silu(v[1]) * v[3]);
-                const uint32_t u0 = __bfloat16_as_ushort(h0), u1 = __bfloat16_as_ushort(h1);
-                const uint32_t n0 = __shfl_down_sync(0xffffffffu, u0, 4), n1 = __shfl_down_sync(0xffffffffu, u1, 4);
-                if (rl < m.n) {
-                    bf16* hrow = a.h + (size_t)(m.row0 + t) * a.Imax + m.f0 + rl;
-                    if (t < m.mt) hrow[0] = h0;
-                    if (t + 1 < m.mt) hrow[a.Imax] = h1;
-                    if (!(rl & 1)) {
-                        uint64_t* w = a.dh + (size_t)(m.row0 + t) * (a.Imax / 2) + (m.f0 + rl) / 2;
-                        const uint64_t hi = (uint64_t)tag << 32;
-                        if (t < m.mt) st_relaxed_u64(w, hi | (n0 << 16) | u0);
-                        if (t + 1 < m.mt) st_relaxed_u64(w + a.Imax / 2, hi | (n1 << 16) | u1);
-                    }
-                }
-            }
-            continue;
-        }
-
-        // kStDown: block b of this stage by warps b*wpb .. b*wpb+wpb-1, each one K slice; the h
-        // rows it needs are gathered first (all consumers)
-        if (meta[s].blk[0] == 0 ? !have_sh : !have_rh) {
-            const bool sh = meta[s].blk[0] == 0;
-            const bool got = sh ? gather_h(a, hs, g.dp, P, T, a.Is, tag, tid) : gather_h(a, hs, g.dp, 0, P, a.I, tag, tid);
-            if (!consumers_all(got) && tid == 0) atomicOr(err, ERR_TIMEOUT);
-            (sh ? have_sh : have_rh) = true;
-        }
-        const int wpb = min(4, kWarps / g.nbs);
-        const int b = warp / wpb, kq = warp - b * wpb;
-        int j = 0, mt = 0, hrow0 = 0;
-        if (b < m.n) {
-            j = meta[s].blk[b];
-            const int inner = j == 0 ? a.Is : a.I;
-            hrow0 = j == 0 ? P : rt.aoff[j - 1];
-            mt = j == 0 ? T : rt.acnt[j - 1];
-            const int r = lane & 15, tt = lane & 7;
-            const uint32_t a_row = sa + (uint32_t)((b * g.ro + (r < ro ? r : 0)) * g.dp);
-            const uint32_t b_row = hs_a + (uint32_t)((hrow0 + (tt < mt ? tt : 0)) * g.dp);
-            const int kl = inner / wpb;
-            mma_rows(d, a_row, b_row, kq * kl, kl / 16, lane);
-        }
-        release();
-        *reinterpret_cast<float4*>(rbuf + (warp * 32 + lane) * 4) = make_float4(d[0], d[1], d[2], d[3]);
-        consumers_sync();
-        rb ^= 1;
-        if (b < m.n && kq == 0) {
-            float v[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int q = 0; q < wpb; ++q) {
-                const float4 q4 = *reinterpret_cast<const float4*>(rbuf + ((b * wpb + q) * 32 + lane) * 4);
-                v[0] += q4.x; v[1] += q4.y; v[2] += q4.z; v[3] += q4.w;
-            }
-            const int rl = lane >> 2, i0 = 2 * (lane & 3);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int r = rl + (q >= 2 ? 8 : 0), i = i0 + (q & 1);
-                if (r < ro && i < mt) Ys[(j == 0 ? P + i : rt.perm[hrow0 + i]) * 16 + r] = v[q];
-            }
-        }
+        a.out[o] = __float2bfloat16_rn(acc);
+    }
+    if (c == 0 && tid == 0) {
+        // every CTA has read this call's tag once all have counted themselves in: move the
+        // tag and the base on for the next call
+        if (!wait_count(&a.hdr->dec_start, sbase, (uint32_t)G)) atomicOr(err, ERR_TIMEOUT);
+        a.hdr->dec_epoch = tag == 0xffffffffu ? 0u : tag;
+        a.hdr->dec_start_base = sbase + (uint32_t)G;
     }
 }
 
-// Geometry for this layer: the most bytes in flight that fit the shared memory of one CTA.
-static bool pick_geom(const LayerArgs& a, int cap, DGeom* g) {
-    static const int cfg[][2] = {{8, 3}, {4, 6}, {4, 5}, {4, 4}, {4, 3}, {8, 2}, {4, 2}};
-    for (const auto& c : cfg)
-        if (decode_geom(a, a.num_sms, c[0], c[1], g) && g->smem <= cap) return true;
-    return false;
+static bool decode_geom(int cap, OGeom* g) {
+    int o = 0;
+    g->o_x = o; o += kOH * 2;
+    g->o_rt = o; o += ((int)sizeof(ORoute) + 127) & ~127;
+    g->o_ys = o; o += (kOMaxK + 1) * kOMaxOut * 4;
+    g->o_bar = o; o += (2 * kOMaxSlots + 2) * 8;
+    g->o_meta = o; o += kOMaxSlots * (int)sizeof(OMeta);
+    o = (o + 1023) & ~1023;
+    g->o_slot = o;
+    const int room = cap - 1024 - o;  // 1024: alignment of the dynamic base
+    g->nslot = room / kOSlot < kOMaxSlots ? room / kOSlot : kOMaxSlots;
+    g->smem = 1024 + o + g->nslot * kOSlot;
+    return g->nslot >= kOWarps;
 }
 
 // Dynamic shared memory one CTA of the kernel may use on the current device (0 on failure).
@@ -760,7 +545,7 @@ static int dynamic_smem_cap() {
         if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
             cudaFuncGetAttributes(&fa, k_decode_fused) != cudaSuccess)
             return 0;
-        const int c = optin - (int)fa.sharedSizeBytes - 1024;
+        const int c = optin - (int)fa.sharedSizeBytes;
         if (c <= 0 ||
             cudaFuncSetAttribute(k_decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, c) != cudaSuccess)
             return 0;
@@ -769,20 +554,26 @@ static int dynamic_smem_cap() {
     return cap[dev];
 }
 
+// The kernel is built for the pages' layer shape (H = 2048, expert widths 512) and one token;
+// other shapes take the routing and streaming kernels.
 bool decode_fused_supported(const LayerArgs& a) {
-    if (!(a.T >= 1 && a.T <= kDTT && a.K <= 8 && a.H <= kDMaxH && a.H % 128 == 0 && a.Imax <= kDMaxI &&
-          a.I % 64 == 0 && a.Is % 64 == 0 && a.E <= 256 && a.num_sms >= 1 && a.dlog && a.dh))
+    if (!(a.T == 1 && a.H == kOH && a.I == kOI && a.Is == kOI && a.K <= kOMaxK && a.E <= 256 && a.num_sms >= 1 &&
+          a.dlog && a.dh))
         return false;
-    DGeom g;
-    return pick_geom(a, dynamic_smem_cap(), &g);
+    // output rows per CTA within one down item; the items issued before the ring is shared
+    // (router rows, shared features) within the ring
+    const int G = a.num_sms;
+    if ((kOH + G - 1) / G > kOMaxOut || (a.E + G) / G + (kOI + G - 1) / G > kOWarps) return false;
+    OGeom g;
+    return decode_geom(dynamic_smem_cap(), &g);
 }
 
 cudaError_t launch_decode_fused(const LayerArgs& a, cudaStream_t s) {
-    DGeom g;
-    if (!pick_geom(a, dynamic_smem_cap(), &g)) return cudaErrorInvalidConfiguration;
+    OGeom g;
+    if (!decode_geom(dynamic_smem_cap(), &g)) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.num_sms);
-    cfg.blockDim = dim3(kDThreads);
+    cfg.blockDim = dim3(kOThreads);
     cfg.dynamicSmemBytes = (size_t)g.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

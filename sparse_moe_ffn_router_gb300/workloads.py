@@ -38,6 +38,7 @@ WORKLOADS = {
         Workload("tiny_T8", 8, 512, 32, 4, 128, 128, seed=0,
                  note="smallest instance: T=8, H=512, 32 experts, top-4, inner 128"),
         Workload("decode_T1", 1, 2048, 256, 8, 512, 512, seed=1, note="decode, one token, full layer shape"),
+        Workload("decode_T8", 8, 2048, 256, 8, 512, 512, seed=5, note="decode batch of 8 tokens, full layer shape"),
         Workload("decode_T64", 64, 2048, 256, 8, 512, 512, seed=2,
                  note="decode batch of 64 tokens, near-uniform routing"),
         Workload("prefill_T4096_zipf", 4096, 2048, 256, 8, 512, 512, seed=3, zipf_s=1.1,
