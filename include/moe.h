@@ -141,7 +141,9 @@ moe_status moe_forward_host_io(const moe_dims* d, const void* host_x, const moe_
  * the touched experts' rows are written; the rest is left as it was), and the experts run
  * from there. One shadow can serve every layer of a model in turn.
  * Errors: MOE_ERR_INVALID_ARG when gate_up or down is not registered host memory mapped into
- * the device (checked with cudaPointerGetAttributes before any launch) or shadow is NULL,
+ * the device (checked with cudaPointerGetAttributes before any launch), when the registered
+ * allocation holding gate_up or down ends before the whole [E, 2I, H] or [E, H, I] tensor
+ * (checked where the driver reports the allocation's range), or shadow is NULL,
  * MOE_ERR_MISALIGNED when shadow is not 16-byte aligned, MOE_ERR_WORKSPACE_TOO_SMALL when
  * shadow_bytes < moe_expert_shadow_size(d); otherwise as moe_forward. */
 size_t moe_expert_shadow_size(const moe_dims* d);
@@ -217,6 +219,27 @@ moe_status moe_set_trace(int kernel, void* const* start_events, void* const* sto
 /* Number of kernels this library has launched in this process so far. */
 uint64_t moe_launch_count(void);
 
+/* Testing aid for the bounded-wait path (the paper has no counterpart). Every wait of the
+ * one-token kernel (moe_forward with T = 1 at the page's layer shape) and of the streaming
+ * expert kernels (2 <= T < 256) gives up after a time limit, sets MOE_ERR_TIMEOUT in the
+ * workspace's error word and lets the kernel run to its end with in-range indices; the calls
+ * after a timeout need moe_workspace_init on that workspace. This sets, process-wide and for
+ * the calls made after it returns:
+ *   wait_ns   the time limit of those waits in nanoseconds; 0 restores the default (~1 s);
+ *             at most 10 s;
+ *   suppress  0 in normal use, or one signal to hold back so that a wait runs out:
+ *             MOE_TEST_SUPPRESS_SCORE  CTA 1 of the one-token kernel does not publish its
+ *                                      router scores (every CTA's wait for the scores runs out);
+ *             MOE_TEST_SUPPRESS_STAGE  CTA 0 of the streaming gate_up kernel (9 <= T < 256)
+ *                                      never loads its first ring stage (its consumers' wait
+ *                                      on the stage's mbarrier runs out).
+ * Results of calls made while a signal is held back are meaningless; no call faults, traps or
+ * hangs. Returns MOE_ERR_INVALID_ARG for another suppress value or wait_ns above 10 s. Not
+ * thread-safe with concurrent calls of the library. */
+#define MOE_TEST_SUPPRESS_SCORE 1
+#define MOE_TEST_SUPPRESS_STAGE 2
+moe_status moe_test_set_wait(uint64_t wait_ns, int suppress);
+
 /* Routing without any device allocation by the caller (the paper has no counterpart: this is
  * for callers of this library that cannot call cudaMalloc, such as a plugin whose host
  * framework owns every device allocation, an engine that reserved all of HBM up front, or a
@@ -226,7 +249,8 @@ uint64_t moe_launch_count(void);
  * process exits. Limits: T <= 64 and the scratch layout must fit (any E <= 256, K <= 8 fit);
  * larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before anything is launched.
  * The first call on a device looks up the array's device address on the current device
- * (cudaGetSymbolAddress); make that first call before any stream capture. Every call shares
+ * (cudaGetSymbolAddress); make that first call before any stream capture. The address is
+ * kept per device and context: the first call after a reset of the device looks it up again. Every call shares
  * the one array: calls that may overlap on the GPU (different streams, or devices sharing it)
  * race and must be ordered by the caller. Each call clears the part that must start at zero.
  * A non-finite router score is not reported (there is no workspace error word). */

@@ -9,6 +9,8 @@ ABI. There is no CPU path: a call fails loudly when the library or a GPU is miss
 """
 from .binding import (  # noqa: F401
     FLAG_BF16_SCORES,
+    TEST_SUPPRESS_SCORE,
+    TEST_SUPPRESS_STAGE,
     ForwardHostIO,
     MoEError,
     Weights,
@@ -21,6 +23,7 @@ from .binding import (  # noqa: F401
     moe_last_device_error,
     moe_launch_count,
     moe_set_trace,
+    moe_test_set_wait,
     moe_rmsnorm,
     moe_route,
     moe_route_noalloc,

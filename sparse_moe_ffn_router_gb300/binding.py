@@ -19,7 +19,8 @@ MOE_STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHA
               4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE"}
 EXPORTED = ["moe_workspace_size", "moe_workspace_init", "moe_route", "moe_forward", "moe_rmsnorm",
             "moe_last_device_error", "moe_workspace_tap", "moe_set_trace", "moe_launch_count", "moe_route_noalloc", "moe_status_string",
-            "moe_router_stats", "moe_expert_shadow_size", "moe_forward_host_experts", "moe_forward_host_io"]
+            "moe_router_stats", "moe_expert_shadow_size", "moe_forward_host_experts", "moe_forward_host_io",
+            "moe_test_set_wait"]
 KERNELS = {"router_scores": 0, "router_topk": 1, "dispatch_local": 2, "dispatch_scan": 3, "dispatch_scatter": 4,
            "gate_up": 5, "down": 6, "combine": 7, "rmsnorm": 8, "shared_gate": 9, "gather": 10, "gemm_plan": 11,
            "decode_fused": 12, "router_stats": 13, "fetch_experts": 14,
@@ -28,6 +29,9 @@ KERNELS = {"router_scores": 0, "router_topk": 1, "dispatch_local": 2, "dispatch_
 
 # moe_dims.flags: router and shared-gate scores rounded to bf16 before ranking and sigmoid
 FLAG_BF16_SCORES = 1
+# moe_test_set_wait: the signal held back so that a bounded device wait runs out
+TEST_SUPPRESS_SCORE = 1
+TEST_SUPPRESS_STAGE = 2
 
 
 class Dims(ctypes.Structure):
@@ -115,6 +119,8 @@ def load_library(build_if_missing: bool = True):
             lib.moe_forward_host_experts.argtypes = [D, P, W, P, P, P, S, P, S, P]
             lib.moe_forward_host_io.restype = st
             lib.moe_forward_host_io.argtypes = [D, P, W, P, P, P, P, P, S, P]
+            lib.moe_test_set_wait.restype = st
+            lib.moe_test_set_wait.argtypes = [ctypes.c_uint64, ctypes.c_int]
             lib.moe_status_string.restype = ctypes.c_char_p
             lib.moe_status_string.argtypes = [ctypes.c_int]
             _lib = lib
@@ -312,6 +318,13 @@ def moe_set_trace(kernel, start_events=(), stop_events=()):
     st = arr(*[e.cuda_event for e in start_events]) if n else None
     sp = arr(*[e.cuda_event for e in stop_events]) if n else None
     _check(load_library().moe_set_trace(kid, st, sp, n), "moe_set_trace")
+
+
+def moe_test_set_wait(wait_ns: int = 0, suppress: int = 0):
+    """Testing aid: time limit (ns, 0 = the default of ~1 s) of the bounded device waits of the
+    one-token and streaming kernels, and a signal to hold back (TEST_SUPPRESS_*) so that a wait
+    runs out; moe_test_set_wait() restores normal operation."""
+    _check(load_library().moe_test_set_wait(int(wait_ns), int(suppress)), "moe_test_set_wait")
 
 
 def moe_launch_count() -> int:

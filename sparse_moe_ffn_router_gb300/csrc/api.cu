@@ -4,6 +4,9 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
+
+#include <cuda.h>
 #include <vector>
 
 #include "launch.h"
@@ -11,6 +14,10 @@
 namespace moe {
 
 static std::atomic<uint64_t> g_launches{0};
+
+// Testing aid (moe_test_set_wait): time limit of the bounded device waits and the signal held back.
+static std::atomic<uint64_t> g_wait_ns{kWaitNs};
+static std::atomic<int> g_suppress{0};
 
 struct TraceSlot {
     int n = 0;
@@ -124,6 +131,8 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
     a->T = p->T; a->H = p->H; a->E = p->E; a->K = p->K; a->I = p->I; a->Is = p->Is;
     a->Imax = p->Imax; a->ldl = p->ldl; a->nb = p->nb; a->P = p->P;
     a->num_sms = sm_count();
+    a->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    a->test_suppress = g_suppress.load(std::memory_order_relaxed);
     return MOE_OK;
 }
 
@@ -159,6 +168,30 @@ bool host_mapped(const void* p, const void** dev) {
     if (at.type != cudaMemoryTypeHost || !at.devicePointer) return false;
     *dev = at.devicePointer;
     return true;
+}
+
+// Whether the pinned allocation that holds p extends at least `bytes` past p. The driver's
+// record of the allocation's range is read through cuPointerGetAttribute (looked up once); when
+// the driver cannot report a range, the check passes and the caller's sizes are trusted.
+bool host_range_covers(const void* p, size_t bytes) {
+    typedef CUresult (*GetAttr)(void*, CUpointer_attribute, CUdeviceptr);
+    static GetAttr fn = nullptr;
+    static bool looked = false;
+    if (!looked) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (GetAttr)f;
+        looked = true;
+    }
+    if (!fn) return true;
+    CUdeviceptr start = 0;
+    size_t size = 0;
+    if (fn(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, (CUdeviceptr)(uintptr_t)p) != CUDA_SUCCESS ||
+        fn(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, (CUdeviceptr)(uintptr_t)p) != CUDA_SUCCESS || size == 0)
+        return true;
+    return (uintptr_t)p + bytes <= (uintptr_t)start + size;
 }
 
 // The kind of memory p points to (cudaMemoryTypeUnregistered for pageable host memory), or
@@ -343,6 +376,10 @@ extern "C" moe_status moe_forward_host_experts(const moe_dims* d, const void* x,
     const void* hgu = nullptr;
     const void* hdn = nullptr;
     if (!host_mapped(w->gate_up, &hgu) || !host_mapped(w->down, &hdn)) return MOE_ERR_INVALID_ARG;
+    // the fetch kernel reads any touched expert's rows: both whole tensors must be mapped
+    if (!host_range_covers(w->gate_up, (size_t)d->E * 2 * d->I * d->H * 2) ||
+        !host_range_covers(w->down, (size_t)d->E * d->H * d->I * 2))
+        return MOE_ERR_INVALID_ARG;
     a.residual = (const bf16*)residual;
     a.out = (bf16*)out;
     bf16* sgu = (bf16*)shadow;
@@ -414,6 +451,15 @@ extern "C" moe_status moe_set_trace(int kernel, void* const* start_events, void*
 }
 
 extern "C" uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+extern "C" moe_status moe_test_set_wait(uint64_t wait_ns, int suppress) {
+    if (wait_ns > 10ull * kWaitNs ||
+        (suppress != 0 && suppress != MOE_TEST_SUPPRESS_SCORE && suppress != MOE_TEST_SUPPRESS_STAGE))
+        return MOE_ERR_INVALID_ARG;
+    g_wait_ns.store(wait_ns ? wait_ns : kWaitNs, std::memory_order_relaxed);
+    g_suppress.store(suppress, std::memory_order_relaxed);
+    return MOE_OK;
+}
 
 extern "C" const char* moe_status_string(moe_status s) {
     switch (s) {

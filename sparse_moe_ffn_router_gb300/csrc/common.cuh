@@ -12,6 +12,9 @@ namespace moe {
 
 typedef __nv_bfloat16 bf16;
 
+// Default time limit of a bounded device wait (~1 s of global time).
+constexpr uint64_t kWaitNs = 1000000000ull;
+
 // Bits of the device error word (first word of the workspace header).
 enum : uint32_t { ERR_NONFINITE_SCORE = 1u, ERR_TIMEOUT = 2u, ERR_BAD_ROUTE = 4u };
 

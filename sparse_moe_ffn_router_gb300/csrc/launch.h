@@ -43,6 +43,8 @@ struct LayerArgs {
     uint64_t* dlog;   // [T, E+1] router scores tagged with their call (fused few-token kernel)
     uint64_t* dh;     // [P+T, Imax/2] gated activation pairs tagged with their call (same kernel)
     WsHeader* hdr;
+    uint64_t wait_ns;   // time limit of the bounded waits of the one-token and streaming kernels
+    int test_suppress;  // MOE_TEST_SUPPRESS_* (testing aid; 0 in normal use)
     bool gemm;
     int flags;        // moe_dims.flags (MOE_FLAG_BF16_SCORES)
     int T, H, E, K, I, Is, Imax, ldl, nb;

@@ -14,6 +14,8 @@
 
 #include <mutex>
 
+#include <cuda.h>
+
 #include "launch.h"
 
 namespace moe {
@@ -45,20 +47,43 @@ ScratchLayout scratch_layout(const moe_dims& d) {
     return s;
 }
 
-// Device address of the scratch array, looked up once per device with that device current.
+// The current CUDA context (the driver's handle), or nullptr when it cannot be read.
+CUcontext current_context() {
+    typedef CUresult (*GetCurrent)(CUcontext*);
+    static GetCurrent fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (GetCurrent)p;
+    });
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return ctx;
+}
+
+// Device address of the scratch array on the current device, looked up with that device
+// current and cached per device together with the context it belongs to: after a reset of
+// the device (a new primary context, where the library image and the array may have moved)
+// the address is looked up again.
 void* scratch_address(int dev, cudaError_t* err) {
     static std::mutex mu;
     static void* addr[128] = {};
+    static CUcontext owner[128] = {};
     if (dev < 0 || dev >= 128) {
         *err = cudaErrorInvalidDevice;
         return nullptr;
     }
+    const CUcontext ctx = current_context();
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || !ctx || owner[dev] != ctx) {
         void* p = nullptr;
         *err = cudaGetSymbolAddress(&p, g_route_scratch);
         if (*err != cudaSuccess) return nullptr;
         addr[dev] = p;
+        owner[dev] = current_context();
     }
     *err = cudaSuccess;
     return addr[dev];

@@ -179,3 +179,14 @@ def test_prepared_host_io_checks_its_tensors():
         binding.ForwardHostIO(FULL, W, cpu(T, H // 2), cpu(T, H), torch.empty(16, dtype=torch.uint8))
     with pytest.raises(ValueError, match="GPU only"):  # the weights and staging must be CUDA tensors
         binding.ForwardHostIO(FULL, W, cpu(T, H), cpu(T, H), torch.empty(16, dtype=torch.uint8))
+
+
+def test_wait_limit_hook_validates_its_arguments(lib):
+    """The testing aid for the bounded waits takes a limit of at most 10 s and a known signal;
+    anything else is rejected on the host, and the defaults are restored."""
+    assert lib.moe_test_set_wait(0, 3) == 1
+    assert lib.moe_test_set_wait(0, -1) == 1
+    assert lib.moe_test_set_wait(10_000_000_001, 0) == 1
+    assert lib.moe_test_set_wait(2_000_000, 1) == 0
+    assert lib.moe_test_set_wait(2_000_000, 2) == 0
+    assert lib.moe_test_set_wait(0, 0) == 0

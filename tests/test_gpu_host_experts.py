@@ -89,3 +89,28 @@ def test_device_pointers_are_refused_as_host_experts():
     assert st == 1
     with pytest.raises(ValueError, match="pinned"):
         moe.moe_forward_host_experts(dims, x.cuda(), Wd, None, out, shadow, ws)
+
+
+def test_mapping_smaller_than_the_expert_tensors_is_rejected():
+    """The fetch kernel may read any expert's rows, so the registered host allocation holding
+    gate_up must cover the whole [E, 2I, H] tensor: a buffer of which only the first half is
+    registered (and mapped) is refused on the host before anything runs. (A router bias keeps
+    the routing on experts 0..K-1, whose rows lie in the registered half, so even a call that
+    slipped through would read registered memory only.)"""
+    dims = (8, 512, 32, 4, 128, 128)
+    x, w, _, Wh = _layer(dims, seed=41)
+    bias = torch.zeros(dims[2], dtype=torch.bfloat16)
+    bias[: dims[3]] = 100.0
+    gu = w["gate_up"].clone()  # pageable; half of it registered below
+    half = gu.numel() * gu.element_size() // 2
+    assert dims[3] * 2 * dims[4] * dims[1] * 2 <= half  # the routed experts' rows are in the registered half
+    cudart = torch.cuda.cudart()
+    assert int(cudart.cudaHostRegister(gu.data_ptr(), half, 2)) == 0  # cudaHostRegisterMapped
+    try:
+        bad = moe.Weights(Wh.router_w, bias.cuda(), gu, Wh.down, Wh.shared_gate_up, Wh.shared_down, Wh.shared_gate)
+        with pytest.raises(binding.MoEError) as e:
+            _run_host(dims, x.cuda(), bad)
+        assert e.value.status == 1  # MOE_ERR_INVALID_ARG
+    finally:
+        torch.cuda.synchronize()
+        cudart.cudaHostUnregister(gu.data_ptr())
