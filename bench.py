@@ -71,7 +71,8 @@ def parse_args():
     p.add_argument("--also-seconds", type=float, default=0.5, help="timed work of each extra workload, in seconds")
     p.add_argument("--also", default="decode_T8,decode_T64,prefill_T4096_zipf,stack40_decode_T32",
                    help="comma-separated extra workloads reported under 'also' ('none' to skip)")
-    p.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--cpu-budget", type=float, default=10.0,
+                   help="seconds of oracle work for cpu_baseline (0: no oracle baseline, e.g. for profiling runs)")
     p.add_argument("--no-graph", action="store_true", help="time plain calls instead of CUDA-graph replays")
     p.add_argument("--rotate", type=int, default=ROTATE,
                    help="distinct layers cycled through by small-T workloads (keeps weights out of L2)")
@@ -887,8 +888,8 @@ def main():
             host[name] = time_host_experts(WORKLOADS[name], device)
             torch.cuda.empty_cache()
     line["host_experts"] = host
-    if rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget, device)
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget, device, tokens=256 if wl.T > 256 else None)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
