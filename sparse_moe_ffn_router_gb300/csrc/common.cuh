@@ -154,6 +154,40 @@ __device__ __forceinline__ float dot8(const uint4& w, const float* x, float acc)
     return acc;
 }
 
+// The same sums with both operands left as bf16: fma.rn.f32.bf16 multiplies two bf16 (the
+// product is exact in fp32) and adds in fp32 with one rounding, so the result is bit for bit
+// dot8's, without the unpacking. x holds 8 packed bf16.
+__device__ __forceinline__ float fma_bf16x2(uint32_t a, uint32_t b, float acc) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+    return acc;
+}
+__device__ __forceinline__ float dot8_bf16(const uint4& w, const uint4& x, float acc) {
+    acc = fma_bf16x2(w.x, x.x, acc);
+    acc = fma_bf16x2(w.y, x.y, acc);
+    acc = fma_bf16x2(w.z, x.z, acc);
+    acc = fma_bf16x2(w.w, x.w, acc);
+    return acc;
+}
+// acc + sum_i w[i] * h[i], i = 0..7, where h[i] is the low half (a bf16) of the 32-bit word
+// hw[i]: the same order and roundings as dot8.
+__device__ __forceinline__ float dot8_bf16_lo(const uint4& w, const uint32_t* hw, float acc) {
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{\n\t.reg .b16 al, ah, h0, h1, u0, u1;\n\t"
+            "mov.b32 {al, ah}, %1;\n\tmov.b32 {h0, u0}, %2;\n\tmov.b32 {h1, u1}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, al, h0, %0;\n\t"
+            "fma.rn.f32.bf16 %0, ah, h1, %0;\n\t}"
+            : "+f"(acc)
+            : "r"(wv[i]), "r"(hw[2 * i]), "r"(hw[2 * i + 1]));
+    return acc;
+}
+
 // Butterfly sum over the warp; every lane ends with the same, order-fixed value.
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -182,36 +216,64 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 
 // Top-K of one token by a warp ("Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256
 // Experts, Router: the 8 highest scores; ties go to the lower expert index). Lane l holds the
-// keys of experts l + 32j in key[j]. Each of K rounds takes the largest remaining key by a warp
-// max and, among equal keys, the lowest expert by a warp min. Lane k < K receives slot k: its
-// score (myv) and expert (mye); every lane receives the slot-0 score (v0).
+// keys of experts l + 32j in key[j]. Each lane first sorts its eight (key, j) pairs, larger key
+// first and, among equal keys, lower j first (Batcher's odd-even merge network, 19 compare-
+// exchanges); then each of K rounds takes the largest head key by a warp max and, among equal
+// heads, the lowest expert by a warp min, and the winning lane drops its head. A lane's head is
+// its lowest expert of its largest remaining key, so every round picks what a scan of all
+// remaining keys would. Lane k < K receives slot k: its score (myv) and expert (mye); every
+// lane receives the slot-0 score (v0).
+__device__ __forceinline__ void topk_cas(uint32_t (&k)[8], uint32_t (&j)[8], int a, int b) {
+    const bool sw = k[b] > k[a] || (k[b] == k[a] && j[b] < j[a]);
+    const uint32_t ka = k[a], ja = j[a];
+    k[a] = sw ? k[b] : ka;
+    j[a] = sw ? j[b] : ja;
+    k[b] = sw ? ka : k[b];
+    j[b] = sw ? ja : j[b];
+}
 __device__ __forceinline__ void warp_topk(const uint32_t (&key)[8], int K, int lane, float& v0, float& myv, int& mye) {
-    uint32_t taken = 0;
+    uint32_t k[8], j[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        k[i] = key[i];
+        j[i] = (uint32_t)i;
+    }
+    topk_cas(k, j, 0, 1); topk_cas(k, j, 2, 3); topk_cas(k, j, 4, 5); topk_cas(k, j, 6, 7);
+    topk_cas(k, j, 0, 2); topk_cas(k, j, 1, 3); topk_cas(k, j, 4, 6); topk_cas(k, j, 5, 7);
+    topk_cas(k, j, 1, 2); topk_cas(k, j, 5, 6);
+    topk_cas(k, j, 0, 4); topk_cas(k, j, 1, 5); topk_cas(k, j, 2, 6); topk_cas(k, j, 3, 7);
+    topk_cas(k, j, 2, 4); topk_cas(k, j, 3, 5);
+    topk_cas(k, j, 1, 2); topk_cas(k, j, 3, 4); topk_cas(k, j, 5, 6);
     v0 = 0.f;
     myv = 0.f;
     mye = 0;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        if (k < K) {
-            uint32_t bk = 0;
-            int bj = 0;
+    for (int r = 0; r < 8; ++r) {
+        if (r < K) {
+            const uint32_t m = __reduce_max_sync(0xffffffffu, k[0]);
+            const uint32_t win = __reduce_min_sync(0xffffffffu, k[0] == m ? (uint32_t)lane + 32u * j[0] : 0xffffffffu);
+            if ((int)(win & 31u) == lane) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (!((taken >> j) & 1u) && key[j] > bk) {
-                    bk = key[j];
-                    bj = j;
+                for (int i = 0; i < 7; ++i) {
+                    k[i] = k[i + 1];
+                    j[i] = j[i + 1];
                 }
-            const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-            const uint32_t win = __reduce_min_sync(0xffffffffu, bk == m ? (uint32_t)(lane + 32 * bj) : 0xffffffffu);
-            if ((int)(win & 31u) == lane) taken |= 1u << (win >> 5);
-            if (k == 0) v0 = key_score(m);
-            if (k == lane) {
+                k[7] = 0u;
+            }
+            if (r == 0) v0 = key_score(m);
+            if (r == lane) {
                 myv = key_score(m);
                 mye = (int)win;
             }
         }
     }
 }
+
+// Programmatic dependent launch: wait until the previous kernel on the stream has completed
+// and its memory is visible (a no-op for a kernel launched without the attribute), and let
+// the next kernel on the stream launch early (it waits the same way before reading ours).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);

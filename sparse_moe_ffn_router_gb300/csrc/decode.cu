@@ -36,23 +36,26 @@
 // Every wait is bounded (~1 s): a timeout sets MOE_ERR_TIMEOUT in the workspace and the
 // kernel still runs to its end with in-range indices. Each CTA counts itself in when it
 // starts; CTA 0 moves the call's tag on at its end once all are in.
+#include <atomic>
 #include "launch.h"
 #include "ring.cuh"
 
 namespace moe {
 
 constexpr int kOWarps = 8;                     // consumer warps
-constexpr int kOThreads = (kOWarps + 1) * 32;  // + the producer warp
+constexpr int kOProducers = 4;                 // producer warps (lane 0 of each issues copies)
+constexpr int kOThreads = (kOWarps + kOProducers) * 32;
 constexpr int kOH = 2048;                      // hidden width (the page's layer shape)
 constexpr int kOI = 512;                       // routed and shared expert widths
 constexpr int kONch = kOH / 256;               // 16-byte chunks of an H-long row per lane
 constexpr int kOIch = kOI / 256;               // 16-byte chunks of an I-long row per lane
 constexpr int kOMaxK = 8;                      // experts per token
 constexpr int kOSlot = 8192;                   // ring slot: one feature's gate and up rows
-constexpr int kOMaxSlots = 28;
+constexpr int kOMaxSlots = 28;                 // a multiple of kOProducers
+static_assert(kOMaxSlots < 32, "one producer lane per slot plus one for the token row");
+constexpr int kOMaxItems = 64;
 constexpr int kOMaxRo = kOSlot / (kOI * 2);    // down rows per item
 constexpr int kOMaxOut = 16;                   // output rows per CTA
-constexpr int kOProducer = kOWarps;
 
 enum : int { kOkRouter = 0, kOkSharedUp = 1, kOkSharedDown = 2, kOkUp = 3, kOkDown = 4 };
 
@@ -86,7 +89,17 @@ struct OPlan {
 
 struct OGeom {
     int nslot;
-    int o_x, o_slot, o_meta, o_bar, o_ys, o_rt, smem;
+    int o_x, o_slot, o_meta, o_bar, o_ys, o_rt, o_iss, smem;
+};
+
+// Item j of a CTA's sequence: router rows, shared features, routed features, then down rows
+// (the shared expert's first, then slots 0..K-1, kOMaxRo rows per item); the copies that load
+// it and what its consumer does with it.
+struct OItem {
+    OMeta m;
+    const void* src0;
+    const void* src1;
+    uint32_t b0, b1;
 };
 
 __device__ __forceinline__ OPlan oplan(const LayerArgs& a, int c, int G) {
@@ -104,16 +117,59 @@ __device__ __forceinline__ OPlan oplan(const LayerArgs& a, int c, int G) {
     return p;
 }
 
-__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+__device__ __forceinline__ OItem item_at(const LayerArgs& a, const OPlan& p, const ORoute& rt, int c, int G, int j) {
+    OItem it;
+    it.src1 = nullptr;
+    it.b1 = 0;
+    if (j < p.nr) {
+        const int row = c + j * G;
+        it.m = OMeta{kOkRouter, a.K, row, 1};
+        it.src0 = row < a.E ? a.router_w + (size_t)row * kOH : a.sg;
+        it.b0 = kOH * 2;
+        return it;
+    }
+    j -= p.nr;
+    if (j < p.nsf) {
+        const int f = p.fs0 + j;
+        it.m = OMeta{kOkSharedUp, a.K, f, 1};
+        it.src0 = a.sgu + (size_t)f * kOH;
+        it.src1 = a.sgu + (size_t)(kOI + f) * kOH;
+        it.b0 = it.b1 = kOH * 2;
+        return it;
+    }
+    j -= p.nsf;
+    if (j < p.nf) {
+        const int fi = p.f0 + j, k = fi / kOI, f = fi - k * kOI;  // (slot, feature) pair
+        it.m = OMeta{kOkUp, k, f, 1};
+        it.src0 = rt.gu[k] + (size_t)f * kOH;
+        it.src1 = rt.gu[k] + (size_t)(kOI + f) * kOH;
+        it.b0 = it.b1 = kOH * 2;
+        return it;
+    }
+    j -= p.nf;
+    const int kk = j / p.dpk, r0 = p.o0 + (j - kk * p.dpk) * kOMaxRo, n = min(kOMaxRo, p.o0 + p.ro - r0);
+    it.m = OMeta{kk == 0 ? kOkSharedDown : kOkDown, kk == 0 ? a.K : kk - 1, r0, n};
+    it.src0 = (kk == 0 ? a.sd : rt.dn[kk - 1]) + (size_t)r0 * kOI;
+    it.b0 = (uint32_t)(n * kOI * 2);
+    return it;
+}
+
+// Publishing a tagged word to the other CTAs: an atomic exchange is carried out at L2, where
+// the other SMs' polls find it within about a microsecond; a plain relaxed store can stay
+// buffered for several microseconds unless a fence follows it, and a fence holds up the
+// memory instructions of the SM's other warps too. (The old value is not used.)
+__device__ __forceinline__ void publish_u64(uint64_t* p, uint64_t v) {
+    uint64_t old;
+    asm volatile("atom.exch.relaxed.gpu.global.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
     uint64_t v;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void publish_u32(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.exch.relaxed.gpu.global.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ uint4 ld_relaxed_v4(const uint32_t* p) {
     uint4 v;
@@ -153,7 +209,7 @@ __device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t base, uin
 // memory; lane l takes the 16-byte chunks l, l+32, ... into two partial sums per row (short
 // dependency chains), added in a fixed order, then the warp sums in a fixed order.
 template <int R>
-__device__ __forceinline__ void dot_rows(const uint32_t (&rows)[R], const float (&xr)[kONch][8], int lane,
+__device__ __forceinline__ void dot_rows(const uint32_t (&rows)[R], const uint4 (&xr)[kONch], int lane,
                                          float (&out)[R]) {
     float acc[R][2];
 #pragma unroll
@@ -171,16 +227,16 @@ __device__ __forceinline__ void dot_rows(const uint32_t (&rows)[R], const float 
 #pragma unroll
             for (int r = 0; r < R; ++r) w[(q + 2) % 3][r] = lds128(rows[r] + 16u * (lane + 32 * (q + 2)));
 #pragma unroll
-        for (int r = 0; r < R; ++r) acc[r][q & 1] = dot8(w[q % 3][r], xr[q], acc[r][q & 1]);
+        for (int r = 0; r < R; ++r) acc[r][q & 1] = dot8_bf16(w[q % 3][r], xr[q], acc[r][q & 1]);
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) out[r] = warp_sum(acc[r][0] + acc[r][1]);
 }
 
-// The h values of expert slot k that this lane multiplies (chunks lane, lane+32, ... of the
-// inner width: 8 values each), polled from their tagged words until all carry `tag16`. False
-// after `limit` ns (the values are then taken as they are).
-__device__ bool poll_h(const uint32_t* words, uint32_t tag16, float (&hv)[kOIch][8], int lane, uint64_t limit) {
+// The tagged h words of expert slot k that this lane multiplies (chunks lane, lane+32, ... of
+// the inner width: 8 words each, the bf16 h in each low half), polled until all carry `tag16`.
+// False after `limit` ns (the words are then taken as they are).
+__device__ bool poll_h(const uint32_t* words, uint32_t tag16, uint32_t (&hv)[kOIch][8], int lane, uint64_t limit) {
     uint32_t need = (1u << kOIch) - 1u;
     const uint64_t t0 = global_ns();
     bool ok = true;
@@ -197,7 +253,7 @@ __device__ bool poll_h(const uint32_t* words, uint32_t tag16, float (&hv)[kOIch]
                 for (int i = 0; i < 8; ++i) fresh &= (w[i] >> 16) == tag16;
                 if (fresh || give_up) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) hv[q][i] = __uint_as_float(w[i] << 16);
+                    for (int i = 0; i < 8; ++i) hv[q][i] = w[i];
                     need &= ~(1u << q);
                 }
             }
@@ -212,7 +268,8 @@ __device__ bool poll_h(const uint32_t* words, uint32_t tag16, float (&hv)[kOIch]
 // tag; each of K rounds takes the largest remaining key and, among equal keys, the lowest
 // expert ("Qwen3.6-35B-A3B -- Architecture Overview", MoE FFN: 256 Experts, Router). The
 // weights are the softmax over the kept scores (the full softmax renormalised over them).
-__device__ void route_one(const LayerArgs& a, ORoute& rt, uint32_t tag, int lane) {
+// Arrives on `routed` once the experts, their weight blocks and dispatch positions are in rt.
+__device__ void route_one(const LayerArgs& a, ORoute& rt, uint32_t tag, int lane, uint64_t* routed) {
     const uint64_t* l = a.dlog;
     uint32_t val[9];
     uint32_t need = 0;
@@ -260,18 +317,22 @@ __device__ void route_one(const LayerArgs& a, ORoute& rt, uint32_t tag, int lane
     float v0, myv;
     int mye;
     warp_topk(key, a.K, lane, v0, myv, mye);
-    const float ex = lane < a.K ? expf(myv - v0) : 0.f;
-    const float s = warp_sum(ex);
     // dispatch position of slot `lane`: the slots whose expert is lower (the K experts differ)
     int pos = 0;
     for (int j = 0; j < a.K; ++j) pos += __shfl_sync(0xffffffffu, mye, j) < mye;
     if (lane < a.K) {
         rt.ids[lane] = mye;
-        rt.w[lane] = ex / s;
         rt.inv[lane] = pos;
         rt.gu[lane] = a.gate_up + (size_t)mye * 2 * kOI * kOH;
         rt.dn[lane] = a.down + (size_t)mye * kOH * kOI;
     }
+    // the producer may issue the routed items now; the weights and the shared gate are read
+    // only after the consumers' barrier before the combine (and by this warp)
+    __syncwarp();
+    if (lane == 0) mbar_arrive(routed);
+    const float ex = lane < a.K ? expf(myv - v0) : 0.f;
+    const float s = warp_sum(ex);
+    if (lane < a.K) rt.w[lane] = ex / s;
     if (lane == 0) {
         const float z = router_score(__uint_as_float(val[8]), a.flags);
         if (!isfinite(z)) bad = true;
@@ -326,46 +387,69 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
     const int G = gridDim.x, c = blockIdx.x;
     const int K = a.K, nslot = g.nslot;
     uint32_t* err = &a.hdr->err;
+    // the kernel parameters the first steps read, fetched together: each first read of a
+    // parameter line misses the constant cache, and in the order of use the misses would come
+    // one after another
+    asm volatile("" ::"l"(a.router_w), "l"(a.sg), "l"(a.sgu), "l"(a.x), "l"(a.hdr), "l"(a.gate_up), "l"(a.down),
+                 "l"(a.dlog), "l"(a.dh), "r"(a.E), "r"(a.K), "r"(a.flags), "r"(g.nslot), "l"(a.wait_ns));
     const OPlan p = oplan(a, c, G);
+    grid_dep_launch();  // the next kernel may be scheduled as this one's CTAs finish
 
-    // ---- producer lane: barriers, then the token row and the router rows before anything else
-    int ps = 0;          // producer's slot cursor
+    // ---- producers: warp kOWarps + q issues items q, q + kOProducers, ... (a slot is always
+    // refilled by the same producer warp: kOProducers divides the slot count)
+    const int pw = warp - kOWarps;
+    uint8_t* issued = base + g.o_iss;  // items whose copies went out
+    bool pok = true;
+    int pj = pw, ps = pw;  // this producer's next item and its slot
     uint32_t pround = 0;
-    auto issue = [&](int kind, int k, int a_, int n, const void* src0, uint32_t b0, const void* src1, uint32_t b1) {
-        meta[ps] = OMeta{kind, k, a_, n};
+    // lane 0 of a producer warp: the next item of its share, once its slot is free (and, for
+    // the routed items, once the routing is known)
+    auto issue_next = [&](bool routed_known) -> bool {
+        if (!routed_known && pj >= p.nr + p.nsf) return false;
+        if (pround > 0 && !mbar_wait(&empty[ps], (pround - 1u) & 1u, a.wait_ns)) {
+            pok = false;
+            return false;
+        }
+        const OItem it = item_at(a, p, rt, c, G, pj);
+        meta[ps] = it.m;
         uint8_t* dst = slots + (size_t)ps * kOSlot;
-        mbar_arrive_expect_tx(&full[ps], b0 + b1);
-        bulk_load(dst, src0, b0, &full[ps]);
-        if (b1) bulk_load(dst + b0, src1, b1, &full[ps]);
-        if (++ps == nslot) {
-            ps = 0;
+        mbar_arrive_expect_tx(&full[ps], it.b0 + it.b1);
+        bulk_load(dst, it.src0, it.b0, &full[ps]);
+        if (it.b1) bulk_load(dst + it.b0, it.src1, it.b1, &full[ps]);
+        issued[pj] = 1;
+        pj += kOProducers;
+        ps += kOProducers;
+        if (ps >= nslot) {
+            ps -= nslot;
             ++pround;
         }
+        return true;
     };
-    // the next slot, once the consumers have released it (false after ~1 s)
-    auto slot_free = [&]() { return pround == 0 || mbar_wait(&empty[ps], (pround - 1u) & 1u, a.wait_ns); };
-    bool pok = true;
-    if (warp == kOProducer && lane == 0) {
-        for (int i = 0; i < nslot; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-        }
-        mbar_init(xbar, 1);
-        mbar_init(routed, 1);
+    if (pw >= 0) {
+        for (int i = pw * 32 + lane; i < 2 * nslot + 2; i += kOProducers * 32)
+            mbar_init(i < nslot ? &full[i] : i < 2 * nslot ? &empty[i - nslot] : i == 2 * nslot ? xbar : routed, 1);
+        for (int j = pw * 32 + lane; j < kOMaxItems; j += kOProducers * 32) issued[j] = 0;
         fence_mbar_init();
-        mbar_arrive_expect_tx(xbar, (uint32_t)(kOH * 2));
-        bulk_load(xs, a.x, (uint32_t)(kOH * 2), xbar);
-        for (int j = 0; j < p.nr && pok; ++j) {
-            const int row = c + j * G;
-            pok = slot_free();
-            if (pok) issue(kOkRouter, K, row, 1, row < a.E ? a.router_w + (size_t)row * kOH : a.sg, kOH * 2, nullptr, 0);
-        }
-        // the shared expert's features: no routing needed
-        for (int f = p.fs0; f < p.fs0 + p.nsf && pok; ++f) {
-            pok = slot_free();
-            if (pok) issue(kOkSharedUp, K, f, 1, a.sgu + (size_t)f * kOH, kOH * 2, a.sgu + (size_t)(kOI + f) * kOH, kOH * 2);
+        __syncwarp();
+        asm volatile("bar.sync 2, %0;" ::"n"(kOProducers * 32) : "memory");
+        if (lane == 0) {
+            // the router rows, then the shared expert's features: weights only, so they go out
+            // before the wait for the previous kernel below
+            while (pok && issue_next(false)) {
+            }
         }
     }
+    // Launched with programmatic serialization, the kernel may start while the previous one on
+    // the stream (the layer before, say, whose output is this token row) is still running:
+    // everything from here on waits for it to complete and for its memory to be visible.
+    grid_dep_wait();
+    if (pw == 0 && lane == 0) {
+        mbar_arrive_expect_tx(xbar, (uint32_t)(kOH * 2));
+        bulk_load(xs, a.x, (uint32_t)(kOH * 2), xbar);
+    }
+    // the residual of this CTA's output rows, read now: at the combine its latency would come
+    // last on the critical path (thread o < ro adds row o0 + o)
+    const float resid = (threadIdx.x < p.ro && a.residual) ? __bfloat162float(a.residual[p.o0 + threadIdx.x]) : 0.f;
     // this call's tags and the CTA starts of earlier calls (both advanced by CTA 0 of the
     // previous call)
     const uint32_t epoch = *(volatile uint32_t*)&a.hdr->dec_epoch;
@@ -376,43 +460,39 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
     const uint32_t tag16 = (tag - 1u) % 65535u + 1u;
     uint32_t* hw = reinterpret_cast<uint32_t*>(a.dh);  // [K + 1][I] tagged h words
 
-    if (warp == kOProducer) {
-        // ================= producer lane: the routed items once the routing is known
+    if (pw >= 0) {
+        // ================= producers: the routed items once the routing is known
         if (lane == 0) {
-            if (pok && !mbar_wait(routed, 0, a.wait_ns)) pok = false;
-            // routed (slot, feature) pairs [f0, f0 + nf): slot k = pair / I
-            for (int fi = p.f0; fi < p.f0 + p.nf && pok; ++fi) {
-                pok = slot_free();
-                if (!pok) break;
-                const int k = fi / kOI, f = fi - k * kOI;
-                const bf16* W = rt.gu[k];
-                issue(kOkUp, k, f, 1, W + (size_t)f * kOH, kOH * 2, W + (size_t)(kOI + f) * kOH, kOH * 2);
+            if (pok && pj < p.n && !mbar_wait(routed, 0, a.wait_ns)) pok = false;
+            while (pok && pj < p.n && issue_next(true)) {
             }
-            // down rows [o0, o0 + ro) in runs of kOMaxRo: the shared expert's, then each routed slot's
-            for (int kk = 0; kk <= K && pok; ++kk)
-                for (int r0 = p.o0; r0 < p.o0 + p.ro && pok; r0 += kOMaxRo) {
-                    const int n = min(kOMaxRo, p.o0 + p.ro - r0);
-                    pok = slot_free();
-                    if (!pok) break;
-                    const bf16* W = kk == 0 ? a.sd : rt.dn[kk - 1];
-                    issue(kk == 0 ? kOkSharedDown : kOkDown, kk == 0 ? K : kk - 1, r0, n, W + (size_t)r0 * kOI,
-                          (uint32_t)(n * kOI * 2), nullptr, 0);
-                }
             if (!pok) atomicOr(err, ERR_TIMEOUT);
-            // every copy issued must land before the CTA can exit
-            const int issued = (int)pround * nslot + ps;
-            for (int j = max(0, issued - nslot); j < issued; ++j)
-                if (!mbar_wait(&full[j % nslot], ((uint32_t)(j / nslot)) & 1u, a.wait_ns)) atomicOr(err, ERR_TIMEOUT);
-            if (!mbar_wait(xbar, 0, a.wait_ns)) atomicOr(err, ERR_TIMEOUT);
+        }
+        // every copy issued must land before the CTA can exit: the latest item of each slot
+        __syncwarp();
+        asm volatile("bar.sync 2, %0;" ::"n"(kOProducers * 32) : "memory");
+        // (lane l of producer 0 takes slot l and lane 31 the token row: a shared-memory
+        // operation waits behind the consumers' loads, so one pass over the slots, not one
+        // per item)
+        if (pw == 0) {
+            bool ok = true;
+            if (lane < nslot && lane < p.n) {
+                int j = lane + nslot * ((p.n - 1 - lane) / nslot);  // the slot's last item
+                while (j >= 0 && !issued[j]) j -= nslot;
+                if (j >= 0) ok = mbar_poll(&full[lane], ((uint32_t)(j / nslot)) & 1u, a.wait_ns);
+            } else if (lane == 31) {
+                ok = mbar_poll(xbar, 0, a.wait_ns);
+            }
+            if (!ok) atomicOr(err, ERR_TIMEOUT);
         }
         return;
     }
 
     // ================= consumers: warp w takes items w, w + 8, ...
-    float xr[kONch][8];
+    uint4 xr[kONch];  // this lane's chunks of x, packed bf16
     if (!warp_wait(xbar, 0, lane, a.wait_ns) && lane == 0) atomicOr(err, ERR_TIMEOUT);
 #pragma unroll
-    for (int q = 0; q < kONch; ++q) unpack8(lds128(smem_u32(xs) + 16u * (lane + 32 * q)), xr[q]);
+    for (int q = 0; q < kONch; ++q) xr[q] = lds128(smem_u32(xs) + 16u * (lane + 32 * q));
     const int up_end = p.n - (K + 1) * p.dpk;  // the down items come last
     int s = warp % nslot;
     uint32_t round = warp / nslot;
@@ -432,8 +512,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
             if (lane == 0 && !(a.test_suppress == MOE_TEST_SUPPRESS_SCORE && c == 1)) {
                 float sc = v[0];
                 if (m.a < a.E && a.router_b) sc += __bfloat162float(a.router_b[m.a]);
-                st_relaxed_u64(a.dlog + m.a, ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(sc));
-                __threadfence();  // a relaxed store alone can take microseconds to reach the other SMs
+                publish_u64(a.dlog + m.a, ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(sc));
             }
         } else if (m.kind == kOkSharedUp || m.kind == kOkUp) {
             // feature a: its gate row, then its up row
@@ -444,11 +523,10 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
                 const bf16 h = __float2bfloat16_rn(silu(v[0]) * v[1]);
                 const int row = m.kind == kOkSharedUp ? K : rt.inv[m.k];  // h tap: routed rows in dispatch order, then the shared row
                 a.h[(size_t)row * kOI + m.a] = h;
-                st_relaxed_u32(hw + (size_t)m.k * kOI + m.a, (tag16 << 16) | (uint32_t)__bfloat16_as_ushort(h));
-                if (m.kind == kOkUp && j + kOWarps >= up_end) __threadfence();  // this warp's last h word
+                publish_u32(hw + (size_t)m.k * kOI + m.a, (tag16 << 16) | (uint32_t)__bfloat16_as_ushort(h));
             }
         } else {
-            float hv[kOIch][8];
+            uint32_t hv[kOIch][8];  // tagged h words: the bf16 h in the low half
             if (!poll_h(hw + (size_t)m.k * kOI, tag16, hv, lane, a.wait_ns) && lane == 0) atomicOr(err, ERR_TIMEOUT);
             float acc[kOMaxRo];
 #pragma unroll
@@ -464,7 +542,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
                 for (int r = r0; r < r0 + 4; ++r) {
                     acc[r] = 0.f;
 #pragma unroll
-                    for (int q = 0; q < kOIch; ++q) acc[r] = dot8(w[r - r0][q], hv[q], acc[r]);
+                    for (int q = 0; q < kOIch; ++q) acc[r] = dot8_bf16_lo(w[r - r0][q], hv[q], acc[r]);
                 }
             }
 #pragma unroll
@@ -478,9 +556,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
         if (j == 0) {
             // warp 0 after its first item: the routing, then the producer may issue the
             // routed items
-            route_one(a, rt, tag, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(routed);
+            route_one(a, rt, tag, lane, routed);
             if (c == 0) write_routing(a, rt, lane);
         }
         s += kOWarps;
@@ -490,17 +566,15 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
         }
     }
     if (warp == 0 && p.n == 0) {  // no item at all: still route, so the producer is released
-        route_one(a, rt, tag, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(routed);
+        route_one(a, rt, tag, lane, routed);
         if (c == 0) write_routing(a, rt, lane);
     }
-    consumers_sync();  // every item's down outputs are in ys
+    asm volatile("bar.sync 1, %0;" ::"n"(kOWarps * 32) : "memory");  // every item's down outputs are in ys
     // residual + gated shared output + weighted slots 0..K-1, in that order
     const int tid = threadIdx.x;
     if (tid < p.ro) {
         const int o = p.o0 + tid;
-        float acc = a.residual ? __bfloat162float(a.residual[o]) : 0.f;
+        float acc = resid;
         const float sh = rt.sg * ys[K * kOMaxOut + tid];
         a.Y[(size_t)K * kOH + o] = sh;
         acc += sh;
@@ -527,11 +601,13 @@ static bool decode_geom(int cap, OGeom* g) {
     g->o_ys = o; o += (kOMaxK + 1) * kOMaxOut * 4;
     g->o_bar = o; o += (2 * kOMaxSlots + 2) * 8;
     g->o_meta = o; o += kOMaxSlots * (int)sizeof(OMeta);
+    g->o_iss = o; o += kOMaxItems;
     o = (o + 1023) & ~1023;
     g->o_slot = o;
     const int room = cap - 1024 - o;  // 1024: alignment of the dynamic base
     g->nslot = room / kOSlot < kOMaxSlots ? room / kOSlot : kOMaxSlots;
     g->smem = 1024 + o + g->nslot * kOSlot;
+    g->nslot -= g->nslot % kOProducers;
     return g->nslot >= kOWarps;
 }
 
@@ -565,7 +641,11 @@ bool decode_fused_supported(const LayerArgs& a) {
     // output rows per CTA within one down item; the items issued before the ring is shared
     // (router rows, shared features) within the ring
     const int G = a.num_sms;
-    if ((kOH + G - 1) / G > kOMaxOut || (a.E + G) / G + (kOI + G - 1) / G > kOWarps) return false;
+    const int ro = (kOH + G - 1) / G;
+    if (ro > kOMaxOut || (a.E + G) / G + (kOI + G - 1) / G > kOWarps) return false;
+    if ((a.E + G) / G + (kOI + G - 1) / G + (a.K * kOI + G - 1) / G + (a.K + 1) * ((ro + kOMaxRo - 1) / kOMaxRo) >
+        kOMaxItems)
+        return false;
     OGeom g;
     return decode_geom(dynamic_smem_cap(), &g);
 }
@@ -578,13 +658,27 @@ cudaError_t launch_decode_fused(const LayerArgs& a, cudaStream_t s) {
     cfg.blockDim = dim3(kOThreads);
     cfg.dynamicSmemBytes = (size_t)g.smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    // co-resident CTAs (they wait on one another), and programmatic serialization: the launch
+    // and each CTA's set-up overlap the end of the previous kernel (the kernel waits for it
+    // before it reads anything that kernel may write). A driver that refuses the pair gets the
+    // cooperative launch alone from then on.
+    static std::atomic<int> pdl_refused{0};
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_refused.load() ? 1 : 2;
     cudaError_t e;
     MOE_LAUNCH(MOE_KERNEL_DECODE_FUSED, s, (e = cudaLaunchKernelEx(&cfg, k_decode_fused, a, g)));
+    if (e != cudaSuccess && cfg.numAttrs == 2 && e != cudaErrorStreamCaptureInvalidated &&
+        e != cudaErrorStreamCaptureUnsupported) {
+        (void)cudaGetLastError();
+        pdl_refused.store(1);
+        cfg.numAttrs = 1;
+        MOE_LAUNCH(MOE_KERNEL_DECODE_FUSED, s, (e = cudaLaunchKernelEx(&cfg, k_decode_fused, a, g)));
+    }
     return e;
 }
 

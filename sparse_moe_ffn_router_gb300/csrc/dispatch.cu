@@ -21,6 +21,8 @@ constexpr int kLocalIds = kDispatchTokens * 8 / 32;  // expert ids per lane of a
 
 __global__ void __launch_bounds__(32) k_dispatch_local(LayerArgs a) {
     __shared__ int cnt[256];
+    grid_dep_wait();  // the top-K's expert ids
+    grid_dep_launch();
     const int lane = threadIdx.x, b = blockIdx.x;
     for (int e = lane; e < a.E; e += 32) cnt[e] = 0;
     const int64_t p0 = (int64_t)b * kDispatchTokens * a.K;
@@ -110,6 +112,8 @@ __global__ void __launch_bounds__(256 * kScanParts) k_dispatch_scan(LayerArgs a,
     __shared__ int off[257];
     __shared__ int sact[256];
     __shared__ int n_act_s;
+    grid_dep_wait();  // the block counts of the local pass
+    grid_dep_launch();
     // thread (q, e) takes blocks [q*nb/4, (q+1)*nb/4) of expert e: its counts in one round of
     // loads (up to kScanRegs of them kept for the bases), then their sum
     const int e = threadIdx.x & 255, q = threadIdx.x >> 8;
@@ -192,6 +196,8 @@ __global__ void __launch_bounds__(256 * kScanParts) k_dispatch_scan(LayerArgs a,
 }
 
 __global__ void __launch_bounds__(256) k_dispatch_scatter(LayerArgs a) {
+    grid_dep_wait();  // the bases of the scan
+    grid_dep_launch();
     const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
     if (i >= a.P) return;
     const int t = (int)(i / a.K);
@@ -206,6 +212,8 @@ __global__ void __launch_bounds__(256) k_dispatch_scatter(LayerArgs a) {
 // position j, then xperm[j] = x[t] (the token rows in dispatch order, 16 bytes per lane per
 // step).
 __global__ void __launch_bounds__(256) k_dispatch_scatter_rows(LayerArgs a) {
+    grid_dep_wait();  // the bases of the scan
+    grid_dep_launch();
     const int64_t i = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (i >= a.P) return;
@@ -224,15 +232,19 @@ __global__ void __launch_bounds__(256) k_dispatch_scatter_rows(LayerArgs a) {
 
 cudaError_t launch_dispatch(const LayerArgs& a, bool with_rows, cudaStream_t s) {
     const int fh = gemm_up_half(a), bn_dn = gemm_down_bn(a);
-    MOE_LAUNCH(MOE_KERNEL_DISPATCH_LOCAL, s, (k_dispatch_local<<<a.nb, 32, 0, s>>>(a)));
-    MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCAN, s, (k_dispatch_scan<<<1, 256 * kScanParts, 0, s>>>(a, fh, bn_dn)));
+    cudaError_t e;
+    MOE_LAUNCH(MOE_KERNEL_DISPATCH_LOCAL, s, (e = launch_pdl(k_dispatch_local, dim3(a.nb), dim3(32), 0, s, a)));
+    if (e != cudaSuccess) return e;
+    MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCAN, s,
+               (e = launch_pdl(k_dispatch_scan, dim3(1), dim3(256 * kScanParts), 0, s, a, fh, bn_dn)));
+    if (e != cudaSuccess) return e;
     if (a.gemm && with_rows)
         MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCATTER, s,
-                   (k_dispatch_scatter_rows<<<(unsigned)((a.P + 7) / 8), 256, 0, s>>>(a)));
+                   (e = launch_pdl(k_dispatch_scatter_rows, dim3((unsigned)((a.P + 7) / 8)), dim3(256), 0, s, a)));
     else
         MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCATTER, s,
-                   (k_dispatch_scatter<<<(unsigned)((a.P + 255) / 256), 256, 0, s>>>(a)));
-    return cudaGetLastError();
+                   (e = launch_pdl(k_dispatch_scatter, dim3((unsigned)((a.P + 255) / 256)), dim3(256), 0, s, a)));
+    return e;
 }
 
 }  // namespace moe

@@ -190,7 +190,8 @@ __device__ __forceinline__ float4 load4(const bf16* p) {
 template <typename YT>
 __global__ void __launch_bounds__(256) k_combine(LayerArgs a, const YT* Y) {
     // no-op unless launched as a programmatic dependent: then wait for the producer of Y
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    grid_dep_wait();
+    grid_dep_launch();
     const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
     const int q = a.H / 4;
     if (i >= (int64_t)a.T * q) return;
@@ -240,11 +241,15 @@ cudaError_t launch_combine_pdl(const LayerArgs& a, cudaStream_t s) {
 cudaError_t launch_combine(const LayerArgs& a, cudaStream_t s) {
     const int64_t nq = (int64_t)a.T * (a.H / 4);
     const unsigned grid = (unsigned)((nq + 255) / 256);
-    if (a.gemm)
-        MOE_LAUNCH(MOE_KERNEL_COMBINE, s, (k_combine<bf16><<<grid, 256, 0, s>>>(a, a.Yb)));
-    else
+    cudaError_t e;
+    if (a.gemm) {
+        const bf16* Y = a.Yb;
+        MOE_LAUNCH(MOE_KERNEL_COMBINE, s, (e = launch_pdl(k_combine<bf16>, dim3(grid), dim3(256), 0, s, a, Y)));
+    } else {
         MOE_LAUNCH(MOE_KERNEL_COMBINE, s, (k_combine<float><<<grid, 256, 0, s>>>(a, a.Y)));
-    return cudaGetLastError();
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 }  // namespace moe

@@ -92,7 +92,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int total = p.dense_rows > 0 ? p.dense_tiles : p.tile_start[*p.n_groups];
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -119,6 +118,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // the set-up above overlaps the previous kernel's tail; the tables, token rows and h it
+    // reads are that kernel's (or an earlier one's) outputs
+    grid_dep_wait();
+    grid_dep_launch();
+    const int total = p.dense_rows > 0 ? p.dense_tiles : p.tile_start[*p.n_groups];
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer
@@ -357,8 +361,8 @@ cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, const CUte
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    k_gemm<EPI, BN><<<grid, kThreads, GemmSmem<BN>::kBytes, s>>>(A0, A1, B0, B1, p, a);
-    return cudaGetLastError();
+    return launch_pdl(k_gemm<EPI, BN>, dim3(grid), dim3(kThreads), (size_t)GemmSmem<BN>::kBytes, s, A0, A1, B0, B1, p,
+                      a);
 }
 
 }  // namespace

@@ -71,6 +71,23 @@ void trace_end(int kernel, cudaStream_t s);
 inline int gemm_up_half(const LayerArgs& a) { return (a.I % 128 == 0 && a.Is % 128 == 0) ? 128 : 64; }
 inline int gemm_down_bn(const LayerArgs& a) { return (a.H % 256 == 0) ? 256 : 128; }
 
+// Launch as a programmatic dependent of the previous kernel on the stream: the kernel may
+// start while that one runs and must execute grid_dep_wait before touching its outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 struct GemmPlan {
     const GemmGroup* groups;
     const int32_t* tile_start;

@@ -15,8 +15,9 @@
 //   arrive in about one memory latency, where a few CTAs streaming the whole matrix were held
 //   to the per-SM copy rate.
 // k_route_small: ceil(T/8) CTAs of 1024 threads. Warp w of CTA c takes token 8c + w: top-K
-//   (warp_topk: K rounds of a warp max over order-preserving score keys and, among equal keys,
-//   a warp min over expert indices), the renormalised weights and the shared gate. The last
+//   (warp_topk: each lane sorts its order-preserving score keys, then K rounds of a warp max
+//   over the lanes' largest remaining keys and, among equal keys, a warp min over expert
+//   indices), the renormalised weights and the shared gate. The last
 //   CTA to finish (a ticket counter in the workspace header, re-armed by that CTA) runs the
 //   dispatch: one stable counting sort of the T*K (token, slot) pairs in chunks of 1024;
 //   within a warp, pairs of one expert are ranked by lane (match_any), across the warps of a

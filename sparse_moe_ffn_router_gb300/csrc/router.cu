@@ -19,6 +19,8 @@ constexpr int kRouterTokens = 8;  // tokens per warp in the fused routing kernel
 // weight p_k / sum_sel p_j equals exp(l_k - l_0) / sum_sel exp(l_j - l_0) (the full
 // softmax denominator cancels), which is what is computed.
 __global__ void __launch_bounds__(256) k_router_topk(LayerArgs a) {
+    grid_dep_wait();  // the scores of the router GEMM
+    grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= a.T) return;
@@ -70,8 +72,8 @@ cudaError_t launch_router(const LayerArgs& a, cudaStream_t s) {
     if (!a.gemm) return cudaErrorNotSupported;
     cudaError_t e = launch_router_gemm(a, s);
     if (e != cudaSuccess) return e;
-    MOE_LAUNCH(MOE_KERNEL_ROUTER_TOPK, s, (k_router_topk<<<(a.T + 7) / 8, 256, 0, s>>>(a)));
-    return cudaGetLastError();
+    MOE_LAUNCH(MOE_KERNEL_ROUTER_TOPK, s, (e = launch_pdl(k_router_topk, dim3((a.T + 7) / 8), dim3(256), 0, s, a)));
+    return e;
 }
 
 // RMSNorm, one CTA per token row: fp32 sum of squares in a fixed order, 1/sqrt, scale, bf16.

@@ -53,6 +53,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of a phase (the thread is never suspended).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// As mbar_wait, polling with test_wait: for a thread that must notice a completed phase at
+// once rather than sleep in try_wait.
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity, uint64_t limit = kWaitNs) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit) return false;
+    }
+}
+
 // Wait for the phase with the given parity to complete; false once `limit` ns have passed
 // (timeout).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit = kWaitNs) {
