@@ -272,9 +272,9 @@ def algorithmic(dims, groups: list[int]) -> dict:
     Method bytes: gate_up reads each touched expert's [2I, H] block and the shared [2Is, H]
     once, x once, and writes h; down reads each touched [H, I] block and the shared [H, Is]
     once and reads h; the layer adds the router [E+1, H], x and out. Implementation bytes:
-    from 256 tokens gate_up reads the token rows in dispatch order (written by the dispatch
-    scatter) instead of x, and down writes Y (bf16 from 256 tokens, fp32 below) for the
-    fixed-order combine, which reads it back."""
+    down writes Y (bf16 from 256 tokens, fp32 below) for the fixed-order combine, which reads
+    it back (the gate_up GEMM gathers its token rows from x, which stays in L2 across the K
+    experts that read a row)."""
     T, H, E, K, I, Is = dims[:6]
     P = T * K
     n = len(groups)
@@ -285,7 +285,7 @@ def algorithmic(dims, groups: list[int]) -> dict:
     router = 2 * (E + 1) * H + 2 * T * H
     layer_bytes = 2 * ((E + 1) * H + n * 3 * I * H + 3 * Is * H) + 2 * 2 * T * H
     flops = 2 * T * (E + 1) * H + 2 * P * 3 * I * H + 2 * T * 3 * Is * H
-    impl_gate_up = gate_up + (2 * P * H if T >= 256 else 0)
+    impl_gate_up = gate_up
     impl_down = down + ysz * (P + T) * H
     combine = ysz * (P + T) * H + 2 * T * H
     return dict(gate_up=gate_up, down=down, router_scores=router, decode_fused=layer_bytes, layer=layer_bytes,

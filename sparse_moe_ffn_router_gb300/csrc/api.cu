@@ -114,7 +114,6 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
     a->lr = (int32_t*)(base + p->o_lr);
     a->cntb = (int32_t*)(base + p->o_cntb);
     a->base = (int32_t*)(base + p->o_base);
-    a->xperm = p->gemm ? (bf16*)(base + p->o_xperm) : nullptr;
     a->act = (int32_t*)(base + p->o_act);
     a->h = (bf16*)(base + p->o_h);
     a->Y = (float*)(base + p->o_y);
@@ -211,12 +210,12 @@ bool host_side(const void* p) {
     return t == cudaMemoryTypeHost || t == cudaMemoryTypeUnregistered;
 }
 
-// experts: the experts run next (from T >= 256 the dispatch then also lays out their token rows)
-cudaError_t launch_routing(const LayerArgs& a, bool experts, cudaStream_t s) {
+// Routing: scores, top-K and the dispatch tables.
+cudaError_t launch_routing(const LayerArgs& a, cudaStream_t s) {
     if (route_cluster_supported(a)) return launch_route_cluster(a, s);
     if (route_small_supported(a)) return launch_route_small(a, s);
     cudaError_t e = launch_router(a, s);
-    if (e == cudaSuccess) e = launch_dispatch(a, experts, s);
+    if (e == cudaSuccess) e = launch_dispatch(a, s);
     return e;
 }
 
@@ -241,7 +240,7 @@ cudaError_t launch_after_routing(const LayerArgs& a, cudaStream_t s) {
 // layer: T=2 37.7 vs 44.7 us, T=4 55.8 vs 85.7 us, T=8 84.8 vs 168.3 us).
 cudaError_t launch_layer(const LayerArgs& a, cudaStream_t s) {
     if (a.T <= kFusedMaxTokens && decode_fused_supported(a)) return launch_decode_fused(a, s);
-    cudaError_t e = launch_routing(a, true, s);
+    cudaError_t e = launch_routing(a, s);
     if (e == cudaSuccess) e = launch_after_routing(a, s);
     return e;
 }
@@ -281,7 +280,7 @@ extern "C" moe_status moe_route(const moe_dims* d, const void* x, const moe_weig
     a.counts = counts;
     a.offsets = offsets;
     a.perm = perm;
-    return cuda_status(launch_routing(a, false, s));
+    return cuda_status(launch_routing(a, s));
 }
 
 extern "C" moe_status moe_router_stats(const moe_dims* d, const void* x, const moe_weights* w, float* P, float* f,
@@ -385,7 +384,7 @@ extern "C" moe_status moe_forward_host_experts(const moe_dims* d, const void* x,
     bf16* sgu = (bf16*)shadow;
     bf16* sdn = sgu + (size_t)d->E * 2 * d->I * d->H;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = launch_routing(a, true, s);
+    cudaError_t e = launch_routing(a, s);
     if (e == cudaSuccess) e = launch_fetch_experts(a, (const bf16*)hgu, (const bf16*)hdn, sgu, sdn, s);
     a.gate_up = sgu;
     a.down = sdn;

@@ -70,7 +70,7 @@ struct Plan {
     int nb;          // token blocks of the dispatch
     bool gemm;       // many-token path (tensor-core GEMMs, bf16 Y) instead of weight streaming
     size_t o_hdr, o_logits, o_ids, o_topw, o_sgate, o_counts, o_offsets, o_perm, o_inv, o_lr, o_cntb, o_base,
-        o_act, o_h, o_y, o_xperm, o_upg, o_dng, o_upt, o_dnt, o_uprec, o_dlog, o_dh, total;
+        o_act, o_h, o_y, o_upg, o_dng, o_upt, o_dnt, o_uprec, o_dlog, o_dh, total;
 };
 
 constexpr int kStatsTokens = 32;     // tokens per block of the load-balancing statistics
@@ -111,7 +111,6 @@ inline bool make_plan(const moe_dims& d, Plan* p) {
     const size_t ybytes = T * (d.K + 1) * d.H * (p->gemm ? 2 : 4);
     const size_t sbytes = (size_t)((d.T + kStatsTokens - 1) / kStatsTokens) * d.E * 8;
     p->o_y = take(ybytes > sbytes ? ybytes : sbytes);
-    p->o_xperm = take(p->gemm ? P * d.H * 2 : 0);
     p->o_upg = take((size_t)(d.E + 1) * sizeof(GemmGroup));
     p->o_dng = take((size_t)(d.E + 1) * sizeof(GemmGroup));
     p->o_upt = take((size_t)(d.E + 2) * 4);

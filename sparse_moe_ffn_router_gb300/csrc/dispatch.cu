@@ -10,9 +10,8 @@
 //   2. one CTA: per-expert totals, the exclusive scan (one warp, shuffles), each (block,
 //      expert) base, the list of experts that received pairs and, on the tensor-core path,
 //      the grouped GEMMs' group and tile tables;
-//   3. scatter: perm[base[block, e] + rank] = p, inv[p] = that position; on the tensor-core
-//      path the same kernel copies each pair's token row to that position of xperm, the
-//      A operand of the grouped gate_up GEMM.
+//   3. scatter: perm[base[block, e] + rank] = p, inv[p] = that position (the grouped gate_up
+//      GEMM gathers its A rows from x through perm).
 #include "launch.h"
 
 namespace moe {
@@ -208,29 +207,7 @@ __global__ void __launch_bounds__(256) k_dispatch_scatter(LayerArgs a) {
     a.inv[i] = j;
 }
 
-// Tensor-core path: the scatter with the gate_up GEMM's A operand, one warp per pair: its
-// position j, then xperm[j] = x[t] (the token rows in dispatch order, 16 bytes per lane per
-// step).
-__global__ void __launch_bounds__(256) k_dispatch_scatter_rows(LayerArgs a) {
-    grid_dep_wait();  // the bases of the scan
-    grid_dep_launch();
-    const int64_t i = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (i >= a.P) return;
-    const int t = (int)(i / a.K);
-    const int b = t / kDispatchTokens;
-    const int e = a.ids[i];
-    const int j = a.base[(size_t)b * a.E + e] + a.lr[i];
-    if (lane == 0) {
-        a.perm[j] = (int)i;
-        a.inv[i] = j;
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H);
-    uint4* dst = reinterpret_cast<uint4*>(a.xperm + (size_t)j * a.H);
-    for (int c = lane; c < a.H / 8; c += 32) dst[c] = ld_ro(src + c);
-}
-
-cudaError_t launch_dispatch(const LayerArgs& a, bool with_rows, cudaStream_t s) {
+cudaError_t launch_dispatch(const LayerArgs& a, cudaStream_t s) {
     const int fh = gemm_up_half(a), bn_dn = gemm_down_bn(a);
     cudaError_t e;
     MOE_LAUNCH(MOE_KERNEL_DISPATCH_LOCAL, s, (e = launch_pdl(k_dispatch_local, dim3(a.nb), dim3(32), 0, s, a)));
@@ -238,12 +215,8 @@ cudaError_t launch_dispatch(const LayerArgs& a, bool with_rows, cudaStream_t s) 
     MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCAN, s,
                (e = launch_pdl(k_dispatch_scan, dim3(1), dim3(256 * kScanParts), 0, s, a, fh, bn_dn)));
     if (e != cudaSuccess) return e;
-    if (a.gemm && with_rows)
-        MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCATTER, s,
-                   (e = launch_pdl(k_dispatch_scatter_rows, dim3((unsigned)((a.P + 7) / 8)), dim3(256), 0, s, a)));
-    else
-        MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCATTER, s,
-                   (e = launch_pdl(k_dispatch_scatter, dim3((unsigned)((a.P + 255) / 256)), dim3(256), 0, s, a)));
+    MOE_LAUNCH(MOE_KERNEL_DISPATCH_SCATTER, s,
+               (e = launch_pdl(k_dispatch_scatter, dim3((unsigned)((a.P + 255) / 256)), dim3(256), 0, s, a)));
     return e;
 }
 

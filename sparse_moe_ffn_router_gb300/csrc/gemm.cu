@@ -18,14 +18,24 @@
 //   warp 0    TMA producer (one lane): A and B tiles into a 4-stage shared-memory ring;
 //   warp 1    TMEM owner and MMA issuer (one lane): 128 x BN x 16 tcgen05.mma steps into one
 //             of two TMEM accumulators, tcgen05.commit frees ring stages / publishes tiles;
-//   warps 2-5 epilogue: tcgen05.ld of the accumulator (warp w reads lanes 32*(w%4)..+31).
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator (warp w reads lanes 32*(w%4)..+31);
+//   warps 6-7 (gate_up only) A gatherers: a routed expert's A rows are token rows of x, row
+//             perm[j] / K for dispatch position j. Each k-block's 128-byte segment of a row is
+//             copied by 8 lanes, 16 bytes each with cp.async (a warp instruction moves 4 rows),
+//             straight from x into the A stage, in the 128-byte swizzled layout the tensor map
+//             would give (16-byte chunk c of row r at r * 128 + (c ^ (r % 8)) * 16); rows past
+//             the group's end are zero-filled. x rows are kept in L2 (evict-last) across the K
+//             experts that read them, and no dispatched copy of x is written or read. The
+//             shared expert's A rows are x itself, loaded by TMA.
 #include "launch.h"
 #include "sm100.cuh"
 
 namespace moe {
 
 constexpr int kBM = 128, kBK = 64;
-constexpr int kThreads = 192;
+constexpr int kGatherWarps = 2;
+template <int EPI>
+constexpr int gemm_threads() { return EPI == 1 ? 192 + 32 * kGatherWarps : 192; }
 constexpr uint32_t kAStage = kBM * kBK * 2;
 
 enum { kLogits = 0, kSwiGLU = 1, kScaleY = 2 };
@@ -37,6 +47,9 @@ struct GemmSmem {
     static constexpr int kStages = (int)((192u * 1024u) / (kAStage + kBStage));
     static constexpr uint32_t kTiles = kStages * (kAStage + kBStage);
     static constexpr uint32_t kBytes = 1024 + kTiles + 256;  // alignment slack + tiles + barriers
+    // full, empty and gathered-A barriers per stage, two accumulators' full and empty, the
+    // MMA-done barrier, the TMEM address and the abort flag
+    static_assert((3 * kStages + 5) * 8 + 8 <= 256, "barrier area");
 };
 
 __device__ __forceinline__ void flag_timeout(uint32_t* err, volatile int* abort_flag) {
@@ -72,7 +85,7 @@ __device__ __forceinline__ bool find_tile(const GemmPlan& p, int t, int& g, Tile
 }
 
 template <int EPI, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
            const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1, const GemmPlan p,
            const LayerArgs a) {
@@ -88,7 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* accf = bars + 2 * kStages;
     uint64_t* acce = accf + 2;
     uint64_t* mma_done = acce + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* fullA = mma_done + 1;  // gathered A stages (gate_up)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullA + kStages);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -103,6 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&acce[b], 4);
         }
         mbar_init(mma_done, 1);
+        if (EPI == kSwiGLU)
+            for (int s = 0; s < kStages; ++s) mbar_init(&fullA[s], 32 * kGatherWarps);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA0);
@@ -143,8 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     flag_timeout(p.err, abort_flag);
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], kAStage + GemmSmem<BN>::kBStage);
-                tma_load_2d(sA + s * kAStage, mA, &full[s], kb * kBK, ti.a_row + ti.m0);
+                const bool gathered = EPI == kSwiGLU && !ti.src;  // A comes from the gatherers
+                mbar_arrive_expect_tx(&full[s], (gathered ? 0u : kAStage) + GemmSmem<BN>::kBStage);
+                if (!gathered) tma_load_2d(sA + s * kAStage, mA, &full[s], kb * kBK, ti.a_row + ti.m0);
                 if (EPI == kSwiGLU) {
                     const int fh = BN / 2;
                     const int half = ti.src ? p.up_off_shared : p.up_off_routed;
@@ -180,11 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < ti.kb; ++kb, ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                if (!mbar_wait(&full[s], ph)) {
+                if (!mbar_wait(&full[s], ph) || (EPI == kSwiGLU && !mbar_wait(&fullA[s], ph))) {
                     flag_timeout(p.err, abort_flag);
                     ok = false;
                     break;
                 }
+                // the gathered rows were written through the generic proxy; the tensor cores
+                // read them through the async proxy
+                if (EPI == kSwiGLU) fence_proxy_async_smem();
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(sA + s * kAStage);
                 const uint32_t b_addr = smem_u32(sB + s * GemmSmem<BN>::kBStage);
@@ -199,7 +219,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(mma_done);
         if (!mbar_wait(mma_done, 0)) flag_timeout(p.err, abort_flag);
-    } else if (warp >= 2) {
+    } else if (EPI == kSwiGLU && warp >= 6) {
+        // ---------------- A gatherers: warp w (0, 1) takes rows 64w + 4i + lane / 8, i < 16,
+        // chunk lane % 8 of each
+        constexpr int kRows = kBM / (4 * kGatherWarps);  // rows per lane
+        const int r0 = (warp - 6) * (kBM / kGatherWarps) + (lane >> 3);
+        const uint32_t c = (uint32_t)(lane & 7);
+        const uint64_t pol_a = l2_evict_last();  // each token row is read by K experts
+        int g = 0, it = 0;
+        for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+            TileInfo ti;
+            if (!find_tile(p, t, g, ti)) break;
+            const bf16* src[kRows];
+            uint32_t live = 0;
+#pragma unroll
+            for (int i = 0; i < kRows; ++i) {
+                const int m = ti.m0 + r0 + 4 * i;
+                src[i] = a.x + c * 8;
+                if (!ti.src && m < ti.rows) {
+                    src[i] += (size_t)(a.perm[ti.a_row + m] / a.K) * a.H;
+                    live |= 1u << i;
+                }
+            }
+            bool ok = true;
+            for (int kb = 0; kb < ti.kb; ++kb, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                // lane 0 waits for the stage to be free, the warp follows its verdict
+                bool fr = lane == 0 ? mbar_wait(&empty[s], ph ^ 1u) : true;
+                fr = __shfl_sync(0xffffffffu, fr, 0);
+                if (!fr) {
+                    if (lane == 0) flag_timeout(p.err, abort_flag);
+                    ok = false;
+                    break;
+                }
+                if (!ti.src) {
+                    const uint32_t st = smem_u32(sA + s * kAStage);
+#pragma unroll
+                    for (int i = 0; i < kRows; ++i) {
+                        const uint32_t r = (uint32_t)(r0 + 4 * i);
+                        cp_async16(st + r * 128u + ((c ^ (r & 7u)) << 4), src[i] + kb * kBK, ((live >> i) & 1u) * 16u,
+                                   pol_a);
+                    }
+                    cp_async_arrive(&fullA[s]);
+                } else {
+                    mbar_arrive(&fullA[s]);  // the shared expert's A stage comes by TMA
+                }
+            }
+            if (!ok) break;
+        }
+        cp_async_wait_all();  // no copy of this CTA may still be in flight when it exits
+    } else if (warp >= 2 && warp < 6) {
         // ---------------- epilogue: TMEM lanes 32*(warp%4) .. +31, one accumulator row each
         const int q = warp & 3;
         const int r = q * 32 + lane;
@@ -361,8 +431,8 @@ cudaError_t launch_gemm(const CUtensorMap& A0, const CUtensorMap& A1, const CUte
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    return launch_pdl(k_gemm<EPI, BN>, dim3(grid), dim3(kThreads), (size_t)GemmSmem<BN>::kBytes, s, A0, A1, B0, B1, p,
-                      a);
+    return launch_pdl(k_gemm<EPI, BN>, dim3(grid), dim3(gemm_threads<EPI>()), (size_t)GemmSmem<BN>::kBytes, s, A0,
+                      A1, B0, B1, p, a);
 }
 
 }  // namespace
@@ -389,8 +459,8 @@ cudaError_t launch_router_gemm(const LayerArgs& a, cudaStream_t s) {
 // Expert GEMMs over the dispatched groups (routed experts + the shared expert).
 cudaError_t launch_expert_gemms(const LayerArgs& a, cudaStream_t s) {
     const int fh = gemm_up_half(a);
-    CUtensorMap mxp, mx, mgu, msgu, mh, mdn, msd;
-    bool ok = make_map(&mxp, a.xperm, a.P, a.H, a.H, kBM) && make_map(&mx, a.x, a.T, a.H, a.H, kBM) &&
+    CUtensorMap mx, mgu, msgu, mh, mdn, msd;
+    bool ok = make_map(&mx, a.x, a.T, a.H, a.H, kBM) &&
               make_map(&mgu, a.gate_up, (uint64_t)a.E * 2 * a.I, a.H, a.H, fh) &&
               make_map(&msgu, a.sgu, (uint64_t)2 * a.Is, a.H, a.H, fh) &&
               make_map(&mh, a.h, a.P + a.T, a.Imax, a.Imax, kBM);
@@ -409,9 +479,9 @@ cudaError_t launch_expert_gemms(const LayerArgs& a, cudaStream_t s) {
     pu.err = &a.hdr->err;
     cudaError_t e;
     if (fh == 128)
-        MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (e = launch_gemm<kSwiGLU, 256>(mxp, mx, mgu, msgu, pu, a, grid, s)));
+        MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (e = launch_gemm<kSwiGLU, 256>(mx, mx, mgu, msgu, pu, a, grid, s)));
     else
-        MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (e = launch_gemm<kSwiGLU, 128>(mxp, mx, mgu, msgu, pu, a, grid, s)));
+        MOE_LAUNCH(MOE_KERNEL_GATE_UP, s, (e = launch_gemm<kSwiGLU, 128>(mx, mx, mgu, msgu, pu, a, grid, s)));
     if (e != cudaSuccess) return e;
     GemmPlan pd{};
     pd.groups = a.dn_groups;

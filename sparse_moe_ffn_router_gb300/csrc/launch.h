@@ -30,7 +30,6 @@ struct LayerArgs {
     int32_t* cntb;    // [nb, E] pairs per expert per token block
     int32_t* base;    // [nb, E] first perm position of each (block, expert)
     int32_t* act;     // experts with pairs, ascending; count in hdr->n_act
-    bf16* xperm;      // [P, H] x rows in dispatch order (tensor-core path)
     bf16* h;          // [P + T, Imax] gated activations
     float* Y;         // [T, K+1, H] weighted expert outputs, slot K = shared expert (fp32 path)
     bf16* Yb;         // the same in bf16 (tensor-core path)
@@ -117,8 +116,7 @@ bool stream_supported(const LayerArgs& a);
 bool decode_fused_supported(const LayerArgs& a);
 cudaError_t launch_decode_fused(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_stream_experts(const LayerArgs& a, cudaStream_t s);
-// with_rows: also copy each pair's token row into xperm (the gate_up GEMM's A operand)
-cudaError_t launch_dispatch(const LayerArgs& a, bool with_rows, cudaStream_t s);
+cudaError_t launch_dispatch(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_experts(const LayerArgs& a, cudaStream_t s);
 cudaError_t launch_rmsnorm(const bf16* x, const bf16* gamma, float eps, bf16* xn, int T, int H, cudaStream_t s);
 
