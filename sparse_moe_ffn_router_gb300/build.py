@@ -35,16 +35,24 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Build the library if any source is newer than it; return its path."""
+LIB_TIMELINE = os.path.join(BUILD, "libmoe_gb300_timeline.so")
+
+
+def build(force: bool = False, verbose: bool = False, timeline: bool = False) -> str:
+    """Build the library if any source is newer than it; return its path. timeline=True builds
+    the variant whose one-token kernel records its in-kernel timeline (MOE_TIMELINE), for
+    `python -m sparse_moe_ffn_router_gb300.timeline`."""
     os.makedirs(BUILD, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
+    lib = LIB_TIMELINE if timeline else LIB
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime():
+        return lib
     nvcc = _nvcc()
+    extra = ["-DMOE_TIMELINE"] if timeline else []
+    suffix = "_tl.o" if timeline else ".o"
 
     def compile_one(src: str):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(BUILD, src.replace(".cu", suffix))
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
@@ -52,18 +60,18 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         results = list(ex.map(compile_one, SOURCES))
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+    with open(os.path.join(BUILD, "ptxas_timeline.log" if timeline else "ptxas.log"), "w") as f:
         for (_, log), src in zip(results, SOURCES):
             f.write(f"==== {src}\n{log}\n")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        print(f"built {LIB}", file=sys.stderr)
-    return LIB
+        print(f"built {lib}", file=sys.stderr)
+    return lib
 
 
 if __name__ == "__main__":

@@ -42,6 +42,26 @@
 
 namespace moe {
 
+// In-kernel timeline (a build with MOE_TIMELINE only): the global timer at fixed points of each
+// CTA's call, read back with moe_timeline_read. Event e of CTA c is g_moe_tl[c * kTlEvents + e]:
+//   0 CTA start                          5 warp 0: every CTA's router scores seen
+//   1 producer 0: weight-only items out  6 warp 0: routing known, producer released
+//   2 producer 0: previous kernel done   7 producer 0: every item issued
+//   3 consumers: token row in shared     8 consumers: every item done (combine starts)
+//   4 a router score published          9 combine done
+constexpr int kTlEvents = 10, kTlCtas = 256;
+#ifdef MOE_TIMELINE
+__device__ unsigned long long g_moe_tl[kTlCtas * kTlEvents];
+#define MOE_TL(ev)                                                                     \
+    do {                                                                               \
+        if (blockIdx.x < kTlCtas) g_moe_tl[blockIdx.x * kTlEvents + (ev)] = global_ns(); \
+    } while (0)
+#else
+#define MOE_TL(ev) \
+    do {           \
+    } while (0)
+#endif
+
 constexpr int kOWarps = 8;                     // consumer warps
 constexpr int kOProducers = 4;                 // producer warps (lane 0 of each issues copies)
 constexpr int kOThreads = (kOWarps + kOProducers) * 32;
@@ -293,7 +313,10 @@ __device__ void route_one(const LayerArgs& a, ORoute& rt, uint32_t tag, int lane
                 still &= ~(1u << j);
             }
         need = still;
-        if (!__any_sync(0xffffffffu, need != 0)) break;
+        if (!__any_sync(0xffffffffu, need != 0)) {
+            if (lane == 0) MOE_TL(5);
+            break;
+        }
         if (global_ns() - t0 > a.wait_ns) {
             timed_out = true;
             break;
@@ -329,7 +352,10 @@ __device__ void route_one(const LayerArgs& a, ORoute& rt, uint32_t tag, int lane
     // the producer may issue the routed items now; the weights and the shared gate are read
     // only after the consumers' barrier before the combine (and by this warp)
     __syncwarp();
-    if (lane == 0) mbar_arrive(routed);
+    if (lane == 0) {
+        MOE_TL(6);
+        mbar_arrive(routed);
+    }
     const float ex = lane < a.K ? expf(myv - v0) : 0.f;
     const float s = warp_sum(ex);
     if (lane < a.K) rt.w[lane] = ex / s;
@@ -386,6 +412,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
     const int K = a.K, nslot = g.nslot;
+    if (threadIdx.x == 0) MOE_TL(0);
     uint32_t* err = &a.hdr->err;
     // the kernel parameters the first steps read, fetched together: each first read of a
     // parameter line misses the constant cache, and in the order of use the misses would come
@@ -437,6 +464,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
             // before the wait for the previous kernel below
             while (pok && issue_next(false)) {
             }
+            if (pw == 0) MOE_TL(1);
         }
     }
     // Launched with programmatic serialization, the kernel may start while the previous one on
@@ -444,6 +472,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
     // everything from here on waits for it to complete and for its memory to be visible.
     grid_dep_wait();
     if (pw == 0 && lane == 0) {
+        MOE_TL(2);
         mbar_arrive_expect_tx(xbar, (uint32_t)(kOH * 2));
         bulk_load(xs, a.x, (uint32_t)(kOH * 2), xbar);
     }
@@ -467,6 +496,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
             while (pok && pj < p.n && issue_next(true)) {
             }
             if (!pok) atomicOr(err, ERR_TIMEOUT);
+            if (pw == 0) MOE_TL(7);
         }
         // every copy issued must land before the CTA can exit: the latest item of each slot
         __syncwarp();
@@ -491,6 +521,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
     // ================= consumers: warp w takes items w, w + 8, ...
     uint4 xr[kONch];  // this lane's chunks of x, packed bf16
     if (!warp_wait(xbar, 0, lane, a.wait_ns) && lane == 0) atomicOr(err, ERR_TIMEOUT);
+    if (warp == 0 && lane == 0) MOE_TL(3);
 #pragma unroll
     for (int q = 0; q < kONch; ++q) xr[q] = lds128(smem_u32(xs) + 16u * (lane + 32 * q));
     const int up_end = p.n - (K + 1) * p.dpk;  // the down items come last
@@ -513,6 +544,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
                 float sc = v[0];
                 if (m.a < a.E && a.router_b) sc += __bfloat162float(a.router_b[m.a]);
                 publish_u64(a.dlog + m.a, ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(sc));
+                MOE_TL(4);
             }
         } else if (m.kind == kOkSharedUp || m.kind == kOkUp) {
             // feature a: its gate row, then its up row
@@ -570,6 +602,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
         if (c == 0) write_routing(a, rt, lane);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kOWarps * 32) : "memory");  // every item's down outputs are in ys
+    if (threadIdx.x == 0) MOE_TL(8);
     // residual + gated shared output + weighted slots 0..K-1, in that order
     const int tid = threadIdx.x;
     if (tid < p.ro) {
@@ -585,6 +618,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
         }
         a.out[o] = __float2bfloat16_rn(acc);
     }
+    if (tid == 0) MOE_TL(9);
     if (c == 0 && tid == 0) {
         // every CTA has read this call's tag once all have counted themselves in: move the
         // tag and the base on for the next call
@@ -593,6 +627,18 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
         a.hdr->dec_start_base = sbase + (uint32_t)G;
     }
 }
+
+#ifdef MOE_TIMELINE
+// Copies the timeline of the last one-token call: kTlCtas * kTlEvents global-timer values (ns).
+extern "C" int moe_timeline_read(unsigned long long* dst) {
+    return (int)cudaMemcpyFromSymbol(dst, g_moe_tl, sizeof(g_moe_tl));
+}
+extern "C" int moe_timeline_shape(int* ctas, int* events) {
+    *ctas = kTlCtas;
+    *events = kTlEvents;
+    return 0;
+}
+#endif
 
 static bool decode_geom(int cap, OGeom* g) {
     int o = 0;
