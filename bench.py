@@ -611,10 +611,32 @@ def time_host_experts(wl, device, n: int = 32, reps: int = 5) -> dict:
     fetched = sum(nbytes[i % HOST_LAYERS] for i in range(n)) / n
     err = moe.moe_last_device_error(ws)
     del layers, shadow
+    link = fetched / (fetch_ms * 1e-3) / 1e9
+    ce = copy_engine_h2d_gbs(device)
     return {"tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_step": round(ms, 5),
             "expert_bytes_per_step": int(fetched), "fetch_ms": round(fetch_ms, 5),
-            "host_link_gbs": round(fetched / (fetch_ms * 1e-3) / 1e9, 1), "layers": HOST_LAYERS,
-            "device_error": err}
+            "host_link_gbs": round(link, 1), "copy_engine_h2d_gbs": round(ce, 1),
+            "fetch_frac_of_copy_engine": round(link / ce, 3), "layers": HOST_LAYERS, "device_error": err}
+
+
+def copy_engine_h2d_gbs(device, nbytes: int = 512 << 20, reps: int = 3) -> float:
+    """The host link's rate as the copy engine sees it on this machine: one pinned-host to device
+    copy of 512 MB (cudaMemcpyAsync through torch), best of `reps`. The fetch kernel's rate is
+    reported beside it as a fraction."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    best = 0.0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(reps):
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (a.elapsed_time(b) * 1e6))
+    del src, dst
+    return best
 
 
 def time_e2e(ls: LayerSet, steps: int, warmup: int) -> dict:

@@ -46,7 +46,8 @@ struct GemmSmem {
     static constexpr uint32_t kBStage = BN * kBK * 2;
     static constexpr int kStages = (int)((192u * 1024u) / (kAStage + kBStage));
     static constexpr uint32_t kTiles = kStages * (kAStage + kBStage);
-    static constexpr uint32_t kBytes = 1024 + kTiles + 256;  // alignment slack + tiles + barriers
+    static constexpr uint32_t kScratch = 4 * 2048;  // epilogue: per warp 32 rows x 64 bytes
+    static constexpr uint32_t kBytes = 1024 + kTiles + 256 + kScratch;  // alignment slack + tiles + barriers
     // full, empty and gathered-A barriers per stage, two accumulators' full and empty, the
     // MMA-done barrier, the TMEM address and the abort flag
     static_assert((3 * kStages + 5) * 8 + 8 <= 256, "barrier area");
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     uint64_t* fullA = mma_done + 1;  // gathered A stages (gate_up)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullA + kStages);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint8_t* epi_scratch = smem + GemmSmem<BN>::kTiles + 256;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -279,6 +281,24 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             if (!find_tile(p, t, g, ti)) break;
             const int b = local & 1;
             const uint32_t use = (uint32_t)(local >> 1) & 1u;
+            const int m = ti.m0 + r;  // row inside the group
+            const bool live = m < ti.rows;
+            // down: the row's token, slot and scale, read before the accumulator wait so that
+            // their latency hides behind it
+            int tok = 0, slot = 0;
+            float sc = 0.f;
+            if (EPI == kScaleY && live) {
+                if (ti.src) {
+                    tok = m;
+                    slot = a.K;
+                    sc = a.sgate[tok];
+                } else {
+                    const int pv = a.perm[ti.a_row + m];
+                    tok = pv / a.K;
+                    slot = pv - tok * a.K;
+                    sc = a.topw[pv];
+                }
+            }
             // lane 0 waits, the warp follows its verdict (tcgen05.ld needs the whole warp)
             bool ready = lane == 0 ? mbar_wait(&accf[b], use) : true;
             ready = __shfl_sync(0xffffffffu, ready, 0);
@@ -289,8 +309,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             __syncwarp();
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
-            const int m = ti.m0 + r;  // row inside the group
-            const bool live = m < ti.rows;
             if (EPI == kLogits) {
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
@@ -338,40 +356,46 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                     }
                 }
             } else {  // kScaleY
-                int tok = 0, slot = 0;
-                float sc = 0.f;
-                if (live) {
-                    if (ti.src) {
-                        tok = m;
-                        slot = a.K;
-                        sc = a.sgate[tok];
-                    } else {
-                        const int pv = a.perm[ti.a_row + m];
-                        tok = pv / a.K;
-                        slot = pv - tok * a.K;
-                        sc = a.topw[pv];
-                    }
+                // Each 32-column chunk of the warp's 32 rows goes through shared memory so that a
+                // store instruction writes 8 rows x 64 contiguous bytes (whole sectors) instead of
+                // 32 scattered 16-byte pieces. Lane l stores its row at l * 64 with its four
+                // 16-byte pieces swizzled by (l / 2) % 4 (conflict-free both ways); in round i
+                // lane l writes piece l % 4 of row l / 4 + 8 i.
+                const uint32_t scr = smem_u32(epi_scratch) + (uint32_t)(warp - 2) * 2048u;
+                const bf16* yrow = a.Yb + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n_idx * BN;
+                const bf16* orow[4];
+                bool olive[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = (lane >> 2) + 8 * i;
+                    orow[i] = reinterpret_cast<const bf16*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(yrow), rr));
+                    olive[i] = __shfl_sync(0xffffffffu, live, rr);
                 }
-                bf16* yrow = a.Yb + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n_idx * BN;
+                const uint32_t pc = (uint32_t)(lane & 3);
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld32(tbase + c * 32, v);
                     tmem_ld_wait();
-                    if (live) {
-                        uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint4 o;
-                            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t ow[4];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int k = j * 8 + i * 2;
-                                ow[i] = pack_bf16x2(sc * __uint_as_float(v[k]), sc * __uint_as_float(v[k + 1]));
-                            }
-                            dst[j] = o;
+                        for (int i = 0; i < 4; ++i) {
+                            const int k = j * 8 + i * 2;
+                            ow[i] = pack_bf16x2(sc * __uint_as_float(v[k]), sc * __uint_as_float(v[k + 1]));
                         }
+                        sts128(scr + (uint32_t)lane * 64u + (((uint32_t)j ^ (((uint32_t)lane >> 1) & 3u)) << 4), ow);
                     }
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t rr = (uint32_t)(lane >> 2) + 8u * i;
+                        const uint4 o = lds128_smem(scr + rr * 64u + ((pc ^ ((rr >> 1) & 3u)) << 4));
+                        if (olive[i])
+                            *reinterpret_cast<uint4*>(const_cast<bf16*>(orow[i]) + c * 32 + pc * 8) = o;
+                    }
+                    __syncwarp();
                 }
             }
             tc_fence_before();

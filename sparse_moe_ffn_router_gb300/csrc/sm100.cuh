@@ -88,6 +88,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     }
 }
 
+// 16-byte shared-memory store / load at a shared-window address (explicit st/ld.shared).
+__device__ __forceinline__ void sts128(uint32_t addr, const uint32_t (&v)[4]) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                 : "memory");
+}
+__device__ __forceinline__ uint4 lds128_smem(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------------------------------
 // cp.async (16-byte copies global -> shared by the issuing thread; completion on an mbarrier)
 
