@@ -34,8 +34,12 @@ namespace moe {
 
 constexpr int kBM = 128, kBK = 64;
 constexpr int kGatherWarps = 2;
+// epilogue warps: the down GEMM's short mainloop (K = I) leaves less time to write a tile out,
+// so it has two per TMEM lane quadrant, each taking half of the tile's columns
 template <int EPI>
-constexpr int gemm_threads() { return EPI == 1 ? 192 + 32 * kGatherWarps : 192; }
+constexpr int epi_warps() { return EPI == 2 ? 8 : 4; }
+template <int EPI>
+constexpr int gemm_threads() { return 64 + 32 * epi_warps<EPI>() + (EPI == 1 ? 32 * kGatherWarps : 0); }
 constexpr uint32_t kAStage = kBM * kBK * 2;
 
 enum { kLogits = 0, kSwiGLU = 1, kScaleY = 2 };
@@ -46,7 +50,7 @@ struct GemmSmem {
     static constexpr uint32_t kBStage = BN * kBK * 2;
     static constexpr int kStages = (int)((192u * 1024u) / (kAStage + kBStage));
     static constexpr uint32_t kTiles = kStages * (kAStage + kBStage);
-    static constexpr uint32_t kScratch = 4 * 2048;  // epilogue: per warp 32 rows x 64 bytes
+    static constexpr uint32_t kScratch = 8 * 2048;  // epilogue: per warp 32 rows x 64 bytes
     static constexpr uint32_t kBytes = 1024 + kTiles + 256 + kScratch;  // alignment slack + tiles + barriers
     // full, empty and gathered-A barriers per stage, two accumulators' full and empty, the
     // MMA-done barrier, the TMEM address and the abort flag
@@ -116,7 +120,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf[b], 1);
-            mbar_init(&acce[b], 4);
+            mbar_init(&acce[b], epi_warps<EPI>());
         }
         mbar_init(mma_done, 1);
         if (EPI == kSwiGLU)
@@ -221,11 +225,11 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
         }
         mma_commit(mma_done);
         if (!mbar_wait(mma_done, 0)) flag_timeout(p.err, abort_flag);
-    } else if (EPI == kSwiGLU && warp >= 6) {
+    } else if (EPI == kSwiGLU && warp >= 2 + epi_warps<EPI>()) {
         // ---------------- A gatherers: warp w (0, 1) takes rows 64w + 4i + lane / 8, i < 16,
         // chunk lane % 8 of each
         constexpr int kRows = kBM / (4 * kGatherWarps);  // rows per lane
-        const int r0 = (warp - 6) * (kBM / kGatherWarps) + (lane >> 3);
+        const int r0 = (warp - 2 - epi_warps<EPI>()) * (kBM / kGatherWarps) + (lane >> 3);
         const uint32_t c = (uint32_t)(lane & 7);
         const uint64_t pol_a = l2_evict_last();  // each token row is read by K experts
         int g = 0, it = 0;
@@ -271,7 +275,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             if (!ok) break;
         }
         cp_async_wait_all();  // no copy of this CTA may still be in flight when it exits
-    } else if (warp >= 2 && warp < 6) {
+    } else if (warp >= 2 && warp < 2 + epi_warps<EPI>()) {
         // ---------------- epilogue: TMEM lanes 32*(warp%4) .. +31, one accumulator row each
         const int q = warp & 3;
         const int r = q * 32 + lane;
@@ -356,12 +360,14 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                     }
                 }
             } else {  // kScaleY
-                // Each 32-column chunk of the warp's 32 rows goes through shared memory so that a
+                // Each 32-column chunk of the warp's 32 rows (in its half of the columns) goes
+                // through shared memory so that a
                 // store instruction writes 8 rows x 64 contiguous bytes (whole sectors) instead of
                 // 32 scattered 16-byte pieces. Lane l stores its row at l * 64 with its four
                 // 16-byte pieces swizzled by (l / 2) % 4 (conflict-free both ways); in round i
                 // lane l writes piece l % 4 of row l / 4 + 8 i.
                 const uint32_t scr = smem_u32(epi_scratch) + (uint32_t)(warp - 2) * 2048u;
+                const int hc = (warp - 2) >> 2;  // the half of the columns this warp writes
                 const bf16* yrow = a.Yb + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n_idx * BN;
                 const bf16* orow[4];
                 bool olive[4];
@@ -373,7 +379,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                 }
                 const uint32_t pc = (uint32_t)(lane & 3);
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = hc * (BN / 64); c < (hc + 1) * (BN / 64); ++c) {
                     uint32_t v[32];
                     tmem_ld32(tbase + c * 32, v);
                     tmem_ld_wait();
