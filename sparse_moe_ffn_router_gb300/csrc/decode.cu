@@ -17,21 +17,25 @@
 //     projection, and their fixed-order combine (residual + gated shared + slots 0..K-1).
 // Its work is a fixed sequence of items, one per 8 KB ring slot: router rows, shared
 // features, routed features, then down rows (shared first, then slots 0..K-1, 8 rows per
-// item). One producer lane copies items into the ring with 1-D TMA bulk copies: the token row
-// and the router rows first, then the shared features, and the rest as soon as the routing
-// is known and a slot is free. Consumer warp w takes items w, w+8, ... in order, so the warps
-// never wait for one another; a warp's dot products read the weights from shared memory with
-// x held in registers (one token: an MMA would use one column of eight).
+// item). Four producer warps (lane 0 of warp q issues items q, q+4, ...) copy items into the
+// ring with 1-D TMA bulk copies: the router rows and shared features first, before the kernel
+// waits for the previous one on the stream (programmatic launch), then the token row, and the
+// rest as soon as the routing is known and a slot is free. (Issuing the shared expert's down
+// rows before the routing too was measured slower: they compete with the token row and the
+// router rows on the critical path.) Consumer warp w takes items w, w+8, ... in order, so the
+// warps never wait for one another; a warp's dot products read the weights from shared memory
+// with x held in registers, bf16 by bf16 (one token: an MMA would use one column of eight).
 //
 // Exchanges between CTAs carry a tag of the call instead of a flag: router scores are 64-bit
-// words (tag, fp32 score), h values 32-bit words (16-bit tag, bf16 h). A reader polls the
-// words it needs until all carry this call's tag; every word is rewritten by every call, so
-// a stale word always carries the previous call's tag. A relaxed store alone can take
-// microseconds to reach the other SMs, so the writer of a router score, and each warp after
-// its last routed h value, issues a fence. Warp 0 of every CTA ranks the E scores itself
-// (top-K with ties to the lower index, renormalised weights, the shared gate) right after its
-// own router row; the producer then issues the routed rows. Down items come last and wait
-// only for the h words of their own expert slot.
+// words (tag, fp32 score), h values 32-bit words (16-bit tag, bf16 h), published with atomic
+// exchanges (carried out at L2, where the other SMs' polls see them within about a
+// microsecond; a plain store would need a fence, which stalls the SM's other warps). A
+// reader polls the words it needs until all carry this call's tag; every word is rewritten by
+// every call, so a stale word always carries the previous call's tag. Warp 0 of every CTA
+// ranks the E scores itself (top-K with ties to the lower index, renormalised weights, the
+// shared gate) right after its own router row and releases the producers as soon as the
+// experts are known. Down items come last and wait only for the h words of their own expert
+// slot.
 //
 // Every wait is bounded (~1 s): a timeout sets MOE_ERR_TIMEOUT in the workspace and the
 // kernel still runs to its end with in-range indices. Each CTA counts itself in when it
@@ -47,7 +51,7 @@ namespace moe {
 //   0 CTA start                          5 warp 0: every CTA's router scores seen
 //   1 producer 0: weight-only items out  6 warp 0: routing known, producer released
 //   2 producer 0: previous kernel done   7 producer 0: every item issued
-//   3 consumers: token row in shared     8 consumers: every item done (combine starts)
+//   3 consumers: token row in registers  8 consumers: every item done (combine starts)
 //   4 a router score published          9 combine done
 constexpr int kTlEvents = 10, kTlCtas = 256;
 #ifdef MOE_TIMELINE
@@ -72,7 +76,7 @@ constexpr int kOIch = kOI / 256;               // 16-byte chunks of an I-long ro
 constexpr int kOMaxK = 8;                      // experts per token
 constexpr int kOSlot = 8192;                   // ring slot: one feature's gate and up rows
 constexpr int kOMaxSlots = 28;                 // a multiple of kOProducers
-static_assert(kOMaxSlots < 32, "one producer lane per slot plus one for the token row");
+static_assert(kOMaxSlots <= 32, "one producer lane per slot in the exit drain");
 constexpr int kOMaxItems = 64;
 constexpr int kOMaxRo = kOSlot / (kOI * 2);    // down rows per item
 constexpr int kOMaxOut = 16;                   // output rows per CTA
@@ -109,7 +113,7 @@ struct OPlan {
 
 struct OGeom {
     int nslot;
-    int o_x, o_slot, o_meta, o_bar, o_ys, o_rt, o_iss, smem;
+    int o_slot, o_meta, o_bar, o_ys, o_rt, o_iss, smem;
 };
 
 // Item j of a CTA's sequence: router rows, shared features, routed features, then down rows
@@ -399,13 +403,11 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    uint8_t* xs = base + g.o_x;
     uint8_t* slots = base + g.o_slot;
     OMeta* meta = reinterpret_cast<OMeta*>(base + g.o_meta);
     uint64_t* full = reinterpret_cast<uint64_t*>(base + g.o_bar);
     uint64_t* empty = full + kOMaxSlots;
-    uint64_t* xbar = empty + kOMaxSlots;
-    uint64_t* routed = xbar + 1;
+    uint64_t* routed = empty + kOMaxSlots;
     float* ys = reinterpret_cast<float*>(base + g.o_ys);  // [K + 1][kOMaxOut] down outputs, unscaled
     ORoute& rt = *reinterpret_cast<ORoute*>(base + g.o_rt);
 
@@ -453,8 +455,8 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
         return true;
     };
     if (pw >= 0) {
-        for (int i = pw * 32 + lane; i < 2 * nslot + 2; i += kOProducers * 32)
-            mbar_init(i < nslot ? &full[i] : i < 2 * nslot ? &empty[i - nslot] : i == 2 * nslot ? xbar : routed, 1);
+        for (int i = pw * 32 + lane; i < 2 * nslot + 1; i += kOProducers * 32)
+            mbar_init(i < nslot ? &full[i] : i < 2 * nslot ? &empty[i - nslot] : routed, 1);
         for (int j = pw * 32 + lane; j < kOMaxItems; j += kOProducers * 32) issued[j] = 0;
         fence_mbar_init();
         __syncwarp();
@@ -471,11 +473,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
     // the stream (the layer before, say, whose output is this token row) is still running:
     // everything from here on waits for it to complete and for its memory to be visible.
     grid_dep_wait();
-    if (pw == 0 && lane == 0) {
-        MOE_TL(2);
-        mbar_arrive_expect_tx(xbar, (uint32_t)(kOH * 2));
-        bulk_load(xs, a.x, (uint32_t)(kOH * 2), xbar);
-    }
+    if (pw == 0 && lane == 0) MOE_TL(2);
     // the residual of this CTA's output rows, read now: at the combine its latency would come
     // last on the critical path (thread o < ro adds row o0 + o)
     const float resid = (threadIdx.x < p.ro && a.residual) ? __bfloat162float(a.residual[p.o0 + threadIdx.x]) : 0.f;
@@ -501,17 +499,14 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
         // every copy issued must land before the CTA can exit: the latest item of each slot
         __syncwarp();
         asm volatile("bar.sync 2, %0;" ::"n"(kOProducers * 32) : "memory");
-        // (lane l of producer 0 takes slot l and lane 31 the token row: a shared-memory
-        // operation waits behind the consumers' loads, so one pass over the slots, not one
-        // per item)
+        // (lane l of producer 0 takes slot l: a shared-memory operation waits behind the
+        // consumers' loads, so one pass over the slots, not one per item)
         if (pw == 0) {
             bool ok = true;
             if (lane < nslot && lane < p.n) {
                 int j = lane + nslot * ((p.n - 1 - lane) / nslot);  // the slot's last item
                 while (j >= 0 && !issued[j]) j -= nslot;
                 if (j >= 0) ok = mbar_poll(&full[lane], ((uint32_t)(j / nslot)) & 1u, a.wait_ns);
-            } else if (lane == 31) {
-                ok = mbar_poll(xbar, 0, a.wait_ns);
             }
             if (!ok) atomicOr(err, ERR_TIMEOUT);
         }
@@ -519,12 +514,15 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
     }
 
     // ================= consumers: warp w takes items w, w + 8, ...
-    uint4 xr[kONch];  // this lane's chunks of x, packed bf16
-    if (!warp_wait(xbar, 0, lane, a.wait_ns) && lane == 0) atomicOr(err, ERR_TIMEOUT);
-    if (warp == 0 && lane == 0) MOE_TL(3);
+    // this lane's chunks of x (packed bf16), straight from global memory into registers (after
+    // the wait for the previous kernel above): one memory round trip, no copy through shared
+    // memory and no barrier hand-off
+    uint4 xr[kONch];
 #pragma unroll
-    for (int q = 0; q < kONch; ++q) xr[q] = lds128(smem_u32(xs) + 16u * (lane + 32 * q));
-    const int up_end = p.n - (K + 1) * p.dpk;  // the down items come last
+    for (int q = 0; q < kONch; ++q) xr[q] = ld_ro(a.x + 8 * (lane + 32 * q));
+#ifdef MOE_TIMELINE
+    if (warp == 0 && lane == 0 && xr[kONch - 1].w != 0xffffffffu) MOE_TL(3);  // the compare waits for the loads
+#endif
     int s = warp % nslot;
     uint32_t round = warp / nslot;
     for (int j = warp; j < p.n; j += kOWarps) {
@@ -642,10 +640,9 @@ extern "C" int moe_timeline_shape(int* ctas, int* events) {
 
 static bool decode_geom(int cap, OGeom* g) {
     int o = 0;
-    g->o_x = o; o += kOH * 2;
     g->o_rt = o; o += ((int)sizeof(ORoute) + 127) & ~127;
     g->o_ys = o; o += (kOMaxK + 1) * kOMaxOut * 4;
-    g->o_bar = o; o += (2 * kOMaxSlots + 2) * 8;
+    g->o_bar = o; o += (2 * kOMaxSlots + 1) * 8;
     g->o_meta = o; o += kOMaxSlots * (int)sizeof(OMeta);
     g->o_iss = o; o += kOMaxItems;
     o = (o + 1023) & ~1023;

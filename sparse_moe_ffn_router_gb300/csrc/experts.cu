@@ -187,6 +187,8 @@ __device__ __forceinline__ float4 load4(const bf16* p) {
     return make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
 }
 
+constexpr int kMaxCombineK = 8;  // slots per token the 8-wide combine keeps in registers
+
 template <typename YT>
 __global__ void __launch_bounds__(256) k_combine(LayerArgs a, const YT* Y) {
     // no-op unless launched as a programmatic dependent: then wait for the producer of Y
@@ -209,6 +211,44 @@ __global__ void __launch_bounds__(256) k_combine(LayerArgs a, const YT* Y) {
     ov.x = pack_bf16x2(acc.x, acc.y);
     ov.y = pack_bf16x2(acc.z, acc.w);
     *reinterpret_cast<uint2*>(a.out + (size_t)t * a.H + o) = ov;
+}
+
+// The bf16-Y combine with 8 outputs per thread: 16-byte loads of each of the K + 1 slot rows
+// (twice the bytes in flight per thread), the same per-element order of additions.
+__global__ void __launch_bounds__(256) k_combine_bf16x8(LayerArgs a, const bf16* Y) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    const int q = a.H / 8;
+    if (i >= (int64_t)a.T * q) return;
+    const int t = (int)(i / q), o = (int)(i - (int64_t)t * q) * 8;
+    float acc[8];
+    if (a.residual) {
+        unpack8(ld_ro(a.residual + (size_t)t * a.H + o), acc);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    }
+    const bf16* yt = Y + (size_t)t * (a.K + 1) * a.H + o;
+    uint4 w[kMaxCombineK + 1];
+    const int nk = a.K + 1;
+#pragma unroll
+    for (int k = 0; k < kMaxCombineK + 1; ++k)
+        if (k < nk) w[k] = ld_ro(yt + (size_t)(k == 0 ? a.K : k - 1) * a.H);  // the shared slot first
+#pragma unroll
+    for (int k = 0; k < kMaxCombineK + 1; ++k)
+        if (k < nk) {
+            float v[8];
+            unpack8(w[k], v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += v[e];
+        }
+    uint4 ov;
+    ov.x = pack_bf16x2(acc[0], acc[1]);
+    ov.y = pack_bf16x2(acc[2], acc[3]);
+    ov.z = pack_bf16x2(acc[4], acc[5]);
+    ov.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(a.out + (size_t)t * a.H + o) = ov;
 }
 
 cudaError_t launch_experts(const LayerArgs& a, cudaStream_t s) {
@@ -242,7 +282,11 @@ cudaError_t launch_combine(const LayerArgs& a, cudaStream_t s) {
     const int64_t nq = (int64_t)a.T * (a.H / 4);
     const unsigned grid = (unsigned)((nq + 255) / 256);
     cudaError_t e;
-    if (a.gemm) {
+    if (a.gemm && a.H % 8 == 0 && a.K <= kMaxCombineK) {
+        const bf16* Y = a.Yb;
+        const unsigned grid8 = (unsigned)(((int64_t)a.T * (a.H / 8) + 255) / 256);
+        MOE_LAUNCH(MOE_KERNEL_COMBINE, s, (e = launch_pdl(k_combine_bf16x8, dim3(grid8), dim3(256), 0, s, a, Y)));
+    } else if (a.gemm) {
         const bf16* Y = a.Yb;
         MOE_LAUNCH(MOE_KERNEL_COMBINE, s, (e = launch_pdl(k_combine<bf16>, dim3(grid), dim3(256), 0, s, a, Y)));
     } else {

@@ -21,7 +21,7 @@ EVENTS = [
     "CTA start",
     "producer 0: weight-only items issued",
     "producer 0: previous kernel complete",
-    "consumers: token row in shared memory",
+    "consumers: token row in registers",
     "a router score published",
     "warp 0: every CTA's router scores seen",
     "warp 0: routing known, producer released",
