@@ -287,15 +287,17 @@ cudaError_t launch_route_fused(const LayerArgs& a, cudaStream_t s) {
 namespace moe {
 
 // ---------------------------------------------------------------------------------------
-// Few-token routing on one thread-block cluster of 8 CTAs (T <= 8, H <= 2048, E <= 256).
-// CTA c bulk-copies its ~(E+1)/8 rows of [Wr; ws] and the token rows into shared memory (one
+// Few-token routing on one thread-block cluster of NC CTAs, the whole grid (16 where the device
+// allows that non-portable size, else 8; T <= 8, H <= 2048, E <= 256).
+// CTA c bulk-copies its ~(E+1)/NC rows of [Wr; ws] and the token rows into shared memory (one
 // copy per row, rows 16 bytes apart modulo 128 so ldmatrix is conflict-free), scores them with
 // warp-level bf16 MMAs (m16n8k16, fp32 accumulate; 16 rows by the tokens, K split over the 8
 // warps and summed in a fixed order), and stores the scores straight into CTA 0's shared memory
 // (distributed shared memory). After one cluster barrier CTA 0 runs top-K for all tokens and
 // the dispatch from its own shared memory and writes the routing to global memory.
 
-constexpr int kRouteCluster = 8;
+constexpr int kRouteCluster = 16;        // cluster size tried first (non-portable)
+constexpr int kRouteClusterPortable = 8; // fallback
 constexpr int kRouteMaxT = 8;
 constexpr int kRoutePad = 16;
 
@@ -334,12 +336,12 @@ __device__ __forceinline__ void mma16816_r(float (&d)[4], uint32_t a0, uint32_t 
 }
 
 struct RouteSmem {
-    __host__ __device__ static int rows(int E) { return (E + 1 + kRouteCluster - 1) / kRouteCluster; }
-    __host__ __device__ static int mtiles(int E) { return (rows(E) + 15) / 16; }
-    static size_t bytes(int T, int H, int E, int ldl) {
+    __host__ __device__ static int rows(int E, int nc) { return (E + 1 + nc - 1) / nc; }
+    __host__ __device__ static int mtiles(int E, int nc) { return (rows(E, nc) + 15) / 16; }
+    static size_t bytes(int T, int H, int E, int ldl, int nc) {
         const size_t pitch = (size_t)H * 2 + kRoutePad;
-        return 128 + (size_t)(rows(E) + kRouteMaxT) * pitch + (size_t)T * ldl * 4 +
-               (size_t)8 * mtiles(E) * 128 * 4 + 64;
+        return 128 + (size_t)(rows(E, nc) + kRouteMaxT) * pitch + (size_t)T * ldl * 4 +
+               (size_t)8 * mtiles(E, nc) * 128 * 4 + 64;
     }
 };
 
@@ -356,7 +358,8 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;  // == rank in the (single) cluster
-    const int R = RouteSmem::rows(a.E), MT = RouteSmem::mtiles(a.E);
+    const int NC = gridDim.x;
+    const int R = RouteSmem::rows(a.E, NC), MT = RouteSmem::mtiles(a.E, NC);
     const int r0 = c * R, r1 = min(a.E + 1, r0 + R), nr = max(r1 - r0, 0);
     const int pitch = a.H * 2 + kRoutePad;
     const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -561,7 +564,7 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
 
 bool route_cluster_supported(const LayerArgs& a) {
     return a.T >= 1 && a.T <= kRouteMaxT && a.E <= 256 && a.H % 128 == 0 &&
-           RouteSmem::bytes(a.T, a.H, a.E, a.ldl) <= 200 * 1024;
+           RouteSmem::bytes(a.T, a.H, a.E, a.ldl, kRouteClusterPortable) <= 200 * 1024;
 }
 
 cudaError_t launch_route_cluster(const LayerArgs& a, cudaStream_t s) {
@@ -569,19 +572,41 @@ cudaError_t launch_route_cluster(const LayerArgs& a, cudaStream_t s) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
+    // the cluster size this device takes: 16 CTAs (half the rows each) when a cluster of that
+    // non-portable size can be resident, else 8
+    static int nc_dev[64] = {};
     if (!configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(k_route_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (e != cudaSuccess) return e;
+        nc_dev[dev] = kRouteClusterPortable;
+        if (cudaFuncSetAttribute(k_route_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(kRouteCluster);
+            q.blockDim = dim3(256);
+            q.dynamicSmemBytes = 200 * 1024;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = kRouteCluster;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, k_route_cluster, &q) == cudaSuccess && clusters >= 1)
+                nc_dev[dev] = kRouteCluster;
+        }
+        (void)cudaGetLastError();  // a refused query leaves no error behind
         configured[dev] = true;
     }
+    const int nc = nc_dev[dev];
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kRouteCluster);
+    cfg.gridDim = dim3(nc);
     cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = RouteSmem::bytes(a.T, a.H, a.E, a.ldl);
+    cfg.dynamicSmemBytes = RouteSmem::bytes(a.T, a.H, a.E, a.ldl, nc);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kRouteCluster;
+    attr[0].val.clusterDim.x = nc;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
