@@ -18,10 +18,13 @@
 //   warp 0    TMA producer (one lane): A and B tiles into a 4-stage shared-memory ring;
 //   warp 1    TMEM owner and MMA issuer (one lane): 128 x BN x 16 tcgen05.mma steps into one
 //             of two TMEM accumulators, tcgen05.commit frees ring stages / publishes tiles;
-//   warps 2-5 epilogue: tcgen05.ld of the accumulator (warp w reads lanes 32*(w%4)..+31);
-//   warps 6-7 (gate_up only) A gatherers: a routed expert's A rows are token rows of x, row
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator (warp w reads lanes 32*(w%4)..+31;
+//             down has eight epilogue warps, 2-9, two per lane quadrant, each half the columns);
+//   warps 6-13 (gate_up only) A gatherers: a routed expert's A rows are token rows of x, row
 //             perm[j] / K for dispatch position j. Each k-block's 128-byte segment of a row is
-//             copied by 8 lanes, 16 bytes each with cp.async (a warp instruction moves 4 rows),
+//             copied by 8 lanes, 16 bytes each with cp.async (a warp instruction moves 4 rows;
+//             eight warps keep enough of these row loads in flight: with two the GEMM ran
+//             ~8 us longer per prefill layer),
 //             straight from x into the A stage, in the 128-byte swizzled layout the tensor map
 //             would give (16-byte chunk c of row r at r * 128 + (c ^ (r % 8)) * 16); rows past
 //             the group's end are zero-filled. x rows are kept in L2 (evict-last) across the K
@@ -33,7 +36,7 @@
 namespace moe {
 
 constexpr int kBM = 128, kBK = 64;
-constexpr int kGatherWarps = 2;
+constexpr int kGatherWarps = 8;
 // epilogue warps: the down GEMM's short mainloop (K = I) leaves less time to write a tile out,
 // so it has two per TMEM lane quadrant, each taking half of the tile's columns
 template <int EPI>
@@ -226,8 +229,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
         mma_commit(mma_done);
         if (!mbar_wait(mma_done, 0)) flag_timeout(p.err, abort_flag);
     } else if (EPI == kSwiGLU && warp >= 2 + epi_warps<EPI>()) {
-        // ---------------- A gatherers: warp w (0, 1) takes rows 64w + 4i + lane / 8, i < 16,
-        // chunk lane % 8 of each
+        // ---------------- A gatherers: gatherer warp w takes rows (128 / kGatherWarps) w +
+        // lane / 8 + 4 i, i < kRows, chunk lane % 8 of each
         constexpr int kRows = kBM / (4 * kGatherWarps);  // rows per lane
         const int r0 = (warp - 2 - epi_warps<EPI>()) * (kBM / kGatherWarps) + (lane >> 3);
         const uint32_t c = (uint32_t)(lane & 7);
