@@ -200,9 +200,9 @@ enum {
     MOE_KERNEL_COMBINE = 7,         /* fixed-order sum into the residual           */
     MOE_KERNEL_RMSNORM = 8,
     MOE_KERNEL_SHARED_GATE = 9,     /* not launched: the top-K kernel scores the shared gate */
-    MOE_KERNEL_GATHER = 10,         /* not launched: the dispatch scatter copies the token rows */
+    MOE_KERNEL_GATHER = 10,         /* not launched: the gate_up GEMM gathers the token rows from x */
     MOE_KERNEL_GEMM_PLAN = 11,      /* not launched: the dispatch scan writes the GEMM tables */
-    MOE_KERNEL_DECODE_FUSED = 12,   /* whole layer in one persistent kernel (T <= 8) */
+    MOE_KERNEL_DECODE_FUSED = 12,   /* whole layer in one persistent kernel (T = 1) */
     MOE_KERNEL_ROUTER_STATS = 13,   /* load-balancing statistics (moe_router_stats) */
     MOE_KERNEL_FETCH_EXPERTS = 14,  /* touched experts copied from host memory (moe_forward_host_experts) */
     MOE_KERNEL_COPY_ROWS = 15,      /* token rows to or from mapped host memory (moe_forward_host_io) */

@@ -138,7 +138,8 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // Router scores, top-K and dispatch: one fused launch for few tokens, else separate kernels.
-// Routing: up to 8 tokens on one thread-block cluster; 9..255 tokens in two kernels (tensor-
+// Routing: up to 8 tokens on one thread-block cluster (16 CTAs where the device allows, else
+// 8); 9..255 tokens in two kernels (tensor-
 // pipe scores, then top-K and the whole dispatch in one CTA); from 256 tokens the scores as a
 // tcgen05 GEMM, top-K one warp per token and the three block-parallel dispatch kernels. (The
 // single-kernel routing of up to 64 tokens is used only by the fixed-scratch entry point.)
