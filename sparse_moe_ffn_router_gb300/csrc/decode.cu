@@ -75,8 +75,9 @@ constexpr int kONch = kOH / 256;               // 16-byte chunks of an H-long ro
 constexpr int kOIch = kOI / 256;               // 16-byte chunks of an I-long row per lane
 constexpr int kOMaxK = 8;                      // experts per token
 constexpr int kOSlot = 8192;                   // ring slot: one feature's gate and up rows
-constexpr int kOMaxSlots = 28;                 // a multiple of kOProducers
+constexpr int kOMaxSlots = 28;                 // ring slots at most (the count used: a multiple of kOWarps)
 static_assert(kOMaxSlots <= 32, "one producer lane per slot in the exit drain");
+static_assert(kOWarps % kOProducers == 0, "slot counts that are multiples of the consumer warps suit the producers");
 constexpr int kOMaxItems = 64;
 constexpr int kOMaxRo = kOSlot / (kOI * 2);    // down rows per item
 constexpr int kOMaxOut = 16;                   // output rows per CTA
@@ -650,7 +651,13 @@ static bool decode_geom(int cap, OGeom* g) {
     const int room = cap - 1024 - o;  // 1024: alignment of the dynamic base
     g->nslot = room / kOSlot < kOMaxSlots ? room / kOSlot : kOMaxSlots;
     g->smem = 1024 + o + g->nslot * kOSlot;
-    g->nslot -= g->nslot % kOProducers;
+    // A multiple of the consumer warps: warp w consumes items w, w + kOWarps, ..., so the items
+    // of one slot (j, j + nslot, ...) are all consumed by the same warp, in order. That is what
+    // makes a parity wait on the slot's barrier exact: a warp never asks for a slot's next
+    // phase before it has consumed the previous one, so the barrier cannot still be a phase
+    // behind (where the parity test would take the phase before that for the one asked for).
+    // kOWarps is a multiple of kOProducers, so each slot also keeps one producer.
+    g->nslot -= g->nslot % kOWarps;
     return g->nslot >= kOWarps;
 }
 
