@@ -650,7 +650,6 @@ static bool decode_geom(int cap, OGeom* g) {
     g->o_slot = o;
     const int room = cap - 1024 - o;  // 1024: alignment of the dynamic base
     g->nslot = room / kOSlot < kOMaxSlots ? room / kOSlot : kOMaxSlots;
-    g->smem = 1024 + o + g->nslot * kOSlot;
     // A multiple of the consumer warps: warp w consumes items w, w + kOWarps, ..., so the items
     // of one slot (j, j + nslot, ...) are all consumed by the same warp, in order. That is what
     // makes a parity wait on the slot's barrier exact: a warp never asks for a slot's next
@@ -658,6 +657,7 @@ static bool decode_geom(int cap, OGeom* g) {
     // behind (where the parity test would take the phase before that for the one asked for).
     // kOWarps is a multiple of kOProducers, so each slot also keeps one producer.
     g->nslot -= g->nslot % kOWarps;
+    g->smem = 1024 + o + g->nslot * kOSlot;
     return g->nslot >= kOWarps;
 }
 
