@@ -1,6 +1,6 @@
-"""Expert parallelism (sparse_moe_ffn_router_gb300/ep.py) in two gloo processes on CPU.
+"""Expert parallelism (sparse_moe_ffn_router_gb300/ep.py) in two and four gloo processes on CPU.
 
-Rank r owns experts [r*E/2, (r+1)*E/2) and is home to tokens [r*T/2, (r+1)*T/2) of a seeded
+Rank r of N owns experts [r*E/N, (r+1)*E/N) and is home to tokens [r*T/N, (r+1)*T/N) of a seeded
 layer. Each rank routes its own tokens with the oracle, runs the exchange (counts, dispatch,
 expert outputs back, fixed-order combine) with the expert math restated in fp64 numpy, and
 the tests check, against the oracle's routing and layer output for all T tokens at once:
@@ -24,8 +24,7 @@ import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-DIMS = (16, 64, 8, 2, 32, 32)  # T (both ranks), H, E, K, I, Is
-WORLD = 2
+DIMS = (16, 64, 8, 2, 32, 32)  # T (all ranks), H, E, K, I, Is
 
 
 def _free_port() -> int:
@@ -34,14 +33,14 @@ def _free_port() -> int:
         return s.getsockname()[1]
 
 
-def _layer(bias_low: bool):
+def _layer(bias_low: bool, world: int):
     from sparse_moe_ffn_router_gb300 import synth
     T, H, E, K, I, Is = DIMS
     w = synth.make_weights(H, E, I, Is, seed=77)
     if bias_low:
-        # experts of rank 0 never win: every pair goes to rank 1
+        # experts of rank 0 never win: every pair goes to the other ranks
         b = torch.zeros(E, dtype=torch.float32)
-        b[: E // WORLD] = -30.0
+        b[: E // world] = -30.0
         w["router_b"] = b.to(torch.bfloat16)
     x = synth.make_x(T, H, seed=78)
     return w, x
@@ -58,7 +57,7 @@ def _f64(t: torch.Tensor) -> np.ndarray:
     return t.float().double().numpy()
 
 
-def _rank_main(rank: int, port: int, bias_low: bool, out_dir: str):
+def _rank_main(rank: int, world: int, port: int, bias_low: bool, out_dir: str):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
@@ -66,10 +65,10 @@ def _rank_main(rank: int, port: int, bias_low: bool, out_dir: str):
     import oracle
     from sparse_moe_ffn_router_gb300 import ep
 
-    dist.init_process_group("gloo", rank=rank, world_size=WORLD)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
     T, H, E, K, I, Is = DIMS
-    Tl = T // WORLD
-    w, x = _layer(bias_low)
+    Tl = T // world
+    w, x = _layer(bias_low, world)
     xr = x[rank * Tl:(rank + 1) * Tl]
     dims_r = (Tl,) + DIMS[1:]
     r = oracle.route(dims_r, xr, w["router_w"], w["router_b"])
@@ -84,23 +83,24 @@ def _rank_main(rank: int, port: int, bias_low: bool, out_dir: str):
     dist.destroy_process_group()
 
 
-def _run(tmp_path, bias_low: bool):
+def _run(tmp_path, bias_low: bool, world: int = 2):
     import oracle
     port = _free_port()
-    mp.start_processes(_rank_main, args=(port, bias_low, str(tmp_path)), nprocs=WORLD, start_method="spawn", join=True)
-    got = [pickle.load(open(tmp_path / f"rank{r}.pkl", "rb")) for r in range(WORLD)]
-    w, x = _layer(bias_low)
+    mp.start_processes(_rank_main, args=(world, port, bias_low, str(tmp_path)), nprocs=world, start_method="spawn",
+                       join=True)
+    got = [pickle.load(open(tmp_path / f"rank{r}.pkl", "rb")) for r in range(world)]
+    w, x = _layer(bias_low, world)
     T, H, E, K, I, Is = DIMS
-    Tl = T // WORLD
+    Tl = T // world
     ref_route = oracle.route(DIMS, x, w["router_w"], w["router_b"])
     ref = oracle.forward(DIMS, x, w)["out"]
     xb = x.view(torch.int16).numpy()
-    for owner in range(WORLD):
+    for owner in range(world):
         g = got[owner]
-        lo, hi = owner * E // WORLD, (owner + 1) * E // WORLD
+        lo, hi = owner * E // world, (owner + 1) * E // world
         # what the owner must receive from each source rank, in (expert, token, slot) order
         want = []
-        for src in range(WORLD):
+        for src in range(world):
             pairs = [(int(ref_route["ids"][t, k]), t - src * Tl, k) for t in range(src * Tl, (src + 1) * Tl)
                      for k in range(K) if lo <= ref_route["ids"][t, k] < hi]
             want += [(src,) + p for p in sorted(pairs)]
@@ -109,14 +109,15 @@ def _run(tmp_path, bias_low: bool):
         for (src, e, tl, k), row in zip(have, g["rows"]):
             assert np.array_equal(row, xb[src * Tl + tl]), f"owner {owner}: row of token {src * Tl + tl}"
         assert int(g["recv_counts"].sum()) == len(want)
-    out = np.concatenate([got[r]["out"] for r in range(WORLD)])
+    out = np.concatenate([got[r]["out"] for r in range(world)])
     scale = np.abs(ref).max()
     np.testing.assert_allclose(out, ref, rtol=0, atol=1e-9 * scale)
     return got
 
 
-def test_expert_parallel_exchange_matches_the_oracle(tmp_path):
-    got = _run(tmp_path, bias_low=False)
+@pytest.mark.parametrize("world", [2, 4])
+def test_expert_parallel_exchange_matches_the_oracle(tmp_path, world):
+    got = _run(tmp_path, bias_low=False, world=world)
     assert all(int(g["recv_counts"].sum()) > 0 for g in got)
 
 
