@@ -13,8 +13,8 @@ from the 129 MB L2. Weights and inputs are resident in HBM before timing starts.
 
 Extra keys: `roofline` (dominant kernel: algorithmic bytes per launch over its CUDA-event
 duration inside the timed region, against the measured HBM copy bandwidth), `e2e` (the same
-metric through moe_forward_host_io: x copied from pinned host memory and the output copied
-back by the library, inside the timed region), `cpu_baseline` (the fp64 C oracle on the host cores on a bounded sample of the same
+metric through moe_forward_host_io: x read from pinned host memory and the output written
+back to it by the library, inside the timed region), `cpu_baseline` (the fp64 C oracle on the host cores on a bounded sample of the same
 workload), `clocks` (nvidia-smi samples taken during the timed region), `layer` (the whole
 layer's fractions of the HBM and tensor peaks and of its binding roofline), `also` (the
 decode T=64, prefill T=4096 and 40-layer stack workloads, shorter runs of the same
@@ -641,9 +641,10 @@ def copy_engine_h2d_gbs(device, nbytes: int = 512 << 20, reps: int = 3) -> float
 
 def time_e2e(ls: LayerSet, steps: int, warmup: int) -> dict:
     """Same metric through the public call with host buffers (moe_forward_host_io, prepared
-    once per layer as a ForwardHostIO): per step, the library copies x from pinned host
-    memory into device staging, runs the layer, and copies the output back to pinned host
-    memory. Also reports the host time to issue one step, taken over the first steps of the
+    once per layer as a ForwardHostIO): per step, the library brings x in from pinned host
+    memory, runs the layer, and puts the output back in pinned host memory (at T = 1 the
+    one-token kernel reads and writes the host rows itself; otherwise copies to and from
+    device staging around the layer). Also reports the host time to issue one step, taken over the first steps of the
     timed loop while the launch queue is still short (a host time close to the step time
     means the loop is issue-bound)."""
     moe = ls.moe

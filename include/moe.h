@@ -119,7 +119,11 @@ moe_status moe_forward(const moe_dims* d, const void* x, const moe_weights* w, c
  * Up to 1 MB of rows (T*H*2 bytes) in pinned host memory mapped into the device move by a
  * small copy kernel (MOE_KERNEL_COPY_ROWS) over the host link; pageable or larger buffers by
  * cudaMemcpyAsync (pageable ones work, but the driver stages them and may block the calling
- * thread). host_out holds the result once `stream` has passed the call.
+ * thread). One token at the shape moe_forward runs in its one-token kernel, with host_x,
+ * host_out and host_residual (when given) all pinned, mapped and 16-byte aligned, takes one
+ * launch and no copy: that kernel reads x and the residual and writes out on the host rows
+ * themselves, and dev_x / dev_out are left as they were. host_out holds the result once
+ * `stream` has passed the call.
  *   host_x, host_residual, host_out  [T, H] bf16, host memory (pinned or pageable);
  *                                    host_out may be the same buffer as host_x or host_residual
  *   dev_x, dev_out                   [T, H] bf16, device memory, 16-byte aligned, disjoint

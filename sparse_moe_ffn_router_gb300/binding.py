@@ -255,8 +255,9 @@ def moe_forward_host_io(dims, x, weights: Weights, residual, out, x_dev, out_dev
     """moe_forward with the token rows in host memory: x (and residual, when given) are CPU
     tensors copied into the device staging tensors x_dev (and out_dev), the layer runs, and
     out_dev is copied back into the CPU tensor out, all in order on `stream`. Pinned host
-    tensors keep the copies asynchronous; out holds the result once the stream has passed
-    the call."""
+    tensors keep the copies asynchronous (and one token, with x, residual and out pinned, runs
+    in one kernel that reads and writes them over the host link, with no copy); out holds the
+    result once the stream has passed the call."""
     d = _dims(dims)
     nbytes = d.T * d.H * 2
     for t in (x_dev, out_dev):

@@ -114,7 +114,7 @@ struct OPlan {
 
 struct OGeom {
     int nslot;
-    int o_slot, o_meta, o_bar, o_ys, o_rt, o_iss, smem;
+    int o_slot, o_meta, o_bar, o_ys, o_rt, o_iss, o_x, smem;
 };
 
 // Item j of a CTA's sequence: router rows, shared features, routed features, then down rows
@@ -517,10 +517,20 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
     // ================= consumers: warp w takes items w, w + 8, ...
     // this lane's chunks of x (packed bf16), straight from global memory into registers (after
     // the wait for the previous kernel above): one memory round trip, no copy through shared
-    // memory and no barrier hand-off
+    // memory and no barrier hand-off. A row in host memory crosses the host link once per CTA
+    // instead (every warp reading it would multiply the link's traffic by the warps): consumer
+    // thread t brings chunk t into shared memory, and each warp takes its chunks from there.
     uint4 xr[kONch];
+    if (a.x_host) {
+        uint4* xs = reinterpret_cast<uint4*>(base + g.o_x);
+        for (int t = threadIdx.x; t < kOH / 8; t += kOWarps * 32) xs[t] = __ldcg(reinterpret_cast<const uint4*>(a.x) + t);
+        asm volatile("bar.sync 1, %0;" ::"n"(kOWarps * 32) : "memory");
 #pragma unroll
-    for (int q = 0; q < kONch; ++q) xr[q] = ld_ro(a.x + 8 * (lane + 32 * q));
+        for (int q = 0; q < kONch; ++q) xr[q] = xs[lane + 32 * q];
+    } else {
+#pragma unroll
+        for (int q = 0; q < kONch; ++q) xr[q] = ld_ro(a.x + 8 * (lane + 32 * q));
+    }
 #ifdef MOE_TIMELINE
     if (warp == 0 && lane == 0 && xr[kONch - 1].w != 0xffffffffu) MOE_TL(3);  // the compare waits for the loads
 #endif
@@ -646,6 +656,8 @@ static bool decode_geom(int cap, OGeom* g) {
     g->o_bar = o; o += (2 * kOMaxSlots + 1) * 8;
     g->o_meta = o; o += kOMaxSlots * (int)sizeof(OMeta);
     g->o_iss = o; o += kOMaxItems;
+    o = (o + 15) & ~15;
+    g->o_x = o; o += kOH * 2;  // the token row, when it is read from host memory
     o = (o + 1023) & ~1023;
     g->o_slot = o;
     const int room = cap - 1024 - o;  // 1024: alignment of the dynamic base

@@ -6,13 +6,17 @@
 // transfer costs more than its bytes: the copy's own latency, and the layer's launch exposed
 // behind it. When the host buffer is pinned and mapped into the device address space,
 // k_copy_rows moves the rows with plain 16-byte loads and stores over the host link instead,
-// so the layer's launch follows a kernel on the same stream.
+// so the layer's launch follows a kernel on the same stream. (One token at the one-token
+// kernel's shape needs neither: that kernel reads and writes the mapped host rows itself.)
 #include "launch.h"
 
 namespace moe {
 
-// dst[i] = src[i] for n 16-byte units; one side is mapped host memory.
+// dst[i] = src[i] for n 16-byte units; one side is mapped host memory. A layer kernel launched
+// with programmatic serialization may start at once (its weight-only copies overlap the trip
+// over the host link): it waits for this grid to complete before it reads the rows.
 __global__ void __launch_bounds__(256) k_copy_rows(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n) {
+    grid_dep_launch();
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) dst[i] = __ldcg(src + i);
 }

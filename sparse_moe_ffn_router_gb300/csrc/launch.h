@@ -45,6 +45,7 @@ struct LayerArgs {
     uint64_t wait_ns;   // time limit of the bounded waits of the one-token and streaming kernels
     int test_suppress;  // MOE_TEST_SUPPRESS_* (testing aid; 0 in normal use)
     bool gemm;
+    bool x_host;      // x is pinned host memory mapped into the device (one-token kernel only)
     int flags;        // moe_dims.flags (MOE_FLAG_BF16_SCORES)
     int T, H, E, K, I, Is, Imax, ldl, nb;
     int64_t P;

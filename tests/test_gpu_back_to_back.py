@@ -51,3 +51,30 @@ def test_chained_calls_back_to_back(name, calls, n_weights, sample):
         ref = oracle.forward(sub, x_in, host[c % n_weights])["out"]
         got = xs[c + 1].cpu()[rows].float().numpy()
         assert_close(got, ref, f"{name}: call {c} of {calls}")
+
+
+def test_chained_host_row_calls_back_to_back():
+    """One-token calls with the token rows in pinned host memory (moe_forward_host_io), back to
+    back with no synchronisation: call c reads host row c, which call c - 1's kernel wrote over
+    the host link, and a residual row written by the call before that."""
+    wl = WORKLOADS["decode_T1"]
+    dims = wl.dims
+    T, H = wl.T, wl.H
+    calls, n_weights = 10, 3
+    dev = torch.device("cuda")
+    weights = [synth.make_weights(H, wl.E, wl.I, wl.Is, wl.seed, l, wl.zipf_s, device=dev) for l in range(n_weights)]
+    Ws = [moe.Weights.from_dict(w) for w in weights]
+    x0, _ = gap_controlled_x(dims, weights[0]["router_w"].cpu(),
+                             None if weights[0]["router_b"] is None else weights[0]["router_b"].cpu(), wl.seed, 0)
+    ws = moe.new_workspace(dims, dev)
+    xd = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    od = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    hs = [x0.clone().pin_memory()] + [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(calls)]
+    for c in range(calls):  # call c reads hs[c] (and hs[c - 1] as its residual) and writes hs[c + 1]
+        moe.moe_forward_host_io(dims, hs[c], Ws[c % n_weights], hs[c - 1] if c else None, hs[c + 1], xd, od, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_last_device_error(ws) == 0
+    host = [{k: (None if v is None else v.cpu()) for k, v in w.items()} for w in weights]
+    for c in range(calls):
+        ref = oracle.forward(dims, hs[c].clone(), host[c % n_weights], hs[c - 1].clone() if c else None)["out"]
+        assert_close(hs[c + 1].float().numpy(), ref, f"host rows: call {c} of {calls}")

@@ -1,5 +1,6 @@
 """The layer with its token rows in host memory (moe_forward_host_io): x and the residual are
-copied from host buffers into device staging, the layer runs, and the output is copied back.
+copied from host buffers into device staging, the layer runs, and the output is copied back
+(or, for one pinned token row, the one-token kernel reads and writes the host rows itself).
 Compared with the oracle, and bit for bit with moe_forward on the same device inputs, in each
 regime the entry point reaches (the fused one-token kernel, the streaming experts, the
 tensor-core GEMMs), with pinned and pageable host buffers, with and without a residual, with
