@@ -99,6 +99,12 @@ def main(argv=None) -> None:
             v = (v[(v >= t0) & (v - t0 < 10 ** 6)] - t0) / 1e3
             if len(v):
                 print(f"{e:2d} {name:44s} {v.min():7.2f} {np.median(v):7.2f} {v.max():7.2f}   n={len(v)}")
+        # the same CTA's time from one event to the next
+        ok = ((tl >= t0) & (tl - t0 < 10 ** 6)).all(axis=1)
+        d = np.diff(tl[ok], axis=1) / 1e3
+        print(f"    per-CTA time from event e-1 to e (min / median / max over {int(ok.sum())} CTAs)")
+        for e in range(1, len(EVENTS)):
+            print(f"{e:2d} {'':44s} {d[:, e - 1].min():7.2f} {np.median(d[:, e - 1]):7.2f} {d[:, e - 1].max():7.2f}")
 
 
 if __name__ == "__main__":
