@@ -28,6 +28,10 @@
  * it ready for the next call. Calls are asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream). Argument errors are detected on the host and returned before
  * anything is launched. A workspace must not be used by two calls that may overlap in time.
+ * Weights are only read. A call may start reading them (never x, residual, out or the
+ * workspace) while the kernel before it on `stream` is still finishing (programmatic
+ * dependent launch), so that kernel must not be one that writes the weights: after writing
+ * weights on `stream`, run any other work there, or synchronize, before the call.
  * Results are deterministic: the same inputs give bit-identical outputs on every call.
  */
 #ifndef MOE_GB300_H

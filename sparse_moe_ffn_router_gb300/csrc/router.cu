@@ -6,6 +6,8 @@
 // Expert) is one more dot product of the same token, so it is scored here as column E.
 #include <math.h>
 
+#include <atomic>
+
 #include "launch.h"
 #include "sm100.cuh"
 
@@ -353,9 +355,9 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
     __shared__ int slr[kRouteMaxT * 8];
     __shared__ int sperm[kRouteMaxT * 8];
     __shared__ int sact[256];
+    __shared__ uint32_t stoks[256];
     __shared__ int s_nact;
     __shared__ uint64_t bar;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;  // == rank in the (single) cluster
     const int NC = gridDim.x;
@@ -369,7 +371,10 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
     float* lg = reinterpret_cast<float*>(xsm + (size_t)kRouteMaxT * pitch);  // [T, ldl] (CTA 0)
     float* red = lg + (size_t)a.T * a.ldl;              // [8 warps][MT][32 lanes][4]
 
-    // 1. one bulk copy per row: this CTA's rows of [Wr; ws] (row E is the shared gate), tokens
+    // 1. one bulk copy per row: this CTA's rows of [Wr; ws] (row E is the shared gate), then
+    // the token rows. Launched with programmatic serialization, the kernel may start while the
+    // previous kernel on the stream is still running: the weight rows go out at once, the
+    // token rows (and every workspace access) only after the wait for that kernel.
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
         fence_mbar_init();
@@ -377,20 +382,16 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
     }
     __syncthreads();
     if (warp == 0) {
-        for (int i = lane; i < nr + a.T; i += 32) {
-            const bf16* src;
-            uint8_t* dst;
-            if (i < nr) {
-                const int r = r0 + i;
-                src = r < a.E ? a.router_w + (size_t)r * a.H : a.sg;
-                dst = wsm + (size_t)i * pitch;
-            } else {
-                src = a.x + (size_t)(i - nr) * a.H;
-                dst = xsm + (size_t)(i - nr) * pitch;
-            }
-            bulk_g2s(dst, src, (uint32_t)(a.H * 2), &bar);
+        for (int i = lane; i < nr; i += 32) {
+            const int r = r0 + i;
+            bulk_g2s(wsm + (size_t)i * pitch, r < a.E ? a.router_w + (size_t)r * a.H : a.sg, (uint32_t)(a.H * 2), &bar);
         }
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // only now may the next kernel start: it reads x before it waits for this one
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (warp == 0 && lane < a.T)
+        bulk_g2s(xsm + (size_t)lane * pitch, a.x + (size_t)lane * a.H, (uint32_t)(a.H * 2), &bar);
     bool ok = mbar_wait(&bar, 0);
     if (!ok) atomicOr(&a.hdr->err, ERR_TIMEOUT);
 
@@ -544,20 +545,29 @@ __global__ void __launch_bounds__(256, 1) k_route_cluster(LayerArgs a) {
     }
     if (!a.uprec) return;
     __syncthreads();
-    // gate_up work records of the routed experts: expert, first h row, 8 features, tokens
+    // gate_up work records of the routed experts: expert, first h row, 8 features, tokens.
+    // The token list of each used expert once (its pairs' tokens in dispatch order, 4 bits
+    // each; T <= 8), then warp w writes the records of experts w, w + 8, ..., lane l those of
+    // feature blocks l, l + 32, ...
     const int fbs = a.I / 8, n = s_nact;
-    for (int idx = threadIdx.x; idx < n * fbs; idx += 256) {
-        const int g = idx / fbs, fb = idx - g * fbs;
+    for (int g = threadIdx.x; g < n; g += 256) {
         const int e = sact[g];
         uint32_t toks = 0;
         for (int j = 0; j < cnt[e]; ++j) toks |= (uint32_t)(sperm[off[e] + j] / a.K) << (4 * j);
+        stoks[g] = toks;
+    }
+    __syncthreads();
+    for (int g = warp; g < n; g += 8) {
+        const int e = sact[g];
         UpRec rec;
         rec.e = e;
         rec.row0 = off[e];
-        rec.f0 = (int16_t)(fb * 8);
         rec.mt = (int16_t)cnt[e];
-        rec.toks = toks;
-        a.uprec[idx] = rec;
+        rec.toks = stoks[g];
+        for (int fb = lane; fb < fbs; fb += 32) {
+            rec.f0 = (int16_t)(fb * 8);
+            a.uprec[(size_t)g * fbs + fb] = rec;
+        }
     }
     if (threadIdx.x == 0) a.hdr->n_uprec = n * fbs;
 }
@@ -604,15 +614,28 @@ cudaError_t launch_route_cluster(const LayerArgs& a, cudaStream_t s) {
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = RouteSmem::bytes(a.T, a.H, a.E, a.ldl, nc);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    // programmatic serialization: the launch and the weight-row copies overlap the end of the
+    // previous kernel (the kernel waits for it before it reads x or the workspace). A driver
+    // that refuses it together with the cluster gets the cluster launch alone from then on.
+    static std::atomic<int> pdl_refused{0};
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = nc;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_refused.load() ? 1 : 2;
     cudaError_t e;
     MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (e = cudaLaunchKernelEx(&cfg, k_route_cluster, a)));
+    if (e != cudaSuccess && cfg.numAttrs == 2 && e != cudaErrorStreamCaptureInvalidated &&
+        e != cudaErrorStreamCaptureUnsupported) {
+        (void)cudaGetLastError();
+        pdl_refused.store(1);
+        cfg.numAttrs = 1;
+        MOE_LAUNCH(MOE_KERNEL_ROUTER_SCORES, s, (e = cudaLaunchKernelEx(&cfg, k_route_cluster, a)));
+    }
     return e;
 }
 
