@@ -285,6 +285,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up(LayerArgs a) {
             ok = issue(a.sgu, a.Is, fb * kFps, (int)a.P + t0, mt, -1 - t0, t0 + (lane < mt ? lane : 0));
         }
         grid_dep_wait();
+        grid_dep_launch();  // the routing is complete: the down kernel may start (see below)
         const int n_act = a.hdr->n_act;
         build_tiles(a, tiles, fb_r);
         const int q1 = routed_split(tiles[n_act], c + 1, G);
@@ -317,6 +318,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up(LayerArgs a) {
     for (int it = 0;; ++it) {
         if (it == my_shared && n_items < 0) {
             grid_dep_wait();
+            // The routing is complete, so the down kernel may launch: it reads the routing
+            // before it waits for this grid, and it waits for this grid before it reads h. Its
+            // CTAs take the SMs this kernel's CTAs leave and stream down weights while the
+            // last gate_up items finish elsewhere.
+            grid_dep_launch();
             const int R = routed_tiles(a, lane) * fb_r;
             n_items = my_shared + routed_split(R, c + 1, G) - routed_split(R, c, G);
         }
@@ -438,6 +444,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up_small(LayerArgs
         for (int i = blockIdx.x;; i += gridDim.x) {
             if (i >= n_shared && n_items < 0) {
                 grid_dep_wait();
+                grid_dep_launch();  // the routing is complete: the down kernel may start
                 n_items = n_shared + *(volatile int*)&a.hdr->n_uprec;
             }
             if (n_items >= 0 && i >= n_items) break;
@@ -508,6 +515,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_up_small(LayerArgs
     for (int i = blockIdx.x;; i += gridDim.x, ++it) {
         if (i >= n_shared && n_items < 0) {
             grid_dep_wait();
+            // the routing is complete: the down kernel may launch (as in k_stream_up)
+            grid_dep_launch();
             n_items = n_shared + *(volatile int*)&a.hdr->n_uprec;
         }
         if (n_items >= 0 && i >= n_items) break;
@@ -658,6 +667,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream_down(LayerArgs a) 
     int ckey = -1;  // h rows are never negative
     uint32_t bfr[kMaxSteps][2];
     grid_dep_wait();  // the h rows of the gate_up kernel
+    // every CTA of this grid is resident by now: the combine kernel may launch (it waits for
+    // this grid before it reads Y), so its launch is done by the time the last item is
+    grid_dep_launch();
     for (int it = 0; it < n_items; ++it) {
         const bool ok = wait_stage(r, it, err, a.wait_ns);
         if (!consumers_all(ok)) break;
