@@ -17,12 +17,12 @@
 //     projection, and their fixed-order combine (residual + gated shared + slots 0..K-1).
 // Its work is a fixed sequence of items, one per 8 KB ring slot: router rows, shared
 // features, routed features, then down rows (shared first, then slots 0..K-1, 8 rows per
-// item). Four producer warps (lane 0 of warp q issues items q, q+4, ...) copy items into the
+// item). Three producer warps (lane 0 of warp q issues items q, q+3, ...) copy items into the
 // ring with 1-D TMA bulk copies: the router rows and shared features first, before the kernel
 // waits for the previous one on the stream (programmatic launch), then the token row, and the
 // rest as soon as the routing is known and a slot is free. (Issuing the shared expert's down
 // rows before the routing too was measured slower: they compete with the token row and the
-// router rows on the critical path.) Consumer warp w takes items w, w+8, ... in order, so the
+// router rows on the critical path.) Consumer warp w takes items w, w+9, ... in order, so the
 // warps never wait for one another; a warp's dot products read the weights from shared memory
 // with x held in registers, bf16 by bf16 (one token: an MMA would use one column of eight).
 //
@@ -66,8 +66,8 @@ __device__ unsigned long long g_moe_tl[kTlCtas * kTlEvents];
     } while (0)
 #endif
 
-constexpr int kOWarps = 8;                     // consumer warps
-constexpr int kOProducers = 4;                 // producer warps (lane 0 of each issues copies)
+constexpr int kOWarps = 9;                     // consumer warps
+constexpr int kOProducers = 3;                 // producer warps (lane 0 of each issues copies)
 constexpr int kOThreads = (kOWarps + kOProducers) * 32;
 constexpr int kOH = 2048;                      // hidden width (the page's layer shape)
 constexpr int kOI = 512;                       // routed and shared expert widths
@@ -75,7 +75,7 @@ constexpr int kONch = kOH / 256;               // 16-byte chunks of an H-long ro
 constexpr int kOIch = kOI / 256;               // 16-byte chunks of an I-long row per lane
 constexpr int kOMaxK = 8;                      // experts per token
 constexpr int kOSlot = 8192;                   // ring slot: one feature's gate and up rows
-constexpr int kOMaxSlots = 28;                 // ring slots at most (the count used: a multiple of kOWarps)
+constexpr int kOMaxSlots = 27;                 // ring slots at most (the count used: a multiple of kOWarps)
 static_assert(kOMaxSlots <= 32, "one producer lane per slot in the exit drain");
 static_assert(kOWarps % kOProducers == 0, "slot counts that are multiples of the consumer warps suit the producers");
 constexpr int kOMaxItems = 64;
@@ -284,7 +284,6 @@ __device__ bool poll_h(const uint32_t* words, uint32_t tag16, uint32_t (&hv)[kOI
             }
         if (!__any_sync(0xffffffffu, need != 0)) return ok;
         if (global_ns() - t0 > limit) ok = false;
-        __nanosleep(32);
     }
 }
 
@@ -326,7 +325,6 @@ __device__ void route_one(const LayerArgs& a, ORoute& rt, uint32_t tag, int lane
             timed_out = true;
             break;
         }
-        __nanosleep(32);
     }
     bool bad = false;
     uint32_t key[8];
@@ -514,7 +512,7 @@ __global__ void __launch_bounds__(kOThreads, 1) k_decode_fused(LayerArgs a, OGeo
         return;
     }
 
-    // ================= consumers: warp w takes items w, w + 8, ...
+    // ================= consumers: warp w takes items w, w + kOWarps, ...
     // this lane's chunks of x (packed bf16), straight from global memory into registers (after
     // the wait for the previous kernel above): one memory round trip, no copy through shared
     // memory and no barrier hand-off. A row in host memory crosses the host link once per CTA
