@@ -12,7 +12,10 @@
 // One CTA per SM (G CTAs). CTA c owns:
 //   - router rows c, c+G, ... (row E is the shared-expert gate);
 //   - shared-expert features [c*Is/G, (c+1)*Is/G) and routed (slot, feature) pairs
-//     [c*F/G, (c+1)*F/G) of the F = K*I: the gate row and the up row of each, giving h;
+//     P = c, c+G, ... of the F = K*I (P = slot * I + feature): the gate row and the up row of
+//     each, giving h. Strided rather than a contiguous run: every CTA then works through the
+//     slots in the same order, all of them on the same expert's rows at a time (measured
+//     16.64 us per layer against 17.03 us for contiguous runs, alternating on one box);
 //   - output rows [c*H/G, (c+1)*H/G) of the shared and of every routed expert's down
 //     projection, and their fixed-order combine (residual + gated shared + slots 0..K-1).
 // Its work is a fixed sequence of items, one per 8 KB ring slot: router rows, shared
@@ -108,7 +111,7 @@ struct OPlan {
     int fs0, nsf;  // shared features
     int o0, ro;    // output rows
     int dpk;       // down items per expert (kOMaxRo rows each)
-    int f0, nf;    // routed (slot, feature) pairs
+    int nf;        // routed (slot, feature) pairs: P = c, c + G, ... of the K*I
     int n;         // items
 };
 
@@ -135,8 +138,7 @@ __device__ __forceinline__ OPlan oplan(const LayerArgs& a, int c, int G) {
     p.o0 = c * kOH / G;
     p.ro = (c + 1) * kOH / G - p.o0;
     const int F = a.K * kOI;
-    p.f0 = c * F / G;
-    p.nf = (c + 1) * F / G - p.f0;
+    p.nf = c < F ? (F - c + G - 1) / G : 0;
     p.dpk = (p.ro + kOMaxRo - 1) / kOMaxRo;
     p.n = p.nr + p.nsf + p.nf + (a.K + 1) * p.dpk;
     return p;
@@ -164,7 +166,7 @@ __device__ __forceinline__ OItem item_at(const LayerArgs& a, const OPlan& p, con
     }
     j -= p.nsf;
     if (j < p.nf) {
-        const int fi = p.f0 + j, k = fi / kOI, f = fi - k * kOI;  // (slot, feature) pair
+        const int fi = c + j * G, k = fi / kOI, f = fi - k * kOI;  // (slot, feature) pair
         it.m = OMeta{kOkUp, k, f, 1};
         it.src0 = rt.gu[k] + (size_t)f * kOH;
         it.src1 = rt.gu[k] + (size_t)(kOI + f) * kOH;
