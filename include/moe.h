@@ -32,6 +32,10 @@
  * workspace) while the kernel before it on `stream` is still finishing (programmatic
  * dependent launch), so that kernel must not be one that writes the weights: after writing
  * weights on `stream`, run any other work there, or synchronize, before the call.
+ * One token at the pages' layer shape (H = 2048, I = Is = 512, T = 1) runs as one grid of one
+ * CTA per SM whose CTAs exchange values with one another, so it needs every SM at once:
+ * kernels on other streams that hold SMs longer than the wait limit (about 1 s) make the
+ * call end with MOE_ERR_TIMEOUT in the workspace's error word rather than wait for them.
  * Results are deterministic: the same inputs give bit-identical outputs on every call.
  */
 #ifndef MOE_GB300_H
