@@ -126,6 +126,7 @@ moe_status prepare(const moe_dims* d, const void* x, const moe_weights* w, void*
     a->uprec = p->T <= kRecTokens ? (UpRec*)(base + p->o_uprec) : nullptr;
     a->dlog = p->T <= kRecTokens ? (uint64_t*)(base + p->o_dlog) : nullptr;
     a->dh = p->T <= kRecTokens ? (uint64_t*)(base + p->o_dh) : nullptr;
+    a->dx = p->T == 1 ? (uint64_t*)(base + p->o_dx) : nullptr;
     a->gemm = p->gemm;
     a->x_host = false;
     a->T = p->T; a->H = p->H; a->E = p->E; a->K = p->K; a->I = p->I; a->Is = p->Is;
@@ -346,13 +347,14 @@ extern "C" moe_status moe_forward_host_io(const moe_dims* d, const void* host_x,
     const void* m = nullptr;
     // One token on the one-token kernel: it reads the token row, the residual and writes the
     // output on the pinned mapped host rows themselves, so the rows cross the host link inside
-    // the layer's own kernel (no copy launch before it and none after it). Each CTA reads the
-    // row once, and only the residual elements of the output rows it owns, before it writes
-    // them; every CTA has read the row before any CTA writes (the router scores, which need all
-    // of it, must reach every CTA first), so the output may replace the host x or residual.
+    // the layer's own kernel (no copy launch before it and none after it). The row crosses the
+    // link once (each CTA reads a share and passes it to the others through L2), each CTA reads
+    // only the residual elements of the output rows it owns, before it writes them, and every
+    // CTA has read the row before any CTA writes (the router scores, which need all of it, must
+    // reach every CTA first), so the output may replace the host x or residual.
     {
         const void *mx = nullptr, *mr = nullptr, *mo = nullptr;
-        if (a.T <= kFusedMaxTokens && decode_fused_supported(a) && mapped(host_x, &mx) && mapped(host_out, &mo) &&
+        if (a.T <= kFusedMaxTokens && a.dx && decode_fused_supported(a) && mapped(host_x, &mx) && mapped(host_out, &mo) &&
             (!host_residual || mapped(host_residual, &mr))) {
             a.x = (const bf16*)mx;
             a.x_host = true;

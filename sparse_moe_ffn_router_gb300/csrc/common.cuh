@@ -70,7 +70,7 @@ struct Plan {
     int nb;          // token blocks of the dispatch
     bool gemm;       // many-token path (tensor-core GEMMs, bf16 Y) instead of weight streaming
     size_t o_hdr, o_logits, o_ids, o_topw, o_sgate, o_counts, o_offsets, o_perm, o_inv, o_lr, o_cntb, o_base,
-        o_act, o_h, o_y, o_upg, o_dng, o_upt, o_dnt, o_uprec, o_dlog, o_dh, total;
+        o_act, o_h, o_y, o_upg, o_dng, o_upt, o_dnt, o_uprec, o_dlog, o_dh, o_dx, total;
 };
 
 constexpr int kStatsTokens = 32;     // tokens per block of the load-balancing statistics
@@ -118,6 +118,7 @@ inline bool make_plan(const moe_dims& d, Plan* p) {
     p->o_uprec = take(d.T <= kRecTokens ? P * (size_t)(d.I / 8) * sizeof(UpRec) : 0);
     p->o_dlog = take(d.T <= kRecTokens ? T * (size_t)(d.E + 1) * 8 : 0);
     p->o_dh = take(d.T <= kRecTokens ? (P + T) * (size_t)(p->Imax / 2) * 8 : 0);
+    p->o_dx = take(d.T == 1 ? (size_t)(d.H / 2) * 8 : 0);  // the token row as tagged words (host rows)
     p->total = o;
     return true;
 }

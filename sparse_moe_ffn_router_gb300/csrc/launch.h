@@ -41,6 +41,7 @@ struct LayerArgs {
     UpRec* uprec;     // routed gate_up records (few-token path), nullptr when not produced
     uint64_t* dlog;   // [T, E+1] router scores tagged with their call (fused few-token kernel)
     uint64_t* dh;     // [P+T, Imax/2] gated activation pairs tagged with their call (same kernel)
+    uint64_t* dx;     // [H/2] the token row's 32-bit words tagged with their call (T = 1, host rows)
     WsHeader* hdr;
     uint64_t wait_ns;   // time limit of the bounded waits of the one-token and streaming kernels
     int test_suppress;  // MOE_TEST_SUPPRESS_* (testing aid; 0 in normal use)
