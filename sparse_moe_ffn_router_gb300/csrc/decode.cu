@@ -30,11 +30,13 @@
 // with x held in registers, bf16 by bf16 (one token: an MMA would use one column of eight).
 //
 // Exchanges between CTAs carry a tag of the call instead of a flag: router scores are 64-bit
-// words (tag, fp32 score), h values 32-bit words (16-bit tag, bf16 h), published with atomic
+// words (tag, fp32 score), h values 32-bit words (16-bit tag, bf16 h), and, when the token row
+// is in host memory, the row's 32-bit words as 64-bit words (tag, word), each CTA reading its
+// share of the row over the host link (moe_forward_host_io); all are published with atomic
 // exchanges (carried out at L2, where the other SMs' polls see them within about a
 // microsecond; a plain store would need a fence, which stalls the SM's other warps). A
-// reader polls the words it needs until all carry this call's tag; every word is rewritten by
-// every call, so a stale word always carries the previous call's tag. Warp 0 of every CTA
+// reader polls the words it needs until all carry this call's tag; a word not yet rewritten
+// by this call carries an earlier call's tag. Warp 0 of every CTA
 // ranks the E scores itself (top-K with ties to the lower index, renormalised weights, the
 // shared gate) right after its own router row and releases the producers as soon as the
 // experts are known. Down items come last and wait only for the h words of their own expert
