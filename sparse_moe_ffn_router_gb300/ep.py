@@ -4,8 +4,8 @@ Unmeasured on hardware: every run of this build has one GPU. The exchange and th
 tested on CPU in two gloo processes (tests/test_ep_gloo.py); on GPUs the same calls run over
 NCCL.
 
-Rank r of N owns experts [r*E/N, (r+1)*E/N) (N divides E) and is the home rank of its own
-tokens. The experts are independent and each token fires K of them ("Qwen3.6-35B-A3B --
+Rank r of N owns experts [floor(r*E/N), floor((r+1)*E/N)) (equal blocks when N divides E) and
+is the home rank of its own tokens. The experts are independent and each token fires K of them ("Qwen3.6-35B-A3B --
 Architecture Overview", MoE FFN: 256 Experts), so the experts are sharded and the token rows
 travel. One call:
   1. routing on the home rank (the router weights are replicated): ids [T, K], w [T, K] and
@@ -30,10 +30,11 @@ import torch.distributed as dist
 
 
 def owners(ids: torch.Tensor, E: int, world: int) -> torch.Tensor:
-    """Rank that owns each expert id (contiguous blocks of E / world experts)."""
-    if E % world:
-        raise ValueError(f"{world} ranks do not divide {E} experts")
-    return torch.div(ids, E // world, rounding_mode="floor")
+    """Rank that owns each expert id: rank r owns [floor(r*E/world), floor((r+1)*E/world)), so
+    expert e belongs to the largest r with floor(r*E/world) <= e, i.e. floor(((e+1)*world - 1) / E)."""
+    if not 1 <= world <= E:
+        raise ValueError(f"{world} ranks cannot share {E} experts")
+    return torch.div((ids.to(torch.int64) + 1) * world - 1, E, rounding_mode="floor")
 
 
 def dispatch_order(ids: torch.Tensor, E: int, world: int):

@@ -1,7 +1,8 @@
-"""Expert parallelism (sparse_moe_ffn_router_gb300/ep.py) in two and four gloo processes on CPU.
+"""Expert parallelism (sparse_moe_ffn_router_gb300/ep.py) in two, three and four gloo processes
+on CPU.
 
-Rank r of N owns experts [r*E/N, (r+1)*E/N) and is home to tokens [r*T/N, (r+1)*T/N) of a seeded
-layer. Each rank routes its own tokens with the oracle, runs the exchange (counts, dispatch,
+Rank r of N owns experts [floor(r*E/N), floor((r+1)*E/N)) and is home to tokens
+[floor(r*T/N), floor((r+1)*T/N)) of a seeded layer (three ranks split both unevenly). Each rank routes its own tokens with the oracle, runs the exchange (counts, dispatch,
 expert outputs back, fixed-order combine) with the expert math restated in fp64 numpy, and
 the tests check, against the oracle's routing and layer output for all T tokens at once:
   - routing, bit for bit: the (expert, token, slot) triples each owner receives are exactly
@@ -67,10 +68,10 @@ def _rank_main(rank: int, world: int, port: int, bias_low: bool, out_dir: str):
 
     dist.init_process_group("gloo", rank=rank, world_size=world)
     T, H, E, K, I, Is = DIMS
-    Tl = T // world
+    t0, t1 = rank * T // world, (rank + 1) * T // world
     w, x = _layer(bias_low, world)
-    xr = x[rank * Tl:(rank + 1) * Tl]
-    dims_r = (Tl,) + DIMS[1:]
+    xr = x[t0:t1]
+    dims_r = (t1 - t0,) + DIMS[1:]
     r = oracle.route(dims_r, xr, w["router_w"], w["router_b"])
     taps = oracle.forward(dims_r, xr, w, taps=True)  # the shared gate and shared output of the home tokens
     gu, dn = _f64(w["gate_up"]), _f64(w["down"])
@@ -91,7 +92,7 @@ def _run(tmp_path, bias_low: bool, world: int = 2):
     got = [pickle.load(open(tmp_path / f"rank{r}.pkl", "rb")) for r in range(world)]
     w, x = _layer(bias_low, world)
     T, H, E, K, I, Is = DIMS
-    Tl = T // world
+    home = [(r * T // world, (r + 1) * T // world) for r in range(world)]
     ref_route = oracle.route(DIMS, x, w["router_w"], w["router_b"])
     ref = oracle.forward(DIMS, x, w)["out"]
     xb = x.view(torch.int16).numpy()
@@ -101,13 +102,14 @@ def _run(tmp_path, bias_low: bool, world: int = 2):
         # what the owner must receive from each source rank, in (expert, token, slot) order
         want = []
         for src in range(world):
-            pairs = [(int(ref_route["ids"][t, k]), t - src * Tl, k) for t in range(src * Tl, (src + 1) * Tl)
+            s0, s1 = home[src]
+            pairs = [(int(ref_route["ids"][t, k]), t - s0, k) for t in range(s0, s1)
                      for k in range(K) if lo <= ref_route["ids"][t, k] < hi]
             want += [(src,) + p for p in sorted(pairs)]
         have = [(int(s),) + tuple(int(v) for v in m) for s, m in zip(g["src"], g["meta"])]
         assert have == want, f"owner {owner}: received pairs"
         for (src, e, tl, k), row in zip(have, g["rows"]):
-            assert np.array_equal(row, xb[src * Tl + tl]), f"owner {owner}: row of token {src * Tl + tl}"
+            assert np.array_equal(row, xb[home[src][0] + tl]), f"owner {owner}: row of token {home[src][0] + tl}"
         assert int(g["recv_counts"].sum()) == len(want)
     out = np.concatenate([got[r]["out"] for r in range(world)])
     scale = np.abs(ref).max()
@@ -115,7 +117,7 @@ def _run(tmp_path, bias_low: bool, world: int = 2):
     return got
 
 
-@pytest.mark.parametrize("world", [2, 4])
+@pytest.mark.parametrize("world", [2, 3, 4])
 def test_expert_parallel_exchange_matches_the_oracle(tmp_path, world):
     got = _run(tmp_path, bias_low=False, world=world)
     assert all(int(g["recv_counts"].sum()) > 0 for g in got)
@@ -134,5 +136,9 @@ def test_dispatch_order_is_the_stable_expert_sort():
     # pairs p = t*K + k: expert 0 <- p3; expert 1 <- p1, p2; expert 2 <- p4; expert 3 <- p0, p5
     assert order.tolist() == [3, 1, 2, 4, 0, 5]
     assert counts.tolist() == [3, 3]
+    # 6 experts over 4 ranks: [0, 1), [1, 3), [3, 4), [4, 6)
+    assert ep.owners(torch.arange(6), 6, 4).tolist() == [0, 1, 1, 2, 3, 3]
+    order, counts = ep.dispatch_order(ids, 6, 4)
+    assert order.tolist() == [3, 1, 2, 4, 0, 5] and counts.tolist() == [1, 3, 2, 0]
     with pytest.raises(ValueError):
-        ep.dispatch_order(ids, 6, 4)  # 4 ranks do not divide 6 experts
+        ep.owners(torch.arange(2), 2, 3)  # more ranks than experts
